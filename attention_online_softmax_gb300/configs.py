@@ -1,0 +1,53 @@
+"""The synthetic workloads this library is measured and checked on.
+
+Each entry names what the workload is, with its sizes.  Inputs come from
+``inputs.py`` with the listed seed.  ``check_rows_per_head`` is the size of the
+seeded query-row subset used when the CPU oracle cannot afford every row.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+
+@dataclass(frozen=True)
+class PrefillConfig:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    seed: int
+    k_scale: float = 1.0
+    check_rows_per_head: int | None = None  # None: every row
+
+
+@dataclass(frozen=True)
+class DecodeConfig:
+    name: str
+    num_seqs: int
+    Hq: int
+    Hkv: int
+    d: int
+    len_lo: int
+    len_hi: int
+    num_pages: int
+    page_size: int
+    seed: int
+
+
+TINY = PrefillConfig("tiny_mha_b1_h2_n128_d64", 1, 2, 2, 128, 128, 64, False, 0)
+BLOCK = PrefillConfig("causal_mha_b4_h16_n512_d64", 4, 16, 16, 512, 512, 64, True, 1)
+LONG = PrefillConfig("causal_mha_b2_h32_n4096_d128", 2, 32, 32, 4096, 4096, 128, True, 2,
+                     check_rows_per_head=256)
+LONG_K4 = PrefillConfig("causal_mha_b2_h32_n4096_d128_kx4", 2, 32, 32, 4096, 4096, 128, True, 2,
+                        k_scale=4.0, check_rows_per_head=256)
+GQA256 = PrefillConfig("causal_gqa16to2_b1_n16384_d256", 1, 16, 2, 16384, 16384, 256, True, 3,
+                       check_rows_per_head=256)
+DECODE = DecodeConfig("paged_gqa32to8_decode_64seq_d128_len512to8192", 64, 32, 8, 128,
+                      512, 8192, 40000, 16, 4)
+
+PREFILL_CONFIGS = (TINY, BLOCK, LONG, LONG_K4, GQA256)
+ALL = {c.name: c for c in PREFILL_CONFIGS + (DECODE,)}

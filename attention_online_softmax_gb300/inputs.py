@@ -1,0 +1,138 @@
+"""Seeded synthetic inputs shared by the oracle side and the CUDA side.
+
+This module holds none of the attention arithmetic: it only draws random
+numbers and lays them out.  Both the tests (which feed the oracle and the
+kernels) and the benchmark import it; it imports neither side.
+
+Recipe (the pages name no generator; this is the reading used throughout):
+
+* ``g = torch.Generator('cpu').manual_seed(seed)``; every draw comes from it
+  in the order documented below, as float32 ``torch.randn`` rounded to
+  bfloat16 (round-to-nearest-even by ``Tensor.to``).
+* Prefill draws Q [B,Hq,Nq,d], then K [B,Hkv,Nk,d], then V [B,Hkv,Nk,d].
+  ``k_scale`` multiplies the bf16 K afterwards (4 is exact: a power of two).
+* Paged decode draws the lengths ``randint(lo, hi + 1, (S,))``, one pool
+  permutation ``randperm(num_pages)``, q [S,Hq,d], then for each sequence in
+  order its K and V rows [L_s, Hkv, d].  Sequence s owns the next
+  ceil(L_s / page_size) pages of the permutation (no page is shared).  Every
+  slot the cache does not use -- tail slots of a sequence's last page and whole
+  unused pages -- holds bf16 NaN, so a stray read shows up in parity.  Unused
+  block-table entries point at a NaN page when one exists.
+* Row subsets for large configurations continue on the same generator after
+  the data: per (b, h), ``randperm(Nq)[:per_head]`` plus rows 0 and Nq-1.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+BF16_NAN = float("nan")
+
+
+def _randn_bf16(g: torch.Generator, shape) -> torch.Tensor:
+    return torch.randn(tuple(shape), generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+@dataclass
+class PrefillInputs:
+    q: torch.Tensor  # [B, Hq, Nq, d] bf16
+    k: torch.Tensor  # [B, Hkv, Nk, d] bf16
+    v: torch.Tensor  # [B, Hkv, Nk, d] bf16
+    causal: bool
+    scale: float
+    generator: torch.Generator
+
+    @property
+    def shape(self):
+        B, Hq, Nq, d = self.q.shape
+        return B, Hq, self.k.shape[1], Nq, self.k.shape[2], d
+
+
+def prefill_inputs(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int,
+                   seed: int, causal: bool, k_scale: float = 1.0,
+                   scale: float | None = None) -> PrefillInputs:
+    g = torch.Generator("cpu").manual_seed(int(seed))
+    q = _randn_bf16(g, (B, Hq, Nq, d))
+    k = _randn_bf16(g, (B, Hkv, Nk, d))
+    v = _randn_bf16(g, (B, Hkv, Nk, d))
+    if k_scale != 1.0:
+        k = (k.float() * k_scale).to(torch.bfloat16)
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+    return PrefillInputs(q, k, v, bool(causal), float(scale), g)
+
+
+def check_rows(g: torch.Generator, B: int, Hq: int, Nq: int, per_head: int) -> torch.Tensor:
+    """Flat row ids ((b*Hq + h)*Nq + i) of a seeded subset, sorted per head."""
+    out = []
+    for bh in range(B * Hq):
+        pick = torch.randperm(Nq, generator=g)[:per_head]
+        rows = torch.unique(torch.cat([pick, torch.tensor([0, Nq - 1])]))
+        out.append(rows + bh * Nq)
+    return torch.cat(out).to(torch.int64)
+
+
+@dataclass
+class DecodeInputs:
+    q: torch.Tensor            # [S, Hq, d] bf16
+    kcache: torch.Tensor       # [P, page_size, Hkv, d] bf16
+    vcache: torch.Tensor       # [P, page_size, Hkv, d] bf16
+    block_table: torch.Tensor  # [S, max_pages] int32
+    seqlens: torch.Tensor      # [S] int32
+    scale: float
+    page_size: int
+    max_seqlen: int
+    generator: torch.Generator
+
+
+def decode_inputs(num_seqs: int, Hq: int, Hkv: int, d: int, len_lo: int, len_hi: int,
+                  num_pages: int, page_size: int, seed: int,
+                  max_pages_per_seq: int | None = None,
+                  lengths: list[int] | None = None,
+                  scale: float | None = None) -> DecodeInputs:
+    """Paged KV cache with seeded lengths (or explicit ``lengths``)."""
+    g = torch.Generator("cpu").manual_seed(int(seed))
+    if lengths is None:
+        lens = torch.randint(len_lo, len_hi + 1, (num_seqs,), generator=g, dtype=torch.int64)
+    else:
+        lens = torch.tensor(list(lengths), dtype=torch.int64)
+        if lens.numel() != num_seqs:
+            raise ValueError("lengths must have num_seqs entries")
+    perm = torch.randperm(num_pages, generator=g)
+    q = _randn_bf16(g, (num_seqs, Hq, d))
+    pages_needed = [(int(L) + page_size - 1) // page_size for L in lens.tolist()]
+    if max_pages_per_seq is None:
+        max_pages_per_seq = max(1, (int(len_hi) + page_size - 1) // page_size)
+    if sum(pages_needed) > num_pages:
+        raise ValueError("page pool too small for the drawn lengths")
+    if max(pages_needed + [0]) > max_pages_per_seq:
+        raise ValueError("max_pages_per_seq too small for the drawn lengths")
+    kc = torch.full((num_pages, page_size, Hkv, d), BF16_NAN, dtype=torch.bfloat16)
+    vc = torch.full((num_pages, page_size, Hkv, d), BF16_NAN, dtype=torch.bfloat16)
+    used = sum(pages_needed)
+    spare = int(perm[used]) if used < num_pages else 0
+    bt = torch.full((num_seqs, max_pages_per_seq), spare, dtype=torch.int32)
+    cursor = 0
+    for s, L in enumerate(lens.tolist()):
+        npg = pages_needed[s]
+        pages = perm[cursor:cursor + npg]
+        cursor += npg
+        bt[s, :npg] = pages.to(torch.int32)
+        ks = _randn_bf16(g, (L, Hkv, d))
+        vs = _randn_bf16(g, (L, Hkv, d))
+        if L == 0:
+            continue
+        full = L // page_size
+        if full:
+            kc[pages[:full]] = ks[:full * page_size].reshape(full, page_size, Hkv, d)
+            vc[pages[:full]] = vs[:full * page_size].reshape(full, page_size, Hkv, d)
+        rem = L - full * page_size
+        if rem:
+            kc[pages[full], :rem] = ks[full * page_size:]
+            vc[pages[full], :rem] = vs[full * page_size:]
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+    return DecodeInputs(q, kc, vc, bt, lens.to(torch.int32), float(scale), page_size,
+                        int(lens.max().item()) if num_seqs else 0, g)

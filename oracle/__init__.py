@@ -1,0 +1,173 @@
+"""Oracle for fused attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The CUDA
+library never imports, links or calls it, and it imports nothing from the CUDA
+library.  Inputs reach both sides from the seeded generators in
+``attention_online_softmax_gb300.inputs``, which hold none of the method's
+arithmetic.
+
+Contents
+--------
+``attn_oracle.c``   plain two-pass attention and paged decode in double
+                    precision (C, OpenMP over query rows); see its header for
+                    the passages it follows and the readings it takes.
+``monoid.py``       the online-softmax recurrence and the associative merge of
+                    partial states (m, l, o), in float64 numpy, written from the
+                    same pages; used by the tests to pin the merge semantics.
+
+Every function here is pinned by ``tests/test_oracle_*.py`` against brute
+force, closed forms and invariants; none of its expected values comes from the
+CUDA path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LOCK = threading.Lock()
+_LIBS: dict[int, ctypes.CDLL] = {}
+
+
+def lib_path(mutant: int = 0) -> str:
+    name = "liboracle.so" if mutant == 0 else f"liboracle_mutant{mutant}.so"
+    return os.path.join(_HERE, "_build", name)
+
+
+def build(mutant: int = 0, force: bool = False) -> str:
+    """Compile the C oracle with gcc (-O2, OpenMP).  Returns the .so path."""
+    out = lib_path(mutant)
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(_SRC)):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = f"{out}.{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           f"-DORACLE_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _load(mutant: int = 0) -> ctypes.CDLL:
+    with _LOCK:
+        lib = _LIBS.get(mutant)
+        if lib is None:
+            lib = ctypes.CDLL(build(mutant))
+            p = ctypes.c_void_p
+            i = ctypes.c_int
+            lib.oracle_attention.argtypes = [p, p, p, i, i, i, i, i, i, i,
+                                             ctypes.c_float, p, ctypes.c_int64,
+                                             p, p, i]
+            lib.oracle_attention.restype = i
+            lib.oracle_decode_paged.argtypes = [p, p, p, p, p, i, i, i, i, i,
+                                                i, i, ctypes.c_float, p, i,
+                                                p, p, i]
+            lib.oracle_decode_paged.restype = i
+            _LIBS[mutant] = lib
+        return lib
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 data as a contiguous uint16 numpy array of its bit patterns.
+
+    Accepts a torch bfloat16 tensor (any device: it is copied to host) or a
+    numpy uint16 array.
+    """
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.uint16:
+            raise TypeError("numpy input must hold bf16 bit patterns as uint16")
+        return np.ascontiguousarray(x)
+    import torch
+    if x.dtype != torch.bfloat16:
+        raise TypeError(f"expected bfloat16, got {x.dtype}")
+    return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def attention(q, k, v, causal: bool, scale: float, rows=None, threads: int = 0,
+              mutant: int = 0):
+    """softmax(scale * Q K^T + mask) V and the row logsumexp, in float64.
+
+    q: [B, Hq, Nq, d], k, v: [B, Hkv, Nk, d] (bf16).  ``rows`` selects flat
+    query rows ((b*Hq + h)*Nq + i); None means all rows.  Returns
+    (O [nrows, d] float64, LSE [nrows] float64, threads_used); with rows=None
+    O is reshaped to [B, Hq, Nq, d] and LSE to [B, Hq, Nq].
+    """
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    if qb.ndim != 4 or kb.ndim != 4 or vb.shape != kb.shape:
+        raise ValueError("q must be [B,Hq,Nq,d]; k, v [B,Hkv,Nk,d]")
+    B, Hq, Nq, d = qb.shape
+    Bk, Hkv, Nk, dk = kb.shape
+    if Bk != B or dk != d:
+        raise ValueError("q/k shape mismatch")
+    if rows is None:
+        nrows = B * Hq * Nq
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows_arr.size
+    o = np.empty((nrows, d), dtype=np.float64)
+    lse = np.empty((nrows,), dtype=np.float64)
+    rc = _load(mutant).oracle_attention(
+        _ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
+        float(scale), None if rows_arr is None else _ptr(rows_arr), nrows,
+        _ptr(o), _ptr(lse), int(threads))
+    if rc < 0:
+        raise ValueError(f"oracle_attention rejected its arguments ({rc})")
+    if rows is None:
+        o = o.reshape(B, Hq, Nq, d)
+        lse = lse.reshape(B, Hq, Nq)
+    return o, lse, rc
+
+
+def decode_paged(q, kcache, vcache, block_table, seqlens, scale: float,
+                 seqs=None, threads: int = 0, mutant: int = 0):
+    """One-row attention per (sequence, query head) over a paged KV cache.
+
+    q: [S, Hq, d]; kcache, vcache: [P, page_size, Hkv, d] (bf16);
+    block_table: [S, max_pages] int32; seqlens: [S] int32.  Returns
+    (O [n, Hq, d] float64, LSE [n, Hq] float64, threads_used) for the selected
+    sequences (all when ``seqs`` is None).
+    """
+    qb, kb, vb = _bits(q), _bits(kcache), _bits(vcache)
+    bt = np.ascontiguousarray(np.asarray(_host(block_table), dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(_host(seqlens), dtype=np.int32))
+    S, Hq, d = qb.shape
+    P, page, Hkv, dk = kb.shape
+    if dk != d or vb.shape != kb.shape or bt.shape[0] != S or sl.shape != (S,):
+        raise ValueError("decode shape mismatch")
+    if seqs is None:
+        n = S
+        seqs_arr = None
+    else:
+        seqs_arr = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        n = seqs_arr.size
+    o = np.empty((n, Hq, d), dtype=np.float64)
+    lse = np.empty((n, Hq), dtype=np.float64)
+    rc = _load(mutant).oracle_decode_paged(
+        _ptr(qb), _ptr(kb), _ptr(vb), _ptr(bt), _ptr(sl), S, Hq, Hkv, d, page,
+        P, bt.shape[1], float(scale), None if seqs_arr is None else _ptr(seqs_arr),
+        n, _ptr(o), _ptr(lse), int(threads))
+    if rc < 0:
+        raise ValueError(f"oracle_decode_paged rejected its arguments ({rc})")
+    return o, lse, rc
+
+
+def _host(x):
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return x.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return x

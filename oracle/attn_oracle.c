@@ -1,0 +1,272 @@
+/*
+ * Oracle for fused scaled-dot-product attention -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only tests/, the smoke check in __graft_entry__.py and the cpu_baseline /
+ * reference legs of bench.py may load this code.  The product path (the CUDA
+ * library under attention_online_softmax_gb300/) never links, loads or calls it,
+ * and this file shares no code, header or table with that library.
+ *
+ * What it computes is the plain two-pass definition of attention, in double
+ * precision, one query row at a time:
+ *
+ *   "Compilers and Kernels", section "FlashAttention changes the algorithm
+ *   around IO", first display equation and the one after it:
+ *       S = Q K^T / sqrt(d) + C,   m_i = max_j S_ij,
+ *       l_i = sum_j exp(S_ij - m_i),   P_ij = exp(S_ij - m_i) / l_i,   O = P V.
+ *   The additive mask C takes the values 0 (key allowed) or -inf (key
+ *   disallowed); a disallowed key is simply left out of the max and the sum.
+ *
+ *   "Don't Write Kernels, Derive Them", section "What happened": logsumexp is
+ *   one of the derived operations.  The row logsumexp of the scaled, masked
+ *   scores is  LSE_i = m_i + ln(l_i).
+ *
+ * Readings where the pages are silent (each one is listed with its reason in
+ * the design notes of the repository):
+ *   - scale: the caller passes the float it wants (1/sqrt(d) in every workload);
+ *     it is widened to double unchanged, so the oracle and the GPU use the same
+ *     number.
+ *   - causal alignment for Nq != Nk is bottom-right: key j is allowed for query
+ *     i iff j <= i + (Nk - Nq).  For Nq == Nk this is "query i attends keys
+ *     0..i".
+ *   - grouped-query attention: query head h reads key/value head
+ *     h / (Hq / Hkv) (consecutive groups).
+ *   - a row with no allowed key (the page assumes there is none) is defined as
+ *     O = 0 and LSE = -inf.
+ *   - inputs arrive as bfloat16 bit patterns; each is widened exactly to double.
+ *
+ * Paged decode is the same definition with one query row per sequence, over
+ * all seqlens[s] cached tokens, where token t of sequence s sits in page
+ * block_table[s][t / page_size], slot t % page_size, of a cache laid out as
+ * [num_pages][page_size][Hkv][d].
+ *
+ * Build switch ORACLE_MUTANT (default 0) plants one deliberate mistake; it
+ * exists only so the test-suite can show that its pins catch each kind of
+ * mistake (a dropped scale, a wrong mask offset, a wrong head, a transposed
+ * operand, a dropped normaliser).  The shipped oracle is built with 0.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+/* bfloat16 is the upper half of an IEEE binary32; widening is exact. */
+static double bf16_to_double(uint16_t bits) {
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/*
+ * One query row against n_keys keys.
+ *   q:  d values (bf16 bits), kv rows fetched through key_row()/val_row().
+ *   Writes d_v doubles to o and returns the row LSE through *lse.
+ * The key/value rows are given as arrays of row pointers so that the same
+ * routine serves contiguous prefill and paged decode.
+ */
+static void attend_row(const uint16_t* q, const uint16_t* const* krows,
+                       const uint16_t* const* vrows, int64_t n_keys, int d,
+                       double scale, double* scratch, double* o, double* lse) {
+    int64_t j;
+    int c;
+    if (n_keys <= 0) {
+        for (c = 0; c < d; ++c) o[c] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    /* pass 1: scores and their maximum */
+    double m = -INFINITY;
+    for (j = 0; j < n_keys; ++j) {
+        double s = 0.0;
+        for (c = 0; c < d; ++c) {
+#if ORACLE_MUTANT == 4
+            /* transposed operand: reads the key matrix column-wise */
+            s += bf16_to_double(q[c]) * bf16_to_double(krows[c % n_keys][j % d]);
+#else
+            s += bf16_to_double(q[c]) * bf16_to_double(krows[j][c]);
+#endif
+        }
+#if ORACLE_MUTANT == 1
+        /* dropped scale */
+        (void)scale;
+#else
+        s *= scale;
+#endif
+        scratch[j] = s;
+        if (s > m) m = s;
+    }
+    /* pass 2: normaliser and the weighted sum of value rows */
+    double l = 0.0;
+    for (c = 0; c < d; ++c) o[c] = 0.0;
+    for (j = 0; j < n_keys; ++j) {
+        double p = exp(scratch[j] - m);
+        l += p;
+        for (c = 0; c < d; ++c) o[c] += p * bf16_to_double(vrows[j][c]);
+    }
+#if ORACLE_MUTANT == 5
+    /* dropped normaliser */
+    (void)l;
+#else
+    for (c = 0; c < d; ++c) o[c] /= l;
+#endif
+    *lse = m + log(l);
+}
+
+static int oracle_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#else
+    nthreads = 1;
+#endif
+    return nthreads;
+}
+
+/*
+ * Prefill / general attention.
+ *   q: [B][Hq][Nq][d], k and v: [B][Hkv][Nk][d], all bf16 bits, contiguous.
+ *   rows: flat query-row ids ((b*Hq + h)*Nq + i), or NULL for every row in
+ *   order; nrows: their count.
+ *   o_out: [nrows][d] doubles, lse_out: [nrows] doubles.
+ *   nthreads <= 0 uses every core OpenMP offers.
+ * Returns the number of threads used, or a negative value on a bad argument.
+ */
+int oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                     float scale, const int64_t* rows, int64_t nrows,
+                     double* o_out, double* lse_out, int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0 || d <= 0) return -1;
+    if (Hq % Hkv != 0) return -1;
+    const int group = Hq / Hkv;
+    const int64_t total = (int64_t)B * Hq * Nq;
+    if (rows == NULL) nrows = total;
+    nthreads = oracle_threads(nthreads);
+    int bad = 0;
+
+#pragma omp parallel num_threads(nthreads)
+    {
+        double* scratch = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        const uint16_t** krows = (const uint16_t**)malloc(sizeof(void*) * (size_t)(Nk > 0 ? Nk : 1));
+        const uint16_t** vrows = (const uint16_t**)malloc(sizeof(void*) * (size_t)(Nk > 0 ? Nk : 1));
+        int64_t r;
+#pragma omp for schedule(dynamic, 4)
+        for (r = 0; r < nrows; ++r) {
+            int64_t flat = rows ? rows[r] : r;
+            if (flat < 0 || flat >= total) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            int64_t i = flat % Nq;
+            int64_t bh = flat / Nq;
+            int64_t h = bh % Hq;
+            int64_t b = bh / Hq;
+#if ORACLE_MUTANT == 3
+            int64_t g = h % Hkv; /* wrong head mapping */
+#else
+            int64_t g = h / group;
+#endif
+            int64_t n_allowed = Nk;
+            if (causal) {
+#if ORACLE_MUTANT == 2
+                int64_t last = i; /* wrong alignment: ignores Nk - Nq */
+#else
+                int64_t last = i + (int64_t)Nk - (int64_t)Nq;
+#endif
+                n_allowed = last + 1;
+                if (n_allowed < 0) n_allowed = 0;
+                if (n_allowed > Nk) n_allowed = Nk;
+            }
+            const uint16_t* kb = k + ((b * Hkv + g) * (int64_t)Nk) * d;
+            const uint16_t* vb = v + ((b * Hkv + g) * (int64_t)Nk) * d;
+            int64_t j;
+            for (j = 0; j < n_allowed; ++j) {
+                krows[j] = kb + j * d;
+                vrows[j] = vb + j * d;
+            }
+            attend_row(q + flat * d, krows, vrows, n_allowed, d, (double)scale,
+                       scratch, o_out + r * d, lse_out + r);
+        }
+        free(scratch);
+        free(krows);
+        free(vrows);
+    }
+    return bad ? -2 : nthreads;
+}
+
+/*
+ * Paged decode: one query row per sequence and query head.
+ *   q: [num_seqs][Hq][d]; kcache, vcache: [num_pages][page_size][Hkv][d];
+ *   block_table: [num_seqs][max_pages_per_seq] int32; seqlens: [num_seqs].
+ *   seqs: sequence ids to evaluate (NULL = all, in order), nseqs their count.
+ *   o_out: [nseqs][Hq][d] doubles, lse_out: [nseqs][Hq] doubles.
+ * Returns threads used, or a negative value when an argument or a block-table
+ * entry is out of range.
+ */
+int oracle_decode_paged(const uint16_t* q, const uint16_t* kcache, const uint16_t* vcache,
+                        const int32_t* block_table, const int32_t* seqlens,
+                        int num_seqs, int Hq, int Hkv, int d, int page_size,
+                        int num_pages, int max_pages_per_seq, float scale,
+                        const int32_t* seqs, int nseqs,
+                        double* o_out, double* lse_out, int nthreads) {
+    if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || page_size <= 0) return -1;
+    if (Hq % Hkv != 0) return -1;
+    const int group = Hq / Hkv;
+    if (seqs == NULL) nseqs = num_seqs;
+    int64_t max_len = 0;
+    int s;
+    for (s = 0; s < num_seqs; ++s) {
+        if (seqlens[s] < 0 || (int64_t)seqlens[s] > (int64_t)max_pages_per_seq * page_size) return -1;
+        if (seqlens[s] > max_len) max_len = seqlens[s];
+    }
+    nthreads = oracle_threads(nthreads);
+    const int64_t work = (int64_t)nseqs * Hq;
+    int bad = 0;
+
+#pragma omp parallel num_threads(nthreads)
+    {
+        double* scratch = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+        const uint16_t** krows = (const uint16_t**)malloc(sizeof(void*) * (size_t)(max_len > 0 ? max_len : 1));
+        const uint16_t** vrows = (const uint16_t**)malloc(sizeof(void*) * (size_t)(max_len > 0 ? max_len : 1));
+        int64_t w;
+#pragma omp for schedule(dynamic, 1)
+        for (w = 0; w < work; ++w) {
+            int si = (int)(w / Hq);
+            int h = (int)(w % Hq);
+            int seq = seqs ? seqs[si] : si;
+            if (seq < 0 || seq >= num_seqs) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            int g = h / group;
+            int64_t n = seqlens[seq];
+            int64_t t;
+            int ok = 1;
+            for (t = 0; t < n; ++t) {
+                int32_t page = block_table[(int64_t)seq * max_pages_per_seq + t / page_size];
+                if (page < 0 || page >= num_pages) { ok = 0; break; }
+                int64_t off = (((int64_t)page * page_size + t % page_size) * Hkv + g) * d;
+                krows[t] = kcache + off;
+                vrows[t] = vcache + off;
+            }
+            if (!ok) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            attend_row(q + ((int64_t)seq * Hq + h) * d, krows, vrows, n, d, (double)scale,
+                       scratch, o_out + w * d, lse_out + w);
+        }
+        free(scratch);
+        free(krows);
+        free(vrows);
+    }
+    return bad ? -2 : nthreads;
+}

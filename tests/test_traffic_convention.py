@@ -1,0 +1,60 @@
+"""The byte-counting convention used for every roofline figure.
+
+Pinned to the fused-versus-unfused example of "Compilers and Kernels",
+section "Roofline is a bound, not a stopwatch" (tests/golden/fusion_traffic_example.txt),
+and to hand counts of the attention workloads.
+"""
+import os
+
+import pytest
+
+from attention_online_softmax_gb300 import roofline
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "fusion_traffic_example.txt")
+
+
+def load_golden():
+    vals = {}
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        k, v = line.split()
+        vals[k] = float(v)
+    return vals
+
+
+def test_fusion_example_traffic():
+    g = load_golden()
+    n, bpe = int(g["elements"]), int(g["bytes_per_element"])
+    ops = n * 3
+    # unfused: three kernels (mul, add, max), each reads one vector and writes one
+    unfused = sum(roofline.materialized_traffic(n, bpe, reads=1, writes=1) for _ in range(3))
+    fused = roofline.materialized_traffic(n, bpe, reads=1, writes=1)
+    assert ops == g["operations"]
+    assert unfused == g["unfused_bytes"] and fused == g["fused_bytes"]
+    assert ops / unfused == pytest.approx(g["unfused_intensity"])
+    assert ops / fused == pytest.approx(g["fused_intensity"])
+    assert unfused / fused == pytest.approx(g["traffic_reduction"])
+
+
+def test_attention_counts_by_hand():
+    # tiny MHA B1 H2 N128 d64: Q,K,V,O bf16 = 4 * 2*128*64*2 B, LSE 2*128*4 B
+    assert roofline.prefill_bytes(1, 2, 2, 128, 128, 64) == 4 * 32768 + 1024
+    assert roofline.prefill_flops(1, 2, 128, 128, 64, False) == 4 * 2 * 128 * 128 * 64
+    assert roofline.prefill_flops(4, 16, 512, 512, 64, True) == 2 * 4 * 16 * 512 * 512 * 64
+    # GQA: K and V are counted once per key/value head
+    assert roofline.prefill_bytes(1, 16, 2, 16384, 16384, 256) == (
+        2 * 16 * 16384 * 256 * 2 + 2 * 2 * 16384 * 256 * 2 + 16 * 16384 * 4)
+    # decode: 2 sequences of 17 and 32 tokens, 8 q heads over 2 kv heads, d 16
+    b = roofline.decode_bytes([17, 32], 8, 2, 16, 16)
+    assert b == 49 * 2 * 16 * 2 * 2 + 2 * 8 * 16 * 2 * 2 + 2 * 8 * 4 + (2 + 2) * 4 + 2 * 4
+
+
+def test_roofline_bound_and_floor():
+    p = roofline.Peaks(hbm_gbs=1000.0, bf16_tflops=100.0, bf16_tflops_sustained=90.0,
+                       source="test")
+    assert roofline.ridge(p) == pytest.approx(100.0)
+    assert roofline.bound_rate(1e12, 1e9, p) == pytest.approx(1e14)  # I=1000 > ridge
+    assert roofline.bound_rate(1e11, 1e10, p) == pytest.approx(1e13)  # I=10 < ridge
+    assert roofline.time_floor_s(1e12, 1e9, p) == pytest.approx(0.01)
