@@ -1,0 +1,154 @@
+"""Thin ctypes binding of the C ABI in include/attn.h (argument marshalling only).
+
+Each function has the name of the C entry point it calls.  Tensors are
+PyTorch CUDA tensors (torch is used for device memory and streams only); the
+binding checks dtype / contiguity / device, passes raw pointers and sizes, and
+raises ``AttnError`` on a non-OK status.  Every step of the computation runs in
+the CUDA kernels of libattn_gb300.so: there is no other code path.  Importing
+this module when the library has not been built raises ``ImportError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+_LIB_PATH = _build.LIB
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"libattn_gb300.so is not built ({_LIB_PATH}); run "
+        "`python -m attention_online_softmax_gb300.build` (needs nvcc)")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _vp]
+_lib.attn_fwd.restype = _i
+_lib.attn_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+_lib.attn_decode_workspace_size.restype = ctypes.c_size_t
+_lib.attn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
+                                   ctypes.c_float, _vp, ctypes.c_size_t, _i, _vp]
+_lib.attn_decode_paged.restype = _i
+_lib.attn_get_device_status.argtypes = [_vp]
+_lib.attn_get_device_status.restype = _i
+_lib.attn_status_string.argtypes = [_i]
+_lib.attn_status_string.restype = ctypes.c_char_p
+_lib.attn_launch_count.argtypes = []
+_lib.attn_launch_count.restype = ctypes.c_uint64
+_lib.attn_abi_version.argtypes = []
+_lib.attn_abi_version.restype = _i
+
+ATTN_OK = 0
+ATTN_BF16 = 0
+ATTN_F32 = 1
+
+#: every symbol include/attn.h declares
+EXPORTS = ("attn_fwd", "attn_decode_workspace_size", "attn_decode_paged", "attn_get_device_status",
+           "attn_status_string", "attn_launch_count", "attn_abi_version")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def attn_status_string(status: int) -> str:
+    return _lib.attn_status_string(int(status)).decode()
+
+
+def attn_launch_count() -> int:
+    return int(_lib.attn_launch_count())
+
+
+def attn_abi_version() -> int:
+    return int(_lib.attn_abi_version())
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check(status: int, where: str) -> None:
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+def _need(t, dtype, name):
+    import torch
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return torch
+
+
+def attn_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """q [B,Hq,Nq,d], k/v [B,Hkv,Nk,d] bf16 -> o [B,Hq,Nq,d] (bf16|f32), lse [B,Hq,Nq] f32."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    if o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be bfloat16 or float32")
+    _need(o, o.dtype, "o")
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nk, _ = k.shape
+    if tuple(o.shape) != (B, Hq, Nq, d) or tuple(lse.shape) != (B, Hq, Nq) or v.shape != k.shape:
+        raise ValueError("shape mismatch between q, k, v, o, lse")
+    st = _lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                       int(bool(causal)), float(scale),
+                       ATTN_F32 if o.dtype == torch.float32 else ATTN_BF16, _stream_ptr(stream))
+    _check(st, "attn_fwd")
+
+
+def attn_decode_workspace_size(num_seqs: int, Hq: int, Hkv: int, d: int, max_seqlen: int) -> int:
+    return int(_lib.attn_decode_workspace_size(num_seqs, Hq, Hkv, d, max_seqlen))
+
+
+def attn_decode_paged(q, kcache, vcache, block_table, seqlens, o, lse, max_seqlen: int,
+                      scale: float, workspace, stream=None) -> None:
+    """Paged decode; shapes as in include/attn.h.  ``workspace`` is a CUDA uint8
+    tensor of at least attn_decode_workspace_size(...) bytes (or None when that
+    size is 0)."""
+    import torch
+    _need(q, torch.bfloat16, "q")
+    _need(kcache, torch.bfloat16, "kcache")
+    _need(vcache, torch.bfloat16, "vcache")
+    _need(block_table, torch.int32, "block_table")
+    _need(seqlens, torch.int32, "seqlens")
+    _need(lse, torch.float32, "lse")
+    _need(o, o.dtype, "o")
+    S, Hq, d = q.shape
+    P, page, Hkv, _ = kcache.shape
+    ws_bytes = 0
+    if workspace is not None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    st = _lib.attn_decode_paged(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(block_table), _ptr(seqlens),
+                                _ptr(o), _ptr(lse), S, Hq, Hkv, d, page, P, block_table.shape[1],
+                                int(max_seqlen), float(scale), _ptr(workspace), ws_bytes,
+                                ATTN_F32 if o.dtype == torch.float32 else ATTN_BF16,
+                                _stream_ptr(stream))
+    _check(st, "attn_decode_paged")
+
+
+def attn_get_device_status(stream=None) -> int:
+    return int(_lib.attn_get_device_status(_stream_ptr(stream)))

@@ -1,0 +1,331 @@
+// C ABI of the GB300 fused-attention library: argument checks, TMA tensor-map
+// encoding, work planning and kernel launches.  Declared in include/attn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn.h"
+#include "decode.cuh"
+#include "prefill_fwd.cuh"
+#include "ptx.cuh"
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// The current device must be a GB300-class part (compute capability 10.3).
+attn_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+// 3-D bf16 map over [heads][rows][d] with a (64 x box_rows x 1) box and the
+// 128-byte swizzle that the tcgen05 operand descriptors expect.
+bool encode_rows_map(CUtensorMap* map, const void* base, int d, int rows, int heads, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 4-D bf16 map over the paged cache [pages][slots][Hkv][d]; one box is the
+// [16 slots][hg heads][d] block of one page (no swizzle).
+bool encode_page_map(CUtensorMap* map, const void* base, int d, int Hkv, int page_size, int num_pages, int hg) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hkv),
+                        static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(Hkv) * d * 2,
+                           static_cast<cuuint64_t>(page_size) * Hkv * d * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(hg),
+                       static_cast<cuuint32_t>(page_size), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, int BN, int STAGES>
+attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                           const attn::PrefillParams& p, int BH, cudaStream_t stream) {
+  using L = attn::PrefillLayout<D, BN, STAGES>;
+  auto kern = attn::prefill_fwd_kernel<D, BN, STAGES>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  const long long blocks = static_cast<long long>(p.n_qtiles) * BH;
+  if (blocks > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
+  kern<<<dim3(static_cast<unsigned>(blocks)), attn::kPrefillThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return ATTN_OK;
+}
+
+// ---------------------------------------------------------------- decode plan
+struct DecodePlan {
+  int hg = 1;
+  int chunk = attn::kChunkMax;
+  int n_splits = 1;
+  size_t ws_o_floats = 0;
+  size_t ws_bytes = 0;
+};
+
+bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int max_seqlen, DecodePlan* out) {
+  if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_seqlen < 0) return false;
+  if (d != 64 && d != 128 && d != 256) return false;
+  DecodePlan pl;
+  for (int c : {8, 4, 2, 1}) {
+    if (Hkv % c == 0 && c * d <= 1024) {
+      pl.hg = c;
+      break;
+    }
+  }
+  const long long groups = static_cast<long long>(num_seqs) * (Hkv / pl.hg);
+  pl.chunk = attn::kChunkMax;
+  while (pl.chunk > 64 && groups * ((max_seqlen + pl.chunk - 1) / pl.chunk) < 1024) pl.chunk /= 2;
+  pl.n_splits = max_seqlen > 0 ? (max_seqlen + pl.chunk - 1) / pl.chunk : 1;
+  if (pl.n_splits > 1) {
+    pl.ws_o_floats = static_cast<size_t>(num_seqs) * pl.n_splits * Hq * d;
+    const size_t lse_floats = static_cast<size_t>(num_seqs) * pl.n_splits * Hq;
+    pl.ws_bytes = ((pl.ws_o_floats + lse_floats) * 4 + 255) & ~static_cast<size_t>(255);
+  }
+  *out = pl;
+  return true;
+}
+
+template <int D, int G>
+attn_status launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, attn::DecodeParams p,
+                          cudaStream_t stream) {
+  const int scores_bytes = p.hg * p.chunk * G * 4;
+  const int budget = 113 * 1024;  // two CTAs per SM
+  int stages = (budget - scores_bytes - 1024 - 2 * attn::kMaxStages * 8) / p.stage_bytes;
+  stages = stages < 2 ? 2 : (stages > 4 ? 4 : stages);
+  p.stages = stages;
+  const int smem = stages * p.stage_bytes + scores_bytes + 2 * attn::kMaxStages * 8 + 1024;
+  auto ks = attn::decode_split_kernel<D, G>;
+  if (cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  const long long gx = static_cast<long long>(p.num_seqs) * p.n_splits;
+  if (gx > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
+  ks<<<dim3(static_cast<unsigned>(gx), p.Hkv / p.hg), (p.hg + 1) * 32, smem, stream>>>(mk, mv, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (p.n_splits > 1) {
+    attn::decode_combine_kernel<D><<<dim3(p.num_seqs, (p.Hq + 3) / 4), 128, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  return ATTN_OK;
+}
+
+template <int D>
+attn_status launch_decode_g(int G, const CUtensorMap& mk, const CUtensorMap& mv, const attn::DecodeParams& p,
+                            cudaStream_t s) {
+  switch (G) {
+    case 1: return launch_decode<D, 1>(mk, mv, p, s);
+    case 2: return launch_decode<D, 2>(mk, mv, p, s);
+    case 4: return launch_decode<D, 4>(mk, mv, p, s);
+    case 8: return launch_decode<D, 8>(mk, mv, p, s);
+    default: return ATTN_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_abi_version(void) { return 1; }
+
+uint64_t attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_MISALIGNED: return "null or misaligned pointer";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_LAUNCH: return "kernel launch failed";
+    case ATTN_ERR_TIMEOUT: return "device wait timed out";
+    case ATTN_ERR_BOUNDS: return "block table entry or sequence length out of range";
+    case ATTN_ERR_NO_DEVICE: return "no usable CUDA device";
+  }
+  return "unknown status";
+}
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int d, int causal, float scale, attn_dtype o_dtype, attn_stream_t stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (o_dtype != ATTN_BF16 && o_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq > 0x7FFFFFFFLL || static_cast<long long>(B) * Hkv > 0x7FFFFFFFLL)
+    return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Nq == 0) return ATTN_OK;  // empty output
+  if (!aligned16(q) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
+  if (Nk > 0 && (!aligned16(k) || !aligned16(v))) return ATTN_ERR_MISALIGNED;
+  attn_status st = check_device();
+  if (st != ATTN_OK) return st;
+
+  CUtensorMap mq, mk, mv;
+  // With Nk == 0 no key tile is ever loaded; the K/V maps then describe q.
+  const void* kb = Nk > 0 ? k : q;
+  const void* vb = Nk > 0 ? v : q;
+  const int nk_map = Nk > 0 ? Nk : 1;
+  const int bhkv = Nk > 0 ? B * Hkv : 1;
+  if (!encode_rows_map(&mq, q, d, Nq, B * Hq, attn::kBM) ||
+      !encode_rows_map(&mk, kb, d, nk_map, bhkv, 128) || !encode_rows_map(&mv, vb, d, nk_map, bhkv, 128))
+    return ATTN_ERR_LAUNCH;
+
+  attn::PrefillParams p;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.causal = causal ? 1 : 0;
+  p.o_f32 = o_dtype == ATTN_F32 ? 1 : 0;
+  p.n_qtiles = (Nq + attn::kBM - 1) / attn::kBM;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (d) {
+    case 64: return launch_prefill<64, 128, 6>(mq, mk, mv, p, B * Hq, s);
+    case 128: return launch_prefill<128, 128, 4>(mq, mk, mv, p, B * Hq, s);
+    case 256: return launch_prefill<256, 128, 2>(mq, mk, mv, p, B * Hq, s);
+  }
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+size_t attn_decode_workspace_size(int num_seqs, int Hq, int Hkv, int d, int max_seqlen) {
+  DecodePlan pl;
+  if (!decode_plan(num_seqs, Hq, Hkv, d, max_seqlen, &pl)) return 0;
+  return pl.ws_bytes;
+}
+
+attn_status attn_decode_paged(const void* q, const void* kcache, const void* vcache, const int32_t* block_table,
+                              const int32_t* seqlens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int d,
+                              int page_size, int num_pages, int max_pages_per_seq, int max_seqlen, float scale,
+                              void* workspace, size_t workspace_bytes, attn_dtype o_dtype, attn_stream_t stream) {
+  if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (num_pages <= 0 || max_pages_per_seq <= 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (o_dtype != ATTN_BF16 && o_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+  if (page_size != attn::kPage) return ATTN_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_seqlen) > static_cast<long long>(max_pages_per_seq) * page_size)
+    return ATTN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return ATTN_OK;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(block_table) ||
+      !aligned16(seqlens) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_MISALIGNED;
+  DecodePlan pl;
+  if (!decode_plan(num_seqs, Hq, Hkv, d, max_seqlen, &pl)) return ATTN_ERR_INVALID_ARG;
+  if (pl.ws_bytes > 0 && (!aligned16(workspace) || workspace_bytes < pl.ws_bytes)) return ATTN_ERR_WORKSPACE;
+  attn_status st = check_device();
+  if (st != ATTN_OK) return st;
+
+  CUtensorMap mk, mv;
+  if (!encode_page_map(&mk, kcache, d, Hkv, page_size, num_pages, pl.hg) ||
+      !encode_page_map(&mv, vcache, d, Hkv, page_size, num_pages, pl.hg))
+    return ATTN_ERR_LAUNCH;
+
+  attn::DecodeParams p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.block_table = block_table;
+  p.seqlens = seqlens;
+  p.o = o;
+  p.lse = lse;
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_lse = pl.ws_bytes > 0 ? static_cast<float*>(workspace) + pl.ws_o_floats : nullptr;
+  p.num_seqs = num_seqs;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.num_pages = num_pages;
+  p.max_pages = max_pages_per_seq;
+  p.max_seqlen = max_seqlen;
+  p.chunk = pl.chunk;
+  p.n_splits = pl.n_splits;
+  p.hg = pl.hg;
+  p.stages = 2;
+  p.stage_bytes = page_size * pl.hg * d * 2;
+  p.o_f32 = o_dtype == ATTN_F32 ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (d) {
+    case 64: return launch_decode_g<64>(G, mk, mv, p, s);
+    case 128: return launch_decode_g<128>(G, mk, mv, p, s);
+    case 256: return launch_decode_g<256>(G, mk, mv, p, s);
+  }
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+attn_status attn_get_device_status(attn_stream_t stream) {
+  attn_status st = check_device();
+  if (st != ATTN_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, attn::g_status, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(attn::g_status, &zero, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  return static_cast<attn_status>(v);
+}
+
+}  // extern "C"

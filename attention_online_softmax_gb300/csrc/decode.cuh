@@ -1,0 +1,377 @@
+// Paged split-KV decode for sm_103a: one query row per (sequence, query head)
+// against a paged KV cache, as a bandwidth-bound GEMV-class stage.
+//
+// decode_split_kernel: one CTA per (sequence, key chunk, group of hg key/value
+// heads).  A producer thread streams the chunk's pages with TMA -- first the
+// K pages, then the V pages -- into a ring of shared-memory stages (one stage
+// = the [16 slots][hg heads][d] block of one page, so every global read is a
+// run of d*2 contiguous bytes per (slot, head)).  Warp w handles key/value
+// head w of the group and the G query heads that share it (grouped-query
+// attention: one read of K/V serves the whole group).  Lanes own 16-byte
+// slices of a key row; partial dot products are reduced across the lanes of a
+// row by a reduce-scatter over shuffles.  The chunk's scores stay in shared
+// memory, so the chunk is softmaxed once (max, 2^(x - m), sum) and then the V
+// pages are accumulated.  The chunk's partial state is stored as (O_c, lse_c)
+// = (o / l, m + ln l) ("online softmax as a monoid", Tang abstract).
+//
+// decode_combine_kernel: merges the chunk partials of each (sequence, head):
+// LSE = logsumexp_c(lse_c), O = sum_c exp(lse_c - LSE) O_c -- the merge of
+// partial states of the block recurrence in "Compilers and Kernels", section
+// "FlashAttention changes the algorithm around IO", applied to whole chunks.
+// Sequences that fit one chunk are finished by the split kernel directly.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int kPage = 16;        // tokens per KV-cache page
+constexpr int kChunkMax = 256;   // tokens per split, upper bound
+constexpr int kMaxStages = 8;
+
+struct DecodeParams {
+  const uint16_t* q;
+  const int32_t* block_table;
+  const int32_t* seqlens;
+  void* o;
+  float* lse;
+  float* ws_o;    // [num_seqs][n_splits][Hq][D] chunk outputs O_c
+  float* ws_lse;  // [num_seqs][n_splits][Hq]    chunk lse_c
+  int num_seqs, Hq, Hkv, num_pages, max_pages, max_seqlen;
+  int chunk;      // tokens per split: multiple of 16, <= kChunkMax
+  int n_splits;   // ceil(max_seqlen / chunk), >= 1
+  int hg;         // key/value heads per CTA (= compute warps)
+  int stages;     // shared-memory ring depth
+  int stage_bytes;
+  int o_f32;
+  float scale_log2;
+};
+
+__device__ __forceinline__ int decode_len(const DecodeParams& p, int seq, bool report) {
+  int L = p.seqlens[seq];
+  const int cap = min(p.max_seqlen, p.max_pages * kPage);
+  if (L < 0 || L > cap) {
+    if (report) report_error(7 /* ATTN_ERR_BOUNDS */, seq, L);
+    L = L < 0 ? 0 : cap;
+  }
+  return L;
+}
+
+template <int D, int G>
+struct DecodeShape {
+  static constexpr int LPT = D / 8;            // lanes per key row (16 bytes each)
+  static constexpr int TPP = 32 / LPT;         // key rows per pass of the warp
+  static constexpr int PASSES = kPage / TPP;   // passes per page
+  static constexpr int R0 = (2 * LPT) / G;
+  static constexpr int R = PASSES < (R0 > 0 ? R0 : 1) ? PASSES : (R0 > 0 ? R0 : 1);  // passes per reduction
+  static constexpr int NV = R * G;             // partial sums per lane per reduction
+  static constexpr int LEVELS = LPT == 32 ? 5 : LPT == 16 ? 4 : 3;
+  static constexpr int LOG_NV = NV >= 64 ? 6 : NV >= 32 ? 5 : NV >= 16 ? 4 : NV >= 8 ? 3 : NV >= 4 ? 2 : NV >= 2 ? 1 : 0;
+  static constexpr int SCAT = LEVELS < LOG_NV ? LEVELS : LOG_NV;  // reduce-scatter levels
+  static constexpr int KEEP = NV >> SCAT;      // sums a lane keeps
+  static_assert(PASSES % R == 0, "reduction rounds");
+  static_assert(D == 64 || D == 128 || D == 256, "head dim");
+};
+
+// Sum v[] across the LPT lanes that share a key row (lane bits below LPT).
+// First reduce-scatter (each level halves the values a lane keeps), then plain
+// butterflies once one value is left.  Afterwards lane `sub` holds the sums
+// with indices [(sub >> (LEVELS - SCAT)) * KEEP, +KEEP).
+template <int NV, int LPT, int SCAT, int LEVELS>
+__device__ __forceinline__ void lane_reduce(float (&v)[NV], int lane) {
+#pragma unroll
+  for (int lev = 0; lev < SCAT; ++lev) {
+    const int off = LPT >> (lev + 1);
+    const int n = NV >> (lev + 1);
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      const float send = upper ? v[i] : v[i + n];
+      const float keep = upper ? v[i + n] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+    }
+  }
+#pragma unroll
+  for (int lev = SCAT; lev < LEVELS; ++lev) {
+    const int off = LPT >> (lev + 1);
+    v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], off);
+  }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(288)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const DecodeParams p) {
+  using S = DecodeShape<D, G>;
+  const int split = static_cast<int>(blockIdx.x % p.n_splits);
+  const int seq = static_cast<int>(blockIdx.x / p.n_splits);
+  const int L = decode_len(p, seq, split == 0 && blockIdx.y == 0);
+  const int t_begin = split * p.chunk;
+  if (t_begin >= L && split > 0) return;  // empty chunk (uniform for the CTA)
+  const int ntok = min(L - t_begin, p.chunk) > 0 ? min(L - t_begin, p.chunk) : 0;
+  const int npages = (ntok + kPage - 1) / kPage;
+  const int n_split_seq = L > 0 ? (L + p.chunk - 1) / p.chunk : 1;
+  const int hg = p.hg;
+  const int kvh0 = blockIdx.y * hg;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t sbase = smem_u32(smem);
+  float* scores = reinterpret_cast<float*>(smem + p.stages * p.stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * p.stage_bytes +
+                                               hg * p.chunk * G * 4);
+  uint64_t* empty = full + kMaxStages;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], hg);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == hg) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0 && npages > 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const int32_t* bt = p.block_table + static_cast<size_t>(seq) * p.max_pages + t_begin / kPage;
+      int issued = 0;
+      for (int item = 0; item < 2 * npages; ++item) {
+        const int st = item % p.stages;
+        const uint32_t ph = (item / p.stages) & 1;
+        if (!mbar_wait(&empty[st], ph ^ 1, 30)) break;
+        const int pg = item < npages ? item : item - npages;
+        const int page = bt[pg];
+        // An out-of-range page index is reported; TMA fills such a box with
+        // zeros instead of reading outside the cache.
+        if (page < 0 || page >= p.num_pages) report_error(7 /* ATTN_ERR_BOUNDS */, seq, page);
+        mbar_expect_tx(&full[st], p.stage_bytes);
+        tma_load_4d(smem + st * p.stage_bytes, item < npages ? &tmK : &tmV, &full[st], 0, kvh0, 0, page);
+        issued = item + 1;
+      }
+      for (int item = max(0, issued - p.stages); item < issued; ++item)
+        mbar_wait(&full[item % p.stages], (item / p.stages) & 1, 31);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ compute warps
+    const int hl = warp;                 // key/value head within the group
+    const int kvh = kvh0 + hl;
+    const int sub = lane % S::LPT;       // 16-byte slice of the key row
+    const int grp = lane / S::LPT;       // which key row of a pass
+    float* sc = scores + hl * p.chunk * G;  // [token][g] scores, then probabilities
+    const uint32_t row_bytes = D * 2;
+    const uint32_t slot_stride = hg * row_bytes;
+
+    float qf[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const uint4 w = *reinterpret_cast<const uint4*>(
+          p.q + (static_cast<size_t>(seq) * p.Hq + kvh * G + g) * D + sub * 8);
+      qf[g][0] = bf16lo(w.x) * p.scale_log2;
+      qf[g][1] = bf16hi(w.x) * p.scale_log2;
+      qf[g][2] = bf16lo(w.y) * p.scale_log2;
+      qf[g][3] = bf16hi(w.y) * p.scale_log2;
+      qf[g][4] = bf16lo(w.z) * p.scale_log2;
+      qf[g][5] = bf16hi(w.z) * p.scale_log2;
+      qf[g][6] = bf16lo(w.w) * p.scale_log2;
+      qf[g][7] = bf16hi(w.w) * p.scale_log2;
+    }
+
+    bool ok = true;
+    // ---- K pages: scores x = (scale log2 e) q . k
+    for (int i = 0; ok && i < npages; ++i) {
+      const int st = i % p.stages;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (i / p.stages) & 1, 32));
+      if (!ok) break;
+      const uint32_t kb = sbase + st * p.stage_bytes + hl * row_bytes + sub * 16;
+#pragma unroll
+      for (int rd = 0; rd < S::PASSES / S::R; ++rd) {
+        float part[S::NV];
+#pragma unroll
+        for (int r = 0; r < S::R; ++r) {
+          const int slot = (rd * S::R + r) * S::TPP + grp;
+          const uint4 w = ld_shared_v4(kb + slot * slot_stride);
+          const float k8[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                               bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float a = qf[g][0] * k8[0];
+#pragma unroll
+            for (int e = 1; e < 8; ++e) a = fmaf(qf[g][e], k8[e], a);
+            part[r * G + g] = a;
+          }
+        }
+        lane_reduce<S::NV, S::LPT, S::SCAT, S::LEVELS>(part, lane);
+        const int dup_bits = S::LEVELS - S::SCAT;
+        if ((sub & ((1 << dup_bits) - 1)) == 0) {
+          const int base = (sub >> dup_bits) * S::KEEP;
+#pragma unroll
+          for (int v = 0; v < S::KEEP; ++v) {
+            const int idx = base + v;
+            const int r = idx / G;
+            const int g = idx - r * G;
+            const int slot = (rd * S::R + r) * S::TPP + grp;
+            sc[(i * kPage + slot) * G + g] = part[v];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    __syncwarp();
+
+    // ---- softmax over the chunk, per query head g = lane % G
+    float m = -INFINITY;
+    float s = 0.f;
+    if (ok) {
+      for (int i = lane; i < ntok * G; i += 32) m = fmaxf(m, sc[i]);
+#pragma unroll
+      for (int off = G; off < 32; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+      for (int i = lane; i < ntok * G; i += 32) {
+        const float e = ex2(sc[i] - m);
+        sc[i] = e;
+        s += e;
+      }
+#pragma unroll
+      for (int off = G; off < 32; off <<= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+    }
+    __syncwarp();
+
+    // ---- V pages: o = sum_j p_j v_j
+    float acc[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+    for (int i = 0; ok && i < npages; ++i) {
+      const int item = npages + i;
+      const int st = item % p.stages;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (item / p.stages) & 1, 33));
+      if (!ok) break;
+      const uint32_t vb = sbase + st * p.stage_bytes + hl * row_bytes + sub * 16;
+#pragma unroll 4
+      for (int ps = 0; ps < S::PASSES; ++ps) {
+        const int slot = ps * S::TPP + grp;
+        const int tok = i * kPage + slot;
+        if (tok < ntok) {
+          const uint4 w = ld_shared_v4(vb + slot * slot_stride);
+          const float v8[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                               bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+          float pg[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) pg[g] = sc[tok * G + g];
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pg[g], v8[e], acc[g][e]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    // rows of a pass were split over lane groups: add them up
+#pragma unroll
+    for (int off = S::LPT; off < 32; off <<= 1)
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xFFFFFFFFu, acc[g][e], off);
+    float mg[G], sg[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      mg[g] = __shfl_sync(0xFFFFFFFFu, m, g);
+      sg[g] = __shfl_sync(0xFFFFFFFFu, s, g);
+    }
+
+    if (ok && grp == 0) {
+      const bool direct = n_split_seq <= 1;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int head = kvh * G + g;
+        const bool any = ntok > 0 && sg[g] > 0.f;
+        const float inv = any ? 1.f / sg[g] : 0.f;
+        const float lse_v = any ? (mg[g] + lg2(sg[g])) * 0.69314718055994531f : -INFINITY;
+        float ov[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ov[e] = acc[g][e] * inv;
+        if (direct) {
+          const size_t off = (static_cast<size_t>(seq) * p.Hq + head) * D + sub * 8;
+          if (p.o_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + off);
+            dst[0] = make_float4(ov[0], ov[1], ov[2], ov[3]);
+            dst[1] = make_float4(ov[4], ov[5], ov[6], ov[7]);
+          } else {
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + off) =
+                make_uint4(pack_bf16(ov[0], ov[1]), pack_bf16(ov[2], ov[3]), pack_bf16(ov[4], ov[5]),
+                           pack_bf16(ov[6], ov[7]));
+          }
+          if (sub == 0) p.lse[static_cast<size_t>(seq) * p.Hq + head] = lse_v;
+        } else {
+          const size_t row = (static_cast<size_t>(seq) * p.n_splits + split) * p.Hq + head;
+          float4* dst = reinterpret_cast<float4*>(p.ws_o + row * D + sub * 8);
+          dst[0] = make_float4(ov[0], ov[1], ov[2], ov[3]);
+          dst[1] = make_float4(ov[4], ov[5], ov[6], ov[7]);
+          if (sub == 0) p.ws_lse[row] = lse_v;
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// One warp per (sequence, query head); lanes own D/32 consecutive elements.
+template <int D>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int seq = blockIdx.x;
+  const int head = blockIdx.y * 4 + warp;
+  if (head >= p.Hq) return;
+  const int L = decode_len(p, seq, false);
+  const int ns = L > 0 ? (L + p.chunk - 1) / p.chunk : 1;
+  if (ns <= 1) return;  // finished by the split kernel
+  const size_t row0 = static_cast<size_t>(seq) * p.n_splits * p.Hq + head;
+  float m = -INFINITY;
+  for (int c = lane; c < ns; c += 32) m = fmaxf(m, p.ws_lse[row0 + static_cast<size_t>(c) * p.Hq]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  for (int c = 0; c < ns; ++c) {
+    const size_t row = row0 + static_cast<size_t>(c) * p.Hq;
+    const float w = ex2((p.ws_lse[row] - m) * 1.4426950408889634f);
+    wsum += w;
+    const float* src = p.ws_o + row * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float2 v = *reinterpret_cast<const float2*>(src + e);
+      acc[e] = fmaf(w, v.x, acc[e]);
+      acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+    }
+  }
+  const float inv = 1.f / wsum;
+  const size_t off = (static_cast<size_t>(seq) * p.Hq + head) * D + lane * E;
+  if (p.o_f32) {
+    float* dst = static_cast<float*>(p.o) + off;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) *reinterpret_cast<float2*>(dst + e) = make_float2(acc[e] * inv, acc[e + 1] * inv);
+  } else {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.o) + off);
+#pragma unroll
+    for (int e = 0; e < E; e += 2) dst[e / 2] = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+  }
+  if (lane == 0) p.lse[static_cast<size_t>(seq) * p.Hq + head] = m + logf(wsum);
+}
+
+}  // namespace attn

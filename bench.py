@@ -1,0 +1,488 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused-attention hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * prefill: attn_fwd on the long causal MHA workload (B=2, H=32, Nq=Nk=4096,
+    d=128, bf16, seed 2), and
+  * paged decode: attn_decode_paged on 64 sequences, Hq=32 over Hkv=8, d=128,
+    lengths uniform in [512, 8192] (seed 4), 16-token pages in a 40000-page pool.
+
+Metric: the step's roofline floor (prefill FLOPs at the measured dense-bf16
+peak, decode bytes at the measured HBM bandwidth; T >= max(F/P, Q/B) for each
+kernel) divided by the measured step time, summed over GPUs.  At N=1 this is
+the fraction of roofline the step reaches.  Inputs are resident in HBM; L2 is
+flushed (256 MiB write) before every timed step.  The same metric is also
+measured end to end through the C ABI from pinned host buffers ("e2e").
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from attention_online_softmax_gb300 import configs, inputs, roofline  # noqa: E402
+
+METRIC = "attention prefill TFLOP/s & decode HBM GB/s, each as fraction of roofline"
+UNIT = "fraction of roofline (step floor time / step time, summed over GPUs)"
+WORKLOAD = ("prefill causal MHA B2 H32 N4096 d128 bf16 + paged GQA decode 64 seqs Hq32 Hkv8 d128 "
+            "len U[512,8192] 16-token pages in a 40000-page pool")
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = [os.path.join(ROOT, "attention_online_softmax_gb300", "csrc", f)
+                  for f in ("attn_api.cu", "ptx.cuh", "prefill_fwd.cuh", "decode.cuh")]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel: str) -> float | None:
+    """Per-launch DRAM bytes recorded in profiles/traffic.txt for this kernel
+    source hash (lines: `<kernel> <source-hash> <bytes>`); None when the kernel
+    changed since the capture."""
+    path = os.path.join(PROFILE_DIR, "traffic.txt")
+    want = kernel_source_hash()
+    try:
+        for line in open(path):
+            parts = line.split()
+            if len(parts) == 3 and parts[0] == kernel and parts[1] == want:
+                return float(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", self.gpu], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_index_for(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# ---------------------------------------------------------------- workloads
+def make_decode_inputs():
+    c = configs.DECODE
+    return inputs.decode_inputs(c.num_seqs, c.Hq, c.Hkv, c.d, c.len_lo, c.len_hi, c.num_pages,
+                                c.page_size, c.seed)
+
+
+def make_prefill_inputs(c=configs.LONG):
+    return inputs.prefill_inputs(c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.seed, c.causal,
+                                 k_scale=c.k_scale)
+
+
+def floors(peaks, pre_flops, pre_bytes, dec_flops, dec_bytes):
+    f_pre = roofline.time_floor_s(pre_flops, pre_bytes, peaks)
+    f_dec = roofline.time_floor_s(dec_flops, dec_bytes, peaks)
+    return f_pre, f_dec
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def oracle_sample(peaks, xp, xd, target_s: float, threads: int = 0):
+    """Time the oracle on a bounded, seeded sample of the step's workload.
+
+    Sample: the same fraction f of prefill query rows (seeded, spread over all
+    heads) and of decode sequences; f is calibrated so the run takes about
+    target_s.  Returns (floor_time_of_sample, seconds, threads, description).
+    """
+    import numpy as np
+    import oracle
+
+    P, Dc = configs.LONG, configs.DECODE
+    total_rows = P.B * P.Hq * P.Nq
+    g = torch.Generator().manual_seed(1234)
+    order = torch.randperm(total_rows, generator=g)
+    seq_order = torch.randperm(Dc.num_seqs, generator=g)
+
+    def work_of(n_rows, n_seqs):
+        rows = order[:n_rows]
+        i = (rows % P.Nq).double()
+        allowed = torch.clamp(i + 1 + (P.Nk - P.Nq), 0, P.Nk) if P.causal else torch.full_like(i, P.Nk)
+        flops = float(4.0 * allowed.sum().item() * P.d)
+        seqs = seq_order[:n_seqs]
+        lens = [int(xd.seqlens[s]) for s in seqs.tolist()]
+        dbytes = roofline.decode_bytes(lens, Dc.Hq, Dc.Hkv, Dc.d, Dc.page_size) if lens else 0
+        dflops = roofline.decode_flops(lens, Dc.Hq, Dc.d)
+        return (flops / (peaks.bf16_tflops * 1e12)
+                + roofline.time_floor_s(dflops, dbytes, peaks)), rows, seqs
+
+    def run(n_rows, n_seqs):
+        _, rows, seqs = work_of(n_rows, n_seqs)
+        t0 = time.perf_counter()
+        _, _, th1 = oracle.attention(xp.q, xp.k, xp.v, P.causal, xp.scale, rows=rows.numpy(),
+                                     threads=threads)
+        th2 = th1
+        if n_seqs:
+            _, _, th2 = oracle.decode_paged(xd.q, xd.kcache, xd.vcache, xd.block_table, xd.seqlens,
+                                            xd.scale, seqs=seqs.numpy(), threads=threads)
+        return time.perf_counter() - t0, max(th1, th2)
+
+    frac = 1.0 / 512
+    t, th = run(max(1, int(total_rows * frac)), max(1, int(round(Dc.num_seqs * frac))))
+    frac = min(1.0, frac * target_s / max(t, 1e-3))
+    n_rows = max(1, int(total_rows * frac))
+    n_seqs = max(1, int(round(Dc.num_seqs * frac)))
+    floor, _, _ = work_of(n_rows, n_seqs)
+    t, th = run(n_rows, n_seqs)
+    desc = (f"{n_rows} of {total_rows} prefill query rows (seeded) and {n_seqs} of {Dc.num_seqs} "
+            f"decode sequences (all heads): fraction {frac:.4f} of one step")
+    return floor, t, th, desc, (n_rows, n_seqs)
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    peaks = roofline.load_peaks()
+    xp = make_prefill_inputs()
+    xd = make_decode_inputs()
+    floor, t, th, desc, sizes = oracle_sample(peaks, xp, xd, target_s=2.0)
+    import oracle
+    P = configs.LONG
+    g = torch.Generator().manual_seed(1234)
+    rows = torch.randperm(P.B * P.Hq * P.Nq, generator=g)[: sizes[0]].numpy()
+    seqs = torch.randperm(configs.DECODE.num_seqs, generator=g)[: sizes[1]].numpy()
+
+    def one():
+        t0 = time.perf_counter()
+        oracle.attention(xp.q, xp.k, xp.v, P.causal, xp.scale, rows=rows)
+        oracle.decode_paged(xd.q, xd.kcache, xd.vcache, xd.block_table, xd.seqlens, xd.scale, seqs=seqs)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        one()
+    times = [one() for _ in range(args.steps)]
+    total = sum(times)
+    value = floor * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 inputs)",
+        "config": {"workload": WORKLOAD, "sample": desc, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": th, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-config table")
+    args = ap.parse_args(argv)
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        dist_init(world, "gloo")
+        return run_reference(args, rank, world)
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    if local == 0:
+        from attention_online_softmax_gb300 import build
+        build.build()
+    barrier(world)
+    from attention_online_softmax_gb300 import abi
+
+    peaks = roofline.load_peaks()
+    P, Dc = configs.LONG, configs.DECODE
+    xp = make_prefill_inputs()
+    xd = make_decode_inputs()
+    pre_flops = roofline.prefill_flops(P.B, P.Hq, P.Nq, P.Nk, P.d, P.causal)
+    pre_bytes = roofline.prefill_bytes(P.B, P.Hq, P.Hkv, P.Nq, P.Nk, P.d)
+    lens = xd.seqlens.tolist()
+    dec_bytes = roofline.decode_bytes(lens, Dc.Hq, Dc.Hkv, Dc.d, Dc.page_size)
+    dec_flops = roofline.decode_flops(lens, Dc.Hq, Dc.d)
+    f_pre, f_dec = floors(peaks, pre_flops, pre_bytes, dec_flops, dec_bytes)
+
+    # device buffers
+    q, k, v = xp.q.to(dev), xp.k.to(dev), xp.v.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    dq = xd.q.to(dev)
+    kc, vc = xd.kcache.to(dev), xd.vcache.to(dev)
+    bt, sl = xd.block_table.to(dev), xd.seqlens.to(dev)
+    do = torch.empty_like(dq)
+    dlse = torch.empty(dq.shape[:2], dtype=torch.float32, device=dev)
+    ws_bytes = abi.attn_decode_workspace_size(Dc.num_seqs, Dc.Hq, Dc.Hkv, Dc.d, xd.max_seqlen)
+    ws = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def prefill():
+        abi.attn_fwd(q, k, v, o, lse, P.causal, xp.scale, stream)
+
+    def decode():
+        abi.attn_decode_paged(dq, kc, vc, bt, sl, do, dlse, xd.max_seqlen, xd.scale, ws, stream)
+
+    for _ in range(max(3, args.warmup)):
+        prefill()
+        decode()
+    torch.cuda.synchronize()
+    if abi.attn_get_device_status() != 0:
+        raise SystemExit("device status error after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_index_for(local))
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    launches0 = abi.attn_launch_count()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        prefill()
+        ev[i][1].record(stream)
+        decode()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = abi.attn_launch_count() - launches0
+    clocks = sampler.stop()
+    t_pre = [ev[i][0].elapsed_time(ev[i][1]) * 1e-3 for i in range(args.steps)]
+    t_dec = [ev[i][1].elapsed_time(ev[i][2]) * 1e-3 for i in range(args.steps)]
+    total = sum(a + b for a, b in zip(t_pre, t_dec))
+    total_max = max_over_ranks(total, world, dev)
+    value = world * args.steps * (f_pre + f_dec) / total_max
+    if abi.attn_get_device_status() != 0:
+        raise SystemExit("device status error in the timed region")
+
+    mean_pre = statistics.fmean(t_pre)
+    mean_dec = statistics.fmean(t_dec)
+    pre_tflops = pre_flops / mean_pre / 1e12
+    dec_gbs = dec_bytes / mean_dec / 1e9
+
+    # ---- end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(abi, xp, xd, dev, stream, min(args.steps, 5), f_pre + f_dec, world)
+
+    extra = None
+    if not args.no_extra and rank == 0:
+        extra = per_config_table(abi, dev, stream, peaks)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        floor, t, th, desc, _ = oracle_sample(peaks, xp, xd, target_s=12.0)
+        cpu = {"value": floor / t, "unit": UNIT, "cores": th, "kind": "oracle", "sample": desc,
+               "seconds": t}
+
+    if rank == 0:
+        peak_src = "of measured" if peaks.source == "measured" else "of fallback"
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": 1e3 * total_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 inputs, NaN-filled unused cache pages)",
+            "config": {"workload": WORKLOAD, "l2": "flushed before every timed step (256 MiB write)",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "peaks": peak_src},
+            "prefill": {"tflops": pre_tflops, "frac": pre_tflops * 1e12 / (peaks.bf16_tflops * 1e12),
+                        "ms": mean_pre * 1e3, "floor_ms": f_pre * 1e3},
+            "decode": {"gbs": dec_gbs, "frac": dec_gbs / peaks.hbm_gbs, "ms": mean_dec * 1e3,
+                       "floor_ms": f_dec * 1e3, "bytes": dec_bytes},
+            "roofline": {"bound": "tensor", "kernel": "prefill_fwd_kernel<128,128,4>",
+                         "achieved": pre_tflops, "peak": peaks.bf16_tflops, "unit": "TFLOP/s",
+                         "frac": pre_tflops / peaks.bf16_tflops, "peak_source": peak_src,
+                         "traffic": traffic_from_profiles("prefill_fwd_c3"),
+                         "algorithmic": {"flops": pre_flops, "bytes": pre_bytes}},
+            "roofline_decode": {"bound": "hbm", "kernel": "decode_split_kernel<128,4> + decode_combine",
+                                "achieved": dec_gbs, "peak": peaks.hbm_gbs, "unit": "GB/s",
+                                "frac": dec_gbs / peaks.hbm_gbs, "peak_source": peak_src,
+                                "traffic": traffic_from_profiles("decode_c5")},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "per_config": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def measure_e2e(abi, xp, xd, dev, stream, steps, floor_s, world):
+    """Same step from pinned host memory: H2D of every input, both calls, D2H of O and LSE."""
+    P, Dc = configs.LONG, configs.DECODE
+    host_in = [t.pin_memory() for t in (xp.q, xp.k, xp.v, xd.q, xd.kcache, xd.vcache,
+                                        xd.block_table, xd.seqlens)]
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+    o = torch.empty_like(dev_in[0])
+    lse = torch.empty(xp.q.shape[:3], dtype=torch.float32, device=dev)
+    do = torch.empty_like(dev_in[3])
+    dlse = torch.empty(xd.q.shape[:2], dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, abi.attn_decode_workspace_size(Dc.num_seqs, Dc.Hq, Dc.Hkv, Dc.d,
+                                                            xd.max_seqlen)),
+                     dtype=torch.uint8, device=dev)
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, do, dlse)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def step():
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        q, k, v, dq, kc, vc, bt, sl = dev_in
+        abi.attn_fwd(q, k, v, o, lse, P.causal, xp.scale, stream)
+        abi.attn_decode_paged(dq, kc, vc, bt, sl, do, dlse, xd.max_seqlen, xd.scale, ws, stream)
+        for h_, d_ in zip(host_out, (o, lse, do, dlse)):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world, dev)
+    return {"value": world * steps * floor_s / t, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * t / steps, "steps": steps}
+
+
+def per_config_table(abi, dev, stream, peaks, reps: int = 10):
+    """Each workload timed alone (median of reps, L2 flushed before each)."""
+    out = {}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for c in configs.PREFILL_CONFIGS:
+        x = make_prefill_inputs(c)
+        q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        for _ in range(3):
+            abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale, stream)
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        t = statistics.median(ts)
+        fl = roofline.prefill_flops(c.B, c.Hq, c.Nq, c.Nk, c.d, c.causal)
+        by = roofline.prefill_bytes(c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d)
+        bound = roofline.bound_rate(fl, by, peaks)
+        out[c.name] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_of_peak": fl / t / (peaks.bf16_tflops * 1e12),
+                       "frac_of_bound": fl / t / bound, "p10_us": sorted(ts)[len(ts) // 10] * 1e6,
+                       "p90_us": sorted(ts)[(9 * len(ts)) // 10] * 1e6}
+        del q, k, v, o, lse
+    torch.cuda.empty_cache()
+    return out
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,145 @@
+/*
+ * attn.h -- C ABI of the GB300 fused-attention library (libattn_gb300.so).
+ *
+ * The operation ("Compilers and Kernels", section "FlashAttention changes the
+ * algorithm around IO", the definition of scaled dot-product attention and the
+ * block recurrence that follows it):
+ *
+ *     S = scale * Q K^T + C,  m_i = max_j S_ij,  l_i = sum_j exp(S_ij - m_i),
+ *     O_i = sum_j exp(S_ij - m_i) V_j / l_i,  LSE_i = m_i + ln l_i,
+ *
+ * computed in one fused pass in which the per-row state (m, l, o) is carried
+ * over key blocks and merged associatively ("Tang: a compiler that derives GPU
+ * kernels ...", abstract: online softmax as a monoid), so the N x N score
+ * matrix never reaches memory.  The logsumexp output is the one named in
+ * "Don't Write Kernels, Derive Them", section "What happened".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *    never frees or retains it after the call returns.  Inputs are read only;
+ *    outputs must not alias inputs or each other.
+ *  - Tensors are dense and row-major with the head dimension innermost
+ *    (strided views are not accepted: copy them first).  bf16 means IEEE
+ *    bfloat16 bit patterns (uint16_t).  Pointers must be 16-byte aligned.
+ *  - C is 0 or -inf: with causal != 0, key j is allowed for query i iff
+ *    j <= i + (Nk - Nq) (bottom-right alignment; "query i attends keys 0..i"
+ *    when Nq == Nk).  A row with no allowed key gets O = 0 and LSE = -inf.
+ *  - Grouped-query attention: query head h reads key/value head
+ *    h / (Hq / Hkv); Hq must be a multiple of Hkv.
+ *  - Head dimension d (for Q, K and V alike) must be 64, 128 or 256.
+ *  - LSE is natural-log, float32.  O is bf16 (o_dtype = ATTN_BF16) or float32
+ *    (ATTN_F32, for diagnostics).  Accumulation is float32 throughout; P is
+ *    rounded to bf16 (round-to-nearest-even) before the P V product.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream):
+ *    arguments are checked synchronously and an error status is returned
+ *    before anything is launched; a launch failure returns ATTN_ERR_LAUNCH.
+ *    Faults the kernels detect while running (a wait that timed out, an
+ *    out-of-range block-table entry or sequence length) are recorded in a
+ *    device status word read by attn_get_device_status().
+ *  - Results are deterministic run to run (fixed work split, no atomics in any
+ *    reduction).
+ *  - The GPU must be compute capability 10.3 (GB300, sm_103a); otherwise
+ *    ATTN_ERR_UNSUPPORTED.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+/* Same object as cudaStream_t / CUstream; declared here so that this header
+ * needs no CUDA header. */
+struct CUstream_st;
+typedef struct CUstream_st* attn_stream_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* a size is negative, zero where it may not be, or inconsistent */
+    ATTN_ERR_UNSUPPORTED = 2,  /* d not in {64,128,256}, page_size != 16, group > 8, wrong GPU */
+    ATTN_ERR_MISALIGNED = 3,   /* a pointer is NULL or not 16-byte aligned */
+    ATTN_ERR_WORKSPACE = 4,    /* decode workspace NULL or smaller than attn_decode_workspace_size() */
+    ATTN_ERR_LAUNCH = 5,       /* the CUDA runtime refused a launch or an attribute */
+    ATTN_ERR_TIMEOUT = 6,      /* device: a pipeline wait exceeded its time limit */
+    ATTN_ERR_BOUNDS = 7,       /* device: block-table entry or sequence length out of range */
+    ATTN_ERR_NO_DEVICE = 8     /* no CUDA device is usable */
+} attn_status;
+
+typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
+
+/*
+ * Prefill / general forward attention.
+ *   q:   [B, Hq, Nq, d] bf16          k, v: [B, Hkv, Nk, d] bf16
+ *   o:   [B, Hq, Nq, d] bf16 or f32   lse:  [B, Hq, Nq] f32
+ *   scale: multiplies Q K^T (1/sqrt(d) for the textbook operator); finite.
+ * B, Hq, Hkv, Nq, Nk >= 0; nothing is launched when the output is empty.
+ * With Nk == 0 (or every key masked) each row is O = 0, LSE = -inf.
+ */
+ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                     float scale, attn_dtype o_dtype, attn_stream_t stream);
+
+/*
+ * Bytes of scratch memory attn_decode_paged() needs for these sizes (the
+ * split partials: one float32 O row and one float32 LSE per sequence, split
+ * and query head).  Pure function of its arguments; 0 on invalid input.
+ */
+ATTN_API size_t attn_decode_workspace_size(int num_seqs, int Hq, int Hkv, int d, int max_seqlen);
+
+/*
+ * Paged decode: one query row per sequence and query head against that
+ * sequence's cached keys/values, split over key chunks whose partial states
+ * are merged by the online-softmax monoid (a split kernel, then a combine
+ * kernel; sequences that fit one chunk are finished by the split kernel).
+ *   q:           [num_seqs, Hq, d] bf16
+ *   kcache/vcache: [num_pages, page_size, Hkv, d] bf16
+ *   block_table: [num_seqs, max_pages_per_seq] int32; token t of sequence s is
+ *                slot t % page_size of page block_table[s][t / page_size]
+ *   seqlens:     [num_seqs] int32, each in [0, max_seqlen] and
+ *                <= max_pages_per_seq * page_size (checked on the device)
+ *   o:           [num_seqs, Hq, d] bf16 or f32;  lse: [num_seqs, Hq] f32
+ *   max_seqlen:  host-side upper bound of seqlens (sizes the split grid)
+ *   workspace:   device scratch of at least attn_decode_workspace_size() bytes,
+ *                16-byte aligned, owned by the caller, contents ignored; it
+ *                must not be shared by two calls that overlap on the GPU.
+ * The query row attends every cached token (no mask).  page_size must be 16.
+ */
+ATTN_API attn_status attn_decode_paged(const void* q, const void* kcache, const void* vcache,
+                              const int32_t* block_table, const int32_t* seqlens,
+                              void* o, float* lse,
+                              int num_seqs, int Hq, int Hkv, int d, int page_size,
+                              int num_pages, int max_pages_per_seq, int max_seqlen,
+                              float scale, void* workspace, size_t workspace_bytes,
+                              attn_dtype o_dtype, attn_stream_t stream);
+
+/*
+ * Waits for `stream`, then returns and clears the device status word of the
+ * current device (ATTN_OK when no kernel recorded a fault since the last
+ * call).  Not for the hot path: it synchronises.
+ */
+ATTN_API attn_status attn_get_device_status(attn_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+ATTN_API const char* attn_status_string(attn_status s);
+
+/* Number of kernels this library has launched in this process. */
+ATTN_API uint64_t attn_launch_count(void);
+
+/* Version of this ABI (bumped on any incompatible change). */
+ATTN_API int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

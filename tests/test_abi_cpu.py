@@ -1,0 +1,131 @@
+"""C ABI checks that need no GPU: the library loads, exports every declared
+symbol, and rejects bad arguments before touching the device.
+
+Only argument combinations that are rejected before any CUDA call are passed
+with fake (never dereferenced) pointers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_online_softmax_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, WORKSPACE, LAUNCH, TIMEOUT, BOUNDS, NO_DEVICE = range(9)
+FAKE = 0x10000      # 16-byte aligned, never dereferenced
+ODD = 0x10008       # 8-byte aligned only
+
+
+@pytest.fixture(scope="module")
+def abi():
+    build.build()
+    from attention_online_softmax_gb300 import abi as mod
+    return mod
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_documented_entry_points():
+    syms = declared_symbols()
+    for name in ("attn_fwd", "attn_decode_paged", "attn_decode_workspace_size",
+                 "attn_get_device_status", "attn_status_string"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(abi):
+    lib = ctypes.CDLL(build.LIB)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(declared_symbols()) == set(abi.EXPORTS)
+    assert abi.attn_abi_version() == 1
+
+
+def test_status_strings(abi):
+    assert abi.attn_status_string(OK) == "ok"
+    names = {abi.attn_status_string(s) for s in range(9)}
+    assert len(names) == 9
+    assert abi.attn_status_string(99) == "unknown status"
+
+
+def fwd(abi, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, Hq=2, Hkv=2, Nq=128, Nk=128, d=64,
+        causal=0, scale=0.125, dt=0):
+    return abi.lib().attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, dt, None)
+
+
+def test_fwd_rejects_bad_arguments_before_any_launch(abi):
+    before = abi.attn_launch_count()
+    assert fwd(abi, d=96) == UNSUPPORTED
+    assert fwd(abi, d=32) == UNSUPPORTED
+    assert fwd(abi, Hq=3, Hkv=2) == INVALID
+    assert fwd(abi, Hkv=0) == INVALID
+    assert fwd(abi, B=-1) == INVALID
+    assert fwd(abi, Nq=-4) == INVALID
+    assert fwd(abi, scale=float("nan")) == INVALID
+    assert fwd(abi, scale=float("inf")) == INVALID
+    assert fwd(abi, dt=7) == INVALID
+    assert fwd(abi, q=ODD) == MISALIGNED
+    assert fwd(abi, o=0) == MISALIGNED
+    assert fwd(abi, lse=ODD) == MISALIGNED
+    assert fwd(abi, k=0) == MISALIGNED
+    # empty outputs are a no-op, with any pointers
+    assert fwd(abi, Nq=0, q=0, o=0, lse=0) == OK
+    assert fwd(abi, B=0, q=0) == OK
+    assert abi.attn_launch_count() == before
+
+
+def test_fwd_without_device_reports_no_device(abi):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; valid arguments would launch")
+    assert fwd(abi) in (NO_DEVICE, UNSUPPORTED)
+
+
+def dec(abi, num_seqs=4, Hq=32, Hkv=8, d=128, page=16, pages=100, max_pages=32, max_len=512,
+        ws=FAKE, ws_bytes=1 << 40, scale=0.088, dt=0, q=FAKE, bt=FAKE, sl=FAKE):
+    return abi.lib().attn_decode_paged(q, FAKE, FAKE, bt, sl, FAKE, FAKE, num_seqs, Hq, Hkv, d, page,
+                                       pages, max_pages, max_len, scale, ws, ws_bytes, dt, None)
+
+
+def test_decode_rejects_bad_arguments(abi):
+    before = abi.attn_launch_count()
+    assert dec(abi, page=32) == UNSUPPORTED
+    assert dec(abi, d=80) == UNSUPPORTED
+    assert dec(abi, Hq=64, Hkv=4) == UNSUPPORTED      # group of 16
+    assert dec(abi, Hq=24, Hkv=8) == UNSUPPORTED      # group of 3
+    assert dec(abi, Hq=30, Hkv=8) == INVALID
+    assert dec(abi, max_len=513, max_pages=32) == INVALID  # beyond the block table
+    assert dec(abi, pages=0) == INVALID
+    assert dec(abi, num_seqs=-1) == INVALID
+    assert dec(abi, scale=float("nan")) == INVALID
+    assert dec(abi, bt=ODD) == MISALIGNED
+    assert dec(abi, sl=0) == MISALIGNED
+    need = abi.attn_decode_workspace_size(4, 32, 8, 128, 512)
+    assert need > 0
+    assert dec(abi, ws_bytes=need - 1) == WORKSPACE
+    assert dec(abi, ws=0) == WORKSPACE
+    assert dec(abi, num_seqs=0, q=0) == OK
+    assert abi.attn_launch_count() == before
+
+
+def test_decode_workspace_size_is_a_pure_plan(abi):
+    ws = abi.attn_decode_workspace_size
+    # 64 sequences x 8 kv heads: one 8-head group per CTA, 256-token chunks,
+    # ceil(8192 / 256) = 32 splits of (128 + 1) floats per query head.
+    assert ws(64, 32, 8, 128, 8192) == ((64 * 32 * 32 * 129 * 4 + 255) // 256) * 256
+    # a sequence that fits one chunk needs no partials
+    assert ws(4096, 32, 8, 128, 256) == 0
+    assert ws(1, 32, 8, 128, 0) == 0
+    # few sequences: smaller chunks to fill the GPU, more splits
+    assert ws(1, 8, 8, 128, 4096) == ((1 * 64 * 8 * 129 * 4 + 255) // 256) * 256
+    assert ws(4, 30, 8, 128, 512) == 0          # invalid -> 0
+    assert ws(4, 32, 8, 96, 512) == 0
+    assert ws(64, 32, 8, 128, 8192) == ws(64, 32, 8, 128, 8192)
