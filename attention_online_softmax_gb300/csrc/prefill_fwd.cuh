@@ -89,8 +89,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x);  // longest causal tiles first
-  const int bh = blockIdx.y;
+  // Flat grid: block = bh * n_qtiles + i, with the query tiles of one head
+  // visited longest (causal) first.
+  const int bh = static_cast<int>(blockIdx.x) / p.n_qtiles;
+  const int qt = p.n_qtiles - 1 - (static_cast<int>(blockIdx.x) - bh * p.n_qtiles);
+  if (bh >= p.B * p.Hq || qt < 0) return;  // never taken with the host's grid
   const int b = bh / p.Hq;
   const int h = bh - b * p.Hq;
   const int kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
