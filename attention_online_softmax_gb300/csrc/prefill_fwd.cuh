@@ -245,21 +245,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
       const int k0 = t * BN;
       const bool need_mask = (k0 + BN > p.Nk) || (p.causal && (k0 + BN - 1 > q0 + diag));
-      float mt = -INFINITY;
+      // Eight independent max chains keep the reduction off the critical path.
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
       if (need_mask) {
         const int lim = p.causal ? min(p.Nk - 1, qrow + diag) - k0 : p.Nk - 1 - k0;
 #pragma unroll
         for (int j = 0; j < BN; ++j) {
           x[j] = (j <= lim) ? x[j] * sl : -INFINITY;
-          mt = fmaxf(mt, x[j]);
+          mx[j & 7] = fmaxf(mx[j & 7], x[j]);
         }
       } else {
 #pragma unroll
         for (int j = 0; j < BN; ++j) {
           x[j] *= sl;
-          mt = fmaxf(mt, x[j]);
+          mx[j & 7] = fmaxf(mx[j & 7], x[j]);
         }
       }
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float m_new = fmaxf(m_ref, mt);
       const bool rescale = m_new > m_ref + kRescaleLog2;
       float alpha = 1.f;
@@ -270,15 +275,18 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       uint32_t pk[BN / 2];
-      float rs = 0.f;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < BN; j += 2) {
         const float p0 = ex2(x[j] - m_use);
         const float p1 = ex2(x[j + 1] - m_use);
-        rs += p0 + p1;
-        pk[j / 2] = pack_bf16(p0, p1);
+        const uint32_t w = pack_bf16(p0, p1);
+        pk[j / 2] = w;
+        // l sums the bf16-rounded weights the P V product uses, so O = o / l
+        // is an exact convex combination of V rows before output rounding.
+        rs[(j >> 1) & 3] += bf16lo(w) + bf16hi(w);
       }
-      l += rs;
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
 
       if (t > 0) {
         // P buffer and O are busy until the previous P V product is complete.
