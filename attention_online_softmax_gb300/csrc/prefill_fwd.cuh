@@ -223,8 +223,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int qrow = q0 + row;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl = p.scale_log2;
+    // l sums the exact weights (for LSE); lr sums the bf16-rounded weights the
+    // P V product uses, so O = o / lr is an exact convex combination of V rows
+    // before output rounding.
     float m_ref = -INFINITY;
     float l = 0.f;
+    float lr = 0.f;
     bool ok = true;
 
     for (int t = 0; t < n_tiles; ++t) {
@@ -272,21 +276,23 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         alpha = ex2(m_ref - m_new);  // 0 when m_ref = -inf
         m_ref = m_new;
         l *= alpha;
+        lr *= alpha;
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       uint32_t pk[BN / 2];
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      float re[2] = {0.f, 0.f};
+      float rr[2] = {0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < BN; j += 2) {
         const float p0 = ex2(x[j] - m_use);
         const float p1 = ex2(x[j + 1] - m_use);
         const uint32_t w = pack_bf16(p0, p1);
         pk[j / 2] = w;
-        // l sums the bf16-rounded weights the P V product uses, so O = o / l
-        // is an exact convex combination of V rows before output rounding.
-        rs[(j >> 1) & 3] += bf16lo(w) + bf16hi(w);
+        re[(j >> 1) & 1] += p0 + p1;
+        rr[(j >> 1) & 1] += bf16lo(w) + bf16hi(w);
       }
-      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      l += re[0] + re[1];
+      lr += rr[0] + rr[1];
 
       if (t > 0) {
         // P buffer and O are busy until the previous P V product is complete.
@@ -326,7 +332,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // Every lane runs the (warp-collective) TMEM loads; only rows < Nq store.
     const bool store = qrow < p.Nq;
     if (ok) {
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
       const size_t row_off = (static_cast<size_t>(bh) * p.Nq + qrow) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
