@@ -274,8 +274,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-config table")
+    ap.add_argument("--profile", choices=["prefill", "prefill_d256", "decode"], default=None,
+                    help="run one kernel of the step a few times (for an ncu capture) and exit")
     args = ap.parse_args(argv)
     rank, world, local = dist_env()
+    if args.profile:
+        return profile_one(args.profile)
 
     if args.impl == "reference":
         dist_init(world, "gloo")
@@ -408,6 +412,39 @@ def main(argv=None):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def profile_one(which: str, launches: int = 3) -> int:
+    """A few launches of one kernel on its bench workload, nothing else timed."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from attention_online_softmax_gb300 import build
+    build.build()
+    from attention_online_softmax_gb300 import abi
+    if which.startswith("prefill"):
+        c = configs.GQA256 if which == "prefill_d256" else configs.LONG
+        x = make_prefill_inputs(c)
+        q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        for _ in range(launches):
+            abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale)
+    else:
+        Dc = configs.DECODE
+        xd = make_decode_inputs()
+        dq, kc, vc = xd.q.to(dev), xd.kcache.to(dev), xd.vcache.to(dev)
+        bt, sl = xd.block_table.to(dev), xd.seqlens.to(dev)
+        do = torch.empty_like(dq)
+        dlse = torch.empty(dq.shape[:2], dtype=torch.float32, device=dev)
+        ws = torch.empty(max(16, abi.attn_decode_workspace_size(Dc.num_seqs, Dc.Hq, Dc.Hkv, Dc.d,
+                                                                xd.max_seqlen)),
+                         dtype=torch.uint8, device=dev)
+        for _ in range(launches):
+            abi.attn_decode_paged(dq, kc, vc, bt, sl, do, dlse, xd.max_seqlen, xd.scale, ws)
+    torch.cuda.synchronize()
+    st = abi.attn_get_device_status()
+    print(json.dumps({"profile": which, "launches": abi.attn_launch_count(), "status": st}))
+    return 0 if st == 0 else 1
 
 
 def measure_e2e(abi, xp, xd, dev, stream, steps, floor_s, world):
