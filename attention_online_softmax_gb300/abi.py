@@ -32,6 +32,9 @@ _lib.attn_decode_workspace_size.restype = ctypes.c_size_t
 _lib.attn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
                                    ctypes.c_float, _vp, ctypes.c_size_t, _i, _vp]
 _lib.attn_decode_paged.restype = _i
+_lib.attn_decode_paged_static.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                          _i, ctypes.c_float, _i, _vp]
+_lib.attn_decode_paged_static.restype = _i
 _lib.attn_get_device_status.argtypes = [_vp]
 _lib.attn_get_device_status.restype = _i
 _lib.attn_status_string.argtypes = [_i]
@@ -46,8 +49,11 @@ ATTN_BF16 = 0
 ATTN_F32 = 1
 
 #: every symbol include/attn.h declares
-EXPORTS = ("attn_fwd", "attn_decode_workspace_size", "attn_decode_paged", "attn_get_device_status",
-           "attn_status_string", "attn_launch_count", "attn_abi_version")
+EXPORTS = ("attn_fwd", "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_static",
+           "attn_get_device_status", "attn_status_string", "attn_launch_count", "attn_abi_version")
+
+#: size of the scratch array built into the library for attn_decode_paged_static
+STATIC_SCRATCH_BYTES = 64 << 20
 
 
 class AttnError(RuntimeError):
@@ -148,6 +154,37 @@ def attn_decode_paged(q, kcache, vcache, block_table, seqlens, o, lse, max_seqle
                                 ATTN_F32 if o.dtype == torch.float32 else ATTN_BF16,
                                 _stream_ptr(stream))
     _check(st, "attn_decode_paged")
+
+
+def attn_decode_paged_static(q, kcache, vcache, block_table, seqlens, o, lse, max_seqlen: int,
+                             scale: float, stream=None) -> None:
+    """attn_decode_paged without a workspace: the library's built-in scratch
+    array holds the split partials, so nothing is allocated for the call.
+
+    For callers that cannot allocate device memory themselves (all of it owned
+    by a framework's fixed pool, or a loop where an allocation's implicit device
+    synchronisation is not acceptable).  Calls that can overlap on the GPU
+    share the one array and must be ordered on one stream; the first call on a
+    device looks up the array's address and should come before any stream
+    capture.  Workloads whose split partials exceed STATIC_SCRATCH_BYTES raise
+    AttnError (status ATTN_ERR_WORKSPACE).
+    """
+    import torch
+    _need(q, torch.bfloat16, "q")
+    _need(kcache, torch.bfloat16, "kcache")
+    _need(vcache, torch.bfloat16, "vcache")
+    _need(block_table, torch.int32, "block_table")
+    _need(seqlens, torch.int32, "seqlens")
+    _need(lse, torch.float32, "lse")
+    _need(o, o.dtype, "o")
+    S, Hq, d = q.shape
+    P, page, Hkv, _ = kcache.shape
+    st = _lib.attn_decode_paged_static(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(block_table),
+                                       _ptr(seqlens), _ptr(o), _ptr(lse), S, Hq, Hkv, d, page, P,
+                                       block_table.shape[1], int(max_seqlen), float(scale),
+                                       ATTN_F32 if o.dtype == torch.float32 else ATTN_BF16,
+                                       _stream_ptr(stream))
+    _check(st, "attn_decode_paged_static")
 
 
 def attn_get_device_status(stream=None) -> int:

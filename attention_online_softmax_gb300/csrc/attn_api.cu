@@ -15,6 +15,12 @@
 #include "prefill_fwd.cuh"
 #include "ptx.cuh"
 
+// Scratch for attn_decode_paged_static(): split partials of one call, in a
+// device array owned by this library (no allocation at call time).  In host
+// code the symbol is only a stand-in; its device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+static __device__ __align__(256) unsigned char g_decode_scratch[ATTN_STATIC_SCRATCH_BYTES];
+
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
@@ -174,6 +180,30 @@ attn_status launch_decode_g(int G, const CUtensorMap& mk, const CUtensorMap& mv,
   }
 }
 
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+attn_status static_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -306,6 +336,24 @@ attn_status attn_decode_paged(const void* q, const void* kcache, const void* vca
     case 256: return launch_decode_g<256>(G, mk, mv, p, s);
   }
   return ATTN_ERR_UNSUPPORTED;
+}
+
+attn_status attn_decode_paged_static(const void* q, const void* kcache, const void* vcache,
+                                     const int32_t* block_table, const int32_t* seqlens, void* o, float* lse,
+                                     int num_seqs, int Hq, int Hkv, int d, int page_size, int num_pages,
+                                     int max_pages_per_seq, int max_seqlen, float scale, attn_dtype o_dtype,
+                                     attn_stream_t stream) {
+  // Too large for the built-in scratch: refuse before touching the device.
+  const size_t need = attn_decode_workspace_size(num_seqs, Hq, Hkv, d, max_seqlen);
+  if (need > static_cast<size_t>(ATTN_STATIC_SCRATCH_BYTES)) return ATTN_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (need > 0) {
+    const attn_status st = static_scratch_address(&scratch);
+    if (st != ATTN_OK) return st;
+  }
+  return attn_decode_paged(q, kcache, vcache, block_table, seqlens, o, lse, num_seqs, Hq, Hkv, d, page_size,
+                           num_pages, max_pages_per_seq, max_seqlen, scale, scratch,
+                           static_cast<size_t>(ATTN_STATIC_SCRATCH_BYTES), o_dtype, stream);
 }
 
 attn_status attn_get_device_status(attn_stream_t stream) {

@@ -123,6 +123,38 @@ ATTN_API attn_status attn_decode_paged(const void* q, const void* kcache, const 
                               attn_dtype o_dtype, attn_stream_t stream);
 
 /*
+ * Paged decode that allocates nothing and takes no workspace argument.
+ *
+ * Same inputs, outputs, checks and results as attn_decode_paged(), but the
+ * split partials live in a scratch array compiled into this library (a
+ * file-scope device array of ATTN_STATIC_SCRATCH_BYTES on every GPU that
+ * loads the library, held until the process exits).  It is meant for callers
+ * that cannot call cudaMalloc or hand over a buffer of their own -- for
+ * example code whose device memory is all owned by a host framework's fixed
+ * pool, or a latency-critical loop where an allocation (which may synchronise
+ * the device) is not acceptable.  The paper has no counterpart to this entry
+ * point; it is a deployment convenience of this library.
+ *
+ *  - Sizes whose attn_decode_workspace_size() exceeds ATTN_STATIC_SCRATCH_BYTES
+ *    are rejected with ATTN_ERR_WORKSPACE before anything is launched.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture begins.
+ *  - Every call on a device shares the one array.  Calls that may overlap on
+ *    the GPU (different streams without ordering between them) race on it and
+ *    corrupt each other's results; order them on one stream.  Nothing in the
+ *    array needs to start at zero: every value a call reads back was written
+ *    earlier in that same call.
+ */
+#define ATTN_STATIC_SCRATCH_BYTES (64u << 20)
+ATTN_API attn_status attn_decode_paged_static(const void* q, const void* kcache, const void* vcache,
+                              const int32_t* block_table, const int32_t* seqlens,
+                              void* o, float* lse,
+                              int num_seqs, int Hq, int Hkv, int d, int page_size,
+                              int num_pages, int max_pages_per_seq, int max_seqlen,
+                              float scale, attn_dtype o_dtype, attn_stream_t stream);
+
+/*
  * Waits for `stream`, then returns and clears the device status word of the
  * current device (ATTN_OK when no kernel recorded a fault since the last
  * call).  Not for the hot path: it synchronises.
