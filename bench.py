@@ -95,6 +95,13 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def aggregate_value(floor_s: float, steps: int, total_max_s: float, world: int) -> float:
+    """Whole-job value: every rank runs `steps` steps of the same workload
+    (weak scaling, no collective on the data path); the job's time is the
+    slowest rank's, so value = world * steps * floor / max-over-ranks time."""
+    return world * steps * floor_s / total_max_s
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -355,7 +362,7 @@ def main(argv=None):
     t_dec = [ev[i][1].elapsed_time(ev[i][2]) * 1e-3 for i in range(args.steps)]
     total = sum(a + b for a, b in zip(t_pre, t_dec))
     total_max = max_over_ranks(total, world, dev)
-    value = world * args.steps * (f_pre + f_dec) / total_max
+    value = aggregate_value(f_pre + f_dec, args.steps, total_max, world)
     if abi.attn_get_device_status() != 0:
         raise SystemExit("device status error in the timed region")
 
