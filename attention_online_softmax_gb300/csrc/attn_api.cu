@@ -92,18 +92,29 @@ bool encode_page_map(CUtensorMap* map, const void* base, int d, int Hkv, int pag
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int BN, int STAGES>
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                               cudaSuccess) {
+    cudaGetLastError();
+    return 148;
+  }
+  return n;
+}
+
+template <int D, int NQ, int STAGES>
 attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                           const attn::PrefillParams& p, int BH, cudaStream_t stream) {
-  using L = attn::PrefillLayout<D, BN, STAGES>;
-  auto kern = attn::prefill_fwd_kernel<D, BN, STAGES>;
+                           attn::PrefillParams p, int BH, cudaStream_t stream) {
+  using L = attn::PrefillLayout<D, NQ, STAGES>;
+  auto kern = attn::prefill_fwd_kernel<D, NQ, STAGES>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
   }
-  const long long blocks = static_cast<long long>(p.n_qtiles) * BH;
+  p.n_units = (p.Nq + attn::kBM * NQ - 1) / (attn::kBM * NQ);
+  const long long blocks = static_cast<long long>(p.n_units) * BH;
   if (blocks > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
-  kern<<<dim3(static_cast<unsigned>(blocks)), attn::kPrefillThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
+  kern<<<dim3(static_cast<unsigned>(blocks)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return ATTN_OK;
@@ -231,7 +242,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      int Nq, int Nk, int d, int causal, float scale, attn_dtype o_dtype, attn_stream_t stream) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (o_dtype != ATTN_BF16 && o_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * Hq > 0x7FFFFFFFLL || static_cast<long long>(B) * Hkv > 0x7FFFFFFFLL)
@@ -262,13 +273,20 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.Nk = Nk;
   p.causal = causal ? 1 : 0;
   p.o_f32 = o_dtype == ATTN_F32 ? 1 : 0;
-  p.n_qtiles = (Nq + attn::kBM - 1) / attn::kBM;
+  p.n_units = 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // Two query tiles per CTA (they share every K/V tile and overlap each
+  // other's softmax with MMAs) unless that leaves the GPU under-filled.
+  const long long pairs = static_cast<long long>((Nq + 2 * attn::kBM - 1) / (2 * attn::kBM)) * B * Hq;
+  const bool two = pairs >= 2LL * sm_count();
   switch (d) {
-    case 64: return launch_prefill<64, 128, 6>(mq, mk, mv, p, B * Hq, s);
-    case 128: return launch_prefill<128, 128, 4>(mq, mk, mv, p, B * Hq, s);
-    case 256: return launch_prefill<256, 128, 2>(mq, mk, mv, p, B * Hq, s);
+    case 64:
+      return two ? launch_prefill<64, 2, 6>(mq, mk, mv, p, B * Hq, s) : launch_prefill<64, 1, 6>(mq, mk, mv, p, B * Hq, s);
+    case 128:
+      return two ? launch_prefill<128, 2, 4>(mq, mk, mv, p, B * Hq, s)
+                 : launch_prefill<128, 1, 4>(mq, mk, mv, p, B * Hq, s);
+    case 256: return launch_prefill<256, 1, 2>(mq, mk, mv, p, B * Hq, s);
   }
   return ATTN_ERR_UNSUPPORTED;
 }
@@ -285,7 +303,7 @@ attn_status attn_decode_paged(const void* q, const void* kcache, const void* vca
                               void* workspace, size_t workspace_bytes, attn_dtype o_dtype, attn_stream_t stream) {
   if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (num_pages <= 0 || max_pages_per_seq <= 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (o_dtype != ATTN_BF16 && o_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   if (page_size != attn::kPage) return ATTN_ERR_UNSUPPORTED;

@@ -81,7 +81,8 @@ typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
  * Prefill / general forward attention.
  *   q:   [B, Hq, Nq, d] bf16          k, v: [B, Hkv, Nk, d] bf16
  *   o:   [B, Hq, Nq, d] bf16 or f32   lse:  [B, Hq, Nq] f32
- *   scale: multiplies Q K^T (1/sqrt(d) for the textbook operator); finite.
+ *   scale: multiplies Q K^T (1/sqrt(d) for the textbook operator); finite
+ *          and > 0.
  * B, Hq, Hkv, Nq, Nk >= 0; nothing is launched when the output is empty.
  * With Nk == 0 (or every key masked) each row is O = 0, LSE = -inf.
  */
@@ -109,6 +110,7 @@ ATTN_API size_t attn_decode_workspace_size(int num_seqs, int Hq, int Hkv, int d,
  *                <= max_pages_per_seq * page_size (checked on the device)
  *   o:           [num_seqs, Hq, d] bf16 or f32;  lse: [num_seqs, Hq] f32
  *   max_seqlen:  host-side upper bound of seqlens (sizes the split grid)
+ *   scale:       as for attn_fwd: finite and > 0
  *   workspace:   device scratch of at least attn_decode_workspace_size() bytes,
  *                16-byte aligned, owned by the caller, contents ignored; it
  *                must not be shared by two calls that overlap on the GPU.

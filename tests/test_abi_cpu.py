@@ -71,6 +71,8 @@ def test_fwd_rejects_bad_arguments_before_any_launch(abi):
     assert fwd(abi, Nq=-4) == INVALID
     assert fwd(abi, scale=float("nan")) == INVALID
     assert fwd(abi, scale=float("inf")) == INVALID
+    assert fwd(abi, scale=0.0) == INVALID
+    assert fwd(abi, scale=-0.125) == INVALID
     assert fwd(abi, dt=7) == INVALID
     assert fwd(abi, q=ODD) == MISALIGNED
     assert fwd(abi, o=0) == MISALIGNED
@@ -106,6 +108,7 @@ def test_decode_rejects_bad_arguments(abi):
     assert dec(abi, pages=0) == INVALID
     assert dec(abi, num_seqs=-1) == INVALID
     assert dec(abi, scale=float("nan")) == INVALID
+    assert dec(abi, scale=-1.0) == INVALID
     assert dec(abi, bt=ODD) == MISALIGNED
     assert dec(abi, sl=0) == MISALIGNED
     need = abi.attn_decode_workspace_size(4, 32, 8, 128, 512)

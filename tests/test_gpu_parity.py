@@ -95,6 +95,23 @@ def test_prefill_small_shapes(abi, shape):
     check_prefill(abi, x)
 
 
+# Enough (batch, head) x 256-row units that the library pairs two query tiles
+# per CTA; ragged tails leave the second tile of the last unit partly or
+# entirely past Nq.
+TWO_TILE = [
+    (1, 200, 200, 500, 500, 64, True),
+    (2, 100, 20, 300, 420, 128, True),
+    (1, 320, 320, 300, 300, 128, False),
+]
+
+
+@pytest.mark.parametrize("shape", TWO_TILE)
+def test_prefill_two_tile_units(abi, shape):
+    B, Hq, Hkv, Nq, Nk, d, causal = shape
+    x = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, seed=3000 + Nq + Hq, causal=causal)
+    check_prefill(abi, x)
+
+
 def test_prefill_zero_keys(abi):
     x = inputs.prefill_inputs(1, 2, 2, 64, 0, 128, seed=5, causal=False)
     o, lse = run_fwd(abi, x)
