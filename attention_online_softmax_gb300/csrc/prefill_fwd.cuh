@@ -60,7 +60,12 @@ template <int D, int NQ, int STAGES>
 struct PrefillLayout {
   static constexpr int kThreads = 64 + 128 * NQ;
   static constexpr int kQBytes = kBM * D * 2;
-  static constexpr int kKVBytes = kBN * D * 2;
+  // K and V tiles stream in items of up to 128 head-dim columns (kH items per
+  // tile), so with d = 256 a 64 KB tile occupies two 32 KB ring stages and
+  // loading the next tile overlaps the current one's MMAs.
+  static constexpr int kDI = D < 128 ? D : 128;  // head-dim columns per item
+  static constexpr int kH = D / kDI;             // items per K (or V) tile
+  static constexpr int kKVBytes = kBN * kDI * 2; // one ring stage
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + NQ * kQBytes;
   static constexpr int kBarOff = kKVOff + STAGES * kKVBytes;
@@ -164,16 +169,18 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
           tma_load_3d(smem + L::kQOff + j * L::kQBytes + c * (kBM * 128), &tmQ, q_full, c * 64, q0 + j * kBM,
                       bh);
       int issued = 0;
-      for (int item = 0; item < 2 * T; ++item) {
+      for (int item = 0; item < 2 * L::kH * T; ++item) {
         const int st = item % STAGES;
         if (!mbar_wait(&kv_empty[st], ((item / STAGES) & 1) ^ 1, 1)) break;
         mbar_expect_tx(&kv_full[st], L::kKVBytes);
-        const CUtensorMap* map = (item & 1) ? &tmV : &tmK;
-        const int krow = (item >> 1) * kBN;
+        const int t = item / (2 * L::kH);
+        const int kind = (item / L::kH) & 1;  // 0: K, 1: V
+        const int hh = item % L::kH;          // which 128-column part of the head dim
+        const CUtensorMap* map = kind ? &tmV : &tmK;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::kKVOff + st * L::kKVBytes + c * (kBN * 128), map, &kv_full[st], c * 64, krow,
-                      kvh);
+        for (int c = 0; c < L::kDI / 64; ++c)
+          tma_load_3d(smem + L::kKVOff + st * L::kKVBytes + c * (kBN * 128), map, &kv_full[st],
+                      hh * L::kDI + c * 64, t * kBN, kvh);
         issued = item + 1;
       }
       // Drain: never leave the CTA with a copy still writing shared memory.
@@ -185,87 +192,114 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && T > 0) {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q K-major, K K-major
-      constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, D, 0, 1);    // P K-major (TMEM), V MN-major
+      constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);      // Q K-major, K K-major
+      constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, L::kDI, 0, 1);   // P K-major (TMEM), V MN-major
       bool ok = mbar_wait(q_full, 0, 10);
 
-      auto issue_s = [&](int j, int slot, int st) {
-        const uint32_t sq = sbase + L::kQOff + j * L::kQBytes;
-        const uint32_t sk = sbase + L::kKVOff + st * L::kKVBytes;
+      // Descriptor bases, computed once: within a group only compile-time
+      // offsets are added (the 14-bit address field cannot carry: every
+      // shared-memory address is below 256 KB), so the issuing thread spends
+      // its time issuing MMAs rather than building descriptors.
+      const uint64_t dq0 = sdesc_sw128(sbase + L::kQOff, 16, 1024);
+      const uint64_t dkv0 = sdesc_sw128(sbase + L::kKVOff, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sbase + L::kKVOff, kBN * 128, 1024);
+      auto item_of = [](int t, int kind, int hh) { return t * 2 * L::kH + kind * L::kH + hh; };
+      auto wait_item = [&](int item, int where) {
+        return mbar_wait(&kv_full[item % STAGES], (item / STAGES) & 1, where);
+      };
+      // S_j(t) = Q_j K_t^T into S slot `slot`; waits for each K item in turn.
+      auto issue_s = [&](int j, int slot, int t, bool wait) -> bool {
+        const uint64_t da = dq0 + static_cast<uint64_t>((j * L::kQBytes) >> 4);
         const uint32_t dst = tmem + L::kSCol + slot * kBN;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t da = sdesc_sw128(sq + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t db = sdesc_sw128(sk + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024);
-          umma_bf16_ss(dst, da, db, kIdescS, kk > 0);
-        }
-      };
-      auto issue_pv = [&](int j, int slot, int st, bool first) {
-        const uint32_t sv = sbase + L::kKVOff + st * L::kKVBytes;
-        const uint32_t pa = tmem + L::kSCol + slot * kBN;
-        const uint32_t dst = tmem + j * D;
+        for (int hh = 0; hh < L::kH; ++hh) {
+          const int item = item_of(t, 0, hh);
+          if (wait) {
+            if (!wait_item(item, 13)) return false;
+            tc_fence_after();
+          }
+          const uint64_t db = dkv0 + static_cast<uint64_t>(((item % STAGES) * L::kKVBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t db = sdesc_sw128(sv + kk * (16 * 128), kBN * 128, 1024);
-          umma_bf16_ts(dst, pa + kk * 8, db, kIdescO, (!first || kk > 0) ? 1u : 0u);
+          for (int k2 = 0; k2 < L::kDI / 16; ++k2) {
+            const int kk = hh * (L::kDI / 16) + k2;
+            const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+            const uint64_t ob = static_cast<uint64_t>(((k2 >> 2) * (kBN * 128) + (k2 & 3) * 32) >> 4);
+            umma_bf16_ss(dst, da + oa, db + ob, kIdescS, kk > 0);
+          }
         }
+        return true;
+      };
+      // O_j (+)= P_j V_t: one N = kDI product per V item.
+      auto issue_pv = [&](int j, int slot, int t, bool wait) -> bool {
+        const uint32_t pa = tmem + L::kSCol + slot * kBN;
+#pragma unroll
+        for (int hh = 0; hh < L::kH; ++hh) {
+          const int item = item_of(t, 1, hh);
+          if (wait) {
+            if (!wait_item(item, 11)) return false;
+            tc_fence_after();
+          }
+          const uint64_t db = dv0 + static_cast<uint64_t>(((item % STAGES) * L::kKVBytes) >> 4);
+          const uint32_t dst = tmem + j * D + hh * L::kDI;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_bf16_ts(dst, pa + kk * 8, db + static_cast<uint64_t>((kk * (16 * 128)) >> 4), kIdescO,
+                         (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        return true;
+      };
+      auto release = [&](int t, int kind) {
+#pragma unroll
+        for (int hh = 0; hh < L::kH; ++hh) umma_commit(&kv_empty[item_of(t, kind, hh) % STAGES]);
       };
 
       for (int t = 0; ok && t <= T; ++t) {
-        const int stK = (2 * t) % STAGES;
-        const int stV = (2 * t - 1 + STAGES) % STAGES;
-        bool haveK = false, haveV = false;
         if (NQ == 2) {
-          // PV_A(t-1), S_A(t), PV_B(t-1), S_B(t)
+          // PV_A(t-1), S_A(t), PV_B(t-1), S_B(t); K/V items are waited for by
+          // their first user and released after their last.
+          bool waitedV = false, waitedK = false;
 #pragma unroll
           for (int j = 0; j < NQ; ++j) {
             if (t >= 1 && t - 1 < ntile[j]) {
-              if (!haveV) {
-                ok = mbar_wait(&kv_full[stV], ((2 * t - 1) / STAGES) & 1, 11);
-                if (!ok) break;
-                haveV = true;
-              }
               ok = mbar_wait(&p_full[j], (t - 1) & 1, 12);
               if (!ok) break;
               tc_fence_after();
-              issue_pv(j, j, stV, t - 1 == 0);
+              ok = issue_pv(j, j, t - 1, !waitedV);
+              if (!ok) break;
+              waitedV = true;
               if (t - 1 == ntile[j] - 1) umma_commit(&o_done[j]);
             }
             if (t < ntile[j]) {
-              if (!haveK) {
-                ok = mbar_wait(&kv_full[stK], ((2 * t) / STAGES) & 1, 13);
-                if (!ok) break;
-                haveK = true;
-                tc_fence_after();
-              }
-              issue_s(j, j, stK);
+              ok = issue_s(j, j, t, !waitedK);
+              if (!ok) break;
+              waitedK = true;
               umma_commit(&s_full[j]);
             }
           }
+          if (!ok) break;
+          if (waitedV) release(t - 1, 1);
+          if (waitedK) release(t, 0);
         } else {
-          // S(t) into slot t&1, then PV(t-1) from slot (t-1)&1
+          // S(t) into slot t&1 (overlaps the softmax of tile t-1), then PV(t-1).
           if (t < T) {
-            ok = mbar_wait(&kv_full[stK], ((2 * t) / STAGES) & 1, 13);
+            ok = issue_s(0, t & 1, t, true);
             if (!ok) break;
-            haveK = true;
-            tc_fence_after();
-            issue_s(0, t & 1, stK);
             umma_commit(&s_full[t & 1]);
+            release(t, 0);
           }
           if (t >= 1) {
-            ok = mbar_wait(&kv_full[stV], ((2 * t - 1) / STAGES) & 1, 11) &&
-                 mbar_wait(&p_full[(t - 1) & 1], ((t - 1) >> 1) & 1, 12);
+            ok = mbar_wait(&p_full[(t - 1) & 1], ((t - 1) >> 1) & 1, 12);
             if (!ok) break;
-            haveV = true;
             tc_fence_after();
-            issue_pv(0, (t - 1) & 1, stV, t - 1 == 0);
+            ok = issue_pv(0, (t - 1) & 1, t - 1, true);
+            if (!ok) break;
             umma_commit(pv_done);
+            release(t - 1, 1);
             if (t - 1 == T - 1) umma_commit(&o_done[0]);
           }
         }
-        if (haveV) umma_commit(&kv_empty[stV]);
-        if (haveK) umma_commit(&kv_empty[stK]);
       }
+      if (!ok) report_error(6 /* ATTN_ERR_TIMEOUT */, 16, 0);
       // Every MMA this thread issued must be complete before TMEM is freed.
       umma_commit(mma_drain);
       mbar_wait(mma_drain, 0, 15);
