@@ -286,7 +286,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
     case 128:
       return two ? launch_prefill<128, 2, 4>(mq, mk, mv, p, B * Hq, s)
                  : launch_prefill<128, 1, 4>(mq, mk, mv, p, B * Hq, s);
-    case 256: return launch_prefill<256, 1, 4>(mq, mk, mv, p, B * Hq, s);
+    case 256: return launch_prefill<256, 1, 5>(mq, mk, mv, p, B * Hq, s);
   }
   return ATTN_ERR_UNSUPPORTED;
 }

@@ -9,20 +9,17 @@
 //     l_t = alpha_t l_{t-1} + sum exp(S - m_t),  o_t = alpha_t o_{t-1} + sum exp(S - m_t) v,
 // and O = o_T / l_T, LSE = m_T + ln l_T at the end.  Scores never leave the SM.
 //
-// Roles (64 + 256*NQ threads):
+// Roles (64 + 128*NQ threads):
 //   warp 0        TMA producer: the NQ query tiles once, then K_t, V_t tiles
 //                 (shared by all query tiles of the CTA) into a STAGES-deep
 //                 shared-memory ring (128-byte swizzle), gated by mbarriers.
 //   warp 1        allocates tensor memory; one thread issues tcgen05.mma:
 //                 S_j = Q_j K_t^T (smem x smem) into TMEM, then
 //                 O_j += P_j V_t with P_j read from TMEM (tmem x smem).
-//   warps 2..     two softmax warpgroups per query tile; a thread owns one
-//                 row and 64 of its 128 scores.  Each reads its half of S from
-//                 TMEM, applies the mask, trades its half-row max with the
-//                 partner warp through shared memory (named barrier per pair),
-//                 updates the running max, writes its half of P = 2^(x - m) as
-//                 bf16 back over S in TMEM, rescales its half of O when the max
-//                 moved, and finally writes its half of O / l (and LSE).
+//   warps 2..     one softmax warpgroup per query tile, one thread per row:
+//                 reads S from TMEM, applies the mask, updates the running max,
+//                 writes P = 2^(x - m) as bf16 back over S in TMEM, rescales O
+//                 in TMEM when the max moved, and writes O / l and LSE.
 //
 // Tensor memory (512 columns): O_j at columns [j*D, (j+1)*D); two S slots of
 // 128 columns after them.  With NQ = 2 slot j belongs to query tile j and the
@@ -61,9 +58,7 @@ struct PrefillParams {
 
 template <int D, int NQ, int STAGES>
 struct PrefillLayout {
-  // Two softmax warpgroups per query tile, each owning 64 of the 128 score
-  // columns of every row.
-  static constexpr int kThreads = 64 + 256 * NQ;
+  static constexpr int kThreads = 64 + 128 * NQ;
   static constexpr int kQBytes = kBM * D * 2;
   // K and V tiles stream in items of up to 128 head-dim columns (kH items per
   // tile), so with d = 256 a 64 KB tile occupies two 32 KB ring stages and
@@ -77,12 +72,7 @@ struct PrefillLayout {
   // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done, o_done[2], mma_drain
   static constexpr int kNumBars = 1 + 2 * STAGES + 2 + 2 + 1 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  // Row-max exchange between the two halves of a tile (double-buffered over
-  // key tiles): [NQ][2 buffers][2 halves][128 rows] floats; then the final
-  // row sums: [NQ][2 halves][128 rows][2] floats.
-  static constexpr int kXMaxOff = kMiscOff + 16;
-  static constexpr int kXSumOff = kXMaxOff + NQ * 2 * 2 * kBM * 4;
-  static constexpr int kBytes = kXSumOff + NQ * 2 * kBM * 2 * 4;
+  static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the dynamic base to 1024
   static constexpr int kTmemCols = 512;
   static constexpr int kSCol = NQ * D;          // first S slot column
@@ -149,7 +139,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 8);
+      mbar_init(&p_full[i], 4);
       mbar_init(&o_done[i], 1);
     }
     mbar_init(pv_done, 1);
@@ -317,24 +307,18 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax warpgroups
-    const int sw = (warp - 2) >> 2;          // softmax warpgroup index
-    const int j = sw >> 1;                   // its query tile
-    const int hf = sw & 1;                   // which 64 score columns (and half of O) it owns
+    const int j = (warp - 2) >> 2;           // query tile of this warpgroup
     const int quarter = warp & 3;            // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;     // row within the tile
     const int r0 = q0 + j * kBM;
     const int qrow = r0 + row;
     const int nt = ntile[j];
-    const int bar_id = 1 + j * 4 + quarter;  // the two warps owning these 32 rows
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    constexpr int kOH = D / 2;               // O columns owned by this half
-    const uint32_t o_cols = lane_base + j * D + hf * kOH;
-    float* xmax = reinterpret_cast<float*>(smem + L::kXMaxOff) + j * (2 * 2 * kBM);
-    float* xsum = reinterpret_cast<float*>(smem + L::kXSumOff) + j * (2 * kBM * 2);
+    const uint32_t o_cols = lane_base + j * D;
     const float sl = p.scale_log2;
     // l sums the exact weights (for LSE); lr sums the bf16-rounded weights the
     // P V product uses, so O = o / lr is an exact convex combination of V rows
-    // before output rounding.  Each half keeps the sums of its own columns.
+    // before output rounding.
     float m_ref = -INFINITY;
     float l0 = 0.f, l1 = 0.f, lr0 = 0.f, lr1 = 0.f;
     bool ok = true;
@@ -345,37 +329,31 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_full[slot], s_par, 20));
       if (!ok) break;
       tc_fence_after();
-      uint32_t r[64];
-      tmem_ld64(lane_base + L::kSCol + slot * kBN + hf * 64, r);
+      uint32_t r[kBN];
+      tmem_ld128(lane_base + L::kSCol + slot * kBN, r);
 
-      // Half-row max of the raw scores (masked keys -> -inf); scale > 0 keeps
-      // the order, so the scaled max is mx * sl.
-      const int k0 = t * kBN + hf * 64;
-      const bool need_mask = (k0 + 64 > p.Nk) || (p.causal && (k0 + 63 > r0 + diag));
+      // Row max of the raw scores (masked keys -> -inf); scale > 0 keeps the
+      // order, so the scaled max is mx * sl.
+      const int k0 = t * kBN;
+      const bool need_mask = (k0 + kBN > p.Nk) || (p.causal && (k0 + kBN - 1 > r0 + diag));
       if (need_mask) {
         const int lim = (p.causal ? min(p.Nk - 1, qrow + diag) : p.Nk - 1) - k0;
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < kBN; ++c)
           if (c > lim) r[c] = 0xFF800000u;  // -inf
       }
       float mx[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 64; c += 8) {
+      for (int c = 0; c < kBN; c += 8) {
         const int a = (c >> 3) & 3;
         mx[a] = fmax3(mx[a], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
         mx[a] = fmax3(mx[a], __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
         mx[a] = fmax3(mx[a], __uint_as_float(r[c + 4]), __uint_as_float(r[c + 5]));
         mx[a] = fmax3(mx[a], __uint_as_float(r[c + 6]), __uint_as_float(r[c + 7]));
       }
-      const float mh = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
-      // Trade half-row maxima with the partner warp.  The barrier also means
-      // both halves finished reading S before either overwrites it with P.
-      float* xb = xmax + (t & 1) * (2 * kBM);
-      xb[hf * kBM + row] = mh;
-      named_bar(bar_id, 64);
-      const float mt = fmaxf(mh, xb[(hf ^ 1) * kBM + row]) * sl;
+      const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * sl;
       const float m_new = fmaxf(m_ref, mt);
       const bool rescale = m_new > m_ref + kRescaleLog2;
       float alpha = 1.f;
@@ -390,9 +368,9 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
       // p = 2^(s * sl - m): P as bf16 pairs, exact and rounded row sums.
-      uint32_t pk[32];
+      uint32_t pk[kBN / 2];
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
+      for (int c = 0; c < kBN; c += 2) {
         float a0, a1;
         ffma2(a0, a1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), sl, sl, neg_m, neg_m);
         const float p0 = ex2(a0);
@@ -411,7 +389,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
           tc_fence_after();
         }
 #pragma unroll 1
-        for (int c = 0; c < kOH / 32; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(o_cols + c * 32, o);
 #pragma unroll
@@ -424,9 +402,8 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
           tmem_st32(o_cols + c * 32, o);
         }
       }
-      // This half of P over columns [32*hf, 32*hf + 32) of the S slot, then
-      // hand it to the MMA thread (p_full counts all eight warps of the tile).
-      tmem_st32(lane_base + L::kSCol + slot * kBN + hf * 32, pk);
+      // P over the first half of the S slot, then hand it to the MMA thread.
+      tmem_st64(lane_base + L::kSCol + slot * kBN, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -437,20 +414,15 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&o_done[j], 0, 22));
       if (ok) tc_fence_after();
     }
-    // Combine the two halves' row sums (every thread of both warps takes part
-    // in the barrier, whatever happened above).
-    xsum[(hf * kBM + row) * 2 + 0] = l0 + l1;
-    xsum[(hf * kBM + row) * 2 + 1] = lr0 + lr1;
-    named_bar(bar_id, 64);
-    const float l = xsum[(0 * kBM + row) * 2 + 0] + xsum[(1 * kBM + row) * 2 + 0];
-    const float lr = xsum[(0 * kBM + row) * 2 + 1] + xsum[(1 * kBM + row) * 2 + 1];
     // Every lane runs the (warp-collective) TMEM loads; only rows < Nq store.
     const bool store = qrow < p.Nq;
     if (ok) {
+      const float lr = lr0 + lr1;
+      const float l = l0 + l1;
       const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
-      const size_t row_off = (static_cast<size_t>(bh) * p.Nq + qrow) * D + hf * kOH;
+      const size_t row_off = (static_cast<size_t>(bh) * p.Nq + qrow) * D;
 #pragma unroll 1
-      for (int c = 0; c < kOH / 32; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         if (nt > 0) {
           tmem_ld32(o_cols + c * 32, o);
@@ -477,7 +449,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
           }
         }
       }
-      if (store && hf == 0)
+      if (store)
         p.lse[static_cast<size_t>(bh) * p.Nq + qrow] =
             (l > 0.f) ? (m_ref + lg2(l)) * 0.69314718055994531f : -INFINITY;
     }
