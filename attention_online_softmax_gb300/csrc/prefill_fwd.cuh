@@ -40,6 +40,13 @@
 
 #include "ptx.cuh"
 
+#ifndef ATTN_MMA_WAIT
+#define ATTN_MMA_WAIT mbar_wait
+#endif
+#ifndef ATTN_SOFTMAX_WAIT
+#define ATTN_SOFTMAX_WAIT mbar_wait
+#endif
+
 namespace attn {
 
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
@@ -69,8 +76,8 @@ struct PrefillLayout {
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + NQ * kQBytes;
   static constexpr int kBarOff = kKVOff + STAGES * kKVBytes;
-  // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2 slots][2 halves], pv_done, o_done[2], mma_drain
-  static constexpr int kNumBars = 1 + 2 * STAGES + 2 + 4 + 1 + 2 + 1;
+  // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done, o_done[2], mma_drain
+  static constexpr int kNumBars = 1 + 2 * STAGES + 2 + 2 + 1 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the dynamic base to 1024
@@ -98,7 +105,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
   uint64_t* kv_empty = kv_full + STAGES;
   uint64_t* s_full = kv_empty + STAGES;
   uint64_t* p_full = s_full + 2;
-  uint64_t* pv_done = p_full + 4;
+  uint64_t* pv_done = p_full + 2;
   uint64_t* o_done = pv_done + 1;
   uint64_t* mma_drain = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -139,8 +146,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[2 * i], 4);
-      mbar_init(&p_full[2 * i + 1], 4);
+      mbar_init(&p_full[i], 4);
       mbar_init(&o_done[i], 1);
     }
     mbar_init(pv_done, 1);
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
       const uint64_t dv0 = sdesc_sw128(sbase + L::kKVOff, kBN * 128, 1024);
       auto item_of = [](int t, int kind, int hh) { return t * 2 * L::kH + kind * L::kH + hh; };
       auto wait_item = [&](int item, int where) {
-        return mbar_wait(&kv_full[item % STAGES], (item / STAGES) & 1, where);
+        return ATTN_MMA_WAIT(&kv_full[item % STAGES], (item / STAGES) & 1, where);
       };
       // S_j(t) = Q_j K_t^T into S slot `slot`; waits for each K item in turn.
       auto issue_s = [&](int j, int slot, int t, bool wait) -> bool {
@@ -230,31 +236,22 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
         }
         return true;
       };
-      // O_j (+)= P_j V_t: one N = kDI product per V item, issued in two key
-      // halves, each as soon as the softmax has written that half of P.
+      // O_j (+)= P_j V_t: one N = kDI product per V item.
       auto issue_pv = [&](int j, int slot, int t, bool wait) -> bool {
         const uint32_t pa = tmem + L::kSCol + slot * kBN;
-        const uint32_t par = NQ == 2 ? (t & 1) : ((t >> 1) & 1);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          if (!mbar_wait(&p_full[2 * slot + half], par, 12)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int hh = 0; hh < L::kH; ++hh) {
-            const int item = item_of(t, 1, hh);
-            if (wait && half == 0) {
-              if (!wait_item(item, 11)) return false;
-              tc_fence_after();
-            }
-            const uint64_t db = dv0 + static_cast<uint64_t>(((item % STAGES) * L::kKVBytes) >> 4);
-            const uint32_t dst = tmem + j * D + hh * L::kDI;
-#pragma unroll
-            for (int k2 = 0; k2 < kBN / 32; ++k2) {
-              const int kk = half * (kBN / 32) + k2;
-              umma_bf16_ts(dst, pa + kk * 8, db + static_cast<uint64_t>((kk * (16 * 128)) >> 4), kIdescO,
-                           (t > 0 || kk > 0) ? 1u : 0u);
-            }
+        for (int hh = 0; hh < L::kH; ++hh) {
+          const int item = item_of(t, 1, hh);
+          if (wait) {
+            if (!wait_item(item, 11)) return false;
+            tc_fence_after();
           }
+          const uint64_t db = dv0 + static_cast<uint64_t>(((item % STAGES) * L::kKVBytes) >> 4);
+          const uint32_t dst = tmem + j * D + hh * L::kDI;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_bf16_ts(dst, pa + kk * 8, db + static_cast<uint64_t>((kk * (16 * 128)) >> 4), kIdescO,
+                         (t > 0 || kk > 0) ? 1u : 0u);
         }
         return true;
       };
@@ -271,6 +268,9 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
 #pragma unroll
           for (int j = 0; j < NQ; ++j) {
             if (t >= 1 && t - 1 < ntile[j]) {
+              ok = ATTN_MMA_WAIT(&p_full[j], (t - 1) & 1, 12);
+              if (!ok) break;
+              tc_fence_after();
               ok = issue_pv(j, j, t - 1, !waitedV);
               if (!ok) break;
               waitedV = true;
@@ -295,6 +295,9 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
             release(t, 0);
           }
           if (t >= 1) {
+            ok = ATTN_MMA_WAIT(&p_full[(t - 1) & 1], ((t - 1) >> 1) & 1, 12);
+            if (!ok) break;
+            tc_fence_after();
             ok = issue_pv(0, (t - 1) & 1, t - 1, true);
             if (!ok) break;
             umma_commit(pv_done);
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
     for (int t = 0; t < nt; ++t) {
       const int slot = NQ == 2 ? j : (t & 1);
       const uint32_t s_par = NQ == 2 ? (t & 1) : ((t >> 1) & 1);
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_full[slot], s_par, 20));
+      ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(&s_full[slot], s_par, 20));
       if (!ok) break;
       tc_fence_after();
       uint32_t r[kBN];
@@ -371,65 +374,47 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
       }
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
-      // p = 2^(s * sl - m) as bf16 pairs with exact and rounded row sums, in
-      // two halves of 64 keys: each half goes over the first half of its S
-      // columns in TMEM and is handed to the MMA thread at once, so the P V
-      // product on keys 0..63 overlaps the exponentials of keys 64..127.
-      auto exps_half = [&](int half, uint32_t (&pk)[32]) {
+      // p = 2^(s * sl - m): P as bf16 pairs, exact and rounded row sums.
+      uint32_t pk[kBN / 2];
 #pragma unroll
-        for (int c2 = 0; c2 < 64; c2 += 2) {
-          const int c = half * 64 + c2;
-          float a0, a1;
-          ffma2(a0, a1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), sl, sl, neg_m, neg_m);
-          const float p0 = ex2(a0);
-          const float p1 = ex2(a1);
-          fadd2(l0, l1, l0, l1, p0, p1);
-          const uint32_t w = pack_bf16(p0, p1);
-          add_bf16x2(lr0, lr1, w);
-          pk[c2 >> 1] = w;
+      for (int c = 0; c < kBN; c += 2) {
+        float a0, a1;
+        ffma2(a0, a1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), sl, sl, neg_m, neg_m);
+        const float p0 = ex2(a0);
+        const float p1 = ex2(a1);
+        fadd2(l0, l1, l0, l1, p0, p1);
+        const uint32_t w = pack_bf16(p0, p1);
+        add_bf16x2(lr0, lr1, w);
+        pk[c >> 1] = w;
+      }
+
+      if (t > 0 && __any_sync(0xFFFFFFFFu, rescale)) {
+        if (NQ == 1) {
+          // O holds tile t-1's contribution only once PV(t-1) is complete.
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(pv_done, (t - 1) & 1, 21));
+          if (!ok) break;
+          tc_fence_after();
         }
-      };
-      auto hand_over = [&](int half, const uint32_t (&pk)[32]) {
-        tmem_st32(lane_base + L::kSCol + slot * kBN + half * 32, pk);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[2 * slot + half]);
-      };
-      {
-        uint32_t pk[32];
-        exps_half(0, pk);
-        // Rescale O before handing over any P of this tile: no P V product of
-        // tile t may accumulate into O until the rescale is done.
-        if (t > 0 && __any_sync(0xFFFFFFFFu, rescale)) {
-          if (NQ == 1) {
-            // O holds tile t-1's contribution only once PV(t-1) is complete.
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(pv_done, (t - 1) & 1, 21));
-            if (!ok) break;
-            tc_fence_after();
-          }
 #pragma unroll 1
-          for (int c = 0; c < D / 16; ++c) {
-            uint32_t o[16];
-            tmem_ld16(o_cols + c * 16, o);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_cols + c * 32, o);
 #pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-              float y0, y1;
-              ffma2(y0, y1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha, 0.f, 0.f);
-              o[i] = __float_as_uint(y0);
-              o[i + 1] = __float_as_uint(y1);
-            }
-            tmem_st16(o_cols + c * 16, o);
+          for (int i = 0; i < 32; i += 2) {
+            float y0, y1;
+            ffma2(y0, y1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha, 0.f, 0.f);
+            o[i] = __float_as_uint(y0);
+            o[i + 1] = __float_as_uint(y1);
           }
-          tmem_st_wait();
+          tmem_st32(o_cols + c * 32, o);
         }
-        hand_over(0, pk);
       }
-      {
-        uint32_t pk[32];
-        exps_half(1, pk);
-        hand_over(1, pk);
-      }
+      // P over the first half of the S slot, then hand it to the MMA thread.
+      tmem_st64(lane_base + L::kSCol + slot * kBN, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[slot]);
     }
 
     if (ok && nt > 0) {
