@@ -112,6 +112,9 @@ attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const C
     return ATTN_ERR_LAUNCH;
   }
   p.n_units = (p.Nq + attn::kBM * NQ - 1) / (attn::kBM * NQ);
+  // Enough heads per scheduling group for two waves of CTAs.
+  const int want = (2 * sm_count() + p.n_units - 1) / p.n_units;
+  p.group = want < 1 ? 1 : (want > BH ? BH : want);
   const long long blocks = static_cast<long long>(p.n_units) * BH;
   if (blocks > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
   kern<<<dim3(static_cast<unsigned>(blocks)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
@@ -274,6 +277,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.causal = causal ? 1 : 0;
   p.o_f32 = o_dtype == ATTN_F32 ? 1 : 0;
   p.n_units = 0;
+  p.group = 1;
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // Two query tiles per CTA (they share every K/V tile and overlap each

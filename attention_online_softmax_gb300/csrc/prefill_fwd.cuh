@@ -60,6 +60,7 @@ struct PrefillParams {
   int causal;
   int o_f32;
   int n_units;       // CTAs per (batch, head): ceil(Nq / (128 * NQ))
+  int group;         // (batch, head) pairs scheduled together, longest units first
   float scale_log2;  // scale * log2(e), > 0
 };
 
@@ -112,11 +113,19 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Flat grid: block = bh * n_units + i, the units of one head visited
-  // longest (causal) first.
-  const int bh = static_cast<int>(blockIdx.x) / p.n_units;
-  const int unit = p.n_units - 1 - (static_cast<int>(blockIdx.x) - bh * p.n_units);
-  if (bh >= p.B * p.Hq || unit < 0) return;  // never taken with the host's grid
+  // Flat grid in groups of `group` (batch, head) pairs; inside a group the
+  // blocks run longest causal unit first across all its heads (the block
+  // scheduler then packs the uneven causal units well), while the group's
+  // K/V stay small enough to be reused from L2.
+  const int BH = p.B * p.Hq;
+  const int per_group = p.group * p.n_units;
+  const int grp = static_cast<int>(blockIdx.x) / per_group;
+  const int idx = static_cast<int>(blockIdx.x) - grp * per_group;
+  const int gsize = min(p.group, BH - grp * p.group);
+  const int rank = gsize > 0 ? idx / gsize : p.n_units;
+  const int bh = grp * p.group + (idx - rank * gsize);
+  const int unit = p.n_units - 1 - rank;
+  if (gsize <= 0 || bh >= BH || unit < 0) return;  // never taken with the host's grid
   const int b = bh / p.Hq;
   const int h = bh - b * p.Hq;
   const int kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
