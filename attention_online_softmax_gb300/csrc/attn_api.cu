@@ -23,6 +23,7 @@ static __device__ __align__(256) unsigned char g_decode_scratch[ATTN_STATIC_SCRA
 
 namespace {
 
+constexpr int kMaxDevices = 64;
 std::atomic<uint64_t> g_launches{0};
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -102,6 +103,41 @@ int sm_count() {
   return n;
 }
 
+// Work counters of the persistent prefill kernel: a ring of per-launch
+// [next unit, finished CTAs] pairs, zero at load time and reset to zero by the
+// last CTA of the launch that used them.  Consecutive launches take
+// consecutive slots, so launches in flight at the same time (up to the ring
+// size, on any streams) never share a counter.
+constexpr int kSchedSlots = 64;
+__device__ int g_prefill_sched[kSchedSlots][2];
+std::atomic<uint32_t> g_sched_seq{0};
+std::mutex g_sched_mu;
+int* g_sched_base[kMaxDevices] = {};
+
+attn_status sched_slot(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  int* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_sched_mu);
+    if (g_sched_base[dev] == nullptr) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_prefill_sched) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH;
+      }
+      g_sched_base[dev] = static_cast<int*>(ptr);
+    }
+    base = g_sched_base[dev];
+  }
+  *out = base + 2 * (g_sched_seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+  return ATTN_OK;
+}
+
 template <int D, int NQ, int STAGES>
 attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            attn::PrefillParams p, int BH, cudaStream_t stream) {
@@ -112,12 +148,17 @@ attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const C
     return ATTN_ERR_LAUNCH;
   }
   p.n_units = (p.Nq + attn::kBM * NQ - 1) / (attn::kBM * NQ);
-  // Enough heads per scheduling group for two waves of CTAs.
-  const int want = (2 * sm_count() + p.n_units - 1) / p.n_units;
+  const int sms = sm_count();
+  // Enough heads per scheduling group for two waves of units.
+  const int want = (2 * sms + p.n_units - 1) / p.n_units;
   p.group = want < 1 ? 1 : (want > BH ? BH : want);
-  const long long blocks = static_cast<long long>(p.n_units) * BH;
-  if (blocks > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
-  kern<<<dim3(static_cast<unsigned>(blocks)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
+  const long long units = static_cast<long long>(p.n_units) * BH;
+  if (units > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
+  const attn_status st = sched_slot(&p.sched);
+  if (st != ATTN_OK) return st;
+  // Persistent: one CTA per SM (or fewer when there are fewer units).
+  const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
+  kern<<<dim3(grid), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return ATTN_OK;
@@ -194,7 +235,6 @@ attn_status launch_decode_g(int G, const CUtensorMap& mk, const CUtensorMap& mv,
   }
 }
 
-constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
@@ -278,6 +318,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.o_f32 = o_dtype == ATTN_F32 ? 1 : 0;
   p.n_units = 0;
   p.group = 1;
+  p.sched = nullptr;
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // Two query tiles per CTA (they share every K/V tile and overlap each

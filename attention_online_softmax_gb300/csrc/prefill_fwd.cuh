@@ -1,19 +1,25 @@
 // Fused attention forward (prefill) for sm_103a.
 //
-// A CTA computes NQ 128-row query tiles (NQ = 2 for d <= 128, 1 for d = 256)
-// of one (batch, query head) against the key/value tiles those rows may see,
-// following the block recurrence of "Compilers and Kernels", section
-// "FlashAttention changes the algorithm around IO": for each key block B_t the
-// row state (m, l, o) is updated by
+// A persistent kernel: one CTA per SM takes work units from a per-launch
+// atomic counter until none are left.  A unit is NQ 128-row query tiles
+// (NQ = 2 for d <= 128, 1 for d = 256) of one (batch, query head), computed
+// against the key/value tiles those rows may see with the block recurrence of
+// "Compilers and Kernels", section "FlashAttention changes the algorithm
+// around IO": for each key block B_t the row state (m, l, o) is updated by
 //     m_t = max(m_{t-1}, b_t),  alpha_t = exp(m_{t-1} - m_t),
 //     l_t = alpha_t l_{t-1} + sum exp(S - m_t),  o_t = alpha_t o_{t-1} + sum exp(S - m_t) v,
 // and O = o_T / l_T, LSE = m_T + ln l_T at the end.  Scores never leave the SM.
+// Units are handed out longest causal unit first within groups of heads, so
+// the uneven causal units pack well while each group's K/V stays in L2.
 //
 // Roles (64 + 128*NQ threads):
-//   warp 0        TMA producer: the NQ query tiles once, then K_t, V_t tiles
-//                 (shared by all query tiles of the CTA) into a STAGES-deep
-//                 shared-memory ring (128-byte swizzle), gated by mbarriers.
-//   warp 1        allocates tensor memory; one thread issues tcgen05.mma:
+//   warp 0        TMA producer: takes the next unit from the work counter and
+//                 passes it to the other roles through a small shared-memory
+//                 queue, loads the unit's NQ query tiles, then its K_t, V_t
+//                 tiles (shared by all query tiles of the unit) into a
+//                 STAGES-deep shared-memory ring (128-byte swizzle) that runs on
+//                 across units, so the next unit's loads overlap this one's end.
+//   warp 1        allocates tensor memory once; one thread issues tcgen05.mma:
 //                 S_j = Q_j K_t^T (smem x smem) into TMEM, then
 //                 O_j += P_j V_t with P_j read from TMEM (tmem x smem).
 //   warps 2..     one softmax warpgroup per query tile, one thread per row:
@@ -28,6 +34,8 @@
 // tiles: S(t+1) is computed while tile t is softmaxed.  P (bf16, 64 columns)
 // overwrites the first half of its S slot; tcgen05 MMAs from one thread run in
 // issue order, so the next S into that slot is issued after the P V product.
+// A unit's first P V product overwrites O_j only after the previous unit's
+// epilogue has read it (barrier o_free).  Barrier phases run on across units.
 //
 // Work is in base 2: x = s * scale * log2(e), p = 2^(x - m); the running
 // reference max only moves when a tile's max exceeds it by more than
@@ -52,14 +60,16 @@ namespace attn {
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;  // keys per tile
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kUnitQ = 4;  // depth of the in-CTA queue of fetched units
 
 struct PrefillParams {
   void* o;
   float* lse;
+  int* sched;        // this launch's [work counter, finished-CTA counter], both 0 at launch
   int B, Hq, Hkv, Nq, Nk;
   int causal;
   int o_f32;
-  int n_units;       // CTAs per (batch, head): ceil(Nq / (128 * NQ))
+  int n_units;       // units per (batch, head): ceil(Nq / (128 * NQ))
   int group;         // (batch, head) pairs scheduled together, longest units first
   float scale_log2;  // scale * log2(e), > 0
 };
@@ -77,11 +87,14 @@ struct PrefillLayout {
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + NQ * kQBytes;
   static constexpr int kBarOff = kKVOff + STAGES * kKVBytes;
-  // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done, o_done[2], mma_drain
-  static constexpr int kNumBars = 1 + 2 * STAGES + 2 + 2 + 1 + 2 + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kBytes = kMiscOff + 16;
-  static constexpr int kAlloc = kBytes + 1024;  // room to align the dynamic base to 1024
+  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done,
+  // o_done[2], o_free[2], unit_full[Q], unit_empty[Q], mma_drain
+  static constexpr int kNumBars = 2 + 2 * STAGES + 2 + 2 + 1 + 2 + 2 + 2 * kUnitQ + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, unit queue
+  static constexpr int kBytes = kMiscOff + 16 + 4 * kUnitQ;
+  // Dynamic shared memory requested: at least 115 KB so that no second CTA
+  // (which would wait for this one's tensor memory) shares the SM.
+  static constexpr int kAlloc = (kBytes + 1024) > 117760 ? (kBytes + 1024) : 117760;
   static constexpr int kTmemCols = 512;
   static constexpr int kSCol = NQ * D;          // first S slot column
   static_assert(NQ * D + 2 * kBN <= kTmemCols, "tensor memory budget");
@@ -89,6 +102,46 @@ struct PrefillLayout {
   static_assert(D % 64 == 0, "head dim");
   static_assert(NQ == 1 || NQ == 2, "query tiles per CTA");
 };
+
+// One work unit: its (batch, head) and first query row, and the key tiles each
+// of its query tiles needs (0 for a tile past Nq or fully masked).
+template <int NQ>
+struct Unit {
+  int bh, kvh, q0, T;
+  int ntile[NQ];
+};
+
+// Unit `idx` of the grouped longest-first order (0 <= idx < B*Hq*n_units).
+template <int NQ>
+__device__ __forceinline__ Unit<NQ> unit_of(const PrefillParams& p, int idx) {
+  Unit<NQ> u;
+  const int BH = p.B * p.Hq;
+  const int per_group = p.group * p.n_units;
+  const int grp = idx / per_group;
+  const int in = idx - grp * per_group;
+  const int gsize = min(p.group, BH - grp * p.group);
+  const int rank = in / gsize;
+  u.bh = grp * p.group + (in - rank * gsize);
+  const int un = p.n_units - 1 - rank;
+  const int b = u.bh / p.Hq;
+  const int h = u.bh - b * p.Hq;
+  u.kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
+  u.q0 = un * (kBM * NQ);
+  const int diag = p.Nk - p.Nq;
+  u.T = 0;
+#pragma unroll
+  for (int j = 0; j < NQ; ++j) {
+    const int r0 = u.q0 + j * kBM;
+    int kend = 0;
+    if (r0 < p.Nq) {
+      kend = p.Nk;
+      if (p.causal) kend = min(p.Nk, min(r0 + kBM, p.Nq) - 1 + diag + 1);
+    }
+    u.ntile[j] = kend > 0 ? (kend + kBN - 1) / kBN : 0;
+    u.T = max(u.T, u.ntile[j]);
+  }
+  return u;
+}
 
 template <int D, int NQ, int STAGES>
 __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
@@ -102,53 +155,27 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;
   uint64_t* kv_empty = kv_full + STAGES;
   uint64_t* s_full = kv_empty + STAGES;
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* o_done = pv_done + 1;
-  uint64_t* mma_drain = o_done + 2;
+  uint64_t* o_free = o_done + 2;
+  uint64_t* unit_full = o_free + 2;
+  uint64_t* unit_empty = unit_full + kUnitQ;
+  uint64_t* mma_drain = unit_empty + kUnitQ;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* unit_q = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 16);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Flat grid in groups of `group` (batch, head) pairs; inside a group the
-  // blocks run longest causal unit first across all its heads (the block
-  // scheduler then packs the uneven causal units well), while the group's
-  // K/V stay small enough to be reused from L2.
-  const int BH = p.B * p.Hq;
-  const int per_group = p.group * p.n_units;
-  const int grp = static_cast<int>(blockIdx.x) / per_group;
-  const int idx = static_cast<int>(blockIdx.x) - grp * per_group;
-  const int gsize = min(p.group, BH - grp * p.group);
-  const int rank = gsize > 0 ? idx / gsize : p.n_units;
-  const int bh = grp * p.group + (idx - rank * gsize);
-  const int unit = p.n_units - 1 - rank;
-  if (gsize <= 0 || bh >= BH || unit < 0) return;  // never taken with the host's grid
-  const int b = bh / p.Hq;
-  const int h = bh - b * p.Hq;
-  const int kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
-  const int q0 = unit * (kBM * NQ);
-  const int diag = p.Nk - p.Nq;  // key j allowed for row i iff j <= i + diag (causal)
-
-  // Key tiles each query tile needs (0 for a tile past Nq or fully masked).
-  int ntile[NQ];
-  int T = 0;
-#pragma unroll
-  for (int j = 0; j < NQ; ++j) {
-    const int r0 = q0 + j * kBM;
-    int kend = 0;
-    if (r0 < p.Nq) {
-      kend = p.Nk;
-      if (p.causal) kend = min(p.Nk, min(r0 + kBM, p.Nq) - 1 + diag + 1);
-    }
-    ntile[j] = kend > 0 ? (kend + kBN - 1) / kBN : 0;
-    T = max(T, ntile[j]);
-  }
+  const int total_units = p.B * p.Hq * p.n_units;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
@@ -157,6 +184,11 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
       mbar_init(&o_done[i], 1);
+      mbar_init(&o_free[i], 4);
+    }
+    for (int i = 0; i < kUnitQ; ++i) {
+      mbar_init(&unit_full[i], 1);
+      mbar_init(&unit_empty[i], 1 + 4 * NQ);  // MMA thread + lane 0 of every softmax warp
     }
     mbar_init(pv_done, 1);
     mbar_init(mma_drain, 1);
@@ -171,47 +203,72 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Consumers' view of the unit queue: the n-th unit this CTA processes
+  // (-1: no work left, -2: the wait timed out).
+  auto next_unit = [&](int n, int where) -> int {
+    const int slot = n % kUnitQ;
+    if (!mbar_wait(&unit_full[slot], (n / kUnitQ) & 1, where)) return -2;
+    return unit_q[slot];
+  };
+
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0 && T > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_expect_tx(q_full, NQ * L::kQBytes);
+      int item = 0;  // K/V items issued so far (the ring runs on across units)
+      int q_uses = 0;
+      bool ok = true;
+      for (int n = 0; ok; ++n) {
+        // Take the next unit and publish it (-1: no work left).
+        const int slot = n % kUnitQ;
+        if (!mbar_wait(&unit_empty[slot], ((n / kUnitQ) & 1) ^ 1, 4)) break;
+        int idx = atomicAdd(p.sched, 1);
+        if (idx >= total_units) idx = -1;
+        unit_q[slot] = idx;
+        mbar_arrive(&unit_full[slot]);
+        if (idx < 0) break;
+        const Unit<NQ> u = unit_of<NQ>(p, idx);
+        if (u.T == 0) continue;
+        // The previous unit's last S MMA must be done with the Q tiles.
+        if (q_uses > 0 && !mbar_wait(q_empty, (q_uses - 1) & 1, 5)) break;
+        mbar_expect_tx(q_full, NQ * L::kQBytes);
 #pragma unroll
-      for (int j = 0; j < NQ; ++j)
+        for (int j = 0; j < NQ; ++j)
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::kQOff + j * L::kQBytes + c * (kBM * 128), &tmQ, q_full, c * 64, q0 + j * kBM,
-                      bh);
-      int issued = 0;
-      for (int item = 0; item < 2 * L::kH * T; ++item) {
-        const int st = item % STAGES;
-        if (!mbar_wait(&kv_empty[st], ((item / STAGES) & 1) ^ 1, 1)) break;
-        mbar_expect_tx(&kv_full[st], L::kKVBytes);
-        const int t = item / (2 * L::kH);
-        const int kind = (item / L::kH) & 1;  // 0: K, 1: V
-        const int hh = item % L::kH;          // which 128-column part of the head dim
-        const CUtensorMap* map = kind ? &tmV : &tmK;
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + L::kQOff + j * L::kQBytes + c * (kBM * 128), &tmQ, q_full, c * 64,
+                        u.q0 + j * kBM, u.bh);
+        ++q_uses;
+        for (int i = 0; i < 2 * L::kH * u.T; ++i, ++item) {
+          const int st = item % STAGES;
+          if (!mbar_wait(&kv_empty[st], ((item / STAGES) & 1) ^ 1, 1)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&kv_full[st], L::kKVBytes);
+          const int t = i / (2 * L::kH);
+          const int kind = (i / L::kH) & 1;  // 0: K, 1: V
+          const int hh = i % L::kH;          // which 128-column part of the head dim
+          const CUtensorMap* map = kind ? &tmV : &tmK;
 #pragma unroll
-        for (int c = 0; c < L::kDI / 64; ++c)
-          tma_load_3d(smem + L::kKVOff + st * L::kKVBytes + c * (kBN * 128), map, &kv_full[st],
-                      hh * L::kDI + c * 64, t * kBN, kvh);
-        issued = item + 1;
+          for (int c = 0; c < L::kDI / 64; ++c)
+            tma_load_3d(smem + L::kKVOff + st * L::kKVBytes + c * (kBN * 128), map, &kv_full[st],
+                        hh * L::kDI + c * 64, t * kBN, u.kvh);
+        }
       }
       // Drain: never leave the CTA with a copy still writing shared memory.
-      mbar_wait(q_full, 0, 2);
-      for (int item = max(0, issued - STAGES); item < issued; ++item)
-        mbar_wait(&kv_full[item % STAGES], (item / STAGES) & 1, 3);
+      if (q_uses > 0) mbar_wait(q_full, (q_uses - 1) & 1, 2);
+      for (int it = max(0, item - STAGES); it < item; ++it)
+        mbar_wait(&kv_full[it % STAGES], (it / STAGES) & 1, 3);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0 && T > 0) {
+    if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);      // Q K-major, K K-major
       constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, L::kDI, 0, 1);   // P K-major (TMEM), V MN-major
-      bool ok = mbar_wait(q_full, 0, 10);
-
       // Descriptor bases, computed once: within a group only compile-time
       // offsets are added (the 14-bit address field cannot carry: every
       // shared-memory address is below 256 KB), so the issuing thread spends
@@ -219,17 +276,22 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
       const uint64_t dq0 = sdesc_sw128(sbase + L::kQOff, 16, 1024);
       const uint64_t dkv0 = sdesc_sw128(sbase + L::kKVOff, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sbase + L::kKVOff, kBN * 128, 1024);
-      auto item_of = [](int t, int kind, int hh) { return t * 2 * L::kH + kind * L::kH + hh; };
+      int item0 = 0;        // first K/V item of the current unit
+      int q_uses = 0;       // units with work so far
+      int cnt[2] = {0, 0};  // S tiles issued: per query tile (NQ = 2), in total (NQ = 1, cnt[0])
+      int o_uses[2] = {0, 0};
+      bool ok = true;
+
       auto wait_item = [&](int item, int where) {
         return ATTN_MMA_WAIT(&kv_full[item % STAGES], (item / STAGES) & 1, where);
       };
-      // S_j(t) = Q_j K_t^T into S slot `slot`; waits for each K item in turn.
-      auto issue_s = [&](int j, int slot, int t, bool wait) -> bool {
+      // S = Q_j K_t^T into S slot `slot`; waits for each K item in turn.
+      auto issue_s = [&](int j, int slot, int kitem, bool wait) -> bool {
         const uint64_t da = dq0 + static_cast<uint64_t>((j * L::kQBytes) >> 4);
         const uint32_t dst = tmem + L::kSCol + slot * kBN;
 #pragma unroll
         for (int hh = 0; hh < L::kH; ++hh) {
-          const int item = item_of(t, 0, hh);
+          const int item = kitem + hh;
           if (wait) {
             if (!wait_item(item, 13)) return false;
             tc_fence_after();
@@ -245,12 +307,12 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
         }
         return true;
       };
-      // O_j (+)= P_j V_t: one N = kDI product per V item.
-      auto issue_pv = [&](int j, int slot, int t, bool wait) -> bool {
+      // O_j (+)= P_j V_t: one N = kDI product per V item; `first` overwrites O_j.
+      auto issue_pv = [&](int j, int slot, int vitem, bool wait, bool first) -> bool {
         const uint32_t pa = tmem + L::kSCol + slot * kBN;
 #pragma unroll
         for (int hh = 0; hh < L::kH; ++hh) {
-          const int item = item_of(t, 1, hh);
+          const int item = vitem + hh;
           if (wait) {
             if (!wait_item(item, 11)) return false;
             tc_fence_after();
@@ -260,62 +322,104 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
             umma_bf16_ts(dst, pa + kk * 8, db + static_cast<uint64_t>((kk * (16 * 128)) >> 4), kIdescO,
-                         (t > 0 || kk > 0) ? 1u : 0u);
+                         (!first || kk > 0) ? 1u : 0u);
         }
         return true;
       };
-      auto release = [&](int t, int kind) {
+      auto release = [&](int first_item) {
 #pragma unroll
-        for (int hh = 0; hh < L::kH; ++hh) umma_commit(&kv_empty[item_of(t, kind, hh) % STAGES]);
+        for (int hh = 0; hh < L::kH; ++hh) umma_commit(&kv_empty[(first_item + hh) % STAGES]);
+      };
+      // Before a unit's first P V into O_j, the previous unit's epilogue must
+      // have read O_j out of tensor memory.
+      auto wait_o_free = [&](int j) -> bool {
+        if (o_uses[j] == 0) return true;
+        if (!ATTN_MMA_WAIT(&o_free[j], (o_uses[j] - 1) & 1, 16)) return false;
+        tc_fence_after();
+        return true;
       };
 
-      for (int t = 0; ok && t <= T; ++t) {
-        if (NQ == 2) {
-          // PV_A(t-1), S_A(t), PV_B(t-1), S_B(t); K/V items are waited for by
-          // their first user and released after their last.
-          bool waitedV = false, waitedK = false;
+      for (int n = 0; ok; ++n) {
+        const int idx = next_unit(n, 17);
+        if (idx == -2) break;
+        mbar_arrive(&unit_empty[n % kUnitQ]);
+        if (idx < 0) break;
+        const Unit<NQ> u = unit_of<NQ>(p, idx);
+        if (u.T == 0) continue;
+        ok = mbar_wait(q_full, q_uses & 1, 10);
+        if (!ok) break;
+        const int T = u.T;
+        for (int t = 0; ok && t <= T; ++t) {
+          const int kit = item0 + t * 2 * L::kH;               // K(t)
+          const int vit = item0 + (t - 1) * 2 * L::kH + L::kH; // V(t-1)
+          if (NQ == 2) {
+            // PV_A(t-1), S_A(t), PV_B(t-1), S_B(t); K/V items are waited for
+            // by their first user and released after their last.
+            bool waitedV = false, waitedK = false;
 #pragma unroll
-          for (int j = 0; j < NQ; ++j) {
-            if (t >= 1 && t - 1 < ntile[j]) {
-              ok = ATTN_MMA_WAIT(&p_full[j], (t - 1) & 1, 12);
+            for (int j = 0; j < NQ; ++j) {
+              if (t >= 1 && t - 1 < u.ntile[j]) {
+                ok = ATTN_MMA_WAIT(&p_full[j], (cnt[j] - 1) & 1, 12);
+                if (!ok) break;
+                tc_fence_after();
+                if (t - 1 == 0) {
+                  ok = wait_o_free(j);
+                  if (!ok) break;
+                }
+                ok = issue_pv(j, j, vit, !waitedV, t - 1 == 0);
+                if (!ok) break;
+                waitedV = true;
+                if (t - 1 == u.ntile[j] - 1) {
+                  umma_commit(&o_done[j]);
+                  ++o_uses[j];
+                }
+              }
+              if (t < u.ntile[j]) {
+                ok = issue_s(j, j, kit, !waitedK);
+                if (!ok) break;
+                waitedK = true;
+                umma_commit(&s_full[j]);
+                ++cnt[j];
+              }
+            }
+            if (!ok) break;
+            if (waitedV) release(vit);
+            if (waitedK) release(kit);
+            if (t == T - 1) umma_commit(q_empty);  // the unit's last S MMA is issued
+          } else {
+            // S(t) into slot c&1 (overlaps the softmax of tile t-1), then PV(t-1).
+            if (t < T) {
+              const int c = cnt[0];
+              ok = issue_s(0, c & 1, kit, true);
+              if (!ok) break;
+              umma_commit(&s_full[c & 1]);
+              ++cnt[0];
+              release(kit);
+              if (t == T - 1) umma_commit(q_empty);
+            }
+            if (t >= 1) {
+              const int c = cnt[0] - (t < T ? 2 : 1);  // running index of tile t-1
+              ok = ATTN_MMA_WAIT(&p_full[c & 1], (c >> 1) & 1, 12);
               if (!ok) break;
               tc_fence_after();
-              ok = issue_pv(j, j, t - 1, !waitedV);
+              if (t - 1 == 0) {
+                ok = wait_o_free(0);
+                if (!ok) break;
+              }
+              ok = issue_pv(0, c & 1, vit, true, t - 1 == 0);
               if (!ok) break;
-              waitedV = true;
-              if (t - 1 == ntile[j] - 1) umma_commit(&o_done[j]);
+              umma_commit(pv_done);
+              release(vit);
+              if (t - 1 == T - 1) {
+                umma_commit(&o_done[0]);
+                ++o_uses[0];
+              }
             }
-            if (t < ntile[j]) {
-              ok = issue_s(j, j, t, !waitedK);
-              if (!ok) break;
-              waitedK = true;
-              umma_commit(&s_full[j]);
-            }
-          }
-          if (!ok) break;
-          if (waitedV) release(t - 1, 1);
-          if (waitedK) release(t, 0);
-        } else {
-          // S(t) into slot t&1 (overlaps the softmax of tile t-1), then PV(t-1).
-          if (t < T) {
-            ok = issue_s(0, t & 1, t, true);
-            if (!ok) break;
-            umma_commit(&s_full[t & 1]);
-            release(t, 0);
-          }
-          if (t >= 1) {
-            ok = ATTN_MMA_WAIT(&p_full[(t - 1) & 1], ((t - 1) >> 1) & 1, 12);
-            if (!ok) break;
-            tc_fence_after();
-            ok = issue_pv(0, (t - 1) & 1, t - 1, true);
-            if (!ok) break;
-            umma_commit(pv_done);
-            release(t - 1, 1);
-            if (t - 1 == T - 1) umma_commit(&o_done[0]);
           }
         }
+        item0 += 2 * L::kH * T;
+        ++q_uses;
       }
-      if (!ok) report_error(6 /* ATTN_ERR_TIMEOUT */, 16, 0);
       // Every MMA this thread issued must be complete before TMEM is freed.
       umma_commit(mma_drain);
       mbar_wait(mma_drain, 0, 15);
@@ -326,135 +430,157 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
     const int j = (warp - 2) >> 2;           // query tile of this warpgroup
     const int quarter = warp & 3;            // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;     // row within the tile
-    const int r0 = q0 + j * kBM;
-    const int qrow = r0 + row;
-    const int nt = ntile[j];
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t o_cols = lane_base + j * D;
     const float sl = p.scale_log2;
-    // l sums the exact weights (for LSE); lr sums the bf16-rounded weights the
-    // P V product uses, so O = o / lr is an exact convex combination of V rows
-    // before output rounding.
-    float m_ref = -INFINITY;
-    float l0 = 0.f, l1 = 0.f, lr0 = 0.f, lr1 = 0.f;
+    const int diag = p.Nk - p.Nq;  // key j allowed for row i iff j <= i + diag (causal)
+    int cnt = 0;                   // tiles softmaxed so far (running S/P barrier phases)
+    int o_uses = 0;
     bool ok = true;
 
-    for (int t = 0; t < nt; ++t) {
-      const int slot = NQ == 2 ? j : (t & 1);
-      const uint32_t s_par = NQ == 2 ? (t & 1) : ((t >> 1) & 1);
-      ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(&s_full[slot], s_par, 20));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t r[kBN];
-      tmem_ld128(lane_base + L::kSCol + slot * kBN, r);
+    for (int n = 0; ok; ++n) {
+      int idx = lane == 0 ? next_unit(n, 23) : 0;
+      idx = __shfl_sync(0xFFFFFFFFu, idx, 0);
+      if (idx == -2) break;
+      if (lane == 0) mbar_arrive(&unit_empty[n % kUnitQ]);
+      if (idx < 0) break;
+      const Unit<NQ> u = unit_of<NQ>(p, idx);
+      const int r0 = u.q0 + j * kBM;
+      if (r0 >= p.Nq) continue;  // this query tile lies past Nq: nothing to write
+      const int qrow = r0 + row;
+      const int nt = u.ntile[j];
+      const int bh = u.bh;
+      // l sums the exact weights (for LSE); lr sums the bf16-rounded weights
+      // the P V product uses, so O = o / lr is an exact convex combination of
+      // V rows before output rounding.
+      float m_ref = -INFINITY;
+      float l0 = 0.f, l1 = 0.f, lr0 = 0.f, lr1 = 0.f;
 
-      // Row max of the raw scores (masked keys -> -inf); scale > 0 keeps the
-      // order, so the scaled max is mx * sl.
-      const int k0 = t * kBN;
-      const bool need_mask = (k0 + kBN > p.Nk) || (p.causal && (k0 + kBN - 1 > r0 + diag));
-      if (need_mask) {
-        const int lim = (p.causal ? min(p.Nk - 1, qrow + diag) : p.Nk - 1) - k0;
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c > lim) r[c] = 0xFF800000u;  // -inf
-      }
-      float mx[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kBN; c += 8) {
-        const int a = (c >> 3) & 3;
-        mx[a] = fmax3(mx[a], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
-        mx[a] = fmax3(mx[a], __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
-        mx[a] = fmax3(mx[a], __uint_as_float(r[c + 4]), __uint_as_float(r[c + 5]));
-        mx[a] = fmax3(mx[a], __uint_as_float(r[c + 6]), __uint_as_float(r[c + 7]));
-      }
-      const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * sl;
-      const float m_new = fmaxf(m_ref, mt);
-      const bool rescale = m_new > m_ref + kRescaleLog2;
-      float alpha = 1.f;
-      if (rescale) {
-        alpha = ex2(m_ref - m_new);  // 0 when m_ref = -inf
-        m_ref = m_new;
-        l0 *= alpha;
-        l1 *= alpha;
-        lr0 *= alpha;
-        lr1 *= alpha;
-      }
-      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      for (int t = 0; t < nt; ++t) {
+        const int slot = NQ == 2 ? j : (cnt & 1);
+        const uint32_t s_par = NQ == 2 ? (cnt & 1) : ((cnt >> 1) & 1);
+        ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(&s_full[slot], s_par, 20));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r[kBN];
+        tmem_ld128(lane_base + L::kSCol + slot * kBN, r);
 
-      // p = 2^(s * sl - m): P as bf16 pairs, exact and rounded row sums.
-      uint32_t pk[kBN / 2];
+        // Row max of the raw scores (masked keys -> -inf); scale > 0 keeps
+        // the order, so the scaled max is mx * sl.
+        const int k0 = t * kBN;
+        const bool need_mask = (k0 + kBN > p.Nk) || (p.causal && (k0 + kBN - 1 > r0 + diag));
+        if (need_mask) {
+          const int lim = (p.causal ? min(p.Nk - 1, qrow + diag) : p.Nk - 1) - k0;
 #pragma unroll
-      for (int c = 0; c < kBN; c += 2) {
-        float a0, a1;
-        ffma2(a0, a1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), sl, sl, neg_m, neg_m);
-        const float p0 = ex2(a0);
-        const float p1 = ex2(a1);
-        fadd2(l0, l1, l0, l1, p0, p1);
-        const uint32_t w = pack_bf16(p0, p1);
-        add_bf16x2(lr0, lr1, w);
-        pk[c >> 1] = w;
-      }
-
-      if (t > 0 && __any_sync(0xFFFFFFFFu, rescale)) {
-        if (NQ == 1) {
-          // O holds tile t-1's contribution only once PV(t-1) is complete.
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(pv_done, (t - 1) & 1, 21));
-          if (!ok) break;
-          tc_fence_after();
+          for (int cc = 0; cc < kBN; ++cc)
+            if (cc > lim) r[cc] = 0xFF800000u;  // -inf
         }
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(o_cols + c * 32, o);
+        float mx[4];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float y0, y1;
-            ffma2(y0, y1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha, 0.f, 0.f);
-            o[i] = __float_as_uint(y0);
-            o[i + 1] = __float_as_uint(y1);
+        for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
+#pragma unroll
+        for (int cc = 0; cc < kBN; cc += 8) {
+          const int a = (cc >> 3) & 3;
+          mx[a] = fmax3(mx[a], __uint_as_float(r[cc]), __uint_as_float(r[cc + 1]));
+          mx[a] = fmax3(mx[a], __uint_as_float(r[cc + 2]), __uint_as_float(r[cc + 3]));
+          mx[a] = fmax3(mx[a], __uint_as_float(r[cc + 4]), __uint_as_float(r[cc + 5]));
+          mx[a] = fmax3(mx[a], __uint_as_float(r[cc + 6]), __uint_as_float(r[cc + 7]));
+        }
+        const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * sl;
+        const float m_new = fmaxf(m_ref, mt);
+        const bool rescale = m_new > m_ref + kRescaleLog2;
+        float alpha = 1.f;
+        if (rescale) {
+          alpha = ex2(m_ref - m_new);  // 0 when m_ref = -inf
+          m_ref = m_new;
+          l0 *= alpha;
+          l1 *= alpha;
+          lr0 *= alpha;
+          lr1 *= alpha;
+        }
+        const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+
+        // p = 2^(s * sl - m): P as bf16 pairs, exact and rounded row sums.
+        uint32_t pk[kBN / 2];
+#pragma unroll
+        for (int cc = 0; cc < kBN; cc += 2) {
+          float a0, a1;
+          ffma2(a0, a1, __uint_as_float(r[cc]), __uint_as_float(r[cc + 1]), sl, sl, neg_m, neg_m);
+          const float p0 = ex2(a0);
+          const float p1 = ex2(a1);
+          fadd2(l0, l1, l0, l1, p0, p1);
+          const uint32_t w = pack_bf16(p0, p1);
+          add_bf16x2(lr0, lr1, w);
+          pk[cc >> 1] = w;
+        }
+
+        if (t > 0 && __any_sync(0xFFFFFFFFu, rescale)) {
+          if (NQ == 1) {
+            // O holds tile t-1's contribution only once PV(t-1) is complete;
+            // P V products are counted like the tiles (one per tile).
+            ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(pv_done, (cnt - 1) & 1, 21));
+            if (!ok) break;
+            tc_fence_after();
           }
-          tmem_st32(o_cols + c * 32, o);
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(o_cols + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float y0, y1;
+              ffma2(y0, y1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha, 0.f, 0.f);
+              o[i] = __float_as_uint(y0);
+              o[i + 1] = __float_as_uint(y1);
+            }
+            tmem_st32(o_cols + cc * 32, o);
+          }
         }
+        // P over the first half of the S slot, then hand it to the MMA thread.
+        tmem_st64(lane_base + L::kSCol + slot * kBN, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[slot]);
+        ++cnt;
       }
-      // P over the first half of the S slot, then hand it to the MMA thread.
-      tmem_st64(lane_base + L::kSCol + slot * kBN, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[slot]);
-    }
+      if (!ok) break;
 
-    if (ok && nt > 0) {
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&o_done[j], 0, 22));
-      if (ok) tc_fence_after();
-    }
-    // Every lane runs the (warp-collective) TMEM loads; only rows < Nq store.
-    const bool store = qrow < p.Nq;
-    if (ok) {
+      if (nt > 0) {
+        ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(&o_done[j], o_uses & 1, 22));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      // Every lane runs the (warp-collective) TMEM loads; only rows < Nq store.
+      const bool store = qrow < p.Nq;
       const float lr = lr0 + lr1;
       const float l = l0 + l1;
       const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
       const size_t row_off = (static_cast<size_t>(bh) * p.Nq + qrow) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         if (nt > 0) {
-          tmem_ld32(o_cols + c * 32, o);
+          tmem_ld32(o_cols + cc * 32, o);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0u;
         }
+        if (nt > 0 && cc == D / 32 - 1) {
+          // O_j has been read: the next unit's first P V may overwrite it.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&o_free[j]);
+        }
         if (!store) continue;
         if (p.o_f32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + row_off + c * 32);
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + row_off + cc * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
                                  __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
         } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + row_off + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + row_off + cc * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int e = 8 * i;
@@ -465,6 +591,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
           }
         }
       }
+      if (nt > 0) ++o_uses;
       if (store)
         p.lse[static_cast<size_t>(bh) * p.Nq + qrow] =
             (l > 0.f) ? (m_ref + lg2(l)) * 0.69314718055994531f : -INFINITY;
@@ -476,6 +603,15 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    // The last CTA to finish resets this launch's counters for a later launch.
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      p.sched[0] = 0;
+      p.sched[1] = 0;
+      __threadfence();
+    }
   }
 }
 
