@@ -103,6 +103,20 @@ struct PrefillLayout {
   static_assert(NQ == 1 || NQ == 2, "query tiles per CTA");
 };
 
+// Position of K(t) / V(t) in a unit's load order, in tile items (each of
+// kH ring stages).  With two query tiles the MMA thread consumes K(t), V(t),
+// K(t+1), ... in that order; with one query tile it computes S(t+1) before
+// P V(t), so it consumes K(0), K(1), V(0), K(2), V(1), ..., V(T-1) -- and the
+// producer loads in the same order, so the ring drains first in, first out.
+template <int NQ>
+__device__ __forceinline__ int k_pos(int t) {
+  return NQ == 2 ? 2 * t : (t == 0 ? 0 : 2 * t - 1);
+}
+template <int NQ>
+__device__ __forceinline__ int v_pos(int t, int T) {
+  return NQ == 2 ? 2 * t + 1 : (t == T - 1 ? 2 * T - 1 : 2 * t + 2);
+}
+
 // One work unit: its (batch, head) and first query row, and the key tiles each
 // of its query tiles needs (0 for a tile past Nq or fully masked).
 template <int NQ>
@@ -248,9 +262,22 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
             break;
           }
           mbar_expect_tx(&kv_full[st], L::kKVBytes);
-          const int t = i / (2 * L::kH);
-          const int kind = (i / L::kH) & 1;  // 0: K, 1: V
-          const int hh = i % L::kH;          // which 128-column part of the head dim
+          const int pos = i / L::kH;   // tile item in the unit's load order
+          const int hh = i % L::kH;    // which 128-column part of the head dim
+          int t, kind;                 // kind 0: K, 1: V
+          if (NQ == 2) {
+            t = pos >> 1;
+            kind = pos & 1;
+          } else if (pos == 0) {
+            t = 0;
+            kind = 0;
+          } else if (pos == 2 * u.T - 1) {
+            t = u.T - 1;
+            kind = 1;
+          } else {
+            kind = (pos & 1) ? 0 : 1;            // odd: K((pos+1)/2), even: V(pos/2 - 1)
+            t = kind == 0 ? (pos + 1) >> 1 : (pos >> 1) - 1;
+          }
           const CUtensorMap* map = kind ? &tmV : &tmK;
 #pragma unroll
           for (int c = 0; c < L::kDI / 64; ++c)
@@ -350,8 +377,8 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
         if (!ok) break;
         const int T = u.T;
         for (int t = 0; ok && t <= T; ++t) {
-          const int kit = item0 + t * 2 * L::kH;               // K(t)
-          const int vit = item0 + (t - 1) * 2 * L::kH + L::kH; // V(t-1)
+          const int kit = item0 + k_pos<NQ>(t) * L::kH;                      // K(t)
+          const int vit = item0 + (t >= 1 ? v_pos<NQ>(t - 1, T) : 0) * L::kH;  // V(t-1)
           if (NQ == 2) {
             // PV_A(t-1), S_A(t), PV_B(t-1), S_B(t); K/V items are waited for
             // by their first user and released after their last.
