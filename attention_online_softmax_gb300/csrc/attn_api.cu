@@ -327,10 +327,10 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   const bool two = pairs >= 2LL * sm_count();
   switch (d) {
     case 64:
-      return two ? launch_prefill<64, 2, 6>(mq, mk, mv, p, B * Hq, s) : launch_prefill<64, 1, 6>(mq, mk, mv, p, B * Hq, s);
+      return two ? launch_prefill<64, 2, 10>(mq, mk, mv, p, B * Hq, s) : launch_prefill<64, 1, 12>(mq, mk, mv, p, B * Hq, s);
     case 128:
-      return two ? launch_prefill<128, 2, 4>(mq, mk, mv, p, B * Hq, s)
-                 : launch_prefill<128, 1, 4>(mq, mk, mv, p, B * Hq, s);
+      return two ? launch_prefill<128, 2, 5>(mq, mk, mv, p, B * Hq, s)
+                 : launch_prefill<128, 1, 6>(mq, mk, mv, p, B * Hq, s);
     case 256: return launch_prefill<256, 1, 5>(mq, mk, mv, p, B * Hq, s);
   }
   return ATTN_ERR_UNSUPPORTED;
