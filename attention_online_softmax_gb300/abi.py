@@ -35,6 +35,8 @@ _lib.attn_decode_paged.restype = _i
 _lib.attn_decode_paged_static.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                           _i, ctypes.c_float, _i, _vp]
 _lib.attn_decode_paged_static.restype = _i
+_lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint32, _vp]
+_lib.attn_selftest_wait_timeout.restype = _i
 _lib.attn_get_device_status.argtypes = [_vp]
 _lib.attn_get_device_status.restype = _i
 _lib.attn_status_string.argtypes = [_i]
@@ -50,7 +52,8 @@ ATTN_F32 = 1
 
 #: every symbol include/attn.h declares
 EXPORTS = ("attn_fwd", "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_static",
-           "attn_get_device_status", "attn_status_string", "attn_launch_count", "attn_abi_version")
+           "attn_get_device_status", "attn_selftest_wait_timeout", "attn_status_string",
+           "attn_launch_count", "attn_abi_version")
 
 #: size of the scratch array built into the library for attn_decode_paged_static
 STATIC_SCRATCH_BYTES = 64 << 20
@@ -185,6 +188,12 @@ def attn_decode_paged_static(q, kcache, vcache, block_table, seqlens, o, lse, ma
                                        ATTN_F32 if o.dtype == torch.float32 else ATTN_BF16,
                                        _stream_ptr(stream))
     _check(st, "attn_decode_paged_static")
+
+
+def attn_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch the failure-detection self-test (a wait that must time out)."""
+    _check(_lib.attn_selftest_wait_timeout(int(limit_us), _stream_ptr(stream)),
+           "attn_selftest_wait_timeout")
 
 
 def attn_get_device_status(stream=None) -> int:

@@ -93,6 +93,18 @@ bool encode_page_map(CUtensorMap* map, const void* base, int d, int Hkv, int pag
   return r == CUDA_SUCCESS;
 }
 
+// One thread waits on a barrier with two expected arrivals after only one
+// arrived: the phase can never complete, so the bounded wait must give up.
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    attn::mbar_init(&bar, 2);
+    attn::fence_mbar_init();
+    attn::mbar_arrive(&bar);
+    attn::mbar_wait_for(&bar, 0, limit_ns, 99);
+  }
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
@@ -200,12 +212,26 @@ template <int D, int G>
 attn_status launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, attn::DecodeParams p,
                           cudaStream_t stream) {
   const int scores_bytes = p.hg * p.chunk * G * 4;
-  const int budget = 113 * 1024;  // two CTAs per SM
-  int stages = (budget - scores_bytes - 1024 - 2 * attn::kMaxStages * 8) / p.stage_bytes;
-  stages = stages < 2 ? 2 : (stages > 4 ? 4 : stages);
-  p.stages = stages;
-  const int smem = stages * p.stage_bytes + scores_bytes + 2 * attn::kMaxStages * 8 + 1024;
+  const int fixed = scores_bytes + 2 * attn::kMaxStages * 8 + 1024;
   auto ks = attn::decode_split_kernel<D, G>;
+  // Ring depth: two CTAs per SM when registers allow it (113 KB each), else
+  // one CTA per SM with a deeper ring, so that enough page bytes are in flight.
+  int stages = (113 * 1024 - fixed) / p.stage_bytes;
+  stages = stages < 2 ? 2 : (stages > 4 ? 4 : stages);
+  {
+    int per_sm = 0;
+    const int threads = (p.hg + 1) * 32;
+    if (cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ks, threads, stages * p.stage_bytes + fixed) ==
+            cudaSuccess &&
+        per_sm < 2) {
+      const int deep = (200 * 1024 - fixed) / p.stage_bytes;
+      stages = deep > attn::kMaxStages ? attn::kMaxStages : (deep < stages ? stages : deep);
+    }
+    cudaGetLastError();
+  }
+  p.stages = stages;
+  const int smem = stages * p.stage_bytes + fixed;
   if (cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
@@ -216,8 +242,22 @@ attn_status launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, attn::De
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (p.n_splits > 1) {
-    attn::decode_combine_kernel<D><<<dim3(p.num_seqs, (p.Hq + 3) / 4), 128, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+    // Programmatic dependent launch: the combine grid is scheduled while the
+    // split grid drains and waits (griddepcontrol.wait) for its partials.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_seqs, (p.Hq + 3) / 4);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, attn::decode_combine_kernel<D>, p) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }
   return ATTN_OK;
@@ -417,6 +457,17 @@ attn_status attn_decode_paged_static(const void* q, const void* kcache, const vo
   return attn_decode_paged(q, kcache, vcache, block_table, seqlens, o, lse, num_seqs, Hq, Hkv, d, page_size,
                            num_pages, max_pages_per_seq, max_seqlen, scale, scratch,
                            static_cast<size_t>(ATTN_STATIC_SCRATCH_BYTES), o_dtype, stream);
+}
+
+attn_status attn_selftest_wait_timeout(uint32_t limit_us, attn_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_INVALID_ARG;
+  attn_status st = check_device();
+  if (st != ATTN_OK) return st;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint64_t>(limit_us) * 1000ull);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return ATTN_OK;
 }
 
 attn_status attn_get_device_status(attn_stream_t stream) {

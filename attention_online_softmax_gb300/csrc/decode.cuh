@@ -325,12 +325,19 @@ __global__ void __launch_bounds__(288)
     }
   }
   __syncthreads();
+  // This CTA's partials are written: the combine kernel (launched as a
+  // programmatic dependent) may start once every CTA got here.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // One warp per (sequence, query head); lanes own D/32 consecutive elements.
+// Launched as a programmatic dependent of the split kernel: it waits on the
+// grid dependency before reading any partial.  Lane c computes the weight of
+// chunk c; the chunk rows are then read with several loads in flight.
 template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
   constexpr int E = D / 32;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int seq = blockIdx.x;
@@ -348,18 +355,36 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float wsum = 0.f;
-  for (int c = 0; c < ns; ++c) {
-    const size_t row = row0 + static_cast<size_t>(c) * p.Hq;
-    const float w = ex2((p.ws_lse[row] - m) * 1.4426950408889634f);
-    wsum += w;
-    const float* src = p.ws_o + row * D + lane * E;
+  for (int c0 = 0; c0 < ns; c0 += 32) {
+    const int cl = c0 + lane;
+    const float wl =
+        cl < ns ? ex2((p.ws_lse[row0 + static_cast<size_t>(cl) * p.Hq] - m) * 1.4426950408889634f) : 0.f;
+    wsum += wl;
+    const int nb = min(32, ns - c0);
+    for (int k = 0; k < nb; k += 4) {
+      float v[4][E];
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      const float2 v = *reinterpret_cast<const float2*>(src + e);
-      acc[e] = fmaf(w, v.x, acc[e]);
-      acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+      for (int u = 0; u < 4; ++u) {
+        const int c = min(c0 + k + u, ns - 1);  // in range; weight 0 past the end
+        const float* src = p.ws_o + (row0 + static_cast<size_t>(c) * p.Hq) * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          const float2 x = *reinterpret_cast<const float2*>(src + e);
+          v[u][e] = x.x;
+          v[u][e + 1] = x.y;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float w = __shfl_sync(0xFFFFFFFFu, wl, (k + u) & 31);
+        if (k + u >= nb) w = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
+      }
     }
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, off);
   const float inv = 1.f / wsum;
   const size_t off = (static_cast<size_t>(seq) * p.Hq + head) * D + lane * E;
   if (p.o_f32) {

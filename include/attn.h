@@ -163,6 +163,18 @@ ATTN_API attn_status attn_decode_paged_static(const void* q, const void* kcache,
  */
 ATTN_API attn_status attn_get_device_status(attn_stream_t stream);
 
+/*
+ * Failure-detection self-test (diagnostics, not part of the attention path).
+ * Launches one CTA whose thread waits on a shared-memory barrier that nothing
+ * will ever complete, using the same bounded-wait routine as the kernels but
+ * with a limit of `limit_us` microseconds (1..1000000).  The wait gives up,
+ * records ATTN_ERR_TIMEOUT in the device status word and the kernel returns,
+ * leaving the CUDA context usable.  Returns ATTN_OK once launched (read the
+ * outcome with attn_get_device_status), ATTN_ERR_INVALID_ARG for a limit out
+ * of range.  No GPU work waits on anything the host or another kernel does.
+ */
+ATTN_API attn_status attn_selftest_wait_timeout(uint32_t limit_us, attn_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 ATTN_API const char* attn_status_string(attn_status s);
 
