@@ -380,6 +380,12 @@ def main(argv=None):
     if not args.no_extra and rank == 0:
         extra = per_config_table(abi, dev, stream, peaks)
 
+    # Decode time floor: traffic at the measured bandwidth plus the launches
+    # and one DRAM round trip the two-kernel split/combine stage cannot avoid.
+    launch_s, dram_s = launch_and_latency_floor(dev, stream)
+    dec_kernels = 2 if ws_bytes > 0 else 1
+    dec_floor = dec_bytes / (peaks.hbm_gbs * 1e9) + dec_kernels * launch_s + dram_s
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         floor, t, th, desc, _ = oracle_sample(peaks, xp, xd, target_s=12.0)
@@ -399,7 +405,11 @@ def main(argv=None):
             "prefill": {"tflops": pre_tflops, "frac": pre_tflops * 1e12 / (peaks.bf16_tflops * 1e12),
                         "ms": mean_pre * 1e3, "floor_ms": f_pre * 1e3},
             "decode": {"gbs": dec_gbs, "frac": dec_gbs / peaks.hbm_gbs, "ms": mean_dec * 1e3,
-                       "floor_ms": f_dec * 1e3, "bytes": dec_bytes},
+                       "floor_ms": f_dec * 1e3, "bytes": dec_bytes,
+                       "time_floor": {"ms": dec_floor * 1e3, "traffic_ms": f_dec * 1e3,
+                                      "launch_us": launch_s * 1e6, "kernels": dec_kernels,
+                                      "dram_latency_us": dram_s * 1e6,
+                                      "measured_over_floor": mean_dec / dec_floor}},
             "roofline": {"bound": "tensor", "kernel": "prefill_fwd_kernel<128,128,4>",
                          "achieved": pre_tflops, "peak": peaks.bf16_tflops, "unit": "TFLOP/s",
                          "frac": pre_tflops / peaks.bf16_tflops, "peak_source": peak_src,
@@ -452,6 +462,43 @@ def profile_one(which: str, launches: int = 3) -> int:
     st = abi.attn_get_device_status()
     print(json.dumps({"profile": which, "launches": abi.attn_launch_count(), "status": st}))
     return 0 if st == 0 else 1
+
+
+def launch_and_latency_floor(dev, stream, reps: int = 200):
+    """Measured costs a GEMV-class stage cannot avoid beyond its traffic.
+
+    launch_s: back-to-back launch interval of a one-element kernel (the cost
+    each additional kernel in a dependent chain adds); dram_s: duration of one
+    kernel that reads and writes a single cold 4-byte word minus launch_s (one
+    DRAM round trip).  Used for the decode time floor: traffic at the measured
+    HBM bandwidth + launches * launch_s + dram_s ("Tang: a compiler that
+    derives GPU kernels ...": the time floor of a GEMV-class stage).
+    """
+    x = torch.zeros(1, device=dev)
+    for _ in range(20):
+        x.add_(1)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        x.add_(1)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launch_s = e0.elapsed_time(e1) * 1e-3 / reps
+    big = torch.zeros(64 << 20, dtype=torch.float32, device=dev)  # 256 MiB, larger than L2
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(20):
+        flush.zero_()  # evicts `big` from L2: the word read below comes from DRAM
+        idx = (i * 999983) % big.numel()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        big[idx:idx + 1].add_(1)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(f0.elapsed_time(f1) * 1e-3)
+    dram_s = max(0.0, statistics.median(ts) - launch_s)
+    return launch_s, dram_s
 
 
 def measure_e2e(abi, xp, xd, dev, stream, steps, floor_s, world):
