@@ -70,6 +70,11 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
                                                 i, i, ctypes.c_float, p, i,
                                                 p, p, i]
             lib.oracle_decode_paged.restype = i
+            i64 = ctypes.c_int64
+            lib.oracle_attention_masked.argtypes = [p, p, p, i, i, i, i, i, i, i,
+                                                    ctypes.c_float, i, p, p, i64, i64,
+                                                    p, i64, p, p, i]
+            lib.oracle_attention_masked.restype = i
             _LIBS[mutant] = lib
         return lib
 
@@ -124,6 +129,41 @@ def attention(q, k, v, causal: bool, scale: float, rows=None, threads: int = 0,
         _ptr(o), _ptr(lse), int(threads))
     if rc < 0:
         raise ValueError(f"oracle_attention rejected its arguments ({rc})")
+    if rows is None:
+        o = o.reshape(B, Hq, Nq, d)
+        lse = lse.reshape(B, Hq, Nq)
+    return o, lse, rc
+
+
+def attention_masked(q, k, v, causal: bool, scale: float, window_left: int = 0, alibi=None,
+                     bias=None, bias_strides=(0, 0), rows=None, threads: int = 0):
+    """Attention with the additive bias C = causal mask + left window + ALiBi
+    + dense bias (see oracle_attention_masked in attn_oracle.c), float64.
+
+    alibi: [Hq] float32 slopes or None; bias: bf16 tensor addressed as
+    bias[b*sb + h*sh + i*Nk + j] with bias_strides = (sb, sh) in elements, or
+    None.  Returns (O, LSE, threads) shaped like ``attention``.
+    """
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    B, Hq, Nq, d = qb.shape
+    _, Hkv, Nk, _ = kb.shape
+    al = None if alibi is None else np.ascontiguousarray(np.asarray(_host(alibi), dtype=np.float32))
+    bb = None if bias is None else _bits(bias).reshape(-1)
+    if rows is None:
+        nrows = B * Hq * Nq
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows_arr.size
+    o = np.empty((nrows, d), dtype=np.float64)
+    lse = np.empty((nrows,), dtype=np.float64)
+    rc = _load().oracle_attention_masked(
+        _ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
+        int(window_left), None if al is None else _ptr(al), None if bb is None else _ptr(bb),
+        int(bias_strides[0]), int(bias_strides[1]),
+        None if rows_arr is None else _ptr(rows_arr), nrows, _ptr(o), _ptr(lse), int(threads))
+    if rc < 0:
+        raise ValueError(f"oracle_attention_masked rejected its arguments ({rc})")
     if rows is None:
         o = o.reshape(B, Hq, Nq, d)
         lse = lse.reshape(B, Hq, Nq)

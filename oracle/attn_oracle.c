@@ -129,6 +129,104 @@ static int oracle_threads(int nthreads) {
 }
 
 /*
+ * Additive bias C of the attention definition, beyond the causal mask:
+ *   window_left > 0: key j is allowed for query i only if
+ *                    j > i + (Nk - Nq) - window_left;
+ *   alibi (may be NULL): adds alibi[h] * (j - i - (Nk - Nq)) to S_ij;
+ *   bias (may be NULL): bf16 bits, adds bias[b*sb + h*sh + i*Nk + j] to S_ij
+ *                       (-inf disallows the key).
+ * A key the mask disallows is left out; a row with no allowed key (or whose
+ * every allowed score is -inf) has O = 0 and LSE = -inf.
+ */
+static void attend_row_biased(const uint16_t* q, const uint16_t* const* krows,
+                              const uint16_t* const* vrows, int64_t n_keys, int d, double scale,
+                              const double* cbias, double* scratch, double* o, double* lse) {
+    int64_t j;
+    int c;
+    double m = -INFINITY;
+    for (j = 0; j < n_keys; ++j) {
+        double s = 0.0;
+        for (c = 0; c < d; ++c) s += bf16_to_double(q[c]) * bf16_to_double(krows[j][c]);
+        s = s * scale + cbias[j];
+        scratch[j] = s;
+        if (s > m) m = s;
+    }
+    for (c = 0; c < d; ++c) o[c] = 0.0;
+    if (m == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double l = 0.0;
+    for (j = 0; j < n_keys; ++j) {
+        double p = exp(scratch[j] - m);
+        l += p;
+        for (c = 0; c < d; ++c) o[c] += p * bf16_to_double(vrows[j][c]);
+    }
+    for (c = 0; c < d; ++c) o[c] /= l;
+    *lse = m + log(l);
+}
+
+int oracle_attention_masked(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                            int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                            float scale, int window_left, const float* alibi,
+                            const uint16_t* bias, int64_t bias_sb, int64_t bias_sh,
+                            const int64_t* rows, int64_t nrows,
+                            double* o_out, double* lse_out, int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0 || d <= 0 || window_left < 0) return -1;
+    if (Hq % Hkv != 0) return -1;
+    const int group = Hq / Hkv;
+    const int64_t total = (int64_t)B * Hq * Nq;
+    if (rows == NULL) nrows = total;
+    nthreads = oracle_threads(nthreads);
+    int bad = 0;
+#pragma omp parallel num_threads(nthreads)
+    {
+        const size_t cap = (size_t)(Nk > 0 ? Nk : 1);
+        double* scratch = (double*)malloc(sizeof(double) * cap);
+        double* cb = (double*)malloc(sizeof(double) * cap);
+        const uint16_t** krows = (const uint16_t**)malloc(sizeof(void*) * cap);
+        const uint16_t** vrows = (const uint16_t**)malloc(sizeof(void*) * cap);
+        int64_t r;
+#pragma omp for schedule(dynamic, 4)
+        for (r = 0; r < nrows; ++r) {
+            int64_t flat = rows ? rows[r] : r;
+            if (flat < 0 || flat >= total) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            int64_t i = flat % Nq;
+            int64_t bh = flat / Nq;
+            int64_t h = bh % Hq;
+            int64_t b = bh / Hq;
+            int64_t g = h / group;
+            int64_t diag = (int64_t)Nk - (int64_t)Nq;
+            const uint16_t* kb = k + ((b * Hkv + g) * (int64_t)Nk) * d;
+            const uint16_t* vb = v + ((b * Hkv + g) * (int64_t)Nk) * d;
+            int64_t n = 0, j;
+            for (j = 0; j < Nk; ++j) {
+                if (causal && j > i + diag) continue;
+                if (window_left > 0 && j <= i + diag - window_left) continue;
+                double c = 0.0;
+                if (alibi) c += (double)alibi[h] * (double)(j - i - diag);
+                if (bias) c += bf16_to_double(bias[b * bias_sb + h * bias_sh + i * (int64_t)Nk + j]);
+                krows[n] = kb + j * d;
+                vrows[n] = vb + j * d;
+                cb[n] = c;
+                ++n;
+            }
+            attend_row_biased(q + flat * d, krows, vrows, n, d, (double)scale, cb, scratch,
+                              o_out + r * d, lse_out + r);
+        }
+        free(scratch);
+        free(cb);
+        free(krows);
+        free(vrows);
+    }
+    return bad ? -2 : nthreads;
+}
+
+/*
  * Prefill / general attention.
  *   q: [B][Hq][Nq][d], k and v: [B][Hkv][Nk][d], all bf16 bits, contiguous.
  *   rows: flat query-row ids ((b*Hq + h)*Nq + i), or NULL for every row in
