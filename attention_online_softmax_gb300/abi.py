@@ -27,6 +27,16 @@ _vp = ctypes.c_void_p
 _i = ctypes.c_int
 _lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _vp]
 _lib.attn_fwd.restype = _i
+class AttnMask(ctypes.Structure):
+    """Mirror of attn_mask in include/attn.h."""
+    _fields_ = [("window_left", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("bias_stride_b", ctypes.c_longlong),
+                ("bias_stride_h", ctypes.c_longlong)]
+
+
+_lib.attn_fwd_masked.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, ctypes.c_float,
+                                 ctypes.POINTER(AttnMask), _i, _vp]
+_lib.attn_fwd_masked.restype = _i
 _lib.attn_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
 _lib.attn_decode_workspace_size.restype = ctypes.c_size_t
 _lib.attn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
@@ -51,7 +61,7 @@ ATTN_BF16 = 0
 ATTN_F32 = 1
 
 #: every symbol include/attn.h declares
-EXPORTS = ("attn_fwd", "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_static",
+EXPORTS = ("attn_fwd", "attn_fwd_masked", "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_static",
            "attn_get_device_status", "attn_selftest_wait_timeout", "attn_status_string",
            "attn_launch_count", "attn_abi_version")
 
@@ -127,6 +137,39 @@ def attn_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
                        int(bool(causal)), float(scale),
                        ATTN_F32 if o.dtype == torch.float32 else ATTN_BF16, _stream_ptr(stream))
     _check(st, "attn_fwd")
+
+
+def attn_fwd_masked(q, k, v, o, lse, causal: bool, scale: float, window_left: int = 0, alibi=None,
+                    bias=None, stream=None) -> None:
+    """attn_fwd with an additive bias: a left window, per-head ALiBi slopes
+    (CUDA float32 [Hq]) and/or a dense bf16 bias broadcastable to
+    [B, Hq, Nq, Nk] (its last two dimensions contiguous)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    _need(o, o.dtype, "o")
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nk, _ = k.shape
+    m = AttnMask(int(window_left), None, None, 0, 0)
+    if alibi is not None:
+        _need(alibi, torch.float32, "alibi")
+        if alibi.numel() != Hq:
+            raise ValueError("alibi must hold Hq slopes")
+        m.alibi_slopes = alibi.data_ptr()
+    if bias is not None:
+        if bias.dtype != torch.bfloat16 or not bias.is_cuda or bias.dim() != 4:
+            raise TypeError("bias must be a 4-D CUDA bfloat16 tensor")
+        if tuple(bias.shape[2:]) != (Nq, Nk) or (Nk > 1 and bias.stride(3) != 1) or \
+                (Nq > 1 and bias.stride(2) != Nk):
+            raise ValueError("bias must end in contiguous [Nq, Nk]")
+        m.bias = bias.data_ptr()
+        m.bias_stride_b = bias.stride(0) if bias.shape[0] == B else 0
+        m.bias_stride_h = bias.stride(1) if bias.shape[1] == Hq else 0
+    st = _lib.attn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                              int(bool(causal)), float(scale), ctypes.byref(m),
+                              ATTN_F32 if o.dtype == torch.float32 else ATTN_BF16, _stream_ptr(stream))
+    _check(st, "attn_fwd_masked")
 
 
 def attn_decode_workspace_size(num_seqs: int, Hq: int, Hkv: int, d: int, max_seqlen: int) -> int:

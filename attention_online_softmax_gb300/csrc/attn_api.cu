@@ -150,11 +150,11 @@ attn_status sched_slot(int** out) {
   return ATTN_OK;
 }
 
-template <int D, int NQ, int STAGES>
+template <int D, int NQ, int STAGES, bool BIAS = false>
 attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            attn::PrefillParams p, int BH, cudaStream_t stream) {
   using L = attn::PrefillLayout<D, NQ, STAGES>;
-  auto kern = attn::prefill_fwd_kernel<D, NQ, STAGES>;
+  auto kern = attn::prefill_fwd_kernel<D, NQ, STAGES, BIAS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
@@ -323,6 +323,18 @@ const char* attn_status_string(attn_status s) {
 
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                      int Nq, int Nk, int d, int causal, float scale, attn_dtype o_dtype, attn_stream_t stream) {
+  return attn_fwd_masked(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, nullptr, o_dtype, stream);
+}
+
+attn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                            int Hkv, int Nq, int Nk, int d, int causal, float scale, const attn_mask* mask,
+                            attn_dtype o_dtype, attn_stream_t stream) {
+  if (mask != nullptr) {
+    if (mask->window_left < 0 || mask->bias_stride_b < 0 || mask->bias_stride_h < 0) return ATTN_ERR_INVALID_ARG;
+    if ((mask->alibi_slopes != nullptr && (reinterpret_cast<uintptr_t>(mask->alibi_slopes) & 3u) != 0) ||
+        (mask->bias != nullptr && (reinterpret_cast<uintptr_t>(mask->bias) & 3u) != 0))
+      return ATTN_ERR_MISALIGNED;
+  }
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
@@ -360,11 +372,26 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.group = 1;
   p.sched = nullptr;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.window = mask ? mask->window_left : 0;
+  p.alibi = mask ? mask->alibi_slopes : nullptr;
+  p.bias = mask ? static_cast<const uint16_t*>(mask->bias) : nullptr;
+  p.bias_sb = mask ? mask->bias_stride_b : 0;
+  p.bias_sh = mask ? mask->bias_stride_h : 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // Two query tiles per CTA (they share every K/V tile and overlap each
   // other's softmax with MMAs) unless that leaves the GPU under-filled.
   const long long pairs = static_cast<long long>((Nq + 2 * attn::kBM - 1) / (2 * attn::kBM)) * B * Hq;
   const bool two = pairs >= 2LL * sm_count();
+  if (p.alibi != nullptr || p.bias != nullptr) {
+    // Additive-bias variants: one query tile per unit (the per-score bias
+    // terms need the registers a second tile's pipeline would take).
+    switch (d) {
+      case 64: return launch_prefill<64, 1, 12, true>(mq, mk, mv, p, B * Hq, s);
+      case 128: return launch_prefill<128, 1, 6, true>(mq, mk, mv, p, B * Hq, s);
+      case 256: return launch_prefill<256, 1, 5, true>(mq, mk, mv, p, B * Hq, s);
+      default: return ATTN_ERR_UNSUPPORTED;
+    }
+  }
   switch (d) {
     case 64:
       return two ? launch_prefill<64, 2, 10>(mq, mk, mv, p, B * Hq, s) : launch_prefill<64, 1, 12>(mq, mk, mv, p, B * Hq, s);

@@ -72,6 +72,11 @@ struct PrefillParams {
   int n_units;       // units per (batch, head): ceil(Nq / (128 * NQ))
   int group;         // (batch, head) pairs scheduled together, longest units first
   float scale_log2;  // scale * log2(e), > 0
+  // Additive bias C beyond the causal mask (all off in the plain call):
+  int window;                 // > 0: key j allowed only if j > i + (Nk - Nq) - window
+  const float* alibi;         // null or [Hq]: adds alibi[h] * (j - i - (Nk - Nq))
+  const uint16_t* bias;       // null or bf16 bias[b*bias_sb + h*bias_sh + i*Nk + j]
+  long long bias_sb, bias_sh;
 };
 
 template <int D, int NQ, int STAGES>
@@ -121,8 +126,9 @@ __device__ __forceinline__ int v_pos(int t, int T) {
 // of its query tiles needs (0 for a tile past Nq or fully masked).
 template <int NQ>
 struct Unit {
-  int bh, kvh, q0, T;
-  int ntile[NQ];
+  int bh, kvh, q0;
+  int tmin, T;           // key tiles loaded: [tmin, tmin + T)
+  int lo[NQ], hi[NQ];    // key tiles each query tile needs: [lo, hi), empty if lo >= hi
 };
 
 // Unit `idx` of the grouped longest-first order (0 <= idx < B*Hq*n_units).
@@ -142,22 +148,30 @@ __device__ __forceinline__ Unit<NQ> unit_of(const PrefillParams& p, int idx) {
   u.kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
   u.q0 = un * (kBM * NQ);
   const int diag = p.Nk - p.Nq;
-  u.T = 0;
+  int tmax = 0;
+  u.tmin = 0x7FFFFFFF;
 #pragma unroll
   for (int j = 0; j < NQ; ++j) {
     const int r0 = u.q0 + j * kBM;
-    int kend = 0;
+    int kbeg = 0, kend = 0;  // keys [kbeg, kend) some row of the tile may see
     if (r0 < p.Nq) {
       kend = p.Nk;
       if (p.causal) kend = min(p.Nk, min(r0 + kBM, p.Nq) - 1 + diag + 1);
+      if (p.window > 0) kbeg = max(0, r0 + diag - p.window + 1);
     }
-    u.ntile[j] = kend > 0 ? (kend + kBN - 1) / kBN : 0;
-    u.T = max(u.T, u.ntile[j]);
+    u.lo[j] = kbeg / kBN;
+    u.hi[j] = kend > kbeg ? (kend + kBN - 1) / kBN : u.lo[j];
+    if (u.hi[j] > u.lo[j]) {
+      u.tmin = min(u.tmin, u.lo[j]);
+      tmax = max(tmax, u.hi[j]);
+    }
   }
+  if (tmax == 0) u.tmin = 0;
+  u.T = tmax - u.tmin;
   return u;
 }
 
-template <int D, int NQ, int STAGES>
+template <int D, int NQ, int STAGES, bool BIAS>
 __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -282,7 +296,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < L::kDI / 64; ++c)
             tma_load_3d(smem + L::kKVOff + st * L::kKVBytes + c * (kBN * 128), map, &kv_full[st],
-                        hh * L::kDI + c * 64, t * kBN, u.kvh);
+                        hh * L::kDI + c * 64, (u.tmin + t) * kBN, u.kvh);
         }
       }
       // Drain: never leave the CTA with a copy still writing shared memory.
@@ -379,29 +393,30 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
         for (int t = 0; ok && t <= T; ++t) {
           const int kit = item0 + k_pos<NQ>(t) * L::kH;                      // K(t)
           const int vit = item0 + (t >= 1 ? v_pos<NQ>(t - 1, T) : 0) * L::kH;  // V(t-1)
+          const int ta = u.tmin + t;  // absolute key tile of S(t); PV is on tile ta - 1
           if (NQ == 2) {
             // PV_A(t-1), S_A(t), PV_B(t-1), S_B(t); K/V items are waited for
             // by their first user and released after their last.
             bool waitedV = false, waitedK = false;
 #pragma unroll
             for (int j = 0; j < NQ; ++j) {
-              if (t >= 1 && t - 1 < u.ntile[j]) {
+              if (t >= 1 && ta - 1 >= u.lo[j] && ta - 1 < u.hi[j]) {
                 ok = ATTN_MMA_WAIT(&p_full[j], (cnt[j] - 1) & 1, 12);
                 if (!ok) break;
                 tc_fence_after();
-                if (t - 1 == 0) {
+                if (ta - 1 == u.lo[j]) {
                   ok = wait_o_free(j);
                   if (!ok) break;
                 }
-                ok = issue_pv(j, j, vit, !waitedV, t - 1 == 0);
+                ok = issue_pv(j, j, vit, !waitedV, ta - 1 == u.lo[j]);
                 if (!ok) break;
                 waitedV = true;
-                if (t - 1 == u.ntile[j] - 1) {
+                if (ta - 1 == u.hi[j] - 1) {
                   umma_commit(&o_done[j]);
                   ++o_uses[j];
                 }
               }
-              if (t < u.ntile[j]) {
+              if (t < T && ta >= u.lo[j] && ta < u.hi[j]) {
                 ok = issue_s(j, j, kit, !waitedK);
                 if (!ok) break;
                 waitedK = true;
@@ -475,15 +490,27 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
       const int r0 = u.q0 + j * kBM;
       if (r0 >= p.Nq) continue;  // this query tile lies past Nq: nothing to write
       const int qrow = r0 + row;
-      const int nt = u.ntile[j];
+      const int nt = u.hi[j] > u.lo[j] ? u.hi[j] - u.lo[j] : 0;
       const int bh = u.bh;
+      // Biased path (ALiBi slopes and/or a dense bias): scores get an additive
+      // term before the max, so the max is taken over the biased, scaled
+      // scores.  In base 2: x = s * sl + (alibi * (j - i - diag) + bias) * log2(e).
+      constexpr bool biased = BIAS;  // instantiated separately: the plain path keeps its registers
+      const int hq = bh % p.Hq;
+      const float slope2 = p.alibi != nullptr ? p.alibi[hq] * 1.4426950408889634f : 0.f;
+      const uint16_t* brow = nullptr;
+      if (p.bias != nullptr && qrow < p.Nq)
+        brow = p.bias + static_cast<long long>(bh / p.Hq) * p.bias_sb + static_cast<long long>(hq) * p.bias_sh +
+               static_cast<long long>(qrow) * p.Nk;
+      const float mul = biased ? 1.f : sl;  // multiplier of r[] in the exponent
       // l sums the exact weights (for LSE); lr sums the bf16-rounded weights
       // the P V product uses, so O = o / lr is an exact convex combination of
       // V rows before output rounding.
       float m_ref = -INFINITY;
       float l0 = 0.f, l1 = 0.f, lr0 = 0.f, lr1 = 0.f;
 
-      for (int t = 0; t < nt; ++t) {
+      for (int ti = 0; ti < nt; ++ti) {
+        const int t = u.lo[j] + ti;  // absolute key tile
         const int slot = NQ == 2 ? j : (cnt & 1);
         const uint32_t s_par = NQ == 2 ? (cnt & 1) : ((cnt >> 1) & 1);
         ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(&s_full[slot], s_par, 20));
@@ -493,14 +520,45 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
         tmem_ld128(lane_base + L::kSCol + slot * kBN, r);
 
         // Row max of the raw scores (masked keys -> -inf); scale > 0 keeps
-        // the order, so the scaled max is mx * sl.
+        // the order, so the scaled max is mx * sl.  On the biased path r[]
+        // first becomes the biased, scaled score and the max is over that.
         const int k0 = t * kBN;
-        const bool need_mask = (k0 + kBN > p.Nk) || (p.causal && (k0 + kBN - 1 > r0 + diag));
+        if (biased) {
+          const float base = slope2 * static_cast<float>(k0 - qrow - diag);
+          if (brow != nullptr) {
+            // The row's bias for this tile, read as aligned 32-bit words (the
+            // bias buffer is 4-byte aligned; when the tile starts on an odd
+            // element the pairs straddle words and are re-paired by a funnel
+            // shift).  Words holding no element of this row's tile are not read.
+            const uint16_t* a = brow + k0;
+            const int odd = static_cast<int>((reinterpret_cast<uintptr_t>(a) >> 1) & 1u);
+            const uint32_t* wp = reinterpret_cast<const uint32_t*>(a - odd);
+            const int nvalid = p.Nk - k0;
+            uint32_t wv[kBN / 2 + 1];
+#pragma unroll
+            for (int i = 0; i <= kBN / 2; ++i) wv[i] = (2 * i - odd < nvalid) ? __ldg(wp + i) : 0u;
+#pragma unroll
+            for (int i = 0; i < kBN / 2; ++i) {
+              const uint32_t pr = __funnelshift_r(wv[i], wv[i + 1], 16u * odd);
+              const float b0 = fmaf(bf16lo(pr), 1.4426950408889634f, base + slope2 * static_cast<float>(2 * i));
+              const float b1 = fmaf(bf16hi(pr), 1.4426950408889634f, base + slope2 * static_cast<float>(2 * i + 1));
+              r[2 * i] = __float_as_uint(fmaf(__uint_as_float(r[2 * i]), sl, b0));
+              r[2 * i + 1] = __float_as_uint(fmaf(__uint_as_float(r[2 * i + 1]), sl, b1));
+            }
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < kBN; ++cc)
+              r[cc] = __float_as_uint(fmaf(__uint_as_float(r[cc]), sl, base + slope2 * static_cast<float>(cc)));
+          }
+        }
+        const bool need_mask = (k0 + kBN > p.Nk) || (p.causal && (k0 + kBN - 1 > r0 + diag)) ||
+                               (p.window > 0 && k0 <= r0 + kBM - 1 + diag - p.window);
         if (need_mask) {
-          const int lim = (p.causal ? min(p.Nk - 1, qrow + diag) : p.Nk - 1) - k0;
+          const int hi_c = (p.causal ? min(p.Nk - 1, qrow + diag) : p.Nk - 1) - k0;
+          const int lo_c = p.window > 0 ? qrow + diag - p.window + 1 - k0 : -1;
 #pragma unroll
           for (int cc = 0; cc < kBN; ++cc)
-            if (cc > lim) r[cc] = 0xFF800000u;  // -inf
+            if (cc > hi_c || cc < lo_c) r[cc] = 0xFF800000u;  // -inf
         }
         float mx[4];
 #pragma unroll
@@ -513,7 +571,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
           mx[a] = fmax3(mx[a], __uint_as_float(r[cc + 4]), __uint_as_float(r[cc + 5]));
           mx[a] = fmax3(mx[a], __uint_as_float(r[cc + 6]), __uint_as_float(r[cc + 7]));
         }
-        const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * sl;
+        const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * mul;
         const float m_new = fmaxf(m_ref, mt);
         const bool rescale = m_new > m_ref + kRescaleLog2;
         float alpha = 1.f;
@@ -532,7 +590,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
 #pragma unroll
         for (int cc = 0; cc < kBN; cc += 2) {
           float a0, a1;
-          ffma2(a0, a1, __uint_as_float(r[cc]), __uint_as_float(r[cc + 1]), sl, sl, neg_m, neg_m);
+          ffma2(a0, a1, __uint_as_float(r[cc]), __uint_as_float(r[cc + 1]), mul, mul, neg_m, neg_m);
           const float p0 = ex2(a0);
           const float p1 = ex2(a1);
           fadd2(l0, l1, l0, l1, p0, p1);
@@ -541,7 +599,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
           pk[cc >> 1] = w;
         }
 
-        if (t > 0 && __any_sync(0xFFFFFFFFu, rescale)) {
+        if (ti > 0 && __any_sync(0xFFFFFFFFu, rescale)) {
           if (NQ == 1) {
             // O holds tile t-1's contribution only once PV(t-1) is complete;
             // P V products are counted like the tiles (one per tile).

@@ -136,3 +136,27 @@ def decode_inputs(num_seqs: int, Hq: int, Hkv: int, d: int, len_lo: int, len_hi:
         scale = float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
     return DecodeInputs(q, kc, vc, bt, lens.to(torch.int32), float(scale), page_size,
                         int(lens.max().item()) if num_seqs else 0, g)
+
+
+def alibi_slopes(Hq: int) -> torch.Tensor:
+    """Per-head ALiBi slopes as float32 [Hq]: the geometric sequence
+    2^(-8 (h + 1) / Hq) of the ALiBi recipe (an input of the biased kernel,
+    not part of the attention arithmetic)."""
+    h = torch.arange(1, Hq + 1, dtype=torch.float64)
+    return torch.pow(2.0, -8.0 * h / Hq).to(torch.float32)
+
+
+def bias_inputs(shape, seed: int, std: float = 2.0, neg_inf_frac: float = 0.0,
+                neg_inf_rows: int = 0) -> torch.Tensor:
+    """A dense additive bias [Bb, Hb, Nq, Nk] as bf16 (Bb, Hb may be 1 for
+    broadcasting): ``std * randn`` from its own generator, then a random
+    ``neg_inf_frac`` of the entries set to -inf, then ``neg_inf_rows`` random
+    query rows of the first (batch, head) slice set to -inf entirely."""
+    g = torch.Generator("cpu").manual_seed(int(seed))
+    b = torch.randn(tuple(shape), generator=g, dtype=torch.float32) * std
+    if neg_inf_frac > 0:
+        b[torch.rand(tuple(shape), generator=g) < neg_inf_frac] = float("-inf")
+    if neg_inf_rows > 0:
+        rows = torch.randperm(shape[2], generator=g)[:neg_inf_rows]
+        b[0, 0, rows, :] = float("-inf")
+    return b.to(torch.bfloat16)

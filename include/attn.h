@@ -91,6 +91,37 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      float scale, attn_dtype o_dtype, attn_stream_t stream);
 
 /*
+ * Additive bias C beyond the causal mask ("Compilers and Kernels": S =
+ * Q K^T / sqrt(d) + C, C in R U {-inf}).  Every field may be left zero.
+ *   window_left:   > 0 keeps, for query i, only keys j > i + (Nk - Nq) - window_left
+ *                  (with causal: the window_left most recent keys up to the
+ *                  diagonal); key tiles wholly outside the window are skipped.
+ *   alibi_slopes:  NULL or a device [Hq] float32 array; adds
+ *                  alibi_slopes[h] * (j - i - (Nk - Nq)) to S_ij.
+ *   bias:          NULL or a device bf16 array read as
+ *                  bias[b*bias_stride_b + h*bias_stride_h + i*Nk + j] (strides in
+ *                  elements, 0 to broadcast); -inf disallows a key.  A dense bias
+ *                  costs one read of Nq*Nk values per (batch, head).
+ * alibi_slopes and bias must be 4-byte aligned.
+ */
+typedef struct {
+    int window_left;
+    const float* alibi_slopes;
+    const void* bias;
+    long long bias_stride_b;
+    long long bias_stride_h;
+} attn_mask;
+
+/*
+ * attn_fwd with the additive bias `mask` (NULL: same as attn_fwd).  A row
+ * whose keys are all disallowed (or all -inf after the bias) gets O = 0 and
+ * LSE = -inf.
+ */
+ATTN_API attn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                     float scale, const attn_mask* mask, attn_dtype o_dtype, attn_stream_t stream);
+
+/*
  * Bytes of scratch memory attn_decode_paged() needs for these sizes (the
  * split partials: one float32 O row and one float32 LSE per sequence, split
  * and query head).  Pure function of its arguments; 0 on invalid input.
