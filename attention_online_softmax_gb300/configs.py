@@ -22,6 +22,9 @@ class PrefillConfig:
     seed: int
     k_scale: float = 1.0
     check_rows_per_head: int | None = None  # None: every row
+    window: int = 0            # left window (0: none)
+    alibi: bool = False        # per-head ALiBi slopes
+    bias: str | None = None    # dense bias: None, "full" [B,Hq,Nq,Nk] or "batch" [1,Hq,Nq,Nk]
 
 
 @dataclass(frozen=True)
@@ -50,4 +53,11 @@ DECODE = DecodeConfig("paged_gqa32to8_decode_64seq_d128_len512to8192", 64, 32, 8
                       512, 8192, 40000, 16, 4)
 
 PREFILL_CONFIGS = (TINY, BLOCK, LONG, LONG_K4, GQA256)
-ALL = {c.name: c for c in PREFILL_CONFIGS + (DECODE,)}
+
+# Additive-bias workloads ("Compilers and Kernels": S = Q K^T / sqrt(d) + C).
+WINDOW = PrefillConfig("causal_window1024_b2_h32_n4096_d128", 2, 32, 32, 4096, 4096, 128, True, 5,
+                       check_rows_per_head=64, window=1024)
+ALIBI_BIAS = PrefillConfig("alibi_densebias_b1_h16_n2048_d128", 1, 16, 16, 2048, 2048, 128, False, 6,
+                           check_rows_per_head=64, alibi=True, bias="batch")
+MASKED_CONFIGS = (WINDOW, ALIBI_BIAS)
+ALL = {c.name: c for c in PREFILL_CONFIGS + MASKED_CONFIGS + (DECODE,)}

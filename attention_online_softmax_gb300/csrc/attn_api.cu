@@ -75,6 +75,30 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int d, int rows, int he
   return r == CUDA_SUCCESS;
 }
 
+// 4-D bf16 map over a dense bias [Bb][Hb][Nq][Nk] (Bb, Hb = 1 when broadcast);
+// one box is [128 query rows][64 keys], 128-byte swizzled.  Strides in
+// elements; false when the layout does not meet the TMA rules (16-byte
+// aligned base and row / head / batch strides).
+bool encode_bias_map(CUtensorMap* map, const void* base, int Nq, int Nk, int Hb, int Bb, long long sh,
+                     long long sb) {
+  auto fn = encode_fn();
+  if (!fn || !aligned16(base) || Nk % 8 != 0) return false;
+  const long long plane = static_cast<long long>(Nq) * Nk;
+  const long long s2 = Hb > 1 ? sh : plane;
+  const long long s3 = Bb > 1 ? sb : s2 * Hb;
+  if (s2 % 8 != 0 || s3 % 8 != 0 || s2 <= 0 || s3 <= 0) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(Nk), static_cast<cuuint64_t>(Nq), static_cast<cuuint64_t>(Hb),
+                        static_cast<cuuint64_t>(Bb)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(Nk) * 2, static_cast<cuuint64_t>(s2) * 2,
+                           static_cast<cuuint64_t>(s3) * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(attn::kBM), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 4-D bf16 map over the paged cache [pages][slots][Hkv][d]; one box is the
 // [16 slots][hg heads][d] block of one page (no swizzle).
 bool encode_page_map(CUtensorMap* map, const void* base, int d, int Hkv, int page_size, int num_pages, int hg) {
@@ -150,10 +174,10 @@ attn_status sched_slot(int** out) {
   return ATTN_OK;
 }
 
-template <int D, int NQ, int STAGES, bool BIAS = false>
+template <int D, int NQ, int STAGES, int BIAS = 0>
 attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                           attn::PrefillParams p, int BH, cudaStream_t stream) {
-  using L = attn::PrefillLayout<D, NQ, STAGES>;
+                           const CUtensorMap& mb, attn::PrefillParams p, int BH, cudaStream_t stream) {
+  using L = attn::PrefillLayout<D, NQ, STAGES, attn::bias_slots<BIAS>()>;
   auto kern = attn::prefill_fwd_kernel<D, NQ, STAGES, BIAS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
     cudaGetLastError();
@@ -170,7 +194,7 @@ attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const C
   if (st != ATTN_OK) return st;
   // Persistent: one CTA per SM (or fewer when there are fewer units).
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
-  kern<<<dim3(grid), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
+  kern<<<dim3(grid), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mb, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return ATTN_OK;
@@ -377,28 +401,49 @@ attn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o
   p.bias = mask ? static_cast<const uint16_t*>(mask->bias) : nullptr;
   p.bias_sb = mask ? mask->bias_stride_b : 0;
   p.bias_sh = mask ? mask->bias_stride_h : 0;
+  p.bias_hmul = 0;
+  p.bias_bmul = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // Two query tiles per CTA (they share every K/V tile and overlap each
   // other's softmax with MMAs) unless that leaves the GPU under-filled.
   const long long pairs = static_cast<long long>((Nq + 2 * attn::kBM - 1) / (2 * attn::kBM)) * B * Hq;
   const bool two = pairs >= 2LL * sm_count();
+  if (p.bias != nullptr && Nk > 0) {
+    // A dense bias whose layout TMA can tile is staged into shared memory by
+    // the producer (coalesced, asynchronous); any other layout is read by the
+    // softmax threads directly.
+    const int Hb = p.bias_sh != 0 ? Hq : 1;
+    const int Bb = p.bias_sb != 0 ? B : 1;
+    CUtensorMap mb;
+    if (encode_bias_map(&mb, p.bias, Nq, Nk, Hb, Bb, p.bias_sh, p.bias_sb)) {
+      p.bias_hmul = Hb > 1 ? 1 : 0;
+      p.bias_bmul = Bb > 1 ? 1 : 0;
+      switch (d) {
+        case 64: return launch_prefill<64, 1, 8, 2>(mq, mk, mv, mb, p, B * Hq, s);
+        case 128: return launch_prefill<128, 1, 4, 2>(mq, mk, mv, mb, p, B * Hq, s);
+        case 256: return launch_prefill<256, 1, 3, 2>(mq, mk, mv, mb, p, B * Hq, s);
+        default: return ATTN_ERR_UNSUPPORTED;
+      }
+    }
+  }
   if (p.alibi != nullptr || p.bias != nullptr) {
     // Additive-bias variants: one query tile per unit (the per-score bias
     // terms need the registers a second tile's pipeline would take).
     switch (d) {
-      case 64: return launch_prefill<64, 1, 12, true>(mq, mk, mv, p, B * Hq, s);
-      case 128: return launch_prefill<128, 1, 6, true>(mq, mk, mv, p, B * Hq, s);
-      case 256: return launch_prefill<256, 1, 5, true>(mq, mk, mv, p, B * Hq, s);
+      case 64: return launch_prefill<64, 1, 12, 1>(mq, mk, mv, mq, p, B * Hq, s);
+      case 128: return launch_prefill<128, 1, 6, 1>(mq, mk, mv, mq, p, B * Hq, s);
+      case 256: return launch_prefill<256, 1, 5, 1>(mq, mk, mv, mq, p, B * Hq, s);
       default: return ATTN_ERR_UNSUPPORTED;
     }
   }
   switch (d) {
     case 64:
-      return two ? launch_prefill<64, 2, 10>(mq, mk, mv, p, B * Hq, s) : launch_prefill<64, 1, 12>(mq, mk, mv, p, B * Hq, s);
+      return two ? launch_prefill<64, 2, 10>(mq, mk, mv, mq, p, B * Hq, s)
+                 : launch_prefill<64, 1, 12>(mq, mk, mv, mq, p, B * Hq, s);
     case 128:
-      return two ? launch_prefill<128, 2, 5>(mq, mk, mv, p, B * Hq, s)
-                 : launch_prefill<128, 1, 6>(mq, mk, mv, p, B * Hq, s);
-    case 256: return launch_prefill<256, 1, 5>(mq, mk, mv, p, B * Hq, s);
+      return two ? launch_prefill<128, 2, 5>(mq, mk, mv, mq, p, B * Hq, s)
+                 : launch_prefill<128, 1, 6>(mq, mk, mv, mq, p, B * Hq, s);
+    case 256: return launch_prefill<256, 1, 5>(mq, mk, mv, mq, p, B * Hq, s);
   }
   return ATTN_ERR_UNSUPPORTED;
 }

@@ -77,11 +77,14 @@ struct PrefillParams {
   const float* alibi;         // null or [Hq]: adds alibi[h] * (j - i - (Nk - Nq))
   const uint16_t* bias;       // null or bf16 bias[b*bias_sb + h*bias_sh + i*Nk + j]
   long long bias_sb, bias_sh;
+  int bias_hmul, bias_bmul;   // staged bias: head / batch coordinate multipliers (0: broadcast)
 };
 
-template <int D, int NQ, int STAGES>
+template <int D, int NQ, int STAGES, int BSLOTS = 0>
 struct PrefillLayout {
-  static constexpr int kThreads = 64 + 128 * NQ;
+  // warp 0 TMA producer, warp 1 MMA issuer, 4 softmax warps per query tile,
+  // and with a staged bias one more warp that loads the bias tiles.
+  static constexpr int kThreads = 64 + 128 * NQ + (BSLOTS > 0 ? 32 : 0);
   static constexpr int kQBytes = kBM * D * 2;
   // K and V tiles stream in items of up to 128 head-dim columns (kH items per
   // tile), so with d = 256 a 64 KB tile occupies two 32 KB ring stages and
@@ -91,10 +94,15 @@ struct PrefillLayout {
   static constexpr int kKVBytes = kBN * kDI * 2; // one ring stage
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + NQ * kQBytes;
-  static constexpr int kBarOff = kKVOff + STAGES * kKVBytes;
+  // Staged dense bias: BSLOTS slots of one 128 x 128 bf16 tile each, as two
+  // 128-byte-swizzled [128 rows][64 keys] boxes.
+  static constexpr int kBiasBytes = kBM * kBN * 2;
+  static constexpr int kBiasOff = kKVOff + STAGES * kKVBytes;
+  static constexpr int kBarOff = kBiasOff + BSLOTS * kBiasBytes;
   // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done,
-  // o_done[2], o_free[2], unit_full[Q], unit_empty[Q], mma_drain
-  static constexpr int kNumBars = 2 + 2 * STAGES + 2 + 2 + 1 + 2 + 2 + 2 * kUnitQ + 1;
+  // o_done[2], o_free[2], unit_full[Q], unit_empty[Q], mma_drain,
+  // bias_full[BSLOTS], bias_empty[BSLOTS]
+  static constexpr int kNumBars = 2 + 2 * STAGES + 2 + 2 + 1 + 2 + 2 + 2 * kUnitQ + 1 + 2 * BSLOTS;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, unit queue
   static constexpr int kBytes = kMiscOff + 16 + 4 * kUnitQ;
   // Dynamic shared memory requested: at least 115 KB so that no second CTA
@@ -171,11 +179,21 @@ __device__ __forceinline__ Unit<NQ> unit_of(const PrefillParams& p, int idx) {
   return u;
 }
 
-template <int D, int NQ, int STAGES, bool BIAS>
-__global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
+// BIAS: 0 no additive bias beyond causal / window masks; 1 ALiBi slopes and/or
+// a dense bias read by the softmax threads from global memory; 2 the dense
+// bias staged tile by tile into shared memory by the producer (tmB).
+template <int BIAS>
+__host__ __device__ constexpr int bias_slots() { return BIAS == 2 ? 2 : 0; }
+template <int BIAS>
+__host__ __device__ constexpr int bias_ring() { return BIAS == 2 ? 2 : 1; }  // modulus (never 0)
+
+template <int D, int NQ, int STAGES, int BIAS>
+__global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>()>::kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
-  using L = PrefillLayout<D, NQ, STAGES>;
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
+                       const PrefillParams p) {
+  using L = PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>()>;
+  static_assert(BIAS == 0 || NQ == 1, "additive-bias variants run one query tile per unit");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -194,6 +212,8 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
   uint64_t* unit_full = o_free + 2;
   uint64_t* unit_empty = unit_full + kUnitQ;
   uint64_t* mma_drain = unit_empty + kUnitQ;
+  uint64_t* bias_full = mma_drain + 1;
+  uint64_t* bias_empty = bias_full + bias_slots<BIAS>();
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* unit_q = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 16);
 
@@ -216,10 +236,15 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
     }
     for (int i = 0; i < kUnitQ; ++i) {
       mbar_init(&unit_full[i], 1);
-      mbar_init(&unit_empty[i], 1 + 4 * NQ);  // MMA thread + lane 0 of every softmax warp
+      // MMA thread + lane 0 of every softmax warp (+ the bias loader)
+      mbar_init(&unit_empty[i], 1 + 4 * NQ + (BIAS == 2 ? 1 : 0));
     }
     mbar_init(pv_done, 1);
     mbar_init(mma_drain, 1);
+    for (int i = 0; i < bias_slots<BIAS>(); ++i) {
+      mbar_init(&bias_full[i], 1);
+      mbar_init(&bias_empty[i], 4);  // lane 0 of every softmax warp
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -303,6 +328,40 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
       if (q_uses > 0) mbar_wait(q_full, (q_uses - 1) & 1, 2);
       for (int it = max(0, item - STAGES); it < item; ++it)
         mbar_wait(&kv_full[it % STAGES], (it / STAGES) & 1, 3);
+
+    }
+    __syncwarp();
+  } else if (BIAS == 2 && warp == 2 + 4 * NQ) {
+    // ---------------------------------------------------------------- bias loader
+    // The bias tile of (query tile, key tile t), in the order the softmax
+    // threads consume them; its own ring, so the K/V stream never waits on it.
+    if (lane == 0) {
+      tma_prefetch_desc(&tmB);
+      int bitem = 0;
+      bool ok = true;
+      for (int n = 0; ok; ++n) {
+        const int idx = next_unit(n, 25);
+        if (idx == -2) break;
+        mbar_arrive(&unit_empty[n % kUnitQ]);
+        if (idx < 0) break;
+        const Unit<NQ> u = unit_of<NQ>(p, idx);
+        const int b = u.bh / p.Hq;
+        const int h = u.bh - b * p.Hq;
+        for (int t = u.lo[0]; t < u.hi[0]; ++t, ++bitem) {
+          const int bs = bitem % bias_ring<BIAS>();
+          if (!mbar_wait(&bias_empty[bs], ((bitem / bias_ring<BIAS>()) & 1) ^ 1, 6)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&bias_full[bs], L::kBiasBytes);
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(smem + L::kBiasOff + bs * L::kBiasBytes + c * (kBM * 128), &tmB, &bias_full[bs],
+                        t * kBN + c * 64, u.q0, h * p.bias_hmul, b * p.bias_bmul);
+        }
+      }
+      for (int it = max(0, bitem - bias_ring<BIAS>()); it < bitem; ++it)
+        mbar_wait(&bias_full[it % bias_ring<BIAS>()], (it / bias_ring<BIAS>()) & 1, 7);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -477,6 +536,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
     const float sl = p.scale_log2;
     const int diag = p.Nk - p.Nq;  // key j allowed for row i iff j <= i + diag (causal)
     int cnt = 0;                   // tiles softmaxed so far (running S/P barrier phases)
+    int bcnt = 0;                  // staged bias tiles consumed so far
     int o_uses = 0;
     bool ok = true;
 
@@ -495,11 +555,11 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
       // Biased path (ALiBi slopes and/or a dense bias): scores get an additive
       // term before the max, so the max is taken over the biased, scaled
       // scores.  In base 2: x = s * sl + (alibi * (j - i - diag) + bias) * log2(e).
-      constexpr bool biased = BIAS;  // instantiated separately: the plain path keeps its registers
+      constexpr bool biased = BIAS != 0;  // instantiated separately: the plain path keeps its registers
       const int hq = bh % p.Hq;
       const float slope2 = p.alibi != nullptr ? p.alibi[hq] * 1.4426950408889634f : 0.f;
       const uint16_t* brow = nullptr;
-      if (p.bias != nullptr && qrow < p.Nq)
+      if (BIAS == 1 && p.bias != nullptr && qrow < p.Nq)
         brow = p.bias + static_cast<long long>(bh / p.Hq) * p.bias_sb + static_cast<long long>(hq) * p.bias_sh +
                static_cast<long long>(qrow) * p.Nk;
       const float mul = biased ? 1.f : sl;  // multiplier of r[] in the exponent
@@ -523,7 +583,32 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES>::kThreads, 1)
         // the order, so the scaled max is mx * sl.  On the biased path r[]
         // first becomes the biased, scaled score and the max is over that.
         const int k0 = t * kBN;
-        if (biased) {
+        if (BIAS == 2) {
+          // Row `row` of the staged bias tile: 16 chunks of 8 keys, chunk c of
+          // a 128-byte row at position c ^ (row & 7) (the TMA 128-byte
+          // swizzle), so the 8 rows of each quarter-warp phase hit distinct banks.
+          const float base = slope2 * static_cast<float>(k0 - qrow - diag);
+          const int bs = bcnt % bias_ring<BIAS>();
+          ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(&bias_full[bs], (bcnt / bias_ring<BIAS>()) & 1, 24));
+          if (!ok) break;
+          const uint32_t brow_s = sbase + L::kBiasOff + bs * L::kBiasBytes + row * 128;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const uint4 w = ld_shared_v4(brow_s + (c >> 3) * (kBM * 128) + (((c & 7) ^ (row & 7)) << 4));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int cc = c * 8 + 2 * e;
+              const float b0 = fmaf(bf16lo(ws[e]), 1.4426950408889634f, base + slope2 * static_cast<float>(cc));
+              const float b1 = fmaf(bf16hi(ws[e]), 1.4426950408889634f, base + slope2 * static_cast<float>(cc + 1));
+              r[cc] = __float_as_uint(fmaf(__uint_as_float(r[cc]), sl, b0));
+              r[cc + 1] = __float_as_uint(fmaf(__uint_as_float(r[cc + 1]), sl, b1));
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bias_empty[bs]);
+          ++bcnt;
+        } else if (biased) {
           const float base = slope2 * static_cast<float>(k0 - qrow - diag);
           if (brow != nullptr) {
             // The row's bias for this tile, read as aligned 32-bit words (the

@@ -36,6 +36,23 @@ def prefill_flops(B: int, Hq: int, Nq: int, Nk: int, d: int, causal: bool) -> fl
     return f / 2.0 if causal else f
 
 
+def allowed_pairs(Nq: int, Nk: int, causal: bool, window: int = 0) -> int:
+    """Number of (query, key) pairs the mask allows in one (batch, head):
+    row i sees keys [max(0, i + Nk - Nq - window + 1), min(Nk - 1, i + Nk - Nq)]
+    (the lower end only with a window, the upper only when causal)."""
+    import numpy as np
+    i = np.arange(Nq, dtype=np.int64)
+    diag = Nk - Nq
+    hi = np.minimum(Nk - 1, i + diag) if causal else np.full(Nq, Nk - 1, dtype=np.int64)
+    lo = np.maximum(0, i + diag - window + 1) if window > 0 else np.zeros(Nq, dtype=np.int64)
+    return int(np.clip(hi - lo + 1, 0, None).sum())
+
+
+def masked_flops(B: int, Hq: int, Nq: int, Nk: int, d: int, causal: bool, window: int = 0) -> float:
+    """4 d flops (two d-long dot products, multiply + add) per allowed pair."""
+    return 4.0 * B * Hq * d * allowed_pairs(Nq, Nk, causal, window)
+
+
 def prefill_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:
     q = B * Hq * Nq * d * BF16
     kv = 2 * B * Hkv * Nk * d * BF16

@@ -175,6 +175,16 @@ def make_prefill_inputs(c=configs.LONG):
                                  k_scale=c.k_scale)
 
 
+def make_mask_inputs(c):
+    """ALiBi slopes and dense bias of an additive-bias workload (None when unused)."""
+    slopes = inputs.alibi_slopes(c.Hq) if c.alibi else None
+    bias = None
+    if c.bias is not None:
+        shape = (c.B if c.bias == "full" else 1, c.Hq, c.Nq, c.Nk)
+        bias = inputs.bias_inputs(shape, seed=c.seed + 100)
+    return slopes, bias
+
+
 def floors(peaks, pre_flops, pre_bytes, dec_flops, dec_bytes):
     f_pre = roofline.time_floor_s(pre_flops, pre_bytes, peaks)
     f_dec = roofline.time_floor_s(dec_flops, dec_bytes, peaks)
@@ -571,6 +581,39 @@ def per_config_table(abi, dev, stream, peaks, reps: int = 10):
                        "frac_of_bound": fl / t / bound, "p10_us": sorted(ts)[len(ts) // 10] * 1e6,
                        "p90_us": sorted(ts)[(9 * len(ts)) // 10] * 1e6}
         del q, k, v, o, lse
+    for c in configs.MASKED_CONFIGS:
+        x = make_prefill_inputs(c)
+        q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        slopes, bias = make_mask_inputs(c)
+        slopes = None if slopes is None else slopes.to(dev)
+        bias = None if bias is None else bias.to(dev)
+
+        def call():
+            abi.attn_fwd_masked(q, k, v, o, lse, c.causal, x.scale, window_left=c.window, alibi=slopes,
+                                bias=bias, stream=stream)
+        for _ in range(3):
+            call()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        t = statistics.median(ts)
+        fl = roofline.masked_flops(c.B, c.Hq, c.Nq, c.Nk, c.d, c.causal, c.window)
+        by = roofline.prefill_bytes(c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d)
+        if bias is not None:
+            by += bias.numel() * 2
+        bound = roofline.bound_rate(fl, by, peaks)
+        out[c.name] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_of_peak": fl / t / (peaks.bf16_tflops * 1e12),
+                       "frac_of_bound": fl / t / bound, "flops": "4 d per allowed (query, key) pair",
+                       "p10_us": sorted(ts)[len(ts) // 10] * 1e6, "p90_us": sorted(ts)[(9 * len(ts)) // 10] * 1e6}
+        del q, k, v, o, lse, slopes, bias
     torch.cuda.empty_cache()
     return out
 

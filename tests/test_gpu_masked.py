@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from attention_online_softmax_gb300 import inputs
+from attention_online_softmax_gb300 import configs, inputs
 from test_gpu_parity import compare
 
 pytestmark = pytest.mark.gpu
@@ -77,6 +77,13 @@ MASKED = [
     (1, 2, 2, 150, 150, 256, True, 64, True, "batch", 0.0),    # all terms, d = 256
     (1, 2, 2, 300, 77, 128, True, 20, True, "full", 0.0),      # Nq > Nk: rows without keys
     (1, 4, 4, 513, 1025, 64, False, 300, True, "both", 0.02),  # all terms, d = 64, ragged
+    # Nk a multiple of 8: the bias is staged into shared memory by TMA
+    (1, 2, 2, 200, 304, 128, False, 0, False, "full", 0.05),
+    (2, 3, 3, 130, 64, 64, False, 0, False, "head", 0.0),      # one partial key tile
+    (2, 2, 1, 129, 256, 128, True, 0, False, "batch", 0.1),
+    (1, 2, 2, 152, 152, 256, True, 64, True, "batch", 0.0),
+    (1, 4, 4, 513, 1024, 64, False, 300, True, "both", 0.02),
+    (1, 2, 2, 300, 80, 128, True, 20, True, "full", 0.0),
 ]
 
 
@@ -91,13 +98,41 @@ def test_masked_prefill(abi, case):
     check_masked(abi, x, window, slopes, bias)
 
 
-def test_bias_rows_all_minus_inf(abi):
+@pytest.mark.parametrize("Nk", [300, 296])  # direct and staged bias reads
+def test_bias_rows_all_minus_inf(abi, Nk):
     # Query rows whose bias is -inf for every key: O = 0, LSE = -inf.
-    B, Hq, Nq, Nk, d = 1, 2, 260, 300, 128
+    B, Hq, Nq, d = 1, 2, 260, 128
     x = inputs.prefill_inputs(B, Hq, Hq, Nq, Nk, d, seed=4200, causal=False)
     bias = inputs.bias_inputs((B, Hq, Nq, Nk), seed=4201, neg_inf_rows=5)
     _, lse_ref = check_masked(abi, x, bias=bias)
     assert np.isneginf(lse_ref).sum() == 5
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_staged_and_direct_bias_reads_agree(abi, d):
+    # The same bias through the shared-memory staging path (16-byte aligned
+    # copy) and through direct loads (a copy 4 bytes off the 16-byte grid)
+    # gives bitwise the same result: both add the same terms in the same order.
+    B, Hq, Nq, Nk = 1, 2, 300, 512
+    x = inputs.prefill_inputs(B, Hq, Hq, Nq, Nk, d, seed=4250 + d, causal=True)
+    bias = inputs.bias_inputs((B, Hq, Nq, Nk), seed=4251, neg_inf_frac=0.05)
+    dev = torch.device("cuda")
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    aligned = bias.to(dev)
+    raw = torch.empty(bias.numel() + 8, dtype=torch.bfloat16, device=dev)
+    off = raw[2:2 + bias.numel()].view(bias.shape)  # 4-byte aligned, not 16
+    off.copy_(aligned)
+    assert off.data_ptr() % 16 != 0 and aligned.data_ptr() % 16 == 0
+    slopes = inputs.alibi_slopes(Hq).to(dev)
+    outs = []
+    for b in (aligned, off):
+        o = torch.empty((B, Hq, Nq, d), dtype=torch.float32, device=dev)
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+        abi.attn_fwd_masked(q, k, v, o, lse, True, x.scale, window_left=400, alibi=slopes, bias=b)
+        outs.append((o, lse))
+    torch.cuda.synchronize()
+    assert abi.attn_get_device_status() == 0
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
 def test_two_tile_units_with_window(abi):
@@ -134,3 +169,26 @@ def test_masked_arguments_rejected(abi):
     misaligned = raw[1:].view(1, 2, 64, 64)  # 2-byte aligned only
     with pytest.raises(abi.AttnError):
         abi.attn_fwd_masked(q, k, v, o, lse, False, x.scale, bias=misaligned)
+
+
+@pytest.mark.parametrize("cfg", configs.MASKED_CONFIGS, ids=lambda c: c.name)
+def test_masked_configs(abi, cfg):
+    # The additive-bias workloads the benchmark times, on a seeded row subset.
+    x = inputs.prefill_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.Nq, cfg.Nk, cfg.d, cfg.seed, cfg.causal)
+    rows = inputs.check_rows(x.generator, cfg.B, cfg.Hq, cfg.Nq, cfg.check_rows_per_head)
+    slopes = inputs.alibi_slopes(cfg.Hq) if cfg.alibi else None
+    bias = None
+    if cfg.bias is not None:
+        shape = (cfg.B if cfg.bias == "full" else 1, cfg.Hq, cfg.Nq, cfg.Nk)
+        bias = inputs.bias_inputs(shape, seed=cfg.seed + 100)
+    strides = (0, 0)
+    if bias is not None:
+        strides = (bias.stride(0) if bias.shape[0] == cfg.B else 0, bias.stride(1))
+    o_ref, lse_ref, _ = oracle.attention_masked(
+        x.q, x.k, x.v, cfg.causal, x.scale, window_left=cfg.window,
+        alibi=None if slopes is None else slopes.numpy(), bias=bias, bias_strides=strides, rows=rows)
+    for dt in (torch.bfloat16, torch.float32):
+        o, lse = run_masked(abi, x, cfg.window, slopes, bias, dt)
+        d = o.shape[-1]
+        compare(o.reshape(-1, d)[rows.numpy()], lse.reshape(-1)[rows.numpy()], o_ref, lse_ref,
+                dt == torch.bfloat16)

@@ -58,3 +58,19 @@ def test_roofline_bound_and_floor():
     assert roofline.bound_rate(1e12, 1e9, p) == pytest.approx(1e14)  # I=1000 > ridge
     assert roofline.bound_rate(1e11, 1e10, p) == pytest.approx(1e13)  # I=10 < ridge
     assert roofline.time_floor_s(1e12, 1e9, p) == pytest.approx(0.01)
+
+
+@pytest.mark.parametrize("Nq,Nk,causal,window", [(7, 7, True, 0), (5, 9, True, 3), (9, 5, True, 2),
+                                                  (6, 11, False, 4), (8, 8, False, 0), (4, 4, True, 1)])
+def test_allowed_pairs_brute_force(Nq, Nk, causal, window):
+    # Count the pairs one by one from the mask's definition.
+    diag = Nk - Nq
+    n = 0
+    for i in range(Nq):
+        for j in range(Nk):
+            if causal and j > i + diag:
+                continue
+            if window > 0 and j <= i + diag - window:
+                continue
+            n += 1
+    assert roofline.allowed_pairs(Nq, Nk, causal, window) == n
