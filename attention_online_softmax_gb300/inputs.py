@@ -160,3 +160,74 @@ def bias_inputs(shape, seed: int, std: float = 2.0, neg_inf_frac: float = 0.0,
         rows = torch.randperm(shape[2], generator=g)[:neg_inf_rows]
         b[0, 0, rows, :] = float("-inf")
     return b.to(torch.bfloat16)
+
+
+@dataclass
+class PagedPrefillInputs:
+    q: torch.Tensor             # [total_q, Hq, d] bf16, sequences packed in order
+    kcache: torch.Tensor        # [P, page_size, Hkv, d] bf16
+    vcache: torch.Tensor        # [P, page_size, Hkv, d] bf16
+    block_table: torch.Tensor   # [S, max_pages] int32
+    cu_seqlens_q: torch.Tensor  # [S + 1] int32
+    seqlens_k: torch.Tensor     # [S] int32 (context length, new tokens included)
+    scale: float
+    page_size: int
+    max_seqlen_q: int
+    generator: torch.Generator
+
+
+def paged_prefill_inputs(q_lens: list[int], k_lens: list[int], Hq: int, Hkv: int, d: int,
+                         num_pages: int, page_size: int, seed: int,
+                         max_pages_per_seq: int | None = None,
+                         scale: float | None = None) -> PagedPrefillInputs:
+    """Chunked prefill: sequence s appends q_lens[s] new tokens to a context
+    that then holds k_lens[s] tokens in the paged cache.
+
+    Draw order: ``perm = randperm(num_pages)``, q [total_q, Hq, d], then for
+    each sequence its K and V rows [k_lens[s], Hkv, d].  Pages are handed out
+    from the permutation in sequence order; unused slots and pages hold bf16
+    NaN and unused block-table entries point at a NaN page when one exists,
+    as for paged decode.
+    """
+    if len(q_lens) != len(k_lens):
+        raise ValueError("q_lens and k_lens differ in length")
+    S = len(q_lens)
+    g = torch.Generator("cpu").manual_seed(int(seed))
+    perm = torch.randperm(num_pages, generator=g)
+    total_q = int(sum(q_lens))
+    q = _randn_bf16(g, (total_q, Hq, d))
+    pages_needed = [(int(L) + page_size - 1) // page_size for L in k_lens]
+    if max_pages_per_seq is None:
+        max_pages_per_seq = max([1] + pages_needed)
+    if sum(pages_needed) > num_pages:
+        raise ValueError("page pool too small for the context lengths")
+    if max(pages_needed + [0]) > max_pages_per_seq:
+        raise ValueError("max_pages_per_seq too small for the context lengths")
+    kc = torch.full((num_pages, page_size, Hkv, d), BF16_NAN, dtype=torch.bfloat16)
+    vc = torch.full((num_pages, page_size, Hkv, d), BF16_NAN, dtype=torch.bfloat16)
+    used = sum(pages_needed)
+    spare = int(perm[used]) if used < num_pages else 0
+    bt = torch.full((S, max_pages_per_seq), spare, dtype=torch.int32)
+    cursor = 0
+    for s, L in enumerate(int(x) for x in k_lens):
+        npg = pages_needed[s]
+        pages = perm[cursor:cursor + npg]
+        cursor += npg
+        bt[s, :npg] = pages.to(torch.int32)
+        ks = _randn_bf16(g, (L, Hkv, d))
+        vs = _randn_bf16(g, (L, Hkv, d))
+        full = L // page_size
+        if full:
+            kc[pages[:full]] = ks[:full * page_size].reshape(full, page_size, Hkv, d)
+            vc[pages[:full]] = vs[:full * page_size].reshape(full, page_size, Hkv, d)
+        rem = L - full * page_size
+        if rem:
+            kc[pages[full], :rem] = ks[full * page_size:]
+            vc[pages[full], :rem] = vs[full * page_size:]
+    cu = torch.zeros(S + 1, dtype=torch.int32)
+    if S:
+        cu[1:] = torch.cumsum(torch.tensor([int(x) for x in q_lens], dtype=torch.int64), 0).to(torch.int32)
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+    return PagedPrefillInputs(q, kc, vc, bt, cu, torch.tensor([int(x) for x in k_lens], dtype=torch.int32),
+                              float(scale), page_size, max([0] + [int(x) for x in q_lens]), g)

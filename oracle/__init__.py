@@ -75,6 +75,9 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
                                                     ctypes.c_float, i, p, p, i64, i64,
                                                     p, i64, p, p, i]
             lib.oracle_attention_masked.restype = i
+            lib.oracle_prefill_paged.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, i, i,
+                                                 ctypes.c_float, p, i64, p, p, i]
+            lib.oracle_prefill_paged.restype = i
             _LIBS[mutant] = lib
         return lib
 
@@ -200,6 +203,48 @@ def decode_paged(q, kcache, vcache, block_table, seqlens, scale: float,
         n, _ptr(o), _ptr(lse), int(threads))
     if rc < 0:
         raise ValueError(f"oracle_decode_paged rejected its arguments ({rc})")
+    return o, lse, rc
+
+
+def prefill_paged(q, kcache, vcache, block_table, cu_seqlens_q, seqlens_k, causal: bool,
+                  scale: float, window_left: int = 0, rows=None, threads: int = 0):
+    """Chunked prefill of ragged sequences against a paged KV cache (see
+    oracle_prefill_paged in attn_oracle.c), float64.
+
+    q: [total_q, Hq, d]; kcache, vcache: [P, page_size, Hkv, d] (bf16);
+    block_table: [S, max_pages] int32; cu_seqlens_q: [S + 1] int32;
+    seqlens_k: [S] int32.  ``rows`` selects flat (token * Hq + h) rows.
+    Returns (O [total_q, Hq, d] or [nrows, d], LSE [total_q, Hq] or [nrows],
+    threads_used).
+    """
+    qb, kb, vb = _bits(q), _bits(kcache), _bits(vcache)
+    bt = np.ascontiguousarray(np.asarray(_host(block_table), dtype=np.int32))
+    cu = np.ascontiguousarray(np.asarray(_host(cu_seqlens_q), dtype=np.int32))
+    sk = np.ascontiguousarray(np.asarray(_host(seqlens_k), dtype=np.int32))
+    total_q, Hq, d = qb.shape
+    P, page, Hkv, dk = kb.shape
+    S = sk.shape[0]
+    if dk != d or vb.shape != kb.shape or cu.shape != (S + 1,) or bt.shape[0] != S:
+        raise ValueError("paged prefill shape mismatch")
+    if S and int(cu[-1]) != total_q:
+        raise ValueError("cu_seqlens_q[-1] must equal total_q")
+    if rows is None:
+        nrows = total_q * Hq
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows_arr.size
+    o = np.empty((nrows, d), dtype=np.float64)
+    lse = np.empty((nrows,), dtype=np.float64)
+    rc = _load().oracle_prefill_paged(
+        _ptr(qb), _ptr(kb), _ptr(vb), _ptr(bt), _ptr(cu), _ptr(sk), S, Hq, Hkv, d, page, P,
+        bt.shape[1] if bt.ndim == 2 else 0, int(bool(causal)), int(window_left), float(scale),
+        None if rows_arr is None else _ptr(rows_arr), nrows, _ptr(o), _ptr(lse), int(threads))
+    if rc < 0:
+        raise ValueError(f"oracle_prefill_paged rejected its arguments ({rc})")
+    if rows is None:
+        o = o.reshape(total_q, Hq, d)
+        lse = lse.reshape(total_q, Hq)
     return o, lse, rc
 
 

@@ -368,3 +368,103 @@ int oracle_decode_paged(const uint16_t* q, const uint16_t* kcache, const uint16_
     }
     return bad ? -2 : nthreads;
 }
+
+/*
+ * Chunked prefill against a paged KV cache, ragged over sequences.
+ *
+ * "Don't Write Kernels, Derive Them", section "What happened": paged KV-cache
+ * access is one of the operations the method covers; "Compilers and Kernels",
+ * section "FlashAttention changes the algorithm around IO", gives the
+ * attention each query row computes (the definition above).
+ *
+ * Sequence s owns query tokens [cu_seqlens_q[s], cu_seqlens_q[s+1]) of the
+ * packed q [total_q][Hq][d]; they are the LAST q_len = cu_seqlens_q[s+1] -
+ * cu_seqlens_q[s] tokens of its context of k_len = seqlens_k[s] tokens, whose
+ * keys and values sit in the paged cache exactly as for paged decode.  Query i
+ * of the chunk (0 <= i < q_len) sees keys j in [lo, hi):
+ *     hi = min(k_len, i + (k_len - q_len) + 1) when causal, else k_len;
+ *     lo = max(0, i + (k_len - q_len) - window_left + 1) when window_left > 0,
+ *          else 0
+ * (the bottom-right causal reading of the plain oracle, with the chunk's
+ * tokens at the end of the context).  q_len = 1 with causal is paged decode.
+ *
+ * rows: NULL for every (token, head) of the batch, else flat indices
+ * token * Hq + h; o_out [nrows][d], lse_out [nrows].  Returns the threads
+ * used, -1 on invalid sizes, -2 on a block-table entry outside the pool.
+ */
+int oracle_prefill_paged(const uint16_t* q, const uint16_t* kcache, const uint16_t* vcache,
+                         const int32_t* block_table, const int32_t* cu_seqlens_q,
+                         const int32_t* seqlens_k, int num_seqs, int Hq, int Hkv, int d,
+                         int page_size, int num_pages, int max_pages_per_seq, int causal,
+                         int window_left, float scale, const int64_t* rows, int64_t nrows,
+                         double* o_out, double* lse_out, int nthreads) {
+    if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || page_size <= 0 || window_left < 0) return -1;
+    if (Hq % Hkv != 0) return -1;
+    const int group = Hq / Hkv;
+    if (num_seqs > 0 && cu_seqlens_q[0] != 0) return -1;
+    int64_t max_len = 1;
+    int s;
+    for (s = 0; s < num_seqs; ++s) {
+        if (cu_seqlens_q[s + 1] < cu_seqlens_q[s]) return -1;
+        if (seqlens_k[s] < 0 || (int64_t)seqlens_k[s] > (int64_t)max_pages_per_seq * page_size) return -1;
+        if (seqlens_k[s] > max_len) max_len = seqlens_k[s];
+    }
+    const int64_t total_q = num_seqs > 0 ? cu_seqlens_q[num_seqs] : 0;
+    if (rows == NULL) nrows = total_q * Hq;
+    nthreads = oracle_threads(nthreads);
+    int bad = 0;
+
+#pragma omp parallel num_threads(nthreads)
+    {
+        double* scratch = (double*)malloc(sizeof(double) * (size_t)max_len);
+        const uint16_t** krows = (const uint16_t**)malloc(sizeof(void*) * (size_t)max_len);
+        const uint16_t** vrows = (const uint16_t**)malloc(sizeof(void*) * (size_t)max_len);
+        int64_t w;
+#pragma omp for schedule(dynamic, 16)
+        for (w = 0; w < nrows; ++w) {
+            const int64_t r = rows ? rows[w] : w;
+            if (r < 0 || r >= total_q * Hq) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            const int64_t token = r / Hq;
+            const int h = (int)(r % Hq);
+            /* the sequence holding this token: last s with cu_seqlens_q[s] <= token */
+            int a = 0, b = num_seqs - 1;
+            while (a < b) {
+                int mid = (a + b + 1) / 2;
+                if (cu_seqlens_q[mid] <= token) a = mid; else b = mid - 1;
+            }
+            const int seq = a;
+            const int64_t q_len = cu_seqlens_q[seq + 1] - cu_seqlens_q[seq];
+            const int64_t k_len = seqlens_k[seq];
+            const int64_t i = token - cu_seqlens_q[seq];
+            const int64_t diag = k_len - q_len;
+            int64_t hi = causal ? i + diag + 1 : k_len;
+            if (hi > k_len) hi = k_len;
+            int64_t lo = window_left > 0 ? i + diag - window_left + 1 : 0;
+            if (lo < 0) lo = 0;
+            const int g = h / group;
+            int64_t t, n = 0;
+            int ok = 1;
+            for (t = lo; t < hi; ++t, ++n) {
+                int32_t page = block_table[(int64_t)seq * max_pages_per_seq + t / page_size];
+                if (page < 0 || page >= num_pages) { ok = 0; break; }
+                int64_t off = (((int64_t)page * page_size + t % page_size) * Hkv + g) * d;
+                krows[n] = kcache + off;
+                vrows[n] = vcache + off;
+            }
+            if (!ok) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            attend_row(q + r * d, krows, vrows, n, d, (double)scale, scratch, o_out + w * d, lse_out + w);
+        }
+        free(scratch);
+        free(krows);
+        free(vrows);
+    }
+    return bad ? -2 : nthreads;
+}
