@@ -37,6 +37,11 @@ class AttnMask(ctypes.Structure):
 _lib.attn_fwd_masked.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, ctypes.c_float,
                                  ctypes.POINTER(AttnMask), _i, _vp]
 _lib.attn_fwd_masked.restype = _i
+_lib.attn_prefill_paged_workspace_size.argtypes = [_i]
+_lib.attn_prefill_paged_workspace_size.restype = ctypes.c_size_t
+_lib.attn_prefill_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
+                                    _i, _i, ctypes.c_float, _vp, ctypes.c_size_t, _i, _vp]
+_lib.attn_prefill_paged.restype = _i
 _lib.attn_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
 _lib.attn_decode_workspace_size.restype = ctypes.c_size_t
 _lib.attn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
@@ -61,7 +66,8 @@ ATTN_BF16 = 0
 ATTN_F32 = 1
 
 #: every symbol include/attn.h declares
-EXPORTS = ("attn_fwd", "attn_fwd_masked", "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_static",
+EXPORTS = ("attn_fwd", "attn_fwd_masked", "attn_prefill_paged_workspace_size", "attn_prefill_paged",
+           "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_static",
            "attn_get_device_status", "attn_selftest_wait_timeout", "attn_status_string",
            "attn_launch_count", "attn_abi_version")
 
@@ -170,6 +176,43 @@ def attn_fwd_masked(q, k, v, o, lse, causal: bool, scale: float, window_left: in
                               int(bool(causal)), float(scale), ctypes.byref(m),
                               ATTN_F32 if o.dtype == torch.float32 else ATTN_BF16, _stream_ptr(stream))
     _check(st, "attn_fwd_masked")
+
+
+def attn_prefill_paged_workspace_size(num_seqs: int) -> int:
+    return int(_lib.attn_prefill_paged_workspace_size(int(num_seqs)))
+
+
+def attn_prefill_paged(q, kcache, vcache, block_table, cu_seqlens_q, seqlens_k, o, lse, causal: bool,
+                       scale: float, window_left: int = 0, workspace=None, stream=None) -> None:
+    """Chunked prefill against a paged KV cache; shapes as in include/attn.h.
+    ``workspace``: CUDA uint8 tensor of attn_prefill_paged_workspace_size(S)
+    bytes (allocated here when None)."""
+    import torch
+    _need(q, torch.bfloat16, "q")
+    _need(kcache, torch.bfloat16, "kcache")
+    _need(vcache, torch.bfloat16, "vcache")
+    _need(block_table, torch.int32, "block_table")
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _need(seqlens_k, torch.int32, "seqlens_k")
+    _need(lse, torch.float32, "lse")
+    if o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be bfloat16 or float32")
+    _need(o, o.dtype, "o")
+    total_q, Hq, d = q.shape
+    P, page_size, Hkv, dk = kcache.shape
+    S = seqlens_k.numel()
+    if dk != d or vcache.shape != kcache.shape or cu_seqlens_q.numel() != S + 1 or block_table.dim() != 2 \
+            or block_table.shape[0] != S or tuple(o.shape) != (total_q, Hq, d) or tuple(lse.shape) != (total_q, Hq):
+        raise ValueError("paged prefill shape mismatch")
+    need = attn_prefill_paged_workspace_size(S)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = _lib.attn_prefill_paged(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(block_table), _ptr(cu_seqlens_q),
+                                 _ptr(seqlens_k), _ptr(o), _ptr(lse), S, total_q, Hq, Hkv, d, page_size, P,
+                                 block_table.shape[1], int(bool(causal)), int(window_left), float(scale),
+                                 _ptr(workspace), workspace.numel(),
+                                 ATTN_F32 if o.dtype == torch.float32 else ATTN_BF16, _stream_ptr(stream))
+    _check(st, "attn_prefill_paged")
 
 
 def attn_decode_workspace_size(num_seqs: int, Hq: int, Hkv: int, d: int, max_seqlen: int) -> int:

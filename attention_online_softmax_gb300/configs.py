@@ -60,4 +60,36 @@ WINDOW = PrefillConfig("causal_window1024_b2_h32_n4096_d128", 2, 32, 32, 4096, 4
 ALIBI_BIAS = PrefillConfig("alibi_densebias_b1_h16_n2048_d128", 1, 16, 16, 2048, 2048, 128, False, 6,
                            check_rows_per_head=64, alibi=True, bias="batch")
 MASKED_CONFIGS = (WINDOW, ALIBI_BIAS)
-ALL = {c.name: c for c in PREFILL_CONFIGS + MASKED_CONFIGS + (DECODE,)}
+
+
+@dataclass(frozen=True)
+class ChunkedConfig:
+    """Chunked prefill against a paged KV cache: each sequence appends
+    ``chunk`` new tokens to a cached context of U[ctx_lo, ctx_hi] tokens."""
+    name: str
+    num_seqs: int
+    chunk: int
+    ctx_lo: int
+    ctx_hi: int
+    Hq: int
+    Hkv: int
+    d: int
+    num_pages: int
+    page_size: int
+    seed: int
+
+
+CHUNKED = ChunkedConfig("chunked_prefill_16seq_512new_ctx0to8192_gqa32to8_d128", 16, 512, 0, 8192, 32, 8, 128,
+                        12000, 16, 7)
+
+
+def chunked_lengths(c: ChunkedConfig):
+    """(q_lens, k_lens) of a chunked-prefill workload: contexts drawn as
+    ``randint(ctx_lo, ctx_hi + 1)`` from a generator seeded with ``seed``."""
+    import torch
+    g = torch.Generator("cpu").manual_seed(int(c.seed))
+    ctx = torch.randint(c.ctx_lo, c.ctx_hi + 1, (c.num_seqs,), generator=g).tolist()
+    return [c.chunk] * c.num_seqs, [int(x) + c.chunk for x in ctx]
+
+
+ALL = {c.name: c for c in PREFILL_CONFIGS + MASKED_CONFIGS + (DECODE, CHUNKED)}

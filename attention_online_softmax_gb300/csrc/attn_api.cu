@@ -99,6 +99,41 @@ bool encode_bias_map(CUtensorMap* map, const void* base, int Nq, int Nk, int Hb,
   return r == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over packed queries [total_q][Hq][d]; one box is 128 tokens of
+// one head x 64 columns, 128-byte swizzled (the same shared-memory image as a
+// [128 rows][64 columns] box of the [B*Hq][Nq][d] layout).
+bool encode_packed_q_map(CUtensorMap* map, const void* base, int d, int Hq, int total_q) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(total_q)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(Hq) * d * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(attn::kBM)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 4-D bf16 map over the paged cache [pages][slots][Hkv][d] for the prefill
+// kernel: one box is the page_size slots of one page and one KV head x 64
+// columns, 128-byte swizzled, so a page lands as page_size consecutive
+// 128-byte rows of a K/V tile (at a multiple of 2 KB: whole swizzle atoms).
+bool encode_paged_rows_map(CUtensorMap* map, const void* base, int d, int Hkv, int page_size, int num_pages) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hkv),
+                        static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(Hkv) * d * 2,
+                           static_cast<cuuint64_t>(page_size) * Hkv * d * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(page_size), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 4-D bf16 map over the paged cache [pages][slots][Hkv][d]; one box is the
 // [16 slots][hg heads][d] block of one page (no swizzle).
 bool encode_page_map(CUtensorMap* map, const void* base, int d, int Hkv, int page_size, int num_pages, int hg) {
@@ -195,6 +230,30 @@ attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const C
   // Persistent: one CTA per SM (or fewer when there are fewer units).
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
   kern<<<dim3(grid), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mb, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return ATTN_OK;
+}
+
+// Paged chunked prefill: the plan kernel writes the unit prefix sums into the
+// workspace, then the persistent prefill kernel (one CTA per SM) takes units
+// up to the total it finds there.
+template <int D, int STAGES>
+attn_status launch_prefill_paged(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                                 attn::PrefillParams p, int total_q, cudaStream_t stream) {
+  using L = attn::PrefillLayout<D, 1, STAGES>;
+  auto kern = attn::prefill_fwd_kernel<D, 1, STAGES, 0, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  const attn_status st = sched_slot(&p.sched);
+  if (st != ATTN_OK) return st;
+  attn::paged_plan_kernel<<<1, 1024, 0, stream>>>(p.cu_q, p.seqlens_k, p.num_seqs, total_q, p.Hq, p.max_pages,
+                                                   p.page_size, const_cast<int32_t*>(p.unit_prefix));
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  kern<<<dim3(static_cast<unsigned>(sm_count())), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mv, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return ATTN_OK;
@@ -444,6 +503,66 @@ attn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o
       return two ? launch_prefill<128, 2, 5>(mq, mk, mv, mq, p, B * Hq, s)
                  : launch_prefill<128, 1, 6>(mq, mk, mv, mq, p, B * Hq, s);
     case 256: return launch_prefill<256, 1, 5>(mq, mk, mv, mq, p, B * Hq, s);
+  }
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+size_t attn_prefill_paged_workspace_size(int num_seqs) {
+  if (num_seqs < 0) return 0;
+  return ((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+}
+
+attn_status attn_prefill_paged(const void* q, const void* kcache, const void* vcache, const int32_t* block_table,
+                               const int32_t* cu_seqlens_q, const int32_t* seqlens_k, void* o, float* lse,
+                               int num_seqs, int total_q, int Hq, int Hkv, int d, int page_size, int num_pages,
+                               int max_pages_per_seq, int causal, int window_left, float scale, void* workspace,
+                               size_t workspace_bytes, attn_dtype o_dtype, attn_stream_t stream) {
+  if (num_seqs < 0 || total_q < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (num_pages <= 0 || max_pages_per_seq <= 0 || window_left < 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (o_dtype != ATTN_BF16 && o_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((static_cast<long long>(total_q) + attn::kBM - 1) / attn::kBM * Hq > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0) return ATTN_OK;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_MISALIGNED;
+  if (block_table == nullptr || cu_seqlens_q == nullptr || seqlens_k == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(workspace) || workspace_bytes < attn_prefill_paged_workspace_size(num_seqs))
+    return ATTN_ERR_WORKSPACE;
+  attn_status st = check_device();
+  if (st != ATTN_OK) return st;
+
+  CUtensorMap mq, mk, mv;
+  if (!encode_packed_q_map(&mq, q, d, Hq, total_q) ||
+      !encode_paged_rows_map(&mk, kcache, d, Hkv, page_size, num_pages) ||
+      !encode_paged_rows_map(&mv, vcache, d, Hkv, page_size, num_pages))
+    return ATTN_ERR_LAUNCH;
+
+  attn::PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.o = o;
+  p.lse = lse;
+  p.B = 1;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.causal = causal ? 1 : 0;
+  p.o_f32 = o_dtype == ATTN_F32 ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.window = window_left;
+  p.cu_q = cu_seqlens_q;
+  p.seqlens_k = seqlens_k;
+  p.block_table = block_table;
+  p.unit_prefix = static_cast<const int32_t*>(workspace);
+  p.num_seqs = num_seqs;
+  p.max_pages = max_pages_per_seq;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (d) {
+    case 64: return launch_prefill_paged<64, 12>(mq, mk, mv, p, total_q, s);
+    case 128: return launch_prefill_paged<128, 6>(mq, mk, mv, p, total_q, s);
+    case 256: return launch_prefill_paged<256, 5>(mq, mk, mv, p, total_q, s);
   }
   return ATTN_ERR_UNSUPPORTED;
 }

@@ -78,6 +78,14 @@ struct PrefillParams {
   const uint16_t* bias;       // null or bf16 bias[b*bias_sb + h*bias_sh + i*Nk + j]
   long long bias_sb, bias_sh;
   int bias_hmul, bias_bmul;   // staged bias: head / batch coordinate multipliers (0: broadcast)
+  // Chunked prefill against a paged KV cache (PAGED kernels only): sequence s
+  // owns packed query tokens [cu_q[s], cu_q[s+1]), the last ones of a context
+  // of seqlens_k[s] tokens whose key t sits in page block_table[s][t / page_size].
+  const int32_t* cu_q;
+  const int32_t* seqlens_k;
+  const int32_t* block_table;
+  const int32_t* unit_prefix;  // [num_seqs + 1] units before each sequence (plan kernel)
+  int num_seqs, max_pages, page_size, num_pages;
 };
 
 template <int D, int NQ, int STAGES, int BSLOTS = 0>
@@ -101,10 +109,11 @@ struct PrefillLayout {
   static constexpr int kBarOff = kBiasOff + BSLOTS * kBiasBytes;
   // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done,
   // o_done[2], o_free[2], unit_full[Q], unit_empty[Q], mma_drain,
-  // bias_full[BSLOTS], bias_empty[BSLOTS]
-  static constexpr int kNumBars = 2 + 2 * STAGES + 2 + 2 + 1 + 2 + 2 + 2 * kUnitQ + 1 + 2 * BSLOTS;
+  // bias_full[BSLOTS], bias_empty[BSLOTS], tail_bar
+  static constexpr int kNumBars = 2 + 2 * STAGES + 2 + 2 + 1 + 2 + 2 + 2 * kUnitQ + 1 + 2 * BSLOTS + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, unit queue
-  static constexpr int kBytes = kMiscOff + 16 + 4 * kUnitQ;
+  static constexpr int kUnitBytes = 64;                      // one decoded unit in the queue
+  static constexpr int kBytes = kMiscOff + 16 + kUnitBytes * kUnitQ;
   // Dynamic shared memory requested: at least 115 KB so that no second CTA
   // (which would wait for this one's tensor memory) shares the SM.
   static constexpr int kAlloc = (kBytes + 1024) > 117760 ? (kBytes + 1024) : 117760;
@@ -134,37 +143,65 @@ __device__ __forceinline__ int v_pos(int t, int T) {
 // of its query tiles needs (0 for a tile past Nq or fully masked).
 template <int NQ>
 struct Unit {
-  int bh, kvh, q0;
+  int idx;               // position in the launch's unit order (-1: no work left, -2: timed out)
+  int bh, kvh, q0;       // (batch, head) row block (paged: the query head), its KV head, first query row
   int tmin, T;           // key tiles loaded: [tmin, tmin + T)
   int lo[NQ], hi[NQ];    // key tiles each query tile needs: [lo, hi), empty if lo >= hi
+  int nq, nk, qbase, seq;  // this problem's query and key counts, first packed query token, sequence
 };
 
-// Unit `idx` of the grouped longest-first order (0 <= idx < B*Hq*n_units).
-template <int NQ>
+// Unit `idx`.  Plain: the grouped longest-first order over (batch, head,
+// query-tile) (0 <= idx < B*Hq*n_units).  Paged: sequence by sequence (unit
+// prefix sums from the plan kernel), within a sequence its last query tile
+// first, heads fastest.
+template <int NQ, bool PAGED>
 __device__ __forceinline__ Unit<NQ> unit_of(const PrefillParams& p, int idx) {
   Unit<NQ> u;
-  const int BH = p.B * p.Hq;
-  const int per_group = p.group * p.n_units;
-  const int grp = idx / per_group;
-  const int in = idx - grp * per_group;
-  const int gsize = min(p.group, BH - grp * p.group);
-  const int rank = in / gsize;
-  u.bh = grp * p.group + (in - rank * gsize);
-  const int un = p.n_units - 1 - rank;
-  const int b = u.bh / p.Hq;
-  const int h = u.bh - b * p.Hq;
-  u.kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
-  u.q0 = un * (kBM * NQ);
-  const int diag = p.Nk - p.Nq;
+  u.idx = idx;
+  if (PAGED) {
+    int a = 0, b = p.num_seqs - 1;  // last sequence whose first unit is <= idx
+    while (a < b) {
+      const int mid = (a + b + 1) >> 1;
+      if (__ldg(p.unit_prefix + mid) <= idx) a = mid;
+      else b = mid - 1;
+    }
+    const int local = idx - __ldg(p.unit_prefix + a);
+    u.seq = a;
+    u.qbase = __ldg(p.cu_q + a);
+    u.nq = __ldg(p.cu_q + a + 1) - u.qbase;
+    u.nk = __ldg(p.seqlens_k + a);
+    const int ntiles = (u.nq + kBM - 1) / kBM;
+    u.bh = local % p.Hq;
+    u.kvh = u.bh / (p.Hq / p.Hkv);
+    u.q0 = (ntiles - 1 - local / p.Hq) * kBM;
+  } else {
+    const int BH = p.B * p.Hq;
+    const int per_group = p.group * p.n_units;
+    const int grp = idx / per_group;
+    const int in = idx - grp * per_group;
+    const int gsize = min(p.group, BH - grp * p.group);
+    const int rank = in / gsize;
+    u.bh = grp * p.group + (in - rank * gsize);
+    const int un = p.n_units - 1 - rank;
+    const int b = u.bh / p.Hq;
+    const int h = u.bh - b * p.Hq;
+    u.kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
+    u.q0 = un * (kBM * NQ);
+    u.nq = p.Nq;
+    u.nk = p.Nk;
+    u.qbase = 0;
+    u.seq = 0;
+  }
+  const int diag = u.nk - u.nq;
   int tmax = 0;
   u.tmin = 0x7FFFFFFF;
 #pragma unroll
   for (int j = 0; j < NQ; ++j) {
     const int r0 = u.q0 + j * kBM;
     int kbeg = 0, kend = 0;  // keys [kbeg, kend) some row of the tile may see
-    if (r0 < p.Nq) {
-      kend = p.Nk;
-      if (p.causal) kend = min(p.Nk, min(r0 + kBM, p.Nq) - 1 + diag + 1);
+    if (r0 < u.nq) {
+      kend = u.nk;
+      if (p.causal) kend = max(0, min(u.nk, min(r0 + kBM, u.nq) - 1 + diag + 1));
       if (p.window > 0) kbeg = max(0, r0 + diag - p.window + 1);
     }
     u.lo[j] = kbeg / kBN;
@@ -179,6 +216,27 @@ __device__ __forceinline__ Unit<NQ> unit_of(const PrefillParams& p, int idx) {
   return u;
 }
 
+// Item i of a unit's K/V load order (kH items per tile): its key tile t
+// (relative to the unit's first), kind (0: K, 1: V) and head-dim part hh.
+template <int NQ, int KH>
+__device__ __forceinline__ void load_item(int i, int T, int& t, int& kind, int& hh) {
+  const int pos = i / KH;
+  hh = i % KH;
+  if (NQ == 2) {
+    t = pos >> 1;
+    kind = pos & 1;
+  } else if (pos == 0) {
+    t = 0;
+    kind = 0;
+  } else if (pos == 2 * T - 1) {
+    t = T - 1;
+    kind = 1;
+  } else {
+    kind = (pos & 1) ? 0 : 1;  // odd: K((pos+1)/2), even: V(pos/2 - 1)
+    t = kind == 0 ? (pos + 1) >> 1 : (pos >> 1) - 1;
+  }
+}
+
 // BIAS: 0 no additive bias beyond causal / window masks; 1 ALiBi slopes and/or
 // a dense bias read by the softmax threads from global memory; 2 the dense
 // bias staged tile by tile into shared memory by the producer (tmB).
@@ -187,13 +245,18 @@ __host__ __device__ constexpr int bias_slots() { return BIAS == 2 ? 2 : 0; }
 template <int BIAS>
 __host__ __device__ constexpr int bias_ring() { return BIAS == 2 ? 2 : 1; }  // modulus (never 0)
 
-template <int D, int NQ, int STAGES, int BIAS>
+// PAGED: Q, O and LSE packed over the sequences' tokens ([total_q][Hq][d],
+// [total_q][Hq]); K and V read page by page from the paged cache (tmK, tmV
+// box one page of one KV head); tmB is unused.
+template <int D, int NQ, int STAGES, int BIAS, bool PAGED = false>
 __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>()>::kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
                        const PrefillParams p) {
   using L = PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>()>;
   static_assert(BIAS == 0 || NQ == 1, "additive-bias variants run one query tile per unit");
+  static_assert(!PAGED || (NQ == 1 && BIAS == 0), "paged prefill: one query tile per unit, no dense bias");
+  static_assert(sizeof(Unit<NQ>) <= L::kUnitBytes, "unit queue entry");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -214,12 +277,21 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
   uint64_t* mma_drain = unit_empty + kUnitQ;
   uint64_t* bias_full = mma_drain + 1;
   uint64_t* bias_empty = bias_full + bias_slots<BIAS>();
+  uint64_t* tail_bar = bias_empty + bias_slots<BIAS>();  // paged: a partly filled value page
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
-  volatile int* unit_q = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 16);
+  Unit<NQ>* unit_q = reinterpret_cast<Unit<NQ>*>(smem + L::kMiscOff + 16);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int total_units = p.B * p.Hq * p.n_units;
+
+  if (PAGED) {
+    // Value rows past a sequence's context are never loaded, so every K/V
+    // ring byte the MMAs read is a real cache row or this zero: no NaN from an
+    // unused cache slot can reach O through a zero weight.
+    for (int i = threadIdx.x; i < STAGES * L::kKVBytes / 16; i += blockDim.x)
+      st_shared_v4(sbase + L::kKVOff + i * 16, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -241,6 +313,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     }
     mbar_init(pv_done, 1);
     mbar_init(mma_drain, 1);
+    mbar_init(tail_bar, 1);
     for (int i = 0; i < bias_slots<BIAS>(); ++i) {
       mbar_init(&bias_full[i], 1);
       mbar_init(&bias_empty[i], 4);  // lane 0 of every softmax warp
@@ -257,32 +330,43 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
   const uint32_t tmem = *tmem_slot;
 
   // Consumers' view of the unit queue: the n-th unit this CTA processes
-  // (-1: no work left, -2: the wait timed out).
-  auto next_unit = [&](int n, int where) -> int {
+  // (idx -1: no work left, -2: the wait timed out).  The entry is copied out
+  // before the caller releases the slot.
+  auto next_unit = [&](int n, int where) -> Unit<NQ> {
     const int slot = n % kUnitQ;
-    if (!mbar_wait(&unit_full[slot], (n / kUnitQ) & 1, where)) return -2;
-    return unit_q[slot];
+    Unit<NQ> u;
+    if (!mbar_wait(&unit_full[slot], (n / kUnitQ) & 1, where)) {
+      u.idx = -2;
+      return u;
+    }
+    u = unit_q[slot];
+    return u;
   };
 
-  if (warp == 0) {
+  if (warp == 0 && !PAGED) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      const int total_units = p.B * p.Hq * p.n_units;
       int item = 0;  // K/V items issued so far (the ring runs on across units)
       int q_uses = 0;
       bool ok = true;
       for (int n = 0; ok; ++n) {
-        // Take the next unit and publish it (-1: no work left).
+        // Take the next unit, decode it and publish it (idx -1: no work left).
         const int slot = n % kUnitQ;
         if (!mbar_wait(&unit_empty[slot], ((n / kUnitQ) & 1) ^ 1, 4)) break;
-        int idx = atomicAdd(p.sched, 1);
-        if (idx >= total_units) idx = -1;
-        unit_q[slot] = idx;
+        const int idx = atomicAdd(p.sched, 1);
+        Unit<NQ> u;
+        if (idx < total_units) {
+          u = unit_of<NQ, false>(p, idx);
+        } else {
+          u.idx = -1;
+        }
+        unit_q[slot] = u;
         mbar_arrive(&unit_full[slot]);
-        if (idx < 0) break;
-        const Unit<NQ> u = unit_of<NQ>(p, idx);
+        if (u.idx < 0) break;
         if (u.T == 0) continue;
         // The previous unit's last S MMA must be done with the Q tiles.
         if (q_uses > 0 && !mbar_wait(q_empty, (q_uses - 1) & 1, 5)) break;
@@ -301,22 +385,8 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
             break;
           }
           mbar_expect_tx(&kv_full[st], L::kKVBytes);
-          const int pos = i / L::kH;   // tile item in the unit's load order
-          const int hh = i % L::kH;    // which 128-column part of the head dim
-          int t, kind;                 // kind 0: K, 1: V
-          if (NQ == 2) {
-            t = pos >> 1;
-            kind = pos & 1;
-          } else if (pos == 0) {
-            t = 0;
-            kind = 0;
-          } else if (pos == 2 * u.T - 1) {
-            t = u.T - 1;
-            kind = 1;
-          } else {
-            kind = (pos & 1) ? 0 : 1;            // odd: K((pos+1)/2), even: V(pos/2 - 1)
-            t = kind == 0 ? (pos + 1) >> 1 : (pos >> 1) - 1;
-          }
+          int t, kind, hh;
+          load_item<NQ, L::kH>(i, u.T, t, kind, hh);
           const CUtensorMap* map = kind ? &tmV : &tmK;
 #pragma unroll
           for (int c = 0; c < L::kDI / 64; ++c)
@@ -328,7 +398,143 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       if (q_uses > 0) mbar_wait(q_full, (q_uses - 1) & 1, 2);
       for (int it = max(0, item - STAGES); it < item; ++it)
         mbar_wait(&kv_full[it % STAGES], (it / STAGES) & 1, 3);
-
+    }
+    __syncwarp();
+  } else if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer, paged cache
+    // The whole warp: a key tile spans 128 / page_size pages, each loaded as
+    // kDI / 64 boxes, one box per lane, so the boxes of an item are issued
+    // together.  Lane 0 does the waits, arrivals and the Q loads.  Each lane
+    // keeps the page id of its box for the tiles of K(t-1), K(t) and K(t+1)
+    // (prev / cur / next): the block-table read of a tile is issued one tile
+    // ahead of its first use.  Pages past the context's end are not loaded
+    // (their keys are masked; their stale rows, real cache rows or zeros, get
+    // zero weight).  A value page the context ends inside is loaded on its own
+    // barrier; the warp then zeroes its slots past the end before the item is
+    // complete, so whatever those cache slots hold never meets a zero weight.
+    constexpr uint32_t kFull = 0xFFFFFFFFu;
+    constexpr int kNone = -0x7FFFFFFF - 1;  // "no page": past the context or not an issuing lane
+    constexpr int kCh = L::kDI / 64;        // boxes per page and item
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    const int total_units = __ldg(p.unit_prefix + p.num_seqs);
+    const int ps = p.page_size;
+    const int g_l = lane / kCh;  // this lane's page within a key tile
+    const int c_l = lane % kCh;  // and 64-column box
+    const bool issuer = g_l < kBN / ps;
+    int item = 0, q_uses = 0, tails = 0;
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int slot = n % kUnitQ;
+      int idx = -2;
+      if (lane == 0 && mbar_wait(&unit_empty[slot], ((n / kUnitQ) & 1) ^ 1, 4)) idx = atomicAdd(p.sched, 1);
+      idx = __shfl_sync(kFull, idx, 0);
+      if (idx == -2) break;
+      Unit<NQ> u;
+      if (idx < total_units) {
+        u = unit_of<NQ, true>(p, idx);
+      } else {
+        u.idx = -1;
+      }
+      if (lane == 0) {
+        unit_q[slot] = u;
+        mbar_arrive(&unit_full[slot]);
+      }
+      if (u.idx < 0) break;
+      if (u.T == 0) continue;
+      int qok = 1;
+      if (lane == 0) {
+        // The previous unit's last S MMA must be done with the Q tile.
+        if (q_uses > 0 && !mbar_wait(q_empty, (q_uses - 1) & 1, 5)) {
+          qok = 0;
+        } else {
+          mbar_expect_tx(q_full, L::kQBytes);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)  // packed [total_q][Hq][d]: 128 tokens of one head
+            tma_load_3d(smem + L::kQOff + c * (kBM * 128), &tmQ, q_full, c * 64, u.bh, u.qbase + u.q0);
+        }
+      }
+      if (!__shfl_sync(kFull, qok, 0)) break;
+      ++q_uses;
+      const long long bt_row = static_cast<long long>(u.seq) * p.max_pages;
+      auto page_of = [&](int t) -> int {
+        const int kp = (u.tmin + t) * kBN + g_l * ps;
+        return (issuer && kp < u.nk) ? __ldg(p.block_table + bt_row + kp / ps) : kNone;
+      };
+      int pg_prev = kNone;
+      int pg_cur = page_of(0);
+      int pg_next = u.T > 1 ? page_of(1) : kNone;
+      for (int i = 0; i < 2 * L::kH * u.T; ++i, ++item) {
+        const int st = item % STAGES;
+        int t, kind, hh;
+        load_item<NQ, L::kH>(i, u.T, t, kind, hh);
+        if (kind == 0 && hh == 0 && t > 0) {
+          pg_prev = pg_cur;
+          pg_cur = pg_next;
+          pg_next = t + 1 < u.T ? page_of(t + 1) : kNone;
+        }
+        int wok = 1;
+        if (lane == 0) wok = mbar_wait(&kv_empty[st], ((item / STAGES) & 1) ^ 1, 1);
+        if (!__shfl_sync(kFull, wok, 0)) {
+          ok = false;
+          break;
+        }
+        // K(t) uses tile t's pages; V(t) comes after K(t+1), except the last.
+        const int pg = (kind == 0 || t == u.T - 1) ? pg_cur : pg_prev;
+        const int kp = (u.tmin + t) * kBN + g_l * ps;
+        const bool valid = pg >= 0 && pg < p.num_pages;
+        if (pg != kNone && !valid) report_error(7 /* ATTN_ERR_BOUNDS */, 8, pg);
+        const bool is_tail = valid && kind == 1 && kp + ps > u.nk;
+        const uint32_t tail_mask = __ballot_sync(kFull, is_tail);
+        const uint32_t load_mask = __ballot_sync(kFull, valid && !is_tail);
+        if (lane == 0) {
+          const uint32_t box = static_cast<uint32_t>(ps) * 128u;
+          if (tail_mask == 0) {
+            mbar_expect_tx(&kv_full[st], __popc(load_mask) * box);  // arrives; 0 bytes completes at once
+          } else {
+            mbar_expect_tx_only(&kv_full[st], __popc(load_mask) * box);
+            mbar_expect_tx(tail_bar, __popc(tail_mask) * box);
+          }
+        }
+        __syncwarp();
+        const CUtensorMap* map = kind ? &tmV : &tmK;
+        if (valid)
+          tma_load_4d(smem + L::kKVOff + st * L::kKVBytes + c_l * (kBN * 128) + g_l * ps * 128, map,
+                      is_tail ? tail_bar : &kv_full[st], hh * L::kDI + c_l * 64, u.kvh, 0, pg);
+        if (tail_mask != 0) {
+          int tok = 1;
+          if (lane == 0) tok = mbar_wait(tail_bar, tails & 1, 26);
+          if (!__shfl_sync(kFull, tok, 0)) {
+            ok = false;
+            break;
+          }
+          ++tails;
+          // Zero slots [rem, ps) of the tail page in each of its boxes.
+          const int tg = (__ffs(tail_mask) - 1) / kCh;
+          const int rem = u.nk - ((u.tmin + t) * kBN + tg * ps);
+          const int nz = ps - rem;
+          const uint32_t stage = sbase + L::kKVOff + st * L::kKVBytes;
+          for (int e = lane; e < kCh * nz * 8; e += 32) {
+            const int k16 = e & 7;
+            const int rr = e >> 3;
+            const int cc = rr / nz;
+            const int r = rem + (rr - cc * nz);
+            st_shared_v4(stage + cc * (kBN * 128) + (tg * ps + r) * 128 + k16 * 16, 0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&kv_full[st]);  // the item's one arrival
+        }
+      }
+    }
+    if (lane == 0) {
+      // Drain: never leave the CTA with a copy still writing shared memory.
+      if (q_uses > 0) mbar_wait(q_full, (q_uses - 1) & 1, 2);
+      for (int it = max(0, item - STAGES); it < item; ++it)
+        mbar_wait(&kv_full[it % STAGES], (it / STAGES) & 1, 3);
     }
     __syncwarp();
   } else if (BIAS == 2 && warp == 2 + 4 * NQ) {
@@ -340,11 +546,10 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       int bitem = 0;
       bool ok = true;
       for (int n = 0; ok; ++n) {
-        const int idx = next_unit(n, 25);
-        if (idx == -2) break;
+        const Unit<NQ> u = next_unit(n, 25);
+        if (u.idx == -2) break;
         mbar_arrive(&unit_empty[n % kUnitQ]);
-        if (idx < 0) break;
-        const Unit<NQ> u = unit_of<NQ>(p, idx);
+        if (u.idx < 0) break;
         const int b = u.bh / p.Hq;
         const int h = u.bh - b * p.Hq;
         for (int t = u.lo[0]; t < u.hi[0]; ++t, ++bitem) {
@@ -440,11 +645,10 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       };
 
       for (int n = 0; ok; ++n) {
-        const int idx = next_unit(n, 17);
-        if (idx == -2) break;
+        const Unit<NQ> u = next_unit(n, 17);
+        if (u.idx == -2) break;
         mbar_arrive(&unit_empty[n % kUnitQ]);
-        if (idx < 0) break;
-        const Unit<NQ> u = unit_of<NQ>(p, idx);
+        if (u.idx < 0) break;
         if (u.T == 0) continue;
         ok = mbar_wait(q_full, q_uses & 1, 10);
         if (!ok) break;
@@ -534,21 +738,24 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t o_cols = lane_base + j * D;
     const float sl = p.scale_log2;
-    const int diag = p.Nk - p.Nq;  // key j allowed for row i iff j <= i + diag (causal)
     int cnt = 0;                   // tiles softmaxed so far (running S/P barrier phases)
     int bcnt = 0;                  // staged bias tiles consumed so far
     int o_uses = 0;
     bool ok = true;
 
     for (int n = 0; ok; ++n) {
-      int idx = lane == 0 ? next_unit(n, 23) : 0;
-      idx = __shfl_sync(0xFFFFFFFFu, idx, 0);
-      if (idx == -2) break;
+      // Lane 0 waits for the entry; after the warp barrier every lane copies it.
+      int got = lane == 0 ? next_unit(n, 23).idx : 0;
+      got = __shfl_sync(0xFFFFFFFFu, got, 0);
+      if (got == -2) break;
+      __syncwarp();
+      const Unit<NQ> u = unit_q[n % kUnitQ];
+      __syncwarp();
       if (lane == 0) mbar_arrive(&unit_empty[n % kUnitQ]);
-      if (idx < 0) break;
-      const Unit<NQ> u = unit_of<NQ>(p, idx);
+      if (u.idx < 0) break;
+      const int diag = u.nk - u.nq;  // key j allowed for row i iff j <= i + diag (causal)
       const int r0 = u.q0 + j * kBM;
-      if (r0 >= p.Nq) continue;  // this query tile lies past Nq: nothing to write
+      if (r0 >= u.nq) continue;  // this query tile lies past the problem's rows: nothing to write
       const int qrow = r0 + row;
       const int nt = u.hi[j] > u.lo[j] ? u.hi[j] - u.lo[j] : 0;
       const int bh = u.bh;
@@ -559,7 +766,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       const int hq = bh % p.Hq;
       const float slope2 = p.alibi != nullptr ? p.alibi[hq] * 1.4426950408889634f : 0.f;
       const uint16_t* brow = nullptr;
-      if (BIAS == 1 && p.bias != nullptr && qrow < p.Nq)
+      if (BIAS == 1 && p.bias != nullptr && qrow < u.nq)
         brow = p.bias + static_cast<long long>(bh / p.Hq) * p.bias_sb + static_cast<long long>(hq) * p.bias_sh +
                static_cast<long long>(qrow) * p.Nk;
       const float mul = biased ? 1.f : sl;  // multiplier of r[] in the exponent
@@ -618,7 +825,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
             const uint16_t* a = brow + k0;
             const int odd = static_cast<int>((reinterpret_cast<uintptr_t>(a) >> 1) & 1u);
             const uint32_t* wp = reinterpret_cast<const uint32_t*>(a - odd);
-            const int nvalid = p.Nk - k0;
+            const int nvalid = u.nk - k0;
             uint32_t wv[kBN / 2 + 1];
 #pragma unroll
             for (int i = 0; i <= kBN / 2; ++i) wv[i] = (2 * i - odd < nvalid) ? __ldg(wp + i) : 0u;
@@ -636,10 +843,10 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
               r[cc] = __float_as_uint(fmaf(__uint_as_float(r[cc]), sl, base + slope2 * static_cast<float>(cc)));
           }
         }
-        const bool need_mask = (k0 + kBN > p.Nk) || (p.causal && (k0 + kBN - 1 > r0 + diag)) ||
+        const bool need_mask = (k0 + kBN > u.nk) || (p.causal && (k0 + kBN - 1 > r0 + diag)) ||
                                (p.window > 0 && k0 <= r0 + kBM - 1 + diag - p.window);
         if (need_mask) {
-          const int hi_c = (p.causal ? min(p.Nk - 1, qrow + diag) : p.Nk - 1) - k0;
+          const int hi_c = (p.causal ? min(u.nk - 1, qrow + diag) : u.nk - 1) - k0;
           const int lo_c = p.window > 0 ? qrow + diag - p.window + 1 - k0 : -1;
 #pragma unroll
           for (int cc = 0; cc < kBN; ++cc)
@@ -722,11 +929,14 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
         tc_fence_after();
       }
       // Every lane runs the (warp-collective) TMEM loads; only rows < Nq store.
-      const bool store = qrow < p.Nq;
+      const bool store = qrow < u.nq;
       const float lr = lr0 + lr1;
       const float l = l0 + l1;
       const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
-      const size_t row_off = (static_cast<size_t>(bh) * p.Nq + qrow) * D;
+      // Plain: O [B*Hq][Nq][d], LSE [B*Hq][Nq].  Paged: O [total_q][Hq][d], LSE [total_q][Hq].
+      const size_t lse_off = PAGED ? static_cast<size_t>(u.qbase + qrow) * p.Hq + bh
+                                   : static_cast<size_t>(bh) * p.Nq + qrow;
+      const size_t row_off = lse_off * D;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -763,7 +973,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       }
       if (nt > 0) ++o_uses;
       if (store)
-        p.lse[static_cast<size_t>(bh) * p.Nq + qrow] =
+        p.lse[lse_off] =
             (l > 0.f) ? (m_ref + lg2(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
@@ -783,6 +993,47 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       __threadfence();
     }
   }
+}
+
+
+// Unit prefix sums of a paged chunked prefill (one block): sequence s gets
+// ceil(q_len / 128) * Hq units.  A sequence whose lengths are inconsistent
+// (negative, past total_q, or a context longer than its block-table row) is
+// flagged in the status word and gets no units, so nothing of it is read.
+__global__ void __launch_bounds__(1024) paged_plan_kernel(const int32_t* cu_q, const int32_t* seqlens_k,
+                                                         int num_seqs, int total_q, int Hq, int max_pages,
+                                                         int page_size, int32_t* unit_prefix) {
+  __shared__ int part[1024];
+  const int per = (num_seqs + blockDim.x - 1) / blockDim.x;
+  const int s0 = min(num_seqs, static_cast<int>(threadIdx.x) * per);
+  const int s1 = min(num_seqs, s0 + per);
+  auto units = [&](int s) -> int {
+    const int a = cu_q[s], b = cu_q[s + 1], k = seqlens_k[s];
+    const bool bad = a < 0 || b < a || b > total_q || k < 0 ||
+                     static_cast<long long>(k) > static_cast<long long>(max_pages) * page_size;
+    if (bad) {
+      report_error(7 /* ATTN_ERR_BOUNDS */, 9, s);
+      return 0;
+    }
+    return ((b - a + kBM - 1) / kBM) * Hq;
+  };
+  int sum = 0;
+  for (int s = s0; s < s1; ++s) sum += units(s);
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  // Exclusive scan of the per-thread sums (Hillis-Steele over 1024 entries).
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int run = threadIdx.x > 0 ? part[threadIdx.x - 1] : 0;
+  for (int s = s0; s < s1; ++s) {
+    unit_prefix[s] = run;
+    run += units(s);
+  }
+  if (threadIdx.x == blockDim.x - 1) unit_prefix[num_seqs] = part[blockDim.x - 1];
 }
 
 }  // namespace attn

@@ -61,6 +61,15 @@ def prefill_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:
     return q + kv + o + lse
 
 
+def paged_prefill_bytes(q_lens, k_lens, Hq: int, Hkv: int, d: int, page_size: int) -> int:
+    """Chunked prefill: new-token Q, O (bf16) and LSE (f32), each sequence's
+    context K and V once per KV head, and the block-table entries used."""
+    tq = sum(int(x) for x in q_lens)
+    kv = sum(int(x) for x in k_lens) * Hkv * d * BF16 * 2
+    bt = sum((int(L) + page_size - 1) // page_size for L in k_lens) * I32
+    return tq * Hq * d * BF16 * 2 + tq * Hq * F32 + kv + bt + (len(q_lens) * 2 + 1) * I32
+
+
 def decode_bytes(seqlens, Hq: int, Hkv: int, d: int, page_size: int) -> int:
     lens = [int(x) for x in seqlens]
     kv = sum(lens) * Hkv * d * BF16 * 2

@@ -614,6 +614,39 @@ def per_config_table(abi, dev, stream, peaks, reps: int = 10):
                        "frac_of_bound": fl / t / bound, "flops": "4 d per allowed (query, key) pair",
                        "p10_us": sorted(ts)[len(ts) // 10] * 1e6, "p90_us": sorted(ts)[(9 * len(ts)) // 10] * 1e6}
         del q, k, v, o, lse, slopes, bias
+    # Chunked prefill against the paged cache.
+    c = configs.CHUNKED
+    q_lens, k_lens = configs.chunked_lengths(c)
+    x = inputs.paged_prefill_inputs(q_lens, k_lens, c.Hq, c.Hkv, c.d, num_pages=c.num_pages,
+                                    page_size=c.page_size, seed=c.seed)
+    q = x.q.to(dev)
+    kc, vc = x.kcache.to(dev), x.vcache.to(dev)
+    bt, cu, sk = x.block_table.to(dev), x.cu_seqlens_q.to(dev), x.seqlens_k.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, abi.attn_prefill_paged_workspace_size(c.num_seqs)), dtype=torch.uint8, device=dev)
+
+    def call_paged():
+        abi.attn_prefill_paged(q, kc, vc, bt, cu, sk, o, lse, True, x.scale, workspace=ws, stream=stream)
+    for _ in range(3):
+        call_paged()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call_paged()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    t = statistics.median(ts)
+    fl = sum(4.0 * c.Hq * c.d * roofline.allowed_pairs(a, b, True) for a, b in zip(q_lens, k_lens))
+    by = roofline.paged_prefill_bytes(q_lens, k_lens, c.Hq, c.Hkv, c.d, c.page_size)
+    bound = roofline.bound_rate(fl, by, peaks)
+    out[c.name] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_of_peak": fl / t / (peaks.bf16_tflops * 1e12),
+                   "frac_of_bound": fl / t / bound, "flops": "4 d per allowed (query, key) pair",
+                   "p10_us": sorted(ts)[len(ts) // 10] * 1e6, "p90_us": sorted(ts)[(9 * len(ts)) // 10] * 1e6}
+    del q, kc, vc, o, lse, ws
     torch.cuda.empty_cache()
     return out
 

@@ -122,6 +122,46 @@ ATTN_API attn_status attn_fwd_masked(const void* q, const void* k, const void* v
                      float scale, const attn_mask* mask, attn_dtype o_dtype, attn_stream_t stream);
 
 /*
+ * Bytes of scratch memory attn_prefill_paged() needs: the per-sequence unit
+ * prefix sums (num_seqs + 1 int32), rounded up to 256.  0 on invalid input.
+ */
+ATTN_API size_t attn_prefill_paged_workspace_size(int num_seqs);
+
+/*
+ * Chunked prefill against a paged KV cache, ragged over sequences
+ * ("Don't Write Kernels, Derive Them", section "What happened": paged
+ * KV-cache access; the attention of each row as in attn_fwd).
+ *   q:            [total_q, Hq, d] bf16, the sequences' new tokens packed in order
+ *   kcache/vcache: [num_pages, page_size, Hkv, d] bf16 (the layout of
+ *                 attn_decode_paged), already holding every context token,
+ *                 the new ones included
+ *   block_table:  [num_seqs, max_pages_per_seq] int32 device
+ *   cu_seqlens_q: [num_seqs + 1] int32 device: sequence s owns query tokens
+ *                 [cu_seqlens_q[s], cu_seqlens_q[s+1]); cu_seqlens_q[0] = 0 and
+ *                 the last entry <= total_q
+ *   seqlens_k:    [num_seqs] int32 device: context length k_len of sequence s
+ *                 (<= max_pages_per_seq * page_size)
+ *   o:            [total_q, Hq, d] bf16 or f32;  lse: [total_q, Hq] f32
+ * The q_len new tokens are the last q_len of the context: with causal, query
+ * i of the chunk sees keys j <= i + k_len - q_len (bottom-right alignment);
+ * window_left > 0 also drops keys j <= i + k_len - q_len - window_left.  A row
+ * with no key gets O = 0 and LSE = -inf.  page_size must be 16, 32, 64 or
+ * 128; workspace: device scratch of attn_prefill_paged_workspace_size()
+ * bytes, 16-byte aligned, caller-owned, not shared by overlapping calls.
+ * Cache slots past a sequence's context are never read as values (they may
+ * hold anything).  Inconsistent lengths or a block-table entry outside the
+ * pool are reported through attn_get_device_status() (ATTN_ERR_BOUNDS); the
+ * affected sequence is skipped or the entry not read.
+ */
+ATTN_API attn_status attn_prefill_paged(const void* q, const void* kcache, const void* vcache,
+                                        const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                        const int32_t* seqlens_k, void* o, float* lse, int num_seqs,
+                                        int total_q, int Hq, int Hkv, int d, int page_size, int num_pages,
+                                        int max_pages_per_seq, int causal, int window_left, float scale,
+                                        void* workspace, size_t workspace_bytes, attn_dtype o_dtype,
+                                        attn_stream_t stream);
+
+/*
  * Bytes of scratch memory attn_decode_paged() needs for these sizes (the
  * split partials: one float32 O row and one float32 LSE per sequence, split
  * and query head).  Pure function of its arguments; 0 on invalid input.
