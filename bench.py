@@ -420,7 +420,7 @@ def main(argv=None):
                                       "launch_us": launch_s * 1e6, "kernels": dec_kernels,
                                       "dram_latency_us": dram_s * 1e6,
                                       "measured_over_floor": mean_dec / dec_floor}},
-            "roofline": {"bound": "tensor", "kernel": "prefill_fwd_kernel<128,128,4>",
+            "roofline": {"bound": "tensor", "kernel": "prefill_fwd_kernel<128,2,5,0,0> (d128, two query tiles per CTA)",
                          "achieved": pre_tflops, "peak": peaks.bf16_tflops, "unit": "TFLOP/s",
                          "frac": pre_tflops / peaks.bf16_tflops, "peak_source": peak_src,
                          "traffic": traffic_from_profiles("prefill_fwd_c3"),
