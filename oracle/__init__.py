@@ -78,6 +78,9 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
             lib.oracle_prefill_paged.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, i, i,
                                                  ctypes.c_float, p, i64, p, p, i]
             lib.oracle_prefill_paged.restype = i
+            lib.oracle_attention_bwd.argtypes = [p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float,
+                                                 p, p, p, i]
+            lib.oracle_attention_bwd.restype = i
             _LIBS[mutant] = lib
         return lib
 
@@ -204,6 +207,29 @@ def decode_paged(q, kcache, vcache, block_table, seqlens, scale: float,
     if rc < 0:
         raise ValueError(f"oracle_decode_paged rejected its arguments ({rc})")
     return o, lse, rc
+
+
+def attention_bwd(q, k, v, dout, causal: bool, scale: float, threads: int = 0):
+    """Gradients (dQ, dK, dV) of the attention output for the upstream
+    gradient dout (see oracle_attention_bwd in attn_oracle.c), float64.
+
+    q, dout: [B, Hq, Nq, d]; k, v: [B, Hkv, Nk, d] (bf16).  Returns
+    (dQ [B,Hq,Nq,d], dK [B,Hkv,Nk,d], dV [B,Hkv,Nk,d], threads_used).
+    """
+    qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
+    B, Hq, Nq, d = qb.shape
+    _, Hkv, Nk, _ = kb.shape
+    if gb.shape != qb.shape or vb.shape != kb.shape:
+        raise ValueError("q/dout or k/v shape mismatch")
+    dq = np.empty((B, Hq, Nq, d), dtype=np.float64)
+    dk = np.empty((B, Hkv, Nk, d), dtype=np.float64)
+    dv = np.empty((B, Hkv, Nk, d), dtype=np.float64)
+    rc = _load().oracle_attention_bwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), B, Hq, Hkv, Nq, Nk, d,
+                                      int(bool(causal)), float(scale), _ptr(dq), _ptr(dk), _ptr(dv),
+                                      int(threads))
+    if rc < 0:
+        raise ValueError(f"oracle_attention_bwd rejected its arguments ({rc})")
+    return dq, dk, dv, rc
 
 
 def prefill_paged(q, kcache, vcache, block_table, cu_seqlens_q, seqlens_k, causal: bool,

@@ -468,3 +468,118 @@ int oracle_prefill_paged(const uint16_t* q, const uint16_t* kcache, const uint16
     }
     return bad ? -2 : nthreads;
 }
+
+/*
+ * Backward pass: the gradients of the attention output with respect to Q, K
+ * and V for an upstream gradient dO.
+ *
+ * The pages fix the forward only ("Compilers and Kernels", section
+ * "FlashAttention changes the algorithm around IO": O = softmax(S) V with
+ * S = scale * Q K^T + C); "Tang: a compiler that derives GPU kernels ...",
+ * abstract: gradients of comprehensions are comprehensions, and a flash-style
+ * attention backward recomputes instead of storing intermediates.  This is the
+ * derivative of that definition, written out by the chain rule, in double
+ * precision, from the exact softmax (two passes per row, no stored state):
+ *
+ *   P_ij  = exp(S_ij - m_i) / l_i            (the forward's weights)
+ *   O_i   = sum_j P_ij V_j                    (exact, not a rounded input)
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . V_j
+ *   D_i   = dO_i . O_i  ( = sum_j P_ij dP_ij )
+ *   dS_ij = P_ij (dP_ij - D_i)                (softmax Jacobian)
+ *   dQ_i  = scale * sum_j dS_ij K_j
+ *   dK_j  = scale * sum_i dS_ij Q_i
+ * With grouped-query attention dK and dV of a kv head sum over the query
+ * heads that read it.  Masked keys (causal, bottom-right) have P = 0 and take
+ * no gradient; a row with no allowed key contributes nothing.
+ *
+ * q, dout: [B][Hq][Nq][d]; k, v: [B][Hkv][Nk][d] (bf16 bits).  dq: [B][Hq][Nq][d],
+ * dk, dv: [B][Hkv][Nk][d] (double).  Returns the threads used, -1 on invalid
+ * sizes.
+ */
+int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                         int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                         double* dq, double* dk, double* dv, int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0 || d <= 0) return -1;
+    if (Hq % Hkv != 0) return -1;
+    const int group = Hq / Hkv;
+    const double sc = (double)scale;
+    nthreads = oracle_threads(nthreads);
+    memset(dq, 0, sizeof(double) * (size_t)B * Hq * Nq * d);
+    memset(dk, 0, sizeof(double) * (size_t)B * Hkv * Nk * d);
+    memset(dv, 0, sizeof(double) * (size_t)B * Hkv * Nk * d);
+    const int64_t pairs = (int64_t)B * Hkv;
+
+#pragma omp parallel num_threads(nthreads)
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        double* dp = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        double* o = (double*)malloc(sizeof(double) * (size_t)d);
+        int64_t w;
+        /* one (batch, kv head) per task: its dK and dV rows are written by it alone */
+#pragma omp for schedule(dynamic, 1)
+        for (w = 0; w < pairs; ++w) {
+            const int64_t b = w / Hkv, g = w % Hkv;
+            const uint16_t* kb = k + (b * Hkv + g) * (int64_t)Nk * d;
+            const uint16_t* vb = v + (b * Hkv + g) * (int64_t)Nk * d;
+            double* dkb = dk + (b * Hkv + g) * (int64_t)Nk * d;
+            double* dvb = dv + (b * Hkv + g) * (int64_t)Nk * d;
+            int hh;
+            for (hh = 0; hh < group; ++hh) {
+                const int64_t h = g * group + hh;
+                int64_t i;
+                for (i = 0; i < Nq; ++i) {
+                    const int64_t row = (b * Hq + h) * (int64_t)Nq + i;
+                    const uint16_t* qi = q + row * d;
+                    const uint16_t* doi = dout + row * d;
+                    int64_t n = Nk;
+                    if (causal) {
+                        n = i + (int64_t)Nk - (int64_t)Nq + 1;
+                        if (n < 0) n = 0;
+                        if (n > Nk) n = Nk;
+                    }
+                    if (n == 0) continue;
+                    int64_t j;
+                    int c;
+                    double m = -INFINITY;
+                    for (j = 0; j < n; ++j) {
+                        double s = 0.0;
+                        for (c = 0; c < d; ++c) s += bf16_to_double(qi[c]) * bf16_to_double(kb[j * d + c]);
+                        p[j] = s * sc;
+                        if (p[j] > m) m = p[j];
+                    }
+                    double l = 0.0;
+                    for (j = 0; j < n; ++j) {
+                        p[j] = exp(p[j] - m);
+                        l += p[j];
+                    }
+                    for (c = 0; c < d; ++c) o[c] = 0.0;
+                    for (j = 0; j < n; ++j) {
+                        p[j] /= l;
+                        for (c = 0; c < d; ++c) o[c] += p[j] * bf16_to_double(vb[j * d + c]);
+                    }
+                    double D = 0.0;
+                    for (c = 0; c < d; ++c) D += bf16_to_double(doi[c]) * o[c];
+                    for (j = 0; j < n; ++j) {
+                        double s = 0.0;
+                        for (c = 0; c < d; ++c) s += bf16_to_double(doi[c]) * bf16_to_double(vb[j * d + c]);
+                        dp[j] = s;
+                    }
+                    double* dqi = dq + row * d;
+                    for (j = 0; j < n; ++j) {
+                        const double ds = p[j] * (dp[j] - D);
+                        for (c = 0; c < d; ++c) {
+                            dqi[c] += sc * ds * bf16_to_double(kb[j * d + c]);
+                            dkb[j * d + c] += sc * ds * bf16_to_double(qi[c]);
+                            dvb[j * d + c] += p[j] * bf16_to_double(doi[c]);
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+        free(o);
+    }
+    return nthreads;
+}
