@@ -42,6 +42,11 @@ _lib.attn_prefill_paged_workspace_size.restype = ctypes.c_size_t
 _lib.attn_prefill_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
                                     _i, _i, ctypes.c_float, _vp, ctypes.c_size_t, _i, _vp]
 _lib.attn_prefill_paged.restype = _i
+_lib.attn_bwd_workspace_size.argtypes = [_i, _i, _i, _i]
+_lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
+_lib.attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, ctypes.c_float,
+                          _i, _vp, ctypes.c_size_t, _vp]
+_lib.attn_bwd.restype = _i
 _lib.attn_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
 _lib.attn_decode_workspace_size.restype = ctypes.c_size_t
 _lib.attn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
@@ -67,6 +72,7 @@ ATTN_F32 = 1
 
 #: every symbol include/attn.h declares
 EXPORTS = ("attn_fwd", "attn_fwd_masked", "attn_prefill_paged_workspace_size", "attn_prefill_paged",
+           "attn_bwd_workspace_size", "attn_bwd",
            "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_static",
            "attn_get_device_status", "attn_selftest_wait_timeout", "attn_status_string",
            "attn_launch_count", "attn_abi_version")
@@ -213,6 +219,37 @@ def attn_prefill_paged(q, kcache, vcache, block_table, cu_seqlens_q, seqlens_k, 
                                  _ptr(workspace), workspace.numel(),
                                  ATTN_F32 if o.dtype == torch.float32 else ATTN_BF16, _stream_ptr(stream))
     _check(st, "attn_prefill_paged")
+
+
+def attn_bwd_workspace_size(B: int, Hq: int, Nq: int, d: int) -> int:
+    return int(_lib.attn_bwd_workspace_size(int(B), int(Hq), int(Nq), int(d)))
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool, scale: float, workspace=None, stream=None) -> None:
+    """Backward of attn_fwd: dq [B,Hq,Nq,d], dk, dv [B,Hkv,Nk,d] (all bf16 or
+    all f32) from q, k, v, the forward's o and lse, and the upstream dout."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    gd = dq.dtype
+    if gd not in (torch.bfloat16, torch.float32) or dk.dtype != gd or dv.dtype != gd:
+        raise TypeError("dq, dk, dv must all be bfloat16 or all float32")
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, gd, n)
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nk, _ = k.shape
+    if (v.shape != k.shape or o.shape != q.shape or dout.shape != q.shape or tuple(lse.shape) != (B, Hq, Nq)
+            or dq.shape != q.shape or dk.shape != k.shape or dv.shape != k.shape):
+        raise ValueError("backward shape mismatch")
+    need = attn_bwd_workspace_size(B, Hq, Nq, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = _lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                       B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
+                       ATTN_F32 if gd == torch.float32 else ATTN_BF16, _ptr(workspace), workspace.numel(),
+                       _stream_ptr(stream))
+    _check(st, "attn_bwd")
 
 
 def attn_decode_workspace_size(num_seqs: int, Hq: int, Hkv: int, d: int, max_seqlen: int) -> int:

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -682,3 +683,5 @@ attn_status attn_get_device_status(attn_stream_t stream) {
 }
 
 }  // extern "C"
+
+#include "bwd_api.cuh"

@@ -1,0 +1,451 @@
+// Attention backward: dQ, dK, dV by recomputing the weights from the saved
+// row logsumexp ("Tang: a compiler that derives GPU kernels and bounds how
+// fast they can run", abstract: a flash-style backward that writes no
+// intermediates; the derivative of the forward of "Compilers and Kernels",
+// section "FlashAttention changes the algorithm around IO").
+//
+// Per (batch, kv head, 128-key tile) one CTA keeps K, V, and the dK, dV
+// accumulators resident and walks every (query head of the group, 128-row
+// query tile) whose rows see its keys:
+//   S^T  = K Q^T              (tensor memory, rows = keys)
+//   P^T  = exp(scale S^T - LSE)      with the mask (0 where disallowed)
+//   dP^T = V dO^T
+//   dS^T = P^T * (dP^T - D),  D = rowsum(dO * O) (prep kernel)
+//   dV  += P^T dO,  dK += dS^T Q     (A operands from tensor memory)
+//   dQ_t = dS K                      (dS staged in shared memory), added to an
+//                                     f32 dQ accumulator in global memory
+// The 1/sqrt(d)-style scale is applied to dK at the end and to dQ as it is
+// accumulated.  Roles: warp 0 TMA producer, warp 1 MMA issuer (one thread),
+// warps 2..5 one thread per key row (weights, dS) and then one thread per
+// query row (the dQ tile's accumulation), with bounded waits everywhere.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace attn {
+
+struct BwdParams {
+  void* dk;            // [B*Hkv][Nk][d] bf16 or f32
+  void* dv;
+  float* dq_acc;       // [B*Hq][Nq][d] f32, zero on entry
+  const float* lse;    // [B*Hq][Nq] forward row logsumexp (natural log)
+  const float* dsum;   // [B*Hq][Nq] rowsum(dO * O) (prep kernel)
+  int B, Hq, Hkv, Nq, Nk;
+  int causal;
+  int g_f32;           // gradients written as f32 (else bf16)
+  float scale;         // > 0
+  float scale_log2;    // scale * log2(e)
+};
+
+template <int D, int STAGES>
+struct BwdLayout {
+  static constexpr int kThreads = 192;
+  static constexpr int kTile = 128 * D * 2;           // one [128][D] bf16 tile, 64-column swizzled boxes
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kTile;
+  static constexpr int kQOff = kVOff + kTile;         // STAGES x (Q tile, dO tile)
+  static constexpr int kStage = 2 * kTile;
+  static constexpr int kDSOff = kQOff + STAGES * kStage;   // dS^T [128 keys][128 queries] bf16
+  static constexpr int kDSBytes = 128 * 128 * 2;
+  static constexpr int kRowOff = kDSOff + kDSBytes;   // 2 x (LSE[128], D[128]) f32, one per item parity
+  static constexpr int kRowBytes = 2 * 128 * 4;
+  static constexpr int kBarOff = kRowOff + 2 * kRowBytes;
+  // kv_full, q_full[S], q_empty[S], s_full, dp_full, ds_full, dq_full, dq_free, dkv_done, rows_ready[2]
+  static constexpr int kNumBars = 1 + 2 * STAGES + 6 + 2;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 128;         // the base is checked for 1024-byte alignment
+  // Tensor memory columns: dK, dV accumulators, the S^T slot (later P^T in its
+  // first 64 columns), the dP^T slot (later dS^T in its first 64 columns), and
+  // the dQ tile (its own columns when they fit, else the S^T slot).
+  static constexpr int kColDK = 0;
+  static constexpr int kColDV = D;
+  static constexpr int kColS = 2 * D;
+  static constexpr int kColDP = 2 * D + 128;
+  static constexpr bool kSharedDQ = 3 * D + 256 > 512;
+  static constexpr int kColDQ = kSharedDQ ? kColS : 2 * D + 256;
+  static_assert(kBytes + 128 <= 232448, "shared memory budget");
+  static_assert(D == 64 || D == 128, "backward head dims");
+};
+
+// D[r] = sum_c O[r][c] dO[r][c] (f32) and the dQ accumulator zeroed; one warp per row.
+__global__ void bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, float* Dsum, float* dq_acc, long long rows,
+                                int d) {
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+       r += nwarps) {
+    float acc = 0.f;
+    for (int c = lane * 8; c < d; c += 256) {
+      const uint4 a = *reinterpret_cast<const uint4*>(o + r * d + c);
+      const uint4 b = *reinterpret_cast<const uint4*>(dout + r * d + c);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(bf16lo(aw[e]), bf16lo(bw[e]), acc);
+        acc = fmaf(bf16hi(aw[e]), bf16hi(bw[e]), acc);
+      }
+      float4* z = reinterpret_cast<float4*>(dq_acc + r * d + c);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+    if (lane == 0) Dsum[r] = acc;
+  }
+}
+
+// dq = dq_acc as bf16 (RNE) or f32.
+__global__ void bwd_post_kernel(const float* dq_acc, void* dq, long long n4, int g_f32) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 v = reinterpret_cast<const float4*>(dq_acc)[i];
+    if (g_f32) {
+      reinterpret_cast<float4*>(dq)[i] = v;
+    } else {
+      reinterpret_cast<uint2*>(dq)[i] = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+    }
+  }
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+template <int D, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const BwdParams p) {
+  using L = BwdLayout<D, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  if (pad + L::kBytes > static_cast<uint32_t>(L::kAlloc)) {
+    // The dynamic shared memory does not start close enough to a 1024-byte
+    // boundary for this layout: report instead of overrunning it.
+    if (threadIdx.x == 0) report_error(5 /* ATTN_ERR_LAUNCH */, 30, static_cast<int>(pad));
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw + pad;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = q_full + STAGES;
+  uint64_t* s_full = q_empty + STAGES;
+  uint64_t* dp_full = s_full + 1;
+  uint64_t* ds_full = dp_full + 1;
+  uint64_t* dq_full = ds_full + 1;
+  uint64_t* dq_free = dq_full + 1;
+  uint64_t* dkv_done = dq_free + 1;
+  uint64_t* rows_ready = dkv_done + 1;  // [2]: the item's LSE / D values are in shared memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int BHkv = p.B * p.Hkv;
+  const int kt = blockIdx.x / BHkv;          // key tile (longest-first: tile 0 is seen by the most rows)
+  const int bkv = blockIdx.x - kt * BHkv;    // batch * Hkv + kv head
+  const int b = bkv / p.Hkv;
+  const int kvh = bkv - b * p.Hkv;
+  const int k0 = kt * 128;
+  const int G = p.Hq / p.Hkv;
+  const int diag = p.Nk - p.Nq;
+  const int ntq = (p.Nq + 127) / 128;
+  // Query tiles whose rows see some key of this tile: i >= k0 - diag when causal.
+  int qt_lo = 0;
+  if (p.causal) qt_lo = max(0, (k0 - diag) / 128);
+  if (p.causal && k0 - diag >= p.Nq) qt_lo = ntq;
+  const int per_head = ntq - qt_lo;
+  const int n_items = G * per_head;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(ds_full, 4);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 4);
+    mbar_init(dkv_done, 1);
+    mbar_init(&rows_ready[0], 128);
+    mbar_init(&rows_ready[1], 128);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Item n: query head bh_q = b*Hq + kvh*G + n / per_head, query tile qt_lo + n % per_head.
+  auto item_bh = [&](int n) { return b * p.Hq + kvh * G + n / per_head; };
+  auto item_q0 = [&](int n) { return (qt_lo + n % per_head) * 128; };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && n_items > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_expect_tx(kv_full, 2 * L::kTile);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(smem + L::kKOff + c * (128 * 128), &tmK, kv_full, c * 64, k0, bkv);
+        tma_load_3d(smem + L::kVOff + c * (128 * 128), &tmV, kv_full, c * 64, k0, bkv);
+      }
+      int n = 0;
+      for (; n < n_items; ++n) {
+        const int st = n % STAGES;
+        if (!mbar_wait(&q_empty[st], ((n / STAGES) & 1) ^ 1, 40)) break;
+        mbar_expect_tx(&q_full[st], L::kStage);
+        const int bh = item_bh(n), q0 = item_q0(n);
+        uint8_t* stage = smem + L::kQOff + st * L::kStage;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(stage + c * (128 * 128), &tmQ, &q_full[st], c * 64, q0, bh);
+          tma_load_3d(stage + L::kTile + c * (128 * 128), &tmDO, &q_full[st], c * 64, q0, bh);
+        }
+      }
+      // Drain: never leave the CTA with a copy still writing shared memory.
+      mbar_wait(kv_full, 0, 41);
+      for (int it = max(0, n - STAGES); it < n; ++it) mbar_wait(&q_full[it % STAGES], (it / STAGES) & 1, 42);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_items > 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T: K-major A and B
+      constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);    // dV, dK: A from TMEM, B MN-major
+      constexpr uint32_t kIdQ = idesc_bf16_f32(128, D, 1, 1);    // dQ: A (dS) and B (K) MN-major
+      const uint64_t dK_a = sdesc_sw128(sbase + L::kKOff, 16, 1024);
+      const uint64_t dV_a = sdesc_sw128(sbase + L::kVOff, 16, 1024);
+      const uint64_t dK_b = sdesc_sw128(sbase + L::kKOff, 128 * 128, 1024);
+      const uint64_t dS_a = sdesc_sw128(sbase + L::kDSOff, 128 * 128, 1024);
+      bool ok = mbar_wait(kv_full, 0, 43);
+      if (ok) tc_fence_after();
+      for (int n = 0; ok && n < n_items; ++n) {
+        const int st = n % STAGES;
+        ok = mbar_wait(&q_full[st], (n / STAGES) & 1, 44);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qs = sbase + L::kQOff + st * L::kStage;
+        const uint64_t dQ_b = sdesc_sw128(qs, 16, 1024);
+        const uint64_t dO_b = sdesc_sw128(qs + L::kTile, 16, 1024);
+        const uint64_t dQ_mn = sdesc_sw128(qs, 128 * 128, 1024);
+        const uint64_t dO_mn = sdesc_sw128(qs + L::kTile, 128 * 128, 1024);
+        if (L::kSharedDQ && n > 0) {
+          // The previous dQ tile (in the S^T columns) must have been read out.
+          ok = mbar_wait(dq_free, (n - 1) & 1, 45);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // S^T = K Q^T and dP^T = V dO^T (K = d).
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+          umma_bf16_ss(tmem + L::kColS, dK_a + o, dQ_b + o, kIdS, kk > 0);
+        }
+        umma_commit(s_full);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+          umma_bf16_ss(tmem + L::kColDP, dV_a + o, dO_b + o, kIdS, kk > 0);
+        }
+        umma_commit(dp_full);
+        ok = mbar_wait(ds_full, n & 1, 46);
+        if (!ok) break;
+        tc_fence_after();
+        // dV += P^T dO, dK += dS^T Q (K = 128 query rows; A from TMEM).
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
+          umma_bf16_ts(tmem + L::kColDV, tmem + L::kColS + kk * 8, dO_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
+          umma_bf16_ts(tmem + L::kColDK, tmem + L::kColDP + kk * 8, dQ_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!L::kSharedDQ && n > 0) {
+          ok = mbar_wait(dq_free, (n - 1) & 1, 47);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // dQ tile = dS K (K = 128 keys).
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
+          umma_bf16_ss(tmem + L::kColDQ, dS_a + o, dK_b + o, kIdQ, kk > 0);
+        }
+        umma_commit(dq_full);
+        umma_commit(&q_empty[st]);
+      }
+      umma_commit(dkv_done);
+      mbar_wait(dkv_done, 0, 48);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- key rows, then query rows
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int kj = k0 + row;  // this thread's key
+    bool ok = true;
+    for (int n = 0; ok && n < n_items; ++n) {
+      const int bh = item_bh(n), q0 = item_q0(n);
+      // The item's 128 LSE and D values: one per thread into shared memory,
+      // then everyone reads all of them (a bounded barrier of the 128 threads).
+      float* lse = reinterpret_cast<float*>(smem + L::kRowOff + (n & 1) * L::kRowBytes);
+      float* dsum = lse + 128;
+      {
+        const int qi = q0 + row;
+        const size_t r = static_cast<size_t>(bh) * p.Nq + qi;
+        lse[row] = qi < p.Nq ? __ldg(p.lse + r) : 0.f;
+        dsum[row] = qi < p.Nq ? __ldg(p.dsum + r) : 0.f;
+        mbar_arrive(&rows_ready[n & 1]);
+      }
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&rows_ready[n & 1], (n >> 1) & 1, 49));
+      if (!ok) break;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(s_full, n & 1, 50));
+      if (!ok) break;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(dp_full, n & 1, 51));
+      if (!ok) break;
+      tc_fence_after();
+      // Query c of the tile is allowed for this key iff c < Nq - q0, and
+      // (causal) kj <= q0 + c + diag.
+      const int c_hi = p.Nq - q0;                           // columns >= c_hi: past Nq
+      const int c_lo = p.causal ? kj - diag - q0 : -0x7FFFFFFF;  // columns < c_lo: masked
+      const bool key_ok = kj < p.Nk;
+      const uint32_t ds_row = sbase + L::kDSOff + row * 128;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {  // 32 query columns per chunk
+        uint32_t s[32], dp[32];
+        tmem_ld32(lane_base + L::kColS + ch * 32, s);
+        tmem_ld32(lane_base + L::kColDP + ch * 32, dp);
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pe[2], de[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = ch * 32 + e + u;
+            const float l2 = lse[c];
+            // LSE = -inf: the row saw no key; its weights are 0.
+            const float m2 = (l2 == -INFINITY) ? INFINITY : l2 * 1.4426950408889634f;
+            const bool allowed = key_ok && c < c_hi && c >= c_lo;
+            const float pv = allowed ? ex2(fmaf(__uint_as_float(s[e + u]), p.scale_log2, -m2)) : 0.f;
+            pe[u] = pv;
+            de[u] = pv * (__uint_as_float(dp[e + u]) - dsum[c]);
+          }
+          pw[e >> 1] = pack_bf16(pe[0], pe[1]);
+          dw[e >> 1] = pack_bf16(de[0], de[1]);
+        }
+        // P^T into the S^T slot, dS^T into the dP^T slot (columns already read).
+        tmem_st16(lane_base + L::kColS + ch * 16, pw);
+        tmem_st16(lane_base + L::kColDP + ch * 16, dw);
+        // dS^T row into shared memory: 16-byte unit u of the 64-query half h at
+        // position u ^ (row & 7) (128-byte swizzle).
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+          const int u = ch * 4 + u4;  // 16-byte unit over the 128 queries
+          const int h = u >> 3;
+          const int uu = u & 7;
+          st_shared_v4(ds_row + h * (128 * 128) + ((uu ^ (row & 7)) << 4), dw[4 * u4], dw[4 * u4 + 1],
+                       dw[4 * u4 + 2], dw[4 * u4 + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+
+      // dQ tile rows (TMEM lane = query row): scale and add into the accumulator.
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(dq_full, n & 1, 52));
+      if (!ok) break;
+      tc_fence_after();
+      const int qi = q0 + row;
+      float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qi) * D;
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + L::kColDQ + ch * 32, v);
+        if (qi < p.Nq) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            red_add_v4(dst + ch * 32 + e, __uint_as_float(v[e]) * p.scale, __uint_as_float(v[e + 1]) * p.scale,
+                       __uint_as_float(v[e + 2]) * p.scale, __uint_as_float(v[e + 3]) * p.scale);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_free);
+    }
+
+    // dK, dV rows of this key (zeros when no query row sees the tile).  The
+    // tensor-memory loads are warp-collective: every lane runs them, and only
+    // the stores depend on the lane's key being inside Nk.
+    if (ok && n_items > 0) {
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(dkv_done, 0, 53));
+      if (ok) tc_fence_after();
+    }
+    if (ok) {
+      const bool store = kj < p.Nk;
+      const size_t off = (static_cast<size_t>(bkv) * p.Nk + kj) * D;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? L::kColDK : L::kColDV;
+        const float mul = which == 0 ? p.scale : 1.f;
+        void* outp = which == 0 ? p.dk : p.dv;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t v[32];
+          if (n_items > 0) {
+            tmem_ld32(lane_base + col + ch * 32, v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          }
+          if (!store) continue;
+          if (p.g_f32) {
+            float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(outp) + off + ch * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              o4[e] = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
+                                  __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
+          } else {
+            uint4* o4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(outp) + off + ch * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int x = 8 * e;
+              o4[e] = make_uint4(pack_bf16(__uint_as_float(v[x]) * mul, __uint_as_float(v[x + 1]) * mul),
+                                 pack_bf16(__uint_as_float(v[x + 2]) * mul, __uint_as_float(v[x + 3]) * mul),
+                                 pack_bf16(__uint_as_float(v[x + 4]) * mul, __uint_as_float(v[x + 5]) * mul),
+                                 pack_bf16(__uint_as_float(v[x + 6]) * mul, __uint_as_float(v[x + 7]) * mul));
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace attn

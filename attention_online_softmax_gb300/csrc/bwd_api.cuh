@@ -1,0 +1,113 @@
+// C entry points of the attention backward (declared in include/attn.h);
+// included at the end of attn_api.cu so that it shares that translation
+// unit's device status word, launch counter and tensor-map helpers.
+#pragma once
+
+#include "bwd.cuh"
+
+namespace {
+
+size_t bwd_align(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+template <int D, int STAGES>
+attn_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
+                       const attn::BwdParams& p, cudaStream_t stream) {
+  using L = attn::BwdLayout<D, STAGES>;
+  auto kern = attn::attn_bwd_kernel<D, STAGES>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  const long long grid = static_cast<long long>(p.B) * p.Hkv * ((p.Nk + 127) / 128);
+  if (grid > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
+  if (grid == 0) return ATTN_OK;
+  kern<<<dim3(static_cast<unsigned>(grid)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mdo, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int d) {
+  if (B < 0 || Hq <= 0 || Nq < 0 || (d != 64 && d != 128)) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * Nq;
+  return bwd_align(rows * sizeof(float)) + bwd_align(rows * d * sizeof(float));
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                     float scale, attn_dtype grad_dtype, void* workspace, size_t workspace_bytes,
+                     attn_stream_t stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (grad_dtype != ATTN_BF16 && grad_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || (Nq == 0 && Nk == 0)) return ATTN_OK;
+  if (Nq > 0 && (!aligned16(q) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) || !aligned16(dq)))
+    return ATTN_ERR_MISALIGNED;
+  if (Nk > 0 && (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv))) return ATTN_ERR_MISALIGNED;
+  const size_t need = attn_bwd_workspace_size(B, Hq, Nq, d);
+  if (!aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  attn_status st = check_device();
+  if (st != ATTN_OK) return st;
+
+  const size_t rows = static_cast<size_t>(B) * Hq * Nq;
+  float* dsum = static_cast<float*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + bwd_align(rows * sizeof(float)));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int sms = sm_count();
+  if (rows > 0) {
+    const long long blocks = std::min<long long>((static_cast<long long>(rows) + 7) / 8, 8LL * sms);
+    attn::bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), dsum, dq_acc,
+        static_cast<long long>(rows), d);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+
+  if (Nk > 0) {
+    CUtensorMap mq, mk, mv, mdo;
+    // With Nq == 0 no query tile is ever loaded; the Q / dO maps then describe k.
+    const void* qb = Nq > 0 ? q : k;
+    const void* db = Nq > 0 ? dout : k;
+    const int nq_map = Nq > 0 ? Nq : Nk;
+    const int bh_map = Nq > 0 ? B * Hq : B * Hkv;
+    if (!encode_rows_map(&mq, qb, d, nq_map, bh_map, 128) || !encode_rows_map(&mdo, db, d, nq_map, bh_map, 128) ||
+        !encode_rows_map(&mk, k, d, Nk, B * Hkv, 128) || !encode_rows_map(&mv, v, d, Nk, B * Hkv, 128))
+      return ATTN_ERR_LAUNCH;
+    attn::BwdParams p;
+    p.dk = dk;
+    p.dv = dv;
+    p.dq_acc = dq_acc;
+    p.lse = lse;
+    p.dsum = dsum;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.causal = causal ? 1 : 0;
+    p.g_f32 = grad_dtype == ATTN_F32 ? 1 : 0;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    st = d == 64 ? launch_bwd<64, 3>(mq, mk, mv, mdo, p, s) : launch_bwd<128, 2>(mq, mk, mv, mdo, p, s);
+    if (st != ATTN_OK) return st;
+  }
+
+  if (rows > 0) {
+    const long long n4 = static_cast<long long>(rows) * d / 4;
+    const long long blocks = std::min<long long>((n4 + 255) / 256, 8LL * sms);
+    attn::bwd_post_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(dq_acc, dq, n4,
+                                                                      grad_dtype == ATTN_F32 ? 1 : 0);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  return ATTN_OK;
+}
+
+}  // extern "C"

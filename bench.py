@@ -41,24 +41,29 @@ UNIT = "fraction of roofline (step floor time / step time, summed over GPUs)"
 WORKLOAD = ("prefill causal MHA B2 H32 N4096 d128 bf16 + paged GQA decode 64 seqs Hq32 Hkv8 d128 "
             "len U[512,8192] 16-token pages in a 40000-page pool")
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = [os.path.join(ROOT, "attention_online_softmax_gb300", "csrc", f)
-                  for f in ("attn_api.cu", "ptx.cuh", "prefill_fwd.cuh", "decode.cuh")]
+_CSRC = os.path.join(ROOT, "attention_online_softmax_gb300", "csrc")
+# The sources that define each profiled kernel: its own header and the shared
+# PTX helpers.
+KERNEL_SOURCES = {
+    "prefill_fwd_c3": [os.path.join(_CSRC, f) for f in ("ptx.cuh", "prefill_fwd.cuh")],
+    "decode_c5": [os.path.join(_CSRC, f) for f in ("ptx.cuh", "decode.cuh")],
+}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in KERNEL_SOURCES[kernel]:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def traffic_from_profiles(kernel: str) -> float | None:
-    """Per-launch DRAM bytes recorded in profiles/traffic.txt for this kernel
+    """Per-launch DRAM bytes recorded in profiles/traffic.txt for this kernel's
     source hash (lines: `<kernel> <source-hash> <bytes>`); None when the kernel
     changed since the capture."""
     path = os.path.join(PROFILE_DIR, "traffic.txt")
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel)
     try:
         for line in open(path):
             parts = line.split()

@@ -162,6 +162,37 @@ ATTN_API attn_status attn_prefill_paged(const void* q, const void* kcache, const
                                         attn_stream_t stream);
 
 /*
+ * Bytes of scratch memory attn_bwd() needs: D = rowsum(dO * O) per query row
+ * (f32) and an f32 dQ accumulator [B, Hq, Nq, d], each rounded up to 256.
+ * 0 on invalid input (d must be 64 or 128).
+ */
+ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int d);
+
+/*
+ * Backward pass of attn_fwd: the gradients of O with respect to Q, K and V
+ * for an upstream gradient dO, recomputing the weights from the saved LSE
+ * ("Tang: a compiler that derives GPU kernels ...", abstract: a flash-style
+ * backward that writes no intermediates).  With P = softmax(S) the forward's
+ * weights and D_i = dO_i . O_i:  dV = P^T dO,  dS = P * (dO V^T - D),
+ * dQ = scale * dS K,  dK = scale * dS^T Q  (dK, dV summed over the query heads
+ * of a kv group).
+ *   q, o, dout: [B, Hq, Nq, d] bf16 (o: the forward's output); lse: [B, Hq, Nq]
+ *   f32 from attn_fwd; k, v: [B, Hkv, Nk, d] bf16; causal, scale as passed to
+ *   attn_fwd.  dq: [B, Hq, Nq, d]; dk, dv: [B, Hkv, Nk, d], bf16 or f32 by
+ *   grad_dtype.  d must be 64 or 128.
+ *   workspace: device scratch of attn_bwd_workspace_size() bytes, 16-byte
+ *   aligned, caller-owned, not shared by overlapping calls.
+ * Three kernels on `stream` (rows D and a zeroed dQ accumulator; the fused
+ * backward, one CTA per (batch, kv head, 128-key tile); the dQ conversion).
+ * dK and dV are deterministic; dQ sums its per-key-tile parts with atomic adds,
+ * so its last bits can differ from run to run.
+ */
+ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                              const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq,
+                              int Nk, int d, int causal, float scale, attn_dtype grad_dtype, void* workspace,
+                              size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * Bytes of scratch memory attn_decode_paged() needs for these sizes (the
  * split partials: one float32 O row and one float32 LSE per sequence, split
  * and query head).  Pure function of its arguments; 0 on invalid input.
