@@ -55,9 +55,10 @@ struct BwdLayout {
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 128;         // the base is checked for 1024-byte alignment
-  // Tensor memory columns: dK, dV accumulators, the S^T slot (later P^T in its
-  // first 64 columns), the dP^T slot (later dS^T in its first 64 columns), and
-  // the dQ tile (its own columns when they fit, else the S^T slot).
+  // Tensor memory columns: dK, dV accumulators, the S^T slot, the dP^T slot
+  // (later dS^T in its first 64 columns and P^T in its last 64), and the dQ
+  // tile (its own columns when they fit, else the S^T slot, free once S^T has
+  // been read).
   static constexpr int kColDK = 0;
   static constexpr int kColDV = D;
   static constexpr int kColS = 2 * D;
@@ -244,51 +245,55 @@ __global__ void __launch_bounds__(192, 1)
         const uint64_t dO_b = sdesc_sw128(qs + L::kTile, 16, 1024);
         const uint64_t dQ_mn = sdesc_sw128(qs, 128 * 128, 1024);
         const uint64_t dO_mn = sdesc_sw128(qs + L::kTile, 128 * 128, 1024);
-        if (L::kSharedDQ && n > 0) {
-          // The previous dQ tile (in the S^T columns) must have been read out.
-          ok = mbar_wait(dq_free, (n - 1) & 1, 45);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        // S^T = K Q^T and dP^T = V dO^T (K = d).
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
-          umma_bf16_ss(tmem + L::kColS, dK_a + o, dQ_b + o, kIdS, kk > 0);
-        }
-        umma_commit(s_full);
+        // dP^T = V dO^T (K = d) first: its slot is free once the previous
+        // item's dV and dK products (issued earlier) have read it.
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
           umma_bf16_ss(tmem + L::kColDP, dV_a + o, dO_b + o, kIdS, kk > 0);
         }
         umma_commit(dp_full);
+        if (L::kSharedDQ && n > 0) {
+          // The previous dQ tile (in the S^T columns) must have been read out.
+          ok = mbar_wait(dq_free, (n - 1) & 1, 45);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // S^T = K Q^T (K = d).
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+          umma_bf16_ss(tmem + L::kColS, dK_a + o, dQ_b + o, kIdS, kk > 0);
+        }
+        umma_commit(s_full);
         ok = mbar_wait(ds_full, n & 1, 46);
         if (!ok) break;
         tc_fence_after();
-        // dV += P^T dO, dK += dS^T Q (K = 128 query rows; A from TMEM).
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
-          umma_bf16_ts(tmem + L::kColDV, tmem + L::kColS + kk * 8, dO_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
-          umma_bf16_ts(tmem + L::kColDK, tmem + L::kColDP + kk * 8, dQ_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
-        }
         if (!L::kSharedDQ && n > 0) {
           ok = mbar_wait(dq_free, (n - 1) & 1, 47);
           if (!ok) break;
           tc_fence_after();
         }
-        // dQ tile = dS K (K = 128 keys).
+        // dQ tile = dS K (K = 128 keys) first, so that its read-out overlaps
+        // the dV and dK products.
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
           umma_bf16_ss(tmem + L::kColDQ, dS_a + o, dK_b + o, kIdQ, kk > 0);
         }
         umma_commit(dq_full);
+        // dV += P^T dO, dK += dS^T Q (K = 128 query rows; A from TMEM).
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
+          umma_bf16_ts(tmem + L::kColDV, tmem + L::kColDP + 64 + kk * 8, dO_mn + o, kIdG,
+                       (n > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
+          umma_bf16_ts(tmem + L::kColDK, tmem + L::kColDP + kk * 8, dQ_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
+        }
         umma_commit(&q_empty[st]);
       }
       umma_commit(dkv_done);
@@ -302,24 +307,43 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int kj = k0 + row;  // this thread's key
     bool ok = true;
+    // This thread's query row of an item: its LSE and D, read one item ahead.
+    auto row_vals = [&](int n, float& l, float& dd) {
+      l = 0.f;
+      dd = 0.f;
+      if (n < n_items) {
+        const int qi = item_q0(n) + row;
+        if (qi < p.Nq) {
+          const size_t r = static_cast<size_t>(item_bh(n)) * p.Nq + qi;
+          l = __ldg(p.lse + r);
+          dd = __ldg(p.dsum + r);
+        }
+      }
+    };
+    float l_next, d_next;
+    row_vals(0, l_next, d_next);
     for (int n = 0; ok && n < n_items; ++n) {
       const int bh = item_bh(n), q0 = item_q0(n);
       // The item's 128 LSE and D values: one per thread into shared memory,
       // then everyone reads all of them (a bounded barrier of the 128 threads).
       float* lse = reinterpret_cast<float*>(smem + L::kRowOff + (n & 1) * L::kRowBytes);
       float* dsum = lse + 128;
-      {
-        const int qi = q0 + row;
-        const size_t r = static_cast<size_t>(bh) * p.Nq + qi;
-        lse[row] = qi < p.Nq ? __ldg(p.lse + r) : 0.f;
-        dsum[row] = qi < p.Nq ? __ldg(p.dsum + r) : 0.f;
-        mbar_arrive(&rows_ready[n & 1]);
-      }
+      lse[row] = l_next;
+      dsum[row] = d_next;
+      mbar_arrive(&rows_ready[n & 1]);
+      row_vals(n + 1, l_next, d_next);
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&rows_ready[n & 1], (n >> 1) & 1, 49));
       if (!ok) break;
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(s_full, n & 1, 50));
-      if (!ok) break;
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(dp_full, n & 1, 51));
+      if (!ok) break;
+      tc_fence_after();
+      // The whole dP^T row first: its columns then take dS^T and P^T.
+      uint32_t dp[128];
+      tmem_ld32(lane_base + L::kColDP + 0, *reinterpret_cast<uint32_t(*)[32]>(dp + 0));
+      tmem_ld32(lane_base + L::kColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(dp + 32));
+      tmem_ld32(lane_base + L::kColDP + 64, *reinterpret_cast<uint32_t(*)[32]>(dp + 64));
+      tmem_ld32(lane_base + L::kColDP + 96, *reinterpret_cast<uint32_t(*)[32]>(dp + 96));
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(s_full, n & 1, 50));
       if (!ok) break;
       tc_fence_after();
       // Query c of the tile is allowed for this key iff c < Nq - q0, and
@@ -328,11 +352,10 @@ __global__ void __launch_bounds__(192, 1)
       const int c_lo = p.causal ? kj - diag - q0 : -0x7FFFFFFF;  // columns < c_lo: masked
       const bool key_ok = kj < p.Nk;
       const uint32_t ds_row = sbase + L::kDSOff + row * 128;
-#pragma unroll 1
+#pragma unroll
       for (int ch = 0; ch < 4; ++ch) {  // 32 query columns per chunk
-        uint32_t s[32], dp[32];
+        uint32_t s[32];
         tmem_ld32(lane_base + L::kColS + ch * 32, s);
-        tmem_ld32(lane_base + L::kColDP + ch * 32, dp);
         uint32_t pw[16], dw[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -346,14 +369,15 @@ __global__ void __launch_bounds__(192, 1)
             const bool allowed = key_ok && c < c_hi && c >= c_lo;
             const float pv = allowed ? ex2(fmaf(__uint_as_float(s[e + u]), p.scale_log2, -m2)) : 0.f;
             pe[u] = pv;
-            de[u] = pv * (__uint_as_float(dp[e + u]) - dsum[c]);
+            de[u] = pv * (__uint_as_float(dp[c]) - dsum[c]);
           }
           pw[e >> 1] = pack_bf16(pe[0], pe[1]);
           dw[e >> 1] = pack_bf16(de[0], de[1]);
         }
-        // P^T into the S^T slot, dS^T into the dP^T slot (columns already read).
-        tmem_st16(lane_base + L::kColS + ch * 16, pw);
+        // dS^T into the first half of the dP^T slot, P^T into its second half
+        // (the row is already in registers).
         tmem_st16(lane_base + L::kColDP + ch * 16, dw);
+        tmem_st16(lane_base + L::kColDP + 64 + ch * 16, pw);
         // dS^T row into shared memory: 16-byte unit u of the 64-query half h at
         // position u ^ (row & 7) (128-byte swizzle).
 #pragma unroll

@@ -61,6 +61,14 @@ def prefill_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:
     return q + kv + o + lse
 
 
+def bwd_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:
+    """Backward: Q, O, dO read and dQ written (bf16) per query head; K, V read
+    and dK, dV written per kv head; LSE read (f32)."""
+    qside = B * Hq * Nq * d * BF16 * 4
+    kside = B * Hkv * Nk * d * BF16 * 4
+    return qside + kside + B * Hq * Nq * F32
+
+
 def paged_prefill_bytes(q_lens, k_lens, Hq: int, Hkv: int, d: int, page_size: int) -> int:
     """Chunked prefill: new-token Q, O (bf16) and LSE (f32), each sequence's
     context K and V once per KV head, and the block-table entries used."""

@@ -619,6 +619,40 @@ def per_config_table(abi, dev, stream, peaks, reps: int = 10):
                        "frac_of_bound": fl / t / bound, "flops": "4 d per allowed (query, key) pair",
                        "p10_us": sorted(ts)[len(ts) // 10] * 1e6, "p90_us": sorted(ts)[(9 * len(ts)) // 10] * 1e6}
         del q, k, v, o, lse, slopes, bias
+    # Backward of the long causal MHA workload (forward output and LSE as inputs).
+    c = configs.LONG
+    x = make_prefill_inputs(c)
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale, stream)
+    g = torch.Generator().manual_seed(c.seed + 50)
+    dout = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(abi.attn_bwd_workspace_size(c.B, c.Hq, c.Nq, c.d), dtype=torch.uint8, device=dev)
+
+    def call_bwd():
+        abi.attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, c.causal, x.scale, workspace=ws, stream=stream)
+    for _ in range(3):
+        call_bwd()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call_bwd()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    t = statistics.median(ts)
+    fl = 2.5 * roofline.prefill_flops(c.B, c.Hq, c.Nq, c.Nk, c.d, c.causal)
+    by = roofline.bwd_bytes(c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d)
+    bound = roofline.bound_rate(fl, by, peaks)
+    out["bwd_" + c.name] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_of_peak": fl / t / (peaks.bf16_tflops * 1e12),
+                            "frac_of_bound": fl / t / bound,
+                            "flops": "5 products of 2 N^2 d per head = 2.5x the forward's",
+                            "p10_us": sorted(ts)[len(ts) // 10] * 1e6, "p90_us": sorted(ts)[(9 * len(ts)) // 10] * 1e6}
+    del q, k, v, o, lse, dout, dq, dk, dv, ws
     # Chunked prefill against the paged cache.
     c = configs.CHUNKED
     q_lens, k_lens = configs.chunked_lengths(c)

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from attention_online_softmax_gb300 import inputs
+from attention_online_softmax_gb300 import configs, inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -53,12 +53,13 @@ def grad_bound(ref, bf16_out):
 
     The kernel's weights P and dS enter the tensor cores as bf16 (relative
     rounding 2^-9 each), D = rowsum(dO * O) uses the bf16-rounded O, and the
-    sums run in f32.  Relative to the size of a gradient tensor (its largest
-    |value|, which bounds the sums the rounding errors scale with) that gives
-    errors of a few 2^-9; we allow 2^-5 of max|ref| (about 3%), plus half a
+    sums run in f32.  Each gradient element is a sum of such rounded terms,
+    so its error is a few 2^-9 of the size of the terms, which the largest
+    |value| of the gradient tensor bounds; measured worst cases sit near
+    2.5 * 2^-9 of max|ref|.  We allow 4 * 2^-9 = 2^-7 of max|ref|, plus half a
     bf16 ulp of each element when the output is bf16.
     """
-    tol = 2.0 ** -5 * np.abs(ref).max(initial=0.0)
+    tol = 2.0 ** -7 * np.abs(ref).max(initial=0.0)
     if bf16_out:
         tol = tol + 2.0 ** -9 * np.abs(ref)
     return tol
@@ -127,3 +128,27 @@ def test_bwd_dk_dv_deterministic(abi):
     b = run_bwd(abi, x, dout, torch.float32)
     assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
     np.testing.assert_allclose(a[0], b[0], atol=1e-5)  # dQ: atomic summation order
+
+
+def test_bwd_large_score_range(abi):
+    # K scaled by 8: peaky weights, many rows dominated by one key.
+    x = inputs.prefill_inputs(1, 2, 2, 384, 384, 128, seed=7500, causal=True, k_scale=8.0)
+    check_bwd(abi, x, seed=7501)
+
+
+def test_bwd_full_config_sampled_heads(abi):
+    # The benchmark's backward launch (causal MHA B2 H32 N4096 d128) checked on
+    # two (batch, head) slices: with Hq = Hkv a head's gradients depend on that
+    # head's inputs only, so the oracle runs on the slices alone.
+    c = configs.LONG
+    x = inputs.prefill_inputs(c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.seed, c.causal)
+    g = torch.Generator().manual_seed(c.seed + 50)
+    dout = torch.randn(x.q.shape, generator=g).to(torch.bfloat16)
+    got = run_bwd(abi, x, dout, torch.float32)
+    for b, h in ((0, 0), (1, 31)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle.attention_bwd(x.q[sl].contiguous(), x.k[sl].contiguous(), x.v[sl].contiguous(),
+                                   dout[sl].contiguous(), True, x.scale)[:3]
+        for name, a, r in zip(("dq", "dk", "dv"), got, ref):
+            err = np.abs(a[sl] - r)
+            assert np.all(err <= grad_bound(r, False)), (name, b, h, err.max())
