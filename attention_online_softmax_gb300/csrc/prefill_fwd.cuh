@@ -108,9 +108,10 @@ struct PrefillLayout {
   static constexpr int kBiasOff = kKVOff + STAGES * kKVBytes;
   static constexpr int kBarOff = kBiasOff + BSLOTS * kBiasBytes;
   // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done,
+  // (s_free[2], pv_free[2] after tail_bar),
   // o_done[2], o_free[2], unit_full[Q], unit_empty[Q], mma_drain,
   // bias_full[BSLOTS], bias_empty[BSLOTS], tail_bar
-  static constexpr int kNumBars = 2 + 2 * STAGES + 2 + 2 + 1 + 2 + 2 + 2 * kUnitQ + 1 + 2 * BSLOTS + 1;
+  static constexpr int kNumBars = 2 + 2 * STAGES + 2 + 2 + 1 + 2 + 2 + 2 * kUnitQ + 1 + 2 * BSLOTS + 1 + 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, unit queue
   static constexpr int kUnitBytes = 64;                      // one decoded unit in the queue
   static constexpr int kBytes = kMiscOff + 16 + kUnitBytes * kUnitQ;
@@ -119,6 +120,11 @@ struct PrefillLayout {
   static constexpr int kAlloc = (kBytes + 1024) > 117760 ? (kBytes + 1024) : 117760;
   static constexpr int kTmemCols = 512;
   static constexpr int kSCol = NQ * D;          // first S slot column
+  // One query tile and d <= 128: P gets its own two 64-column slots after the
+  // S slots, so the next S products need not wait for the P V products.
+  static constexpr bool kPSep = NQ == 1 && D <= 128;
+  static constexpr int kPCol = kSCol + 2 * kBN;
+  static_assert(!kPSep || kPCol + kBN <= 512, "tensor memory for separate P slots");
   static_assert(NQ * D + 2 * kBN <= kTmemCols, "tensor memory budget");
   static_assert(kAlloc <= 232448, "shared memory budget");
   static_assert(D % 64 == 0, "head dim");
@@ -130,12 +136,17 @@ struct PrefillLayout {
 // K(t+1), ... in that order; with one query tile it computes S(t+1) before
 // P V(t), so it consumes K(0), K(1), V(0), K(2), V(1), ..., V(T-1) -- and the
 // producer loads in the same order, so the ring drains first in, first out.
-template <int NQ>
+//
+// With separate P slots (PSEP) the MMA thread issues S(t+2) before P V(t):
+// K(0), K(1), then K(t+2), V(t) for t = 0 .. T-3, then V(T-2), V(T-1).
+template <int NQ, bool PSEP = false>
 __device__ __forceinline__ int k_pos(int t) {
+  if (PSEP) return t < 2 ? t : 2 * t - 2;
   return NQ == 2 ? 2 * t : (t == 0 ? 0 : 2 * t - 1);
 }
-template <int NQ>
+template <int NQ, bool PSEP = false>
 __device__ __forceinline__ int v_pos(int t, int T) {
+  if (PSEP) return T == 1 ? 1 : (t <= T - 3 ? 2 * t + 3 : T + t);
   return NQ == 2 ? 2 * t + 1 : (t == T - 1 ? 2 * T - 1 : 2 * t + 2);
 }
 
@@ -218,11 +229,26 @@ __device__ __forceinline__ Unit<NQ> unit_of(const PrefillParams& p, int idx) {
 
 // Item i of a unit's K/V load order (kH items per tile): its key tile t
 // (relative to the unit's first), kind (0: K, 1: V) and head-dim part hh.
-template <int NQ, int KH>
+template <int NQ, int KH, bool PSEP = false>
 __device__ __forceinline__ void load_item(int i, int T, int& t, int& kind, int& hh) {
   const int pos = i / KH;
   hh = i % KH;
-  if (NQ == 2) {
+  if (PSEP) {
+    if (T == 1) {
+      t = 0;
+      kind = pos;
+    } else if (pos < 2) {
+      t = pos;
+      kind = 0;
+    } else if (pos - 2 < 2 * (T - 2)) {
+      const int q = pos - 2;
+      kind = q & 1;                      // even: K(q/2 + 2), odd: V(q/2)
+      t = (q >> 1) + (kind == 0 ? 2 : 0);
+    } else {
+      t = T - 2 + (pos - 2 - 2 * (T - 2));
+      kind = 1;
+    }
+  } else if (NQ == 2) {
     t = pos >> 1;
     kind = pos & 1;
   } else if (pos == 0) {
@@ -278,6 +304,8 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
   uint64_t* bias_full = mma_drain + 1;
   uint64_t* bias_empty = bias_full + bias_slots<BIAS>();
   uint64_t* tail_bar = bias_empty + bias_slots<BIAS>();  // paged: a partly filled value page
+  uint64_t* s_free = tail_bar + 1;   // [2] separate P slots: the softmax has read S from this slot
+  uint64_t* pv_free = s_free + 2;    // [2] separate P slots: the P V product of this P slot is complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   Unit<NQ>* unit_q = reinterpret_cast<Unit<NQ>*>(smem + L::kMiscOff + 16);
 
@@ -314,6 +342,10 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     mbar_init(pv_done, 1);
     mbar_init(mma_drain, 1);
     mbar_init(tail_bar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_free[i], 4);
+      mbar_init(&pv_free[i], 1);
+    }
     for (int i = 0; i < bias_slots<BIAS>(); ++i) {
       mbar_init(&bias_full[i], 1);
       mbar_init(&bias_empty[i], 4);  // lane 0 of every softmax warp
@@ -386,7 +418,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
           }
           mbar_expect_tx(&kv_full[st], L::kKVBytes);
           int t, kind, hh;
-          load_item<NQ, L::kH>(i, u.T, t, kind, hh);
+          load_item<NQ, L::kH, L::kPSep>(i, u.T, t, kind, hh);
           const CUtensorMap* map = kind ? &tmV : &tmK;
 #pragma unroll
           for (int c = 0; c < L::kDI / 64; ++c)
@@ -405,9 +437,9 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     // The whole warp: a key tile spans 128 / page_size pages, each loaded as
     // kDI / 64 boxes, one box per lane, so the boxes of an item are issued
     // together.  Lane 0 does the waits, arrivals and the Q loads.  Each lane
-    // keeps the page id of its box for the tiles of K(t-1), K(t) and K(t+1)
-    // (prev / cur / next): the block-table read of a tile is issued one tile
-    // ahead of its first use.  Pages past the context's end are not loaded
+    // keeps the page id of its box for the tiles t-2 .. t+1 around the latest
+    // K(t) (a value tile is loaded at most two key tiles after its own): the
+    // block-table read of a tile is issued one tile ahead of its first use.  Pages past the context's end are not loaded
     // (their keys are masked; their stale rows, real cache rows or zeros, get
     // zero weight).  A value page the context ends inside is loaded on its own
     // barrier; the warp then zeroes its slots past the end before the item is
@@ -464,17 +496,20 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
         const int kp = (u.tmin + t) * kBN + g_l * ps;
         return (issuer && kp < u.nk) ? __ldg(p.block_table + bt_row + kp / ps) : kNone;
       };
-      int pg_prev = kNone;
+      int pg_m2 = kNone, pg_m1 = kNone;
       int pg_cur = page_of(0);
       int pg_next = u.T > 1 ? page_of(1) : kNone;
+      int kt_cur = 0;  // tile of the latest K item
       for (int i = 0; i < 2 * L::kH * u.T; ++i, ++item) {
         const int st = item % STAGES;
         int t, kind, hh;
-        load_item<NQ, L::kH>(i, u.T, t, kind, hh);
+        load_item<NQ, L::kH, L::kPSep>(i, u.T, t, kind, hh);
         if (kind == 0 && hh == 0 && t > 0) {
-          pg_prev = pg_cur;
+          pg_m2 = pg_m1;
+          pg_m1 = pg_cur;
           pg_cur = pg_next;
           pg_next = t + 1 < u.T ? page_of(t + 1) : kNone;
+          kt_cur = t;
         }
         int wok = 1;
         if (lane == 0) wok = mbar_wait(&kv_empty[st], ((item / STAGES) & 1) ^ 1, 1);
@@ -482,8 +517,9 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
           ok = false;
           break;
         }
-        // K(t) uses tile t's pages; V(t) comes after K(t+1), except the last.
-        const int pg = (kind == 0 || t == u.T - 1) ? pg_cur : pg_prev;
+        // K(t) uses tile t's pages; V(t) comes zero to two key tiles later.
+        const int back = kind == 0 ? 0 : kt_cur - t;
+        const int pg = back == 0 ? pg_cur : (back == 1 ? pg_m1 : pg_m2);
         const int kp = (u.tmin + t) * kBN + g_l * ps;
         const bool valid = pg >= 0 && pg < p.num_pages;
         if (pg != kNone && !valid) report_error(7 /* ATTN_ERR_BOUNDS */, 8, pg);
@@ -614,7 +650,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       };
       // O_j (+)= P_j V_t: one N = kDI product per V item; `first` overwrites O_j.
       auto issue_pv = [&](int j, int slot, int vitem, bool wait, bool first) -> bool {
-        const uint32_t pa = tmem + L::kSCol + slot * kBN;
+        const uint32_t pa = L::kPSep ? tmem + L::kPCol + slot * (kBN / 2) : tmem + L::kSCol + slot * kBN;
 #pragma unroll
         for (int hh = 0; hh < L::kH; ++hh) {
           const int item = vitem + hh;
@@ -653,71 +689,116 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
         ok = mbar_wait(q_full, q_uses & 1, 10);
         if (!ok) break;
         const int T = u.T;
-        for (int t = 0; ok && t <= T; ++t) {
-          const int kit = item0 + k_pos<NQ>(t) * L::kH;                      // K(t)
-          const int vit = item0 + (t >= 1 ? v_pos<NQ>(t - 1, T) : 0) * L::kH;  // V(t-1)
-          const int ta = u.tmin + t;  // absolute key tile of S(t); PV is on tile ta - 1
-          if (NQ == 2) {
-            // PV_A(t-1), S_A(t), PV_B(t-1), S_B(t); K/V items are waited for
-            // by their first user and released after their last.
-            bool waitedV = false, waitedK = false;
+        if (L::kPSep) {
+          // S(c) for the unit's tiles into slot c & 1 as soon as the softmax
+          // of tile c - 2 has read that slot, two tiles ahead of the P V
+          // products, which read P from its own slots.
+          const int c0 = cnt[0];
+          auto s_tile = [&](int t) -> bool {
+            const int c = c0 + t;
+            if (c >= 2) {
+              if (!ATTN_MMA_WAIT(&s_free[c & 1], ((c - 2) >> 1) & 1, 18)) return false;
+              tc_fence_after();
+            }
+            const int kit = item0 + k_pos<1, true>(t) * L::kH;
+            if (!issue_s(0, c & 1, kit, true)) return false;
+            umma_commit(&s_full[c & 1]);
+            release(kit);
+            if (t == T - 1) umma_commit(q_empty);  // the unit's last S MMA is issued
+            return true;
+          };
+          for (int t = 0; ok && t < T && t < 2; ++t) ok = s_tile(t);
+          for (int t = 0; ok && t < T; ++t) {
+            if (t + 2 < T) {
+              ok = s_tile(t + 2);
+              if (!ok) break;
+            }
+            const int c = c0 + t;
+            ok = ATTN_MMA_WAIT(&p_full[c & 1], (c >> 1) & 1, 12);
+            if (!ok) break;
+            tc_fence_after();
+            if (t == 0) {
+              ok = wait_o_free(0);
+              if (!ok) break;
+            }
+            const int vit = item0 + v_pos<1, true>(t, T) * L::kH;
+            ok = issue_pv(0, c & 1, vit, true, t == 0);
+            if (!ok) break;
+            umma_commit(&pv_free[c & 1]);
+            release(vit);
+            if (t == T - 1) {
+              umma_commit(&o_done[0]);
+              ++o_uses[0];
+            }
+          }
+          cnt[0] += T;
+        } else {
+          for (int t = 0; ok && t <= T; ++t) {
+            const int kit = item0 + k_pos<NQ>(t) * L::kH;                      // K(t)
+            const int vit = item0 + (t >= 1 ? v_pos<NQ>(t - 1, T) : 0) * L::kH;  // V(t-1)
+            const int ta = u.tmin + t;  // absolute key tile of S(t); PV is on tile ta - 1
+            if (NQ == 2) {
+              // PV_A(t-1), S_A(t), PV_B(t-1), S_B(t); K/V items are waited for
+              // by their first user and released after their last.
+              bool waitedV = false, waitedK = false;
 #pragma unroll
-            for (int j = 0; j < NQ; ++j) {
-              if (t >= 1 && ta - 1 >= u.lo[j] && ta - 1 < u.hi[j]) {
-                ok = ATTN_MMA_WAIT(&p_full[j], (cnt[j] - 1) & 1, 12);
+              for (int j = 0; j < NQ; ++j) {
+                if (t >= 1 && ta - 1 >= u.lo[j] && ta - 1 < u.hi[j]) {
+                  ok = ATTN_MMA_WAIT(&p_full[j], (cnt[j] - 1) & 1, 12);
+                  if (!ok) break;
+                  tc_fence_after();
+                  if (ta - 1 == u.lo[j]) {
+                    ok = wait_o_free(j);
+                    if (!ok) break;
+                  }
+                  ok = issue_pv(j, j, vit, !waitedV, ta - 1 == u.lo[j]);
+                  if (!ok) break;
+                  waitedV = true;
+                  if (ta - 1 == u.hi[j] - 1) {
+                    umma_commit(&o_done[j]);
+                    ++o_uses[j];
+                  }
+                }
+                if (t < T && ta >= u.lo[j] && ta < u.hi[j]) {
+                  ok = issue_s(j, j, kit, !waitedK);
+                  if (!ok) break;
+                  waitedK = true;
+                  umma_commit(&s_full[j]);
+                  ++cnt[j];
+                }
+              }
+              if (!ok) break;
+              if (waitedV) release(vit);
+              if (waitedK) release(kit);
+              if (t == T - 1) umma_commit(q_empty);  // the unit's last S MMA is issued
+            } else {
+              // S(t) into slot c&1 (overlaps the softmax of tile t-1), then PV(t-1).
+              if (t < T) {
+                const int c = cnt[0];
+                ok = issue_s(0, c & 1, kit, true);
+                if (!ok) break;
+                umma_commit(&s_full[c & 1]);
+                ++cnt[0];
+                release(kit);
+                if (t == T - 1) umma_commit(q_empty);
+              }
+              if (t >= 1) {
+                const int c = cnt[0] - (t < T ? 2 : 1);  // running index of tile t-1
+                ok = ATTN_MMA_WAIT(&p_full[c & 1], (c >> 1) & 1, 12);
                 if (!ok) break;
                 tc_fence_after();
-                if (ta - 1 == u.lo[j]) {
-                  ok = wait_o_free(j);
+                if (t - 1 == 0) {
+                  ok = wait_o_free(0);
                   if (!ok) break;
                 }
-                ok = issue_pv(j, j, vit, !waitedV, ta - 1 == u.lo[j]);
+                ok = issue_pv(0, c & 1, vit, true, t - 1 == 0);
                 if (!ok) break;
-                waitedV = true;
-                if (ta - 1 == u.hi[j] - 1) {
-                  umma_commit(&o_done[j]);
-                  ++o_uses[j];
+                umma_commit(pv_done);
+                release(vit);
+                if (t - 1 == T - 1) {
+                  umma_commit(&o_done[0]);
+                  ++o_uses[0];
                 }
-              }
-              if (t < T && ta >= u.lo[j] && ta < u.hi[j]) {
-                ok = issue_s(j, j, kit, !waitedK);
-                if (!ok) break;
-                waitedK = true;
-                umma_commit(&s_full[j]);
-                ++cnt[j];
-              }
-            }
-            if (!ok) break;
-            if (waitedV) release(vit);
-            if (waitedK) release(kit);
-            if (t == T - 1) umma_commit(q_empty);  // the unit's last S MMA is issued
-          } else {
-            // S(t) into slot c&1 (overlaps the softmax of tile t-1), then PV(t-1).
-            if (t < T) {
-              const int c = cnt[0];
-              ok = issue_s(0, c & 1, kit, true);
-              if (!ok) break;
-              umma_commit(&s_full[c & 1]);
-              ++cnt[0];
-              release(kit);
-              if (t == T - 1) umma_commit(q_empty);
-            }
-            if (t >= 1) {
-              const int c = cnt[0] - (t < T ? 2 : 1);  // running index of tile t-1
-              ok = ATTN_MMA_WAIT(&p_full[c & 1], (c >> 1) & 1, 12);
-              if (!ok) break;
-              tc_fence_after();
-              if (t - 1 == 0) {
-                ok = wait_o_free(0);
-                if (!ok) break;
-              }
-              ok = issue_pv(0, c & 1, vit, true, t - 1 == 0);
-              if (!ok) break;
-              umma_commit(pv_done);
-              release(vit);
-              if (t - 1 == T - 1) {
-                umma_commit(&o_done[0]);
-                ++o_uses[0];
               }
             }
           }
@@ -785,6 +866,12 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
         tc_fence_after();
         uint32_t r[kBN];
         tmem_ld128(lane_base + L::kSCol + slot * kBN, r);
+        if (L::kPSep) {
+          // S is in registers: the MMA thread may reuse the slot for S(c + 2).
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[slot]);
+        }
 
         // Row max of the raw scores (masked keys -> -inf); scale > 0 keeps
         // the order, so the scaled max is mx * sl.  On the biased path r[]
@@ -895,7 +982,9 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
           if (NQ == 1) {
             // O holds tile t-1's contribution only once PV(t-1) is complete;
             // P V products are counted like the tiles (one per tile).
-            ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(pv_done, (cnt - 1) & 1, 21));
+            ok = __all_sync(0xFFFFFFFFu,
+                            L::kPSep ? ATTN_SOFTMAX_WAIT(&pv_free[(cnt - 1) & 1], ((cnt - 1) >> 1) & 1, 21)
+                                     : ATTN_SOFTMAX_WAIT(pv_done, (cnt - 1) & 1, 21));
             if (!ok) break;
             tc_fence_after();
           }
@@ -914,7 +1003,17 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
           }
         }
         // P over the first half of the S slot, then hand it to the MMA thread.
-        tmem_st64(lane_base + L::kSCol + slot * kBN, pk);
+        if (L::kPSep) {
+          // P slot `slot` is free once the P V product of tile cnt - 2 is done.
+          if (cnt >= 2) {
+            ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(&pv_free[slot], ((cnt - 2) >> 1) & 1, 27));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          tmem_st64(lane_base + L::kPCol + slot * (kBN / 2), pk);
+        } else {
+          tmem_st64(lane_base + L::kSCol + slot * kBN, pk);
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
