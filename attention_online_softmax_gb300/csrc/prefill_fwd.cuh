@@ -92,7 +92,10 @@ template <int D, int NQ, int STAGES, int BSLOTS = 0>
 struct PrefillLayout {
   // warp 0 TMA producer, warp 1 MMA issuer, 4 softmax warps per query tile,
   // and with a staged bias one more warp that loads the bias tiles.
-  static constexpr int kThreads = 64 + 128 * NQ + (BSLOTS > 0 ? 32 : 0);
+  // With separate P slots a second MMA-issuing warp takes the P V products.
+  static constexpr bool kPSep = NQ == 1 && D <= 128;
+  static constexpr int kPVWarp = 2 + 4 * NQ + (BSLOTS > 0 ? 1 : 0);
+  static constexpr int kThreads = 64 + 128 * NQ + (BSLOTS > 0 ? 32 : 0) + (kPSep ? 32 : 0);
   static constexpr int kQBytes = kBM * D * 2;
   // K and V tiles stream in items of up to 128 head-dim columns (kH items per
   // tile), so with d = 256 a 64 KB tile occupies two 32 KB ring stages and
@@ -122,7 +125,6 @@ struct PrefillLayout {
   static constexpr int kSCol = NQ * D;          // first S slot column
   // One query tile and d <= 128: P gets its own two 64-column slots after the
   // S slots, so the next S products need not wait for the P V products.
-  static constexpr bool kPSep = NQ == 1 && D <= 128;
   static constexpr int kPCol = kSCol + 2 * kBN;
   static_assert(!kPSep || kPCol + kBN <= 512, "tensor memory for separate P slots");
   static_assert(NQ * D + 2 * kBN <= kTmemCols, "tensor memory budget");
@@ -337,10 +339,10 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     for (int i = 0; i < kUnitQ; ++i) {
       mbar_init(&unit_full[i], 1);
       // MMA thread + lane 0 of every softmax warp (+ the bias loader)
-      mbar_init(&unit_empty[i], 1 + 4 * NQ + (BIAS == 2 ? 1 : 0));
+      mbar_init(&unit_empty[i], 1 + 4 * NQ + (BIAS == 2 ? 1 : 0) + (L::kPSep ? 1 : 0));
     }
     mbar_init(pv_done, 1);
-    mbar_init(mma_drain, 1);
+    mbar_init(mma_drain, L::kPSep ? 2 : 1);  // one commit per MMA-issuing thread
     mbar_init(tail_bar, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_free[i], 4);
@@ -605,8 +607,12 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
         mbar_wait(&bias_full[it % bias_ring<BIAS>()], (it / bias_ring<BIAS>()) & 1, 7);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || (L::kPSep && warp == L::kPVWarp)) {
+    // ---------------------------------------------------------------- MMA issuer(s)
+    // With separate P slots warp 1 issues the S products and warp kPVWarp the
+    // P V products: while one thread waits, the other keeps the tensor pipe
+    // fed (an issuing thread blocks until the pipe accepts its MMA).
+    const bool pv_thread = warp != 1;
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);      // Q K-major, K K-major
       constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, L::kDI, 0, 1);   // P K-major (TMEM), V MN-major
@@ -686,8 +692,10 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
         mbar_arrive(&unit_empty[n % kUnitQ]);
         if (u.idx < 0) break;
         if (u.T == 0) continue;
-        ok = mbar_wait(q_full, q_uses & 1, 10);
-        if (!ok) break;
+        if (!pv_thread) {
+          ok = mbar_wait(q_full, q_uses & 1, 10);
+          if (!ok) break;
+        }
         const int T = u.T;
         if (L::kPSep) {
           // S(c) for the unit's tiles into slot c & 1 as soon as the softmax
@@ -707,12 +715,10 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
             if (t == T - 1) umma_commit(q_empty);  // the unit's last S MMA is issued
             return true;
           };
-          for (int t = 0; ok && t < T && t < 2; ++t) ok = s_tile(t);
-          for (int t = 0; ok && t < T; ++t) {
-            if (t + 2 < T) {
-              ok = s_tile(t + 2);
-              if (!ok) break;
-            }
+          if (!pv_thread) {
+            for (int t = 0; ok && t < T; ++t) ok = s_tile(t);
+          }
+          for (int t = 0; pv_thread && ok && t < T; ++t) {
             const int c = c0 + t;
             ok = ATTN_MMA_WAIT(&p_full[c & 1], (c >> 1) & 1, 12);
             if (!ok) break;
