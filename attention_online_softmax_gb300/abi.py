@@ -47,6 +47,8 @@ _lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
 _lib.attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, ctypes.c_float,
                           _i, _vp, ctypes.c_size_t, _vp]
 _lib.attn_bwd.restype = _i
+_lib.attn_probe_dram_latency.argtypes = [_vp, ctypes.c_size_t, _i, _vp, _vp]
+_lib.attn_probe_dram_latency.restype = _i
 _lib.attn_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
 _lib.attn_decode_workspace_size.restype = ctypes.c_size_t
 _lib.attn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
@@ -72,7 +74,7 @@ ATTN_F32 = 1
 
 #: every symbol include/attn.h declares
 EXPORTS = ("attn_fwd", "attn_fwd_masked", "attn_prefill_paged_workspace_size", "attn_prefill_paged",
-           "attn_bwd_workspace_size", "attn_bwd",
+           "attn_bwd_workspace_size", "attn_bwd", "attn_probe_dram_latency",
            "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_static",
            "attn_get_device_status", "attn_selftest_wait_timeout", "attn_status_string",
            "attn_launch_count", "attn_abi_version")
@@ -250,6 +252,16 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool, scale: float, work
                        ATTN_F32 if gd == torch.float32 else ATTN_BF16, _ptr(workspace), workspace.numel(),
                        _stream_ptr(stream))
     _check(st, "attn_bwd")
+
+
+def attn_probe_dram_latency(chain, hops: int, out_ns, stream=None) -> None:
+    """chain: CUDA int32 tensor (a cycle of indices, see include/attn.h);
+    out_ns: CUDA int64 tensor of 2 elements."""
+    import torch
+    _need(chain, torch.int32, "chain")
+    _need(out_ns, torch.int64, "out_ns")
+    _check(_lib.attn_probe_dram_latency(_ptr(chain), chain.numel(), int(hops), _ptr(out_ns), _stream_ptr(stream)),
+           "attn_probe_dram_latency")
 
 
 def attn_decode_workspace_size(num_seqs: int, Hq: int, Hkv: int, d: int, max_seqlen: int) -> int:

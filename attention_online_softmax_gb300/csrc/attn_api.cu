@@ -213,7 +213,7 @@ attn_status sched_slot(int** out) {
 template <int D, int NQ, int STAGES, int BIAS = 0>
 attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            const CUtensorMap& mb, attn::PrefillParams p, int BH, cudaStream_t stream) {
-  using L = attn::PrefillLayout<D, NQ, STAGES, attn::bias_slots<BIAS>()>;
+  using L = attn::PrefillLayout<D, NQ, STAGES, attn::bias_slots<BIAS>(), attn::psep_path<BIAS, false>()>;
   auto kern = attn::prefill_fwd_kernel<D, NQ, STAGES, BIAS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
     cudaGetLastError();
@@ -242,7 +242,7 @@ attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const C
 template <int D, int STAGES>
 attn_status launch_prefill_paged(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                                  attn::PrefillParams p, int total_q, cudaStream_t stream) {
-  using L = attn::PrefillLayout<D, 1, STAGES>;
+  using L = attn::PrefillLayout<D, 1, STAGES, 0, attn::psep_path<0, true>()>;
   auto kern = attn::prefill_fwd_kernel<D, 1, STAGES, 0, true>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
     cudaGetLastError();
@@ -685,3 +685,15 @@ attn_status attn_get_device_status(attn_stream_t stream) {
 }  // extern "C"
 
 #include "bwd_api.cuh"
+#include "probe.cuh"
+
+extern "C" attn_status attn_probe_dram_latency(const uint32_t* chain, size_t chain_len, int hops,
+                                               unsigned long long* out_ns, attn_stream_t stream) {
+  if (chain == nullptr || out_ns == nullptr || hops <= 0 || chain_len == 0) return ATTN_ERR_INVALID_ARG;
+  attn_status st = check_device();
+  if (st != ATTN_OK) return st;
+  attn::dram_latency_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(chain, hops, out_ns);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return ATTN_OK;
+}

@@ -88,14 +88,16 @@ struct PrefillParams {
   int num_seqs, max_pages, page_size, num_pages;
 };
 
-template <int D, int NQ, int STAGES, int BSLOTS = 0>
+template <int D, int NQ, int STAGES, int BSLOTS = 0, bool PSEP = false>
 struct PrefillLayout {
   // warp 0 TMA producer, warp 1 MMA issuer, 4 softmax warps per query tile,
   // and with a staged bias one more warp that loads the bias tiles.
-  // With separate P slots a second MMA-issuing warp takes the P V products.
-  static constexpr bool kPSep = NQ == 1 && D <= 128;
+  // Separate P slots (PSEP, one query tile, d <= 128): a second MMA-issuing
+  // warp takes the P V products.
+  static constexpr bool kPSep = PSEP && NQ == 1 && D <= 128;
+  static constexpr bool kSplit = kPSep;
   static constexpr int kPVWarp = 2 + 4 * NQ + (BSLOTS > 0 ? 1 : 0);
-  static constexpr int kThreads = 64 + 128 * NQ + (BSLOTS > 0 ? 32 : 0) + (kPSep ? 32 : 0);
+  static constexpr int kThreads = 64 + 128 * NQ + (BSLOTS > 0 ? 32 : 0) + (kSplit ? 32 : 0);
   static constexpr int kQBytes = kBM * D * 2;
   // K and V tiles stream in items of up to 128 head-dim columns (kH items per
   // tile), so with d = 256 a 64 KB tile occupies two 32 KB ring stages and
@@ -276,12 +278,19 @@ __host__ __device__ constexpr int bias_ring() { return BIAS == 2 ? 2 : 1; }  // 
 // PAGED: Q, O and LSE packed over the sequences' tokens ([total_q][Hq][d],
 // [total_q][Hq]); K and V read page by page from the paged cache (tmK, tmV
 // box one page of one KV head); tmB is unused.
+// Separate P slots and split MMA issue pay off for the plain kernel (measured:
+// +9% at B1 H16 N2048 d128); the additive-bias and paged variants, whose
+// softmax or producer warps are busier, measured slower with them and keep
+// P in the S slot with one MMA-issuing thread.
+template <int BIAS, bool PAGED>
+__host__ __device__ constexpr bool psep_path() { return BIAS == 0 && !PAGED; }
+
 template <int D, int NQ, int STAGES, int BIAS, bool PAGED = false>
-__global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>()>::kThreads, 1)
+__global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(), psep_path<BIAS, PAGED>()>::kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
                        const PrefillParams p) {
-  using L = PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>()>;
+  using L = PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(), psep_path<BIAS, PAGED>()>;
   static_assert(BIAS == 0 || NQ == 1, "additive-bias variants run one query tile per unit");
   static_assert(!PAGED || (NQ == 1 && BIAS == 0), "paged prefill: one query tile per unit, no dense bias");
   static_assert(sizeof(Unit<NQ>) <= L::kUnitBytes, "unit queue entry");
@@ -339,10 +348,10 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     for (int i = 0; i < kUnitQ; ++i) {
       mbar_init(&unit_full[i], 1);
       // MMA thread + lane 0 of every softmax warp (+ the bias loader)
-      mbar_init(&unit_empty[i], 1 + 4 * NQ + (BIAS == 2 ? 1 : 0) + (L::kPSep ? 1 : 0));
+      mbar_init(&unit_empty[i], 1 + 4 * NQ + (BIAS == 2 ? 1 : 0) + (L::kSplit ? 1 : 0));
     }
     mbar_init(pv_done, 1);
-    mbar_init(mma_drain, L::kPSep ? 2 : 1);  // one commit per MMA-issuing thread
+    mbar_init(mma_drain, L::kSplit ? 2 : 1);  // one commit per MMA-issuing thread
     mbar_init(tail_bar, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_free[i], 4);
@@ -607,7 +616,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
         mbar_wait(&bias_full[it % bias_ring<BIAS>()], (it / bias_ring<BIAS>()) & 1, 7);
     }
     __syncwarp();
-  } else if (warp == 1 || (L::kPSep && warp == L::kPVWarp)) {
+  } else if (warp == 1 || (L::kSplit && warp == L::kPVWarp)) {
     // ---------------------------------------------------------------- MMA issuer(s)
     // With separate P slots warp 1 issues the S products and warp kPVWarp the
     // P V products: while one thread waits, the other keeps the tensor pipe
@@ -715,26 +724,33 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
             if (t == T - 1) umma_commit(q_empty);  // the unit's last S MMA is issued
             return true;
           };
-          if (!pv_thread) {
-            for (int t = 0; ok && t < T; ++t) ok = s_tile(t);
-          }
-          for (int t = 0; pv_thread && ok && t < T; ++t) {
+          auto pv_tile = [&](int t) -> bool {
             const int c = c0 + t;
-            ok = ATTN_MMA_WAIT(&p_full[c & 1], (c >> 1) & 1, 12);
-            if (!ok) break;
+            if (!ATTN_MMA_WAIT(&p_full[c & 1], (c >> 1) & 1, 12)) return false;
             tc_fence_after();
-            if (t == 0) {
-              ok = wait_o_free(0);
-              if (!ok) break;
-            }
+            if (t == 0 && !wait_o_free(0)) return false;
             const int vit = item0 + v_pos<1, true>(t, T) * L::kH;
-            ok = issue_pv(0, c & 1, vit, true, t == 0);
-            if (!ok) break;
+            if (!issue_pv(0, c & 1, vit, true, t == 0)) return false;
             umma_commit(&pv_free[c & 1]);
             release(vit);
             if (t == T - 1) {
               umma_commit(&o_done[0]);
               ++o_uses[0];
+            }
+            return true;
+          };
+          if (L::kSplit) {
+            // This thread's half: every S, or every P V.
+            for (int t = 0; ok && t < T; ++t) ok = pv_thread ? pv_tile(t) : s_tile(t);
+          } else {
+            // One thread: S(0), S(1), then S(t + 2) before P V(t).
+            for (int t = 0; ok && t < T && t < 2; ++t) ok = s_tile(t);
+            for (int t = 0; ok && t < T; ++t) {
+              if (t + 2 < T) {
+                ok = s_tile(t + 2);
+                if (!ok) break;
+              }
+              ok = pv_tile(t);
             }
           }
           cnt[0] += T;

@@ -1,0 +1,22 @@
+// Measurement aid for the decode time floor ("Tang: a compiler that derives
+// GPU kernels and bounds how fast they can run", abstract: a time floor built
+// on the traffic bound, the measured launch cost and the DRAM latency).  One
+// thread follows a chain of dependent loads through a buffer larger than L2;
+// the elapsed global time divided by the number of hops is one DRAM round trip.
+#pragma once
+
+#include <cstdint>
+
+namespace attn {
+
+__global__ void dram_latency_kernel(const uint32_t* chain, int hops, unsigned long long* out_ns) {
+  uint32_t idx = 0;
+  unsigned long long t0, t1;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (int h = 0; h < hops; ++h) idx = __ldcg(chain + idx);  // L2-only load: no L1 hit on a revisit
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+  out_ns[0] = t1 - t0;
+  out_ns[1] = idx;  // keeps the chain live
+}
+
+}  // namespace attn

@@ -397,7 +397,7 @@ def main(argv=None):
 
     # Decode time floor: traffic at the measured bandwidth plus the launches
     # and one DRAM round trip the two-kernel split/combine stage cannot avoid.
-    launch_s, dram_s = launch_and_latency_floor(dev, stream)
+    launch_s, dram_s = launch_and_latency_floor(dev, stream, abi)
     dec_kernels = 2 if ws_bytes > 0 else 1
     dec_floor = dec_bytes / (peaks.hbm_gbs * 1e9) + dec_kernels * launch_s + dram_s
 
@@ -479,41 +479,61 @@ def profile_one(which: str, launches: int = 3) -> int:
     return 0 if st == 0 else 1
 
 
-def launch_and_latency_floor(dev, stream, reps: int = 200):
+def launch_and_latency_floor(dev, stream, abi=None, reps: int = 200):
     """Measured costs a GEMV-class stage cannot avoid beyond its traffic.
 
-    launch_s: back-to-back launch interval of a one-element kernel (the cost
-    each additional kernel in a dependent chain adds); dram_s: duration of one
-    kernel that reads and writes a single cold 4-byte word minus launch_s (one
-    DRAM round trip).  Used for the decode time floor: traffic at the measured
-    HBM bandwidth + launches * launch_s + dram_s ("Tang: a compiler that
-    derives GPU kernels ...": the time floor of a GEMV-class stage).
+    launch_s: the GPU-side interval between dependent one-element kernels
+    replayed from a CUDA graph (the cost each additional kernel in a chain
+    adds, without host launch overhead); dram_s: one DRAM round
+    trip, from a single thread chasing dependent loads through a cycle of
+    128-byte lines in a buffer larger than L2 (flushed first), the elapsed
+    time divided by the hops (`attn_probe_dram_latency`).  Used for the decode
+    time floor: traffic at the measured HBM bandwidth + launches * launch_s +
+    dram_s ("Tang: a compiler that derives GPU kernels ...": the time floor of
+    a GEMV-class stage).
     """
+    # GPU-side cost of one more kernel in a chain: `reps` one-element kernels
+    # captured in a CUDA graph (no host launch overhead), replayed and timed.
     x = torch.zeros(1, device=dev)
-    for _ in range(20):
-        x.add_(1)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(20):
+            x.add_(1)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(reps):
+            x.add_(1)
+    graph.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        x.add_(1)
-    e1.record(stream)
+    e0.record()
+    graph.replay()
+    e1.record()
     torch.cuda.synchronize()
     launch_s = e0.elapsed_time(e1) * 1e-3 / reps
-    big = torch.zeros(64 << 20, dtype=torch.float32, device=dev)  # 256 MiB, larger than L2
+    del graph
+    if abi is None:
+        return launch_s, 0.0
+    # A random cycle through 2M lines of 128 bytes (256 MiB): entry 32*a holds 32*next(a).
+    lines = 1 << 21
+    g = torch.Generator().manual_seed(1234)
+    perm = torch.randperm(lines, generator=g).to(dev)
+    chain = torch.zeros(lines * 32, dtype=torch.int32, device=dev)
+    chain[perm * 32] = (torch.roll(perm, -1) * 32).to(torch.int32)
+    # Line 0 lies on the cycle, so the chase may start at index 0.
+    out = torch.zeros(2, dtype=torch.int64, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    ts = []
-    for i in range(20):
-        flush.zero_()  # evicts `big` from L2: the word read below comes from DRAM
-        idx = (i * 999983) % big.numel()
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        big[idx:idx + 1].add_(1)
-        f1.record(stream)
+    hops = 2000
+    ns = []
+    for _ in range(5):
+        flush.zero_()
+        abi.attn_probe_dram_latency(chain, hops, out, stream)
         torch.cuda.synchronize()
-        ts.append(f0.elapsed_time(f1) * 1e-3)
-    dram_s = max(0.0, statistics.median(ts) - launch_s)
-    return launch_s, dram_s
+        ns.append(int(out[0].item()) / hops)
+    del chain, flush, perm
+    return launch_s, statistics.median(ns) * 1e-9
 
 
 def measure_e2e(abi, xp, xd, dev, stream, steps, floor_s, world):

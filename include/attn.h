@@ -193,6 +193,18 @@ ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const
                               size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * Measurement aid for the decode time floor: one thread follows
+ * idx = chain[idx] (starting at 0) for `hops` dependent loads that bypass L1
+ * and writes the elapsed nanoseconds to out_ns[0] (out_ns[1] receives the last
+ * index).  chain: device uint32 array of chain_len entries whose every visited
+ * entry holds an index < chain_len (the caller builds a cycle through a
+ * buffer larger than L2, one entry per 128-byte line, and flushes L2 first);
+ * out_ns: device array of 2 uint64.  One DRAM round trip = out_ns[0] / hops.
+ */
+ATTN_API attn_status attn_probe_dram_latency(const uint32_t* chain, size_t chain_len, int hops,
+                                             unsigned long long* out_ns, attn_stream_t stream);
+
+/*
  * Bytes of scratch memory attn_decode_paged() needs for these sizes (the
  * split partials: one float32 O row and one float32 LSE per sequence, split
  * and query head).  Pure function of its arguments; 0 on invalid input.
