@@ -13,7 +13,7 @@
 //   dS^T = P^T * (dP^T - D),  D = rowsum(dO * O) (prep kernel)
 //   dV  += P^T dO,  dK += dS^T Q     (A operands from tensor memory)
 //   dQ_t = dS K                      (dS staged in shared memory), added to an
-//                                     f32 dQ accumulator in global memory
+//                                     f32 dQ accumulator by TMA reduce-adds
 // The 1/sqrt(d)-style scale is applied to dK at the end and to dQ as it is
 // accumulated.  Roles: warp 0 TMA producer, warp 1 MMA issuer (one thread),
 // warps 2..5 one thread per key row (weights, dS) and then one thread per
@@ -50,8 +50,9 @@ struct BwdLayout {
   static constexpr int kRowOff = kDSOff + kDSBytes;   // 2 x (LSE[128], D[128]) f32, one per item parity
   static constexpr int kRowBytes = 2 * 128 * 4;
   static constexpr int kBarOff = kRowOff + 2 * kRowBytes;
-  // kv_full, q_full[S], q_empty[S], s_full, dp_full, ds_full, dq_full, dq_free, dkv_done, rows_ready[2]
-  static constexpr int kNumBars = 1 + 2 * STAGES + 6 + 2;
+  // kv_full, q_full[S], q_empty[S], s_full, dp_full, ds_full, dq_full, dq_free, dkv_done, rows_ready[2],
+  // red_full[2], red_free[2]
+  static constexpr int kNumBars = 1 + 2 * STAGES + 6 + 2 + 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 128;         // the base is checked for 1024-byte alignment
@@ -109,16 +110,28 @@ __global__ void bwd_post_kernel(const float* dq_acc, void* dq, long long n4, int
   }
 }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
+// out[box at (x, y, z)] += smem box, f32, by the TMA unit (rows past the
+// tensor's extent are not written).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
 }
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N committed bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D, int STAGES>
 __global__ void __launch_bounds__(192, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using L = BwdLayout<D, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -143,6 +156,9 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* dq_free = dq_full + 1;
   uint64_t* dkv_done = dq_free + 1;
   uint64_t* rows_ready = dkv_done + 1;  // [2]: the item's LSE / D values are in shared memory
+  // dQ tiles leave through two 16 KB staging buffers in the dS region:
+  uint64_t* red_full = rows_ready + 2;  // [2] a [128 rows][32 columns] f32 chunk is staged
+  uint64_t* red_free = red_full + 2;    // [2] the TMA reduce has finished reading it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
 
   const int warp = threadIdx.x >> 5;
@@ -177,6 +193,10 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(dkv_done, 1);
     mbar_init(&rows_ready[0], 128);
     mbar_init(&rows_ready[1], 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&red_full[i], 128);
+      mbar_init(&red_free[i], 1);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -352,6 +372,14 @@ __global__ void __launch_bounds__(192, 1)
       const int c_lo = p.causal ? kj - diag - q0 : -0x7FFFFFFF;  // columns < c_lo: masked
       const bool key_ok = kj < p.Nk;
       const uint32_t ds_row = sbase + L::kDSOff + row * 128;
+      if (n > 0) {
+        // The dS region held the previous item's staged dQ chunks: their TMA
+        // reduces must have finished reading it.
+        const int g1 = n * (D / 32) - 1;  // that item's last chunk
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[g1 & 1], (g1 >> 1) & 1, 54) &&
+                                         mbar_wait(&red_free[(g1 - 1) & 1], ((g1 - 1) >> 1) & 1, 55));
+        if (!ok) break;
+      }
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {  // 32 query columns per chunk
         uint32_t s[32];
@@ -399,22 +427,55 @@ __global__ void __launch_bounds__(192, 1)
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(dq_full, n & 1, 52));
       if (!ok) break;
       tc_fence_after();
-      const int qi = q0 + row;
-      float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qi) * D;
+      // 32 columns at a time: scale, stage as [128 rows][32] f32 (128-byte
+      // swizzle, conflict-free row writes) in a 16 KB buffer of the dS region
+      // (free: the dQ product has read dS), and one thread adds the chunk
+      // into the f32 accumulator with a TMA reduce.
+      const bool issuer = threadIdx.x == 64;
 #pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int ch = 0; ok && ch < D / 32; ++ch) {
+        const int g = n * (D / 32) + ch;  // running chunk index
+        const int buf = g & 1;
         uint32_t v[32];
         tmem_ld32(lane_base + L::kColDQ + ch * 32, v);
-        if (qi < p.Nq) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            red_add_v4(dst + ch * 32 + e, __uint_as_float(v[e]) * p.scale, __uint_as_float(v[e + 1]) * p.scale,
-                       __uint_as_float(v[e + 2]) * p.scale, __uint_as_float(v[e + 3]) * p.scale);
+        if (ch == D / 32 - 1) {
+          // The whole dQ tile is in registers or staged: the next dQ product may start.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dq_free);
         }
+        if (g >= 2 && ch >= 2) {
+          // Chunk g - 2 used this buffer within this item.
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[buf], ((g - 2) >> 1) & 1, 56));
+          if (!ok) break;
+        }
+        const uint32_t stg = sbase + L::kDSOff + buf * (128 * 128) + row * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(stg + ((k ^ (row & 7)) << 4), __float_as_uint(__uint_as_float(v[4 * k]) * p.scale),
+                       __float_as_uint(__uint_as_float(v[4 * k + 1]) * p.scale),
+                       __float_as_uint(__uint_as_float(v[4 * k + 2]) * p.scale),
+                       __float_as_uint(__uint_as_float(v[4 * k + 3]) * p.scale));
+        fence_proxy_async_smem();
+        mbar_arrive(&red_full[buf]);
+        if (issuer) {
+          if (!mbar_wait(&red_full[buf], (g >> 1) & 1, 57)) {
+            ok = false;
+          } else {
+            tma_reduce_add_3d(&tmDQ, smem + L::kDSOff + buf * (128 * 128), ch * 32, q0, bh);
+            bulk_commit();
+            // Chunks before g have been read once at most one group is pending.
+            bulk_wait_read<1>();
+            if (ch > 0) mbar_arrive(&red_free[(g - 1) & 1]);
+            if (ch == D / 32 - 1) {
+              bulk_wait_read<0>();
+              mbar_arrive(&red_free[buf]);
+            }
+          }
+        }
+        ok = __all_sync(0xFFFFFFFFu, ok);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
+      if (!ok) break;
     }
 
     // dK, dV rows of this key (zeros when no query row sees the tile).  The
@@ -464,6 +525,8 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
+  // Every dQ reduce of this CTA must have completed before it exits.
+  if (threadIdx.x == 64) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

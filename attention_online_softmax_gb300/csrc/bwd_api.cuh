@@ -9,9 +9,24 @@ namespace {
 
 size_t bwd_align(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
+// 3-D f32 map over the dQ accumulator [B*Hq][Nq][d]; one box is [128 rows][32
+// columns], 128-byte swizzled (the staging layout of the backward kernel).
+bool encode_dq_map(CUtensorMap* map, void* base, int d, int rows, int heads) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(rows) * d * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int D, int STAGES>
 attn_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
-                       const attn::BwdParams& p, cudaStream_t stream) {
+                       const CUtensorMap& mdq, const attn::BwdParams& p, cudaStream_t stream) {
   using L = attn::BwdLayout<D, STAGES>;
   auto kern = attn::attn_bwd_kernel<D, STAGES>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
@@ -21,7 +36,7 @@ attn_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
   const long long grid = static_cast<long long>(p.B) * p.Hkv * ((p.Nk + 127) / 128);
   if (grid > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
   if (grid == 0) return ATTN_OK;
-  kern<<<dim3(static_cast<unsigned>(grid)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mdo, p);
+  kern<<<dim3(static_cast<unsigned>(grid)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mdo, mdq, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return ATTN_OK;
@@ -71,7 +86,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   }
 
   if (Nk > 0) {
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mdq;
     // With Nq == 0 no query tile is ever loaded; the Q / dO maps then describe k.
     const void* qb = Nq > 0 ? q : k;
     const void* db = Nq > 0 ? dout : k;
@@ -79,6 +94,10 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
     const int bh_map = Nq > 0 ? B * Hq : B * Hkv;
     if (!encode_rows_map(&mq, qb, d, nq_map, bh_map, 128) || !encode_rows_map(&mdo, db, d, nq_map, bh_map, 128) ||
         !encode_rows_map(&mk, k, d, Nk, B * Hkv, 128) || !encode_rows_map(&mv, v, d, Nk, B * Hkv, 128))
+      return ATTN_ERR_LAUNCH;
+    // With Nq == 0 no dQ chunk is ever written; the map then describes one row.
+    if (!encode_dq_map(&mdq, Nq > 0 ? static_cast<void*>(dq_acc) : workspace, d, Nq > 0 ? Nq : 1,
+                       Nq > 0 ? B * Hq : 1))
       return ATTN_ERR_LAUNCH;
     attn::BwdParams p;
     p.dk = dk;
@@ -95,7 +114,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
     p.g_f32 = grad_dtype == ATTN_F32 ? 1 : 0;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
-    st = d == 64 ? launch_bwd<64, 3>(mq, mk, mv, mdo, p, s) : launch_bwd<128, 2>(mq, mk, mv, mdo, p, s);
+    st = d == 64 ? launch_bwd<64, 3>(mq, mk, mv, mdo, mdq, p, s) : launch_bwd<128, 2>(mq, mk, mv, mdo, mdq, p, s);
     if (st != ATTN_OK) return st;
   }
 

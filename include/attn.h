@@ -184,8 +184,8 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int d);
  *   aligned, caller-owned, not shared by overlapping calls.
  * Three kernels on `stream` (rows D and a zeroed dQ accumulator; the fused
  * backward, one CTA per (batch, kv head, 128-key tile); the dQ conversion).
- * dK and dV are deterministic; dQ sums its per-key-tile parts with atomic adds,
- * so its last bits can differ from run to run.
+ * dK and dV are deterministic; dQ sums its per-key-tile parts with TMA
+ * reduce-adds in no fixed order, so its last bits can differ from run to run.
  */
 ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq,
