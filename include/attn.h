@@ -37,8 +37,9 @@
  *    Faults the kernels detect while running (a wait that timed out, an
  *    out-of-range block-table entry or sequence length) are recorded in a
  *    device status word read by attn_get_device_status().
- *  - Results are deterministic run to run (fixed work split, no atomics in any
- *    reduction).
+ *  - Forward and decode results are deterministic run to run (fixed work
+ *    split, no atomics in any reduction); attn_bwd's dQ is the one exception
+ *    (see there).
  *  - The GPU must be compute capability 10.3 (GB300, sm_103a); otherwise
  *    ATTN_ERR_UNSUPPORTED.
  */
