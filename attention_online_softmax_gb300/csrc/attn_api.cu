@@ -239,11 +239,11 @@ attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const C
 // Paged chunked prefill: the plan kernel writes the unit prefix sums into the
 // workspace, then the persistent prefill kernel (one CTA per SM) takes units
 // up to the total it finds there.
-template <int D, int STAGES>
+template <int D, int NQ, int STAGES>
 attn_status launch_prefill_paged(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                                  attn::PrefillParams p, int total_q, cudaStream_t stream) {
-  using L = attn::PrefillLayout<D, 1, STAGES, 0, attn::psep_path<0, true>()>;
-  auto kern = attn::prefill_fwd_kernel<D, 1, STAGES, 0, true>;
+  using L = attn::PrefillLayout<D, NQ, STAGES, 0, attn::psep_path<0, true>()>;
+  auto kern = attn::prefill_fwd_kernel<D, NQ, STAGES, 0, true>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
@@ -251,7 +251,8 @@ attn_status launch_prefill_paged(const CUtensorMap& mq, const CUtensorMap& mk, c
   const attn_status st = sched_slot(&p.sched);
   if (st != ATTN_OK) return st;
   attn::paged_plan_kernel<<<1, 1024, 0, stream>>>(p.cu_q, p.seqlens_k, p.num_seqs, total_q, p.Hq, p.max_pages,
-                                                   p.page_size, const_cast<int32_t*>(p.unit_prefix));
+                                                   p.page_size, attn::kBM * NQ,
+                                                   const_cast<int32_t*>(p.unit_prefix));
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   kern<<<dim3(static_cast<unsigned>(sm_count())), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mv, p);
@@ -560,10 +561,18 @@ attn_status attn_prefill_paged(const void* q, const void* kcache, const void* vc
   p.page_size = page_size;
   p.num_pages = num_pages;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // Two query tiles per unit (halving the page boxes per query row) when the
+  // packed rows still give at least two such units per SM (an upper bound on
+  // the unit count: sequences are ragged, only the total is known here).
+  const bool two = (static_cast<long long>(total_q) / (2 * attn::kBM)) * Hq >= 2LL * sm_count();
   switch (d) {
-    case 64: return launch_prefill_paged<64, 12>(mq, mk, mv, p, total_q, s);
-    case 128: return launch_prefill_paged<128, 6>(mq, mk, mv, p, total_q, s);
-    case 256: return launch_prefill_paged<256, 5>(mq, mk, mv, p, total_q, s);
+    case 64:
+      return two ? launch_prefill_paged<64, 2, 10>(mq, mk, mv, p, total_q, s)
+                 : launch_prefill_paged<64, 1, 12>(mq, mk, mv, p, total_q, s);
+    case 128:
+      return two ? launch_prefill_paged<128, 2, 5>(mq, mk, mv, p, total_q, s)
+                 : launch_prefill_paged<128, 1, 6>(mq, mk, mv, p, total_q, s);
+    case 256: return launch_prefill_paged<256, 1, 5>(mq, mk, mv, p, total_q, s);
   }
   return ATTN_ERR_UNSUPPORTED;
 }

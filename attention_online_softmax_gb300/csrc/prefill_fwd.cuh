@@ -185,10 +185,10 @@ __device__ __forceinline__ Unit<NQ> unit_of(const PrefillParams& p, int idx) {
     u.qbase = __ldg(p.cu_q + a);
     u.nq = __ldg(p.cu_q + a + 1) - u.qbase;
     u.nk = __ldg(p.seqlens_k + a);
-    const int ntiles = (u.nq + kBM - 1) / kBM;
+    const int ntiles = (u.nq + kBM * NQ - 1) / (kBM * NQ);  // units of NQ query tiles
     u.bh = local % p.Hq;
     u.kvh = u.bh / (p.Hq / p.Hkv);
-    u.q0 = (ntiles - 1 - local / p.Hq) * kBM;
+    u.q0 = (ntiles - 1 - local / p.Hq) * (kBM * NQ);
   } else {
     const int BH = p.B * p.Hq;
     const int per_group = p.group * p.n_units;
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
                        const PrefillParams p) {
   using L = PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(), psep_path<BIAS, PAGED>()>;
   static_assert(BIAS == 0 || NQ == 1, "additive-bias variants run one query tile per unit");
-  static_assert(!PAGED || (NQ == 1 && BIAS == 0), "paged prefill: one query tile per unit, no dense bias");
+  static_assert(!PAGED || BIAS == 0, "paged prefill: no dense bias");
   static_assert(sizeof(Unit<NQ>) <= L::kUnitBytes, "unit queue entry");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -494,10 +494,13 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
         if (q_uses > 0 && !mbar_wait(q_empty, (q_uses - 1) & 1, 5)) {
           qok = 0;
         } else {
-          mbar_expect_tx(q_full, L::kQBytes);
+          mbar_expect_tx(q_full, NQ * L::kQBytes);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)  // packed [total_q][Hq][d]: 128 tokens of one head
-            tma_load_3d(smem + L::kQOff + c * (kBM * 128), &tmQ, q_full, c * 64, u.bh, u.qbase + u.q0);
+          for (int j = 0; j < NQ; ++j)
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)  // packed [total_q][Hq][d]: 128 tokens of one head
+              tma_load_3d(smem + L::kQOff + j * L::kQBytes + c * (kBM * 128), &tmQ, q_full, c * 64, u.bh,
+                          u.qbase + u.q0 + j * kBM);
         }
       }
       if (!__shfl_sync(kFull, qok, 0)) break;
@@ -1118,12 +1121,12 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
 
 
 // Unit prefix sums of a paged chunked prefill (one block): sequence s gets
-// ceil(q_len / 128) * Hq units.  A sequence whose lengths are inconsistent
+// ceil(q_len / unit_rows) * Hq units (unit_rows = 128 x query tiles per unit).  A sequence whose lengths are inconsistent
 // (negative, past total_q, or a context longer than its block-table row) is
 // flagged in the status word and gets no units, so nothing of it is read.
 __global__ void __launch_bounds__(1024) paged_plan_kernel(const int32_t* cu_q, const int32_t* seqlens_k,
                                                          int num_seqs, int total_q, int Hq, int max_pages,
-                                                         int page_size, int32_t* unit_prefix) {
+                                                         int page_size, int unit_rows, int32_t* unit_prefix) {
   __shared__ int part[1024];
   const int per = (num_seqs + blockDim.x - 1) / blockDim.x;
   const int s0 = min(num_seqs, static_cast<int>(threadIdx.x) * per);
@@ -1136,7 +1139,7 @@ __global__ void __launch_bounds__(1024) paged_plan_kernel(const int32_t* cu_q, c
       report_error(7 /* ATTN_ERR_BOUNDS */, 9, s);
       return 0;
     }
-    return ((b - a + kBM - 1) / kBM) * Hq;
+    return ((b - a + unit_rows - 1) / unit_rows) * Hq;
   };
   int sum = 0;
   for (int s = s0; s < s1; ++s) sum += units(s);

@@ -80,6 +80,27 @@ def test_paged_prefill(abi, case):
     check_paged(abi, x, causal, window)
 
 
+# Enough heads that the library pairs two query tiles per unit; ragged chunks
+# leave a unit's second tile partly or wholly past its sequence.
+TWO_TILE = [
+    ([300, 1, 200, 77], [1000, 33, 300, 77], 160, 32, 64, 16, True, 0),
+    ([260, 520], [900, 520], 128, 16, 128, 16, True, 0),
+    ([384, 129], [384, 700], 128, 32, 128, 32, False, 0),
+]
+
+
+@pytest.mark.parametrize("case", TWO_TILE)
+def test_paged_prefill_two_tile_units(abi, case):
+    q_lens, k_lens, Hq, Hkv, d, ps, causal, window = case
+    pages = sum((k + ps - 1) // ps for k in k_lens) + 9
+    x = inputs.paged_prefill_inputs(q_lens, k_lens, Hq, Hkv, d, num_pages=pages, page_size=ps,
+                                    seed=6500 + sum(q_lens) + d)
+    g = torch.Generator().manual_seed(6501)
+    total = x.q.shape[0] * Hq
+    rows = np.concatenate([torch.randperm(total, generator=g)[:20000].numpy(), [0, total - 1]])
+    check_paged(abi, x, causal, window, rows=rows)
+
+
 def test_one_token_chunks_match_the_oracle_decode(abi):
     # One new token per sequence is paged decode; the prefill kernel handles it too.
     k_lens = [1, 17, 64, 200, 5, 4097]
