@@ -162,9 +162,13 @@ def attn_fwd_masked(q, k, v, o, lse, causal: bool, scale: float, window_left: in
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, torch.bfloat16, n)
     _need(lse, torch.float32, "lse")
+    if o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be bfloat16 or float32")
     _need(o, o.dtype, "o")
     B, Hq, Nq, d = q.shape
     _, Hkv, Nk, _ = k.shape
+    if tuple(o.shape) != (B, Hq, Nq, d) or tuple(lse.shape) != (B, Hq, Nq) or v.shape != k.shape:
+        raise ValueError("shape mismatch between q, k, v, o, lse")
     m = AttnMask(int(window_left), None, None, 0, 0)
     if alibi is not None:
         _need(alibi, torch.float32, "alibi")
