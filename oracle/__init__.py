@@ -142,7 +142,7 @@ def attention(q, k, v, causal: bool, scale: float, rows=None, threads: int = 0,
 
 
 def attention_masked(q, k, v, causal: bool, scale: float, window_left: int = 0, alibi=None,
-                     bias=None, bias_strides=(0, 0), rows=None, threads: int = 0):
+                     bias=None, bias_strides=(0, 0), rows=None, threads: int = 0, mutant: int = 0):
     """Attention with the additive bias C = causal mask + left window + ALiBi
     + dense bias (see oracle_attention_masked in attn_oracle.c), float64.
 
@@ -163,7 +163,7 @@ def attention_masked(q, k, v, causal: bool, scale: float, window_left: int = 0, 
         nrows = rows_arr.size
     o = np.empty((nrows, d), dtype=np.float64)
     lse = np.empty((nrows,), dtype=np.float64)
-    rc = _load().oracle_attention_masked(
+    rc = _load(mutant).oracle_attention_masked(
         _ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
         int(window_left), None if al is None else _ptr(al), None if bb is None else _ptr(bb),
         int(bias_strides[0]), int(bias_strides[1]),
@@ -209,7 +209,7 @@ def decode_paged(q, kcache, vcache, block_table, seqlens, scale: float,
     return o, lse, rc
 
 
-def attention_bwd(q, k, v, dout, causal: bool, scale: float, threads: int = 0):
+def attention_bwd(q, k, v, dout, causal: bool, scale: float, threads: int = 0, mutant: int = 0):
     """Gradients (dQ, dK, dV) of the attention output for the upstream
     gradient dout (see oracle_attention_bwd in attn_oracle.c), float64.
 
@@ -224,7 +224,7 @@ def attention_bwd(q, k, v, dout, causal: bool, scale: float, threads: int = 0):
     dq = np.empty((B, Hq, Nq, d), dtype=np.float64)
     dk = np.empty((B, Hkv, Nk, d), dtype=np.float64)
     dv = np.empty((B, Hkv, Nk, d), dtype=np.float64)
-    rc = _load().oracle_attention_bwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), B, Hq, Hkv, Nq, Nk, d,
+    rc = _load(mutant).oracle_attention_bwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), B, Hq, Hkv, Nq, Nk, d,
                                       int(bool(causal)), float(scale), _ptr(dq), _ptr(dk), _ptr(dv),
                                       int(threads))
     if rc < 0:
@@ -233,7 +233,7 @@ def attention_bwd(q, k, v, dout, causal: bool, scale: float, threads: int = 0):
 
 
 def prefill_paged(q, kcache, vcache, block_table, cu_seqlens_q, seqlens_k, causal: bool,
-                  scale: float, window_left: int = 0, rows=None, threads: int = 0):
+                  scale: float, window_left: int = 0, rows=None, threads: int = 0, mutant: int = 0):
     """Chunked prefill of ragged sequences against a paged KV cache (see
     oracle_prefill_paged in attn_oracle.c), float64.
 
@@ -262,7 +262,7 @@ def prefill_paged(q, kcache, vcache, block_table, cu_seqlens_q, seqlens_k, causa
         nrows = rows_arr.size
     o = np.empty((nrows, d), dtype=np.float64)
     lse = np.empty((nrows,), dtype=np.float64)
-    rc = _load().oracle_prefill_paged(
+    rc = _load(mutant).oracle_prefill_paged(
         _ptr(qb), _ptr(kb), _ptr(vb), _ptr(bt), _ptr(cu), _ptr(sk), S, Hq, Hkv, d, page, P,
         bt.shape[1] if bt.ndim == 2 else 0, int(bool(causal)), int(window_left), float(scale),
         None if rows_arr is None else _ptr(rows_arr), nrows, _ptr(o), _ptr(lse), int(threads))

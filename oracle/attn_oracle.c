@@ -42,7 +42,10 @@
  * Build switch ORACLE_MUTANT (default 0) plants one deliberate mistake; it
  * exists only so the test-suite can show that its pins catch each kind of
  * mistake (a dropped scale, a wrong mask offset, a wrong head, a transposed
- * operand, a dropped normaliser).  The shipped oracle is built with 0.
+ * operand, a dropped normaliser; in the backward a dropped D term or a
+ * dropped dK scale; in the chunked prefill a causal bound off by one or a
+ * wrong kv head; in the additive bias an ALiBi distance of the wrong sign).
+ * The shipped oracle is built with 0.
  */
 #include <math.h>
 #include <stdint.h>
@@ -208,7 +211,11 @@ int oracle_attention_masked(const uint16_t* q, const uint16_t* k, const uint16_t
                 if (causal && j > i + diag) continue;
                 if (window_left > 0 && j <= i + diag - window_left) continue;
                 double c = 0.0;
+#if ORACLE_MUTANT == 9
+                if (alibi) c += (double)alibi[h] * (double)(i - j + diag);  /* distance of the wrong sign */
+#else
                 if (alibi) c += (double)alibi[h] * (double)(j - i - diag);
+#endif
                 if (bias) c += bf16_to_double(bias[b * bias_sb + h * bias_sh + i * (int64_t)Nk + j]);
                 krows[n] = kb + j * d;
                 vrows[n] = vb + j * d;
@@ -441,11 +448,19 @@ int oracle_prefill_paged(const uint16_t* q, const uint16_t* kcache, const uint16
             const int64_t k_len = seqlens_k[seq];
             const int64_t i = token - cu_seqlens_q[seq];
             const int64_t diag = k_len - q_len;
+#if ORACLE_MUTANT == 8
+            int64_t hi = causal ? i + diag : k_len;  /* causal bound off by one */
+#else
             int64_t hi = causal ? i + diag + 1 : k_len;
+#endif
             if (hi > k_len) hi = k_len;
             int64_t lo = window_left > 0 ? i + diag - window_left + 1 : 0;
             if (lo < 0) lo = 0;
+#if ORACLE_MUTANT == 10
+            const int g = h % Hkv;  /* wrong kv head */
+#else
             const int g = h / group;
+#endif
             int64_t t, n = 0;
             int ok = 1;
             for (t = lo; t < hi; ++t, ++n) {
@@ -567,10 +582,18 @@ int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v
                     }
                     double* dqi = dq + row * d;
                     for (j = 0; j < n; ++j) {
+#if ORACLE_MUTANT == 6
+                        const double ds = p[j] * dp[j];  /* dropped D */
+#else
                         const double ds = p[j] * (dp[j] - D);
+#endif
                         for (c = 0; c < d; ++c) {
                             dqi[c] += sc * ds * bf16_to_double(kb[j * d + c]);
+#if ORACLE_MUTANT == 7
+                            dkb[j * d + c] += ds * bf16_to_double(qi[c]);  /* dropped scale */
+#else
                             dkb[j * d + c] += sc * ds * bf16_to_double(qi[c]);
+#endif
                             dvb[j * d + c] += p[j] * bf16_to_double(doi[c]);
                         }
                     }

@@ -146,3 +146,14 @@ def test_masked_oracle_against_torch_sdpa_float64():
     fin = torch.isfinite(lse).numpy()
     np.testing.assert_allclose(O[fin], ref.numpy()[fin], atol=1e-12)
     np.testing.assert_allclose(L[fin], lse.numpy()[fin], atol=1e-12)
+
+
+def test_planted_alibi_sign_mistake_is_caught():
+    # An ALiBi distance of the wrong sign (mutant 9) must fail the decimal pin.
+    B, Hq, Hkv, Nq, Nk, d, causal, window = 1, 2, 1, 7, 15, 4, True, 3
+    x = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, seed=720, causal=causal)
+    slopes = np.array([0.5, 0.25], dtype=np.float32)
+    O, L, _ = oracle.attention_masked(x.q, x.k, x.v, causal, x.scale, window_left=window, alibi=slopes, mutant=9)
+    C = c_matrix(B, Hq, Nq, Nk, causal, window, slopes, None)
+    Ob, Lb = decimal_with_bias(bf16_np(x.q), bf16_np(x.k), bf16_np(x.v), x.scale, C)
+    assert not (close(O, Ob, 1e-6) and close(L, Lb, 1e-6))

@@ -122,3 +122,24 @@ def test_bwd_rows_without_keys_take_no_gradient():
     dq, dk, dv, _ = oracle.attention_bwd(x.q, x.k, x.v, dout, True, x.scale)
     assert np.all(dq[0, 0, :5] == 0.0)
     assert np.any(dq[0, 0, 5:] != 0.0)
+
+
+@pytest.mark.parametrize("mutant", [6, 7])
+def test_planted_backward_mistakes_are_caught(mutant):
+    # A dropped D term (6) or a dropped dK scale (7) must fail the autograd pin.
+    B, Hq, Hkv, Nq, Nk, d = 1, 2, 1, 9, 13, 8
+    x = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, seed=60, causal=True)
+    dout = dout_for((B, Hq, Nq, d), 61)
+    dq, dk, dv, _ = oracle.attention_bwd(x.q, x.k, x.v, dout, True, x.scale, mutant=mutant)
+    q = x.q.double().requires_grad_()
+    k = x.k.double().requires_grad_()
+    v = x.v.double().requires_grad_()
+    i = torch.arange(Nq)[:, None]
+    j = torch.arange(Nk)[None, :]
+    out = torch.nn.functional.scaled_dot_product_attention(
+        q, k.repeat_interleave(Hq // Hkv, 1), v.repeat_interleave(Hq // Hkv, 1), attn_mask=j <= i + Nk - Nq,
+        scale=x.scale)
+    out.backward(dout.double())
+    agree = (np.allclose(dq, q.grad.numpy(), atol=1e-9) and np.allclose(dk, k.grad.numpy(), atol=1e-9)
+             and np.allclose(dv, v.grad.numpy(), atol=1e-9))
+    assert not agree

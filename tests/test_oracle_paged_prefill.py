@@ -140,3 +140,22 @@ def test_bad_block_table_entry_is_rejected():
     with pytest.raises(ValueError):
         oracle.prefill_paged(x.q, x.kcache, x.vcache, x.block_table, x.cu_seqlens_q, x.seqlens_k,
                              True, x.scale)
+
+
+@pytest.mark.parametrize("mutant", [8, 10])
+def test_planted_paged_mistakes_are_caught(mutant):
+    # A causal bound off by one (8) or a wrong kv head (10) must fail the pin
+    # against the plain oracle on gathered rows.
+    q_lens, k_lens = [37, 20], [100, 150]
+    x = inputs.paged_prefill_inputs(q_lens, k_lens, 4, 2, 16, num_pages=40, page_size=8, seed=906)
+    O, L, _ = oracle.prefill_paged(x.q, x.kcache, x.vcache, x.block_table, x.cu_seqlens_q, x.seqlens_k,
+                                   True, x.scale, mutant=mutant)
+    agree = True
+    for s in range(len(q_lens)):
+        a, b = seq_slice(x, s)
+        k, v = gather(x, s)
+        Op, Lp, _ = oracle.attention(x.q[a:b].permute(1, 0, 2).unsqueeze(0).contiguous(),
+                                     k.permute(1, 0, 2).unsqueeze(0).contiguous(),
+                                     v.permute(1, 0, 2).unsqueeze(0).contiguous(), True, x.scale)
+        agree = agree and np.allclose(O[a:b], Op[0].transpose(1, 0, 2), atol=1e-9)
+    assert not agree
