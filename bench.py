@@ -578,7 +578,7 @@ def measure_e2e(abi, xp, xd, dev, stream, steps, floor_s, world):
             "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * t / steps, "steps": steps}
 
 
-def per_config_table(abi, dev, stream, peaks, reps: int = 10):
+def per_config_table(abi, dev, stream, peaks, reps: int = 30):
     """Each workload timed alone (median of reps, L2 flushed before each)."""
     out = {}
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
