@@ -2,7 +2,9 @@
 //
 // A persistent kernel: one CTA per SM takes work units from a per-launch
 // atomic counter until none are left.  A unit is NQ 128-row query tiles
-// (NQ = 2 for d <= 128, 1 for d = 256) of one (batch, query head), computed
+// (NQ = 2 for d <= 128 when that still gives two units per SM, else 1) of one
+// (batch, query head) -- or, in the PAGED variant, of one sequence and query
+// head of a chunked prefill against a paged KV cache -- computed
 // against the key/value tiles those rows may see with the block recurrence of
 // "Compilers and Kernels", section "FlashAttention changes the algorithm
 // around IO": for each key block B_t the row state (m, l, o) is updated by
@@ -12,7 +14,8 @@
 // Units are handed out longest causal unit first within groups of heads, so
 // the uneven causal units pack well while each group's K/V stays in L2.
 //
-// Roles (64 + 128*NQ threads):
+// Roles (64 + 128*NQ threads, plus a bias-loader warp for a staged dense bias
+// and a second MMA-issuing warp with separate P slots):
 //   warp 0        TMA producer: takes the next unit from the work counter and
 //                 passes it to the other roles through a small shared-memory
 //                 queue, loads the unit's NQ query tiles, then its K_t, V_t
@@ -23,9 +26,10 @@
 //                 S_j = Q_j K_t^T (smem x smem) into TMEM, then
 //                 O_j += P_j V_t with P_j read from TMEM (tmem x smem).
 //   warps 2..     one softmax warpgroup per query tile, one thread per row:
-//                 reads S from TMEM, applies the mask, updates the running max,
-//                 writes P = 2^(x - m) as bf16 back over S in TMEM, rescales O
-//                 in TMEM when the max moved, and writes O / l and LSE.
+//                 reads S from TMEM, adds the bias terms and applies the masks,
+//                 updates the running max, writes P = 2^(x - m) as bf16 to
+//                 TMEM, rescales O in TMEM when the max moved, and writes O / l
+//                 and LSE.
 //
 // Tensor memory (512 columns): O_j at columns [j*D, (j+1)*D); two S slots of
 // 128 columns after them.  With NQ = 2 slot j belongs to query tile j and the
@@ -34,6 +38,10 @@
 // tiles: S(t+1) is computed while tile t is softmaxed.  P (bf16, 64 columns)
 // overwrites the first half of its S slot; tcgen05 MMAs from one thread run in
 // issue order, so the next S into that slot is issued after the P V product.
+// The plain kernel with NQ = 1 and d <= 128 instead keeps P in two slots of
+// its own after the S slots (O + 2 S + 2 P = 512 columns at d = 128): S(t+2)
+// is issued once the softmax has read S(t), and a second thread issues the
+// P V products.
 // A unit's first P V product overwrites O_j only after the previous unit's
 // epilogue has read it (barrier o_free).  Barrier phases run on across units.
 //
