@@ -69,6 +69,9 @@ constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;  // keys per tile
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kUnitQ = 4;  // depth of the in-CTA queue of fetched units
+// Ring of per-step K/V barriers (plain kernel, two query tiles): more entries
+// than any producer lead over the MMA thread, so phases never alias.
+constexpr int kStepR = 16;
 
 struct PrefillParams {
   void* o;
@@ -121,10 +124,10 @@ struct PrefillLayout {
   static constexpr int kBiasOff = kKVOff + STAGES * kKVBytes;
   static constexpr int kBarOff = kBiasOff + BSLOTS * kBiasBytes;
   // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done,
-  // (s_free[2], pv_free[2] after tail_bar),
+  // (s_free[2], pv_free[2], step_full[kStepR], step_empty[kStepR] after tail_bar),
   // o_done[2], o_free[2], unit_full[Q], unit_empty[Q], mma_drain,
   // bias_full[BSLOTS], bias_empty[BSLOTS], tail_bar
-  static constexpr int kNumBars = 2 + 2 * STAGES + 2 + 2 + 1 + 2 + 2 + 2 * kUnitQ + 1 + 2 * BSLOTS + 1 + 4;
+  static constexpr int kNumBars = 2 + 2 * STAGES + 2 + 2 + 1 + 2 + 2 + 2 * kUnitQ + 1 + 2 * BSLOTS + 1 + 4 + 2 * kStepR;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, unit queue
   static constexpr int kUnitBytes = 64;                      // one decoded unit in the queue
   static constexpr int kBytes = kMiscOff + 16 + kUnitBytes * kUnitQ;
@@ -325,6 +328,13 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
   uint64_t* tail_bar = bias_empty + bias_slots<BIAS>();  // paged: a partly filled value page
   uint64_t* s_free = tail_bar + 1;   // [2] separate P slots: the softmax has read S from this slot
   uint64_t* pv_free = s_free + 2;    // [2] separate P slots: the P V product of this P slot is complete
+  uint64_t* step_full = pv_free + 2;         // [kStepR] step ring: V(t-1) and K(t) have landed
+  uint64_t* step_empty = step_full + kStepR;  // [kStepR] step ring: the step's products are done with them
+  // Plain kernel with two query tiles: the K/V ring is gated per MMA step
+  // (V(t-1) and K(t), consecutive items) rather than per item -- one barrier
+  // wait and one commit per step for the issuing thread instead of two each.
+  constexpr bool kStepRing = NQ == 2 && !PAGED;
+  static_assert(!kStepRing || L::kH == 1, "step ring: one item per K or V tile");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   Unit<NQ>* unit_q = reinterpret_cast<Unit<NQ>*>(smem + L::kMiscOff + 16);
 
@@ -365,6 +375,10 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       mbar_init(&s_free[i], 4);
       mbar_init(&pv_free[i], 1);
     }
+    for (int i = 0; i < kStepR; ++i) {
+      mbar_init(&step_full[i], 1);
+      mbar_init(&step_empty[i], 1);
+    }
     for (int i = 0; i < bias_slots<BIAS>(); ++i) {
       mbar_init(&bias_full[i], 1);
       mbar_init(&bias_empty[i], 4);  // lane 0 of every softmax warp
@@ -402,6 +416,10 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       tma_prefetch_desc(&tmV);
       const int total_units = p.B * p.Hq * p.n_units;
       int item = 0;  // K/V items issued so far (the ring runs on across units)
+      int step = 0;  // step ring: steps issued so far
+      int slot_rel[STAGES];  // step ring: the step that releases each slot's item (-1: none yet)
+#pragma unroll
+      for (int i = 0; i < STAGES; ++i) slot_rel[i] = -1;
       int q_uses = 0;
       bool ok = true;
       for (int n = 0; ok; ++n) {
@@ -429,26 +447,56 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
             tma_load_3d(smem + L::kQOff + j * L::kQBytes + c * (kBM * 128), &tmQ, q_full, c * 64,
                         u.q0 + j * kBM, u.bh);
         ++q_uses;
-        for (int i = 0; i < 2 * L::kH * u.T; ++i, ++item) {
-          const int st = item % STAGES;
-          if (!mbar_wait(&kv_empty[st], ((item / STAGES) & 1) ^ 1, 1)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(&kv_full[st], L::kKVBytes);
-          int t, kind, hh;
-          load_item<NQ, L::kH, L::kPSep>(i, u.T, t, kind, hh);
-          const CUtensorMap* map = kind ? &tmV : &tmK;
+        if constexpr (kStepRing) {
+          // Step t of the unit brings V(t-1) and K(t) (items 2t-1, 2t) on one
+          // barrier; a slot is refilled once the step that read it is done.
+          for (int t = 0; ok && t <= u.T; ++t, ++step) {
+            const int nv = t >= 1 ? 1 : 0, nk = t < u.T ? 1 : 0;
+            for (int i = 0; i < nv + nk; ++i) {
+              const int r = slot_rel[(item + i) % STAGES];
+              if (r >= 0 && !mbar_wait(&step_empty[r % kStepR], (r / kStepR) & 1, 1)) ok = false;
+            }
+            if (!ok) break;
+            uint64_t* bar = &step_full[step % kStepR];
+            mbar_expect_tx(bar, (nv + nk) * L::kKVBytes);
+            for (int i = 0; i < nv + nk; ++i, ++item) {
+              const int st = item % STAGES;
+              const bool is_v = i < nv;
+              const int tt = is_v ? t - 1 : t;
 #pragma unroll
-          for (int c = 0; c < L::kDI / 64; ++c)
-            tma_load_3d(smem + L::kKVOff + st * L::kKVBytes + c * (kBN * 128), map, &kv_full[st],
-                        hh * L::kDI + c * 64, (u.tmin + t) * kBN, u.kvh);
+              for (int c = 0; c < L::kDI / 64; ++c)
+                tma_load_3d(smem + L::kKVOff + st * L::kKVBytes + c * (kBN * 128), is_v ? &tmV : &tmK, bar,
+                            c * 64, (u.tmin + tt) * kBN, u.kvh);
+              slot_rel[st] = step;
+            }
+          }
+        } else {
+          for (int i = 0; i < 2 * L::kH * u.T; ++i, ++item) {
+            const int st = item % STAGES;
+            if (!mbar_wait(&kv_empty[st], ((item / STAGES) & 1) ^ 1, 1)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&kv_full[st], L::kKVBytes);
+            int t, kind, hh;
+            load_item<NQ, L::kH, L::kPSep>(i, u.T, t, kind, hh);
+            const CUtensorMap* map = kind ? &tmV : &tmK;
+#pragma unroll
+            for (int c = 0; c < L::kDI / 64; ++c)
+              tma_load_3d(smem + L::kKVOff + st * L::kKVBytes + c * (kBN * 128), map, &kv_full[st],
+                          hh * L::kDI + c * 64, (u.tmin + t) * kBN, u.kvh);
+          }
         }
       }
       // Drain: never leave the CTA with a copy still writing shared memory.
       if (q_uses > 0) mbar_wait(q_full, (q_uses - 1) & 1, 2);
-      for (int it = max(0, item - STAGES); it < item; ++it)
-        mbar_wait(&kv_full[it % STAGES], (it / STAGES) & 1, 3);
+      if (kStepRing) {
+        for (int st = max(0, step - kStepR); st < step; ++st)
+          mbar_wait(&step_full[st % kStepR], (st / kStepR) & 1, 3);
+      } else {
+        for (int it = max(0, item - STAGES); it < item; ++it)
+          mbar_wait(&kv_full[it % STAGES], (it / STAGES) & 1, 3);
+      }
     }
     __syncwarp();
   } else if (warp == 0) {
@@ -644,6 +692,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       const uint64_t dkv0 = sdesc_sw128(sbase + L::kKVOff, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sbase + L::kKVOff, kBN * 128, 1024);
       int item0 = 0;        // first K/V item of the current unit
+      int step = 0;         // step ring: steps consumed so far
       int q_uses = 0;       // units with work so far
       int cnt[2] = {0, 0};  // S tiles issued: per query tile (NQ = 2), in total (NQ = 1, cnt[0])
       int o_uses[2] = {0, 0};
@@ -774,6 +823,13 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
               // PV_A(t-1), S_A(t), PV_B(t-1), S_B(t); K/V items are waited for
               // by their first user and released after their last.
               bool waitedV = false, waitedK = false;
+              if (kStepRing) {
+                // Both of the step's items on one barrier (every step reads one).
+                ok = ATTN_MMA_WAIT(&step_full[step % kStepR], (step / kStepR) & 1, 13);
+                if (!ok) break;
+                tc_fence_after();
+                waitedV = waitedK = true;
+              }
 #pragma unroll
               for (int j = 0; j < NQ; ++j) {
                 if (t >= 1 && ta - 1 >= u.lo[j] && ta - 1 < u.hi[j]) {
@@ -801,8 +857,13 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
                 }
               }
               if (!ok) break;
-              if (waitedV) release(vit);
-              if (waitedK) release(kit);
+              if (kStepRing) {
+                umma_commit(&step_empty[step % kStepR]);
+                ++step;
+              } else {
+                if (waitedV) release(vit);
+                if (waitedK) release(kit);
+              }
               if (t == T - 1) umma_commit(q_empty);  // the unit's last S MMA is issued
             } else {
               // S(t) into slot c&1 (overlaps the softmax of tile t-1), then PV(t-1).
