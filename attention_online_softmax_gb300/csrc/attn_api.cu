@@ -210,6 +210,20 @@ attn_status sched_slot(int** out) {
   return ATTN_OK;
 }
 
+// (Batch, head) pairs per scheduling group of the plain prefill: at least
+// `want` (enough heads for two waves of units), and groups of equal size --
+// a short last group would start its longest units last and leave the end of
+// the launch to a few SMs.  A divisor of BH up to twice `want` if there is
+// one, else BH split into near-equal groups of about `want`.
+int sched_group(int BH, int want) {
+  if (want < 1) want = 1;
+  if (want >= BH) return BH;
+  for (int d = want; d <= 2 * want && d <= BH; ++d)
+    if (BH % d == 0) return d;
+  const int groups = BH / want;
+  return (BH + groups - 1) / groups;
+}
+
 template <int D, int NQ, int STAGES, int BIAS = 0>
 attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            const CUtensorMap& mb, attn::PrefillParams p, int BH, cudaStream_t stream) {
@@ -221,9 +235,7 @@ attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const C
   }
   p.n_units = (p.Nq + attn::kBM * NQ - 1) / (attn::kBM * NQ);
   const int sms = sm_count();
-  // Enough heads per scheduling group for two waves of units.
-  const int want = (2 * sms + p.n_units - 1) / p.n_units;
-  p.group = want < 1 ? 1 : (want > BH ? BH : want);
+  p.group = sched_group(BH, (2 * sms + p.n_units - 1) / p.n_units);
   const long long units = static_cast<long long>(p.n_units) * BH;
   if (units > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
   const attn_status st = sched_slot(&p.sched);
@@ -502,7 +514,7 @@ attn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o
       return two ? launch_prefill<64, 2, 10>(mq, mk, mv, mq, p, B * Hq, s)
                  : launch_prefill<64, 1, 12>(mq, mk, mv, mq, p, B * Hq, s);
     case 128:
-      return two ? launch_prefill<128, 2, 5>(mq, mk, mv, mq, p, B * Hq, s)
+      return two ? launch_prefill<128, 2, 4>(mq, mk, mv, mq, p, B * Hq, s)
                  : launch_prefill<128, 1, 6>(mq, mk, mv, mq, p, B * Hq, s);
     case 256: return launch_prefill<256, 1, 5>(mq, mk, mv, mq, p, B * Hq, s);
   }

@@ -45,8 +45,9 @@ _CSRC = os.path.join(ROOT, "attention_online_softmax_gb300", "csrc")
 # The sources that define each profiled kernel: its own header and the shared
 # PTX helpers.
 KERNEL_SOURCES = {
-    "prefill_fwd_c3": [os.path.join(_CSRC, f) for f in ("ptx.cuh", "prefill_fwd.cuh")],
-    "decode_c5": [os.path.join(_CSRC, f) for f in ("ptx.cuh", "decode.cuh")],
+    # The kernel's header and the launch code (stages, scheduling) that sets it up.
+    "prefill_fwd_c3": [os.path.join(_CSRC, f) for f in ("ptx.cuh", "prefill_fwd.cuh", "attn_api.cu")],
+    "decode_c5": [os.path.join(_CSRC, f) for f in ("ptx.cuh", "decode.cuh", "attn_api.cu")],
 }
 
 
@@ -425,7 +426,7 @@ def main(argv=None):
                                       "launch_us": launch_s * 1e6, "kernels": dec_kernels,
                                       "dram_latency_us": dram_s * 1e6,
                                       "measured_over_floor": mean_dec / dec_floor}},
-            "roofline": {"bound": "tensor", "kernel": "prefill_fwd_kernel<128,2,5,0,0> (d128, two query tiles per CTA)",
+            "roofline": {"bound": "tensor", "kernel": "prefill_fwd_kernel<128,2,4,0,0> (d128, two query tiles per CTA)",
                          "achieved": pre_tflops, "peak": peaks.bf16_tflops, "unit": "TFLOP/s",
                          "frac": pre_tflops / peaks.bf16_tflops, "peak_source": peak_src,
                          "traffic": traffic_from_profiles("prefill_fwd_c3"),
