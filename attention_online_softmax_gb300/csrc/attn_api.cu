@@ -264,7 +264,8 @@ attn_status launch_prefill_paged(const CUtensorMap& mq, const CUtensorMap& mk, c
   if (st != ATTN_OK) return st;
   attn::paged_plan_kernel<<<1, 1024, 0, stream>>>(p.cu_q, p.seqlens_k, p.num_seqs, total_q, p.Hq, p.max_pages,
                                                    p.page_size, attn::kBM * NQ,
-                                                   const_cast<int32_t*>(p.unit_prefix));
+                                                   const_cast<int32_t*>(p.unit_prefix),
+                                                   const_cast<int32_t*>(p.seq_order));
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   kern<<<dim3(static_cast<unsigned>(sm_count())), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mv, p);
@@ -397,6 +398,14 @@ attn_status static_scratch_address(void** out) {
 
 }  // namespace
 
+namespace {
+// Bytes of the paged prefill's unit prefix sums in its workspace (then the
+// sequences' dispatch order).
+size_t paged_prefix_bytes(int num_seqs) {
+  return ((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+}
+}  // namespace
+
 extern "C" {
 
 int attn_abi_version(void) { return 1; }
@@ -523,7 +532,9 @@ attn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o
 
 size_t attn_prefill_paged_workspace_size(int num_seqs) {
   if (num_seqs < 0) return 0;
-  return ((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+  // Unit prefix sums, then the sequences' dispatch order.
+  return paged_prefix_bytes(num_seqs) +
+         ((static_cast<size_t>(num_seqs) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255));
 }
 
 attn_status attn_prefill_paged(const void* q, const void* kcache, const void* vcache, const int32_t* block_table,
@@ -568,6 +579,7 @@ attn_status attn_prefill_paged(const void* q, const void* kcache, const void* vc
   p.seqlens_k = seqlens_k;
   p.block_table = block_table;
   p.unit_prefix = static_cast<const int32_t*>(workspace);
+  p.seq_order = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(workspace) + paged_prefix_bytes(num_seqs));
   p.num_seqs = num_seqs;
   p.max_pages = max_pages_per_seq;
   p.page_size = page_size;

@@ -95,7 +95,8 @@ struct PrefillParams {
   const int32_t* cu_q;
   const int32_t* seqlens_k;
   const int32_t* block_table;
-  const int32_t* unit_prefix;  // [num_seqs + 1] units before each sequence (plan kernel)
+  const int32_t* unit_prefix;  // [num_seqs + 1] units before each rank of seq_order (plan kernel)
+  const int32_t* seq_order;    // [num_seqs] sequences in dispatch order, longest context first (plan kernel)
   int num_seqs, max_pages, page_size, num_pages;
 };
 
@@ -177,25 +178,26 @@ struct Unit {
 };
 
 // Unit `idx`.  Plain: the grouped longest-first order over (batch, head,
-// query-tile) (0 <= idx < B*Hq*n_units).  Paged: sequence by sequence (unit
-// prefix sums from the plan kernel), within a sequence its last query tile
-// first, heads fastest.
+// query-tile) (0 <= idx < B*Hq*n_units).  Paged: sequence by sequence in the
+// plan kernel's order (longest context first; unit prefix sums over that
+// order), within a sequence its last query tile first, heads fastest.
 template <int NQ, bool PAGED>
 __device__ __forceinline__ Unit<NQ> unit_of(const PrefillParams& p, int idx) {
   Unit<NQ> u;
   u.idx = idx;
   if (PAGED) {
-    int a = 0, b = p.num_seqs - 1;  // last sequence whose first unit is <= idx
+    int a = 0, b = p.num_seqs - 1;  // last rank whose first unit is <= idx
     while (a < b) {
       const int mid = (a + b + 1) >> 1;
       if (__ldg(p.unit_prefix + mid) <= idx) a = mid;
       else b = mid - 1;
     }
     const int local = idx - __ldg(p.unit_prefix + a);
-    u.seq = a;
-    u.qbase = __ldg(p.cu_q + a);
-    u.nq = __ldg(p.cu_q + a + 1) - u.qbase;
-    u.nk = __ldg(p.seqlens_k + a);
+    const int s = __ldg(p.seq_order + a);
+    u.seq = s;
+    u.qbase = __ldg(p.cu_q + s);
+    u.nq = __ldg(p.cu_q + s + 1) - u.qbase;
+    u.nk = __ldg(p.seqlens_k + s);
     const int ntiles = (u.nq + kBM * NQ - 1) / (kBM * NQ);  // units of NQ query tiles
     u.bh = local % p.Hq;
     u.kvh = u.bh / (p.Hq / p.Hkv);
@@ -1189,44 +1191,67 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
 }
 
 
-// Unit prefix sums of a paged chunked prefill (one block): sequence s gets
-// ceil(q_len / unit_rows) * Hq units (unit_rows = 128 x query tiles per unit).  A sequence whose lengths are inconsistent
-// (negative, past total_q, or a context longer than its block-table row) is
-// flagged in the status word and gets no units, so nothing of it is read.
+// Dispatch order and unit prefix sums of a paged chunked prefill (one block).
+// Sequences are handed out longest context first (ties by index), so the
+// persistent grid ends on short units rather than on one long sequence; up to
+// 1024 sequences are ranked (one per thread), more keep their given order.
+// Sequence s gets ceil(q_len / unit_rows) * Hq units (unit_rows = 128 x query
+// tiles per unit).  A sequence whose lengths are inconsistent (negative, past
+// total_q, or a context longer than its block-table row) is flagged in the
+// status word and gets no units, so nothing of it is read.
 __global__ void __launch_bounds__(1024) paged_plan_kernel(const int32_t* cu_q, const int32_t* seqlens_k,
                                                          int num_seqs, int total_q, int Hq, int max_pages,
-                                                         int page_size, int unit_rows, int32_t* unit_prefix) {
+                                                         int page_size, int unit_rows, int32_t* unit_prefix,
+                                                         int32_t* seq_order) {
   __shared__ int part[1024];
-  const int per = (num_seqs + blockDim.x - 1) / blockDim.x;
-  const int s0 = min(num_seqs, static_cast<int>(threadIdx.x) * per);
-  const int s1 = min(num_seqs, s0 + per);
-  auto units = [&](int s) -> int {
+  __shared__ int key[1024];
+  __shared__ int order[1024];
+  const int tid = static_cast<int>(threadIdx.x);
+  const bool ranked = num_seqs <= 1024;
+  auto units = [&](int s, bool report) -> int {
     const int a = cu_q[s], b = cu_q[s + 1], k = seqlens_k[s];
     const bool bad = a < 0 || b < a || b > total_q || k < 0 ||
                      static_cast<long long>(k) > static_cast<long long>(max_pages) * page_size;
     if (bad) {
-      report_error(7 /* ATTN_ERR_BOUNDS */, 9, s);
+      if (report) report_error(7 /* ATTN_ERR_BOUNDS */, 9, s);
       return 0;
     }
     return ((b - a + unit_rows - 1) / unit_rows) * Hq;
   };
+  if (ranked) {
+    if (tid < num_seqs) key[tid] = seqlens_k[tid];
+    __syncthreads();
+    if (tid < num_seqs) {
+      const int k = key[tid];
+      int rank = 0;
+      for (int j = 0; j < num_seqs; ++j) rank += (key[j] > k || (key[j] == k && j < tid)) ? 1 : 0;
+      order[rank] = tid;
+    }
+    __syncthreads();
+  }
+  auto seq_at = [&](int r) { return ranked ? order[r] : r; };
+  const int per = (num_seqs + blockDim.x - 1) / blockDim.x;
+  const int r0 = min(num_seqs, tid * per);
+  const int r1 = min(num_seqs, r0 + per);
   int sum = 0;
-  for (int s = s0; s < s1; ++s) sum += units(s);
-  part[threadIdx.x] = sum;
+  for (int r = r0; r < r1; ++r) sum += units(seq_at(r), true);
+  part[tid] = sum;
   __syncthreads();
   // Exclusive scan of the per-thread sums (Hillis-Steele over 1024 entries).
   for (int off = 1; off < 1024; off <<= 1) {
-    const int v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+    const int v = tid >= off ? part[tid - off] : 0;
     __syncthreads();
-    part[threadIdx.x] += v;
+    part[tid] += v;
     __syncthreads();
   }
-  int run = threadIdx.x > 0 ? part[threadIdx.x - 1] : 0;
-  for (int s = s0; s < s1; ++s) {
-    unit_prefix[s] = run;
-    run += units(s);
+  int run = tid > 0 ? part[tid - 1] : 0;
+  for (int r = r0; r < r1; ++r) {
+    const int s = seq_at(r);
+    unit_prefix[r] = run;
+    seq_order[r] = s;
+    run += units(s, false);
   }
-  if (threadIdx.x == blockDim.x - 1) unit_prefix[num_seqs] = part[blockDim.x - 1];
+  if (tid == blockDim.x - 1) unit_prefix[num_seqs] = part[blockDim.x - 1];
 }
 
 }  // namespace attn

@@ -123,8 +123,9 @@ ATTN_API attn_status attn_fwd_masked(const void* q, const void* k, const void* v
                      float scale, const attn_mask* mask, attn_dtype o_dtype, attn_stream_t stream);
 
 /*
- * Bytes of scratch memory attn_prefill_paged() needs: the per-sequence unit
- * prefix sums (num_seqs + 1 int32), rounded up to 256.  0 on invalid input.
+ * Bytes of scratch memory attn_prefill_paged() needs: the unit prefix sums
+ * (num_seqs + 1 int32) and the sequences' dispatch order (num_seqs int32),
+ * each rounded up to 256.  0 on invalid input.
  */
 ATTN_API size_t attn_prefill_paged_workspace_size(int num_seqs);
 

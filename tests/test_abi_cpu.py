@@ -132,3 +132,13 @@ def test_decode_workspace_size_is_a_pure_plan(abi):
     assert ws(4, 30, 8, 128, 512) == 0          # invalid -> 0
     assert ws(4, 32, 8, 96, 512) == 0
     assert ws(64, 32, 8, 128, 8192) == ws(64, 32, 8, 128, 8192)
+
+
+def test_paged_prefill_workspace_size(abi):
+    # Unit prefix sums (num_seqs + 1 int32) and the dispatch order (num_seqs
+    # int32), each rounded up to 256 bytes.
+    ws = abi.attn_prefill_paged_workspace_size
+    up = lambda n: (n + 255) // 256 * 256
+    for n in (0, 1, 16, 63, 64, 1000, 5000):
+        assert ws(n) == up((n + 1) * 4) + up(n * 4)
+    assert ws(-1) == 0

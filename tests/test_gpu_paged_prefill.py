@@ -140,3 +140,24 @@ def test_chunked_prefill_config(abi):
     rows = torch.randperm(total, generator=g)[:4096].numpy()
     rows = np.concatenate([rows, [0, total - 1]])
     check_paged(abi, x, True, 0, rows=rows)
+
+
+def test_more_sequences_than_the_plan_ranks(abi):
+    # Past 1024 sequences the plan kernel keeps the given dispatch order
+    # instead of ranking by context length; every row must still be right.
+    n = 1100
+    g = torch.Generator().manual_seed(6600)
+    q_lens = torch.randint(0, 3, (n,), generator=g).tolist()
+    k_lens = [q + int(e) for q, e in zip(q_lens, torch.randint(0, 40, (n,), generator=g).tolist())]
+    pages = sum((k + 15) // 16 for k in k_lens) + 9
+    x = inputs.paged_prefill_inputs(q_lens, k_lens, 4, 2, 64, num_pages=pages, page_size=16, seed=6601)
+    check_paged(abi, x, True)
+
+
+def test_equal_context_lengths_tie_in_index_order(abi):
+    # Ranked dispatch with ties (equal contexts) and a spread of lengths.
+    q_lens = [100, 37, 100, 1, 256, 100]
+    k_lens = [600, 600, 100, 600, 900, 600]
+    pages = sum((k + 15) // 16 for k in k_lens) + 9
+    x = inputs.paged_prefill_inputs(q_lens, k_lens, 8, 2, 128, num_pages=pages, page_size=16, seed=6602)
+    check_paged(abi, x, True)
