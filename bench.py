@@ -42,10 +42,9 @@ WORKLOAD = ("prefill causal MHA B2 H32 N4096 d128 bf16 + paged GQA decode 64 seq
             "len U[512,8192] 16-token pages in a 40000-page pool")
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 _CSRC = os.path.join(ROOT, "attention_online_softmax_gb300", "csrc")
-# The sources that define each profiled kernel: its own header and the shared
-# PTX helpers.
+# The sources that define each profiled kernel: its own header, the shared PTX
+# helpers and the launch code that sets its stages and scheduling.
 KERNEL_SOURCES = {
-    # The kernel's header and the launch code (stages, scheduling) that sets it up.
     "prefill_fwd_c3": [os.path.join(_CSRC, f) for f in ("ptx.cuh", "prefill_fwd.cuh", "attn_api.cu")],
     "decode_c5": [os.path.join(_CSRC, f) for f in ("ptx.cuh", "decode.cuh", "attn_api.cu")],
 }
@@ -297,7 +296,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-config table")
-    ap.add_argument("--profile", choices=["prefill", "prefill_d256", "decode"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "prefill_d256", "decode", "bwd", "chunked"], default=None,
                     help="run one kernel of the step a few times (for an ncu capture) and exit")
     args = ap.parse_args(argv)
     rank, world, local = dist_env()
@@ -454,14 +453,37 @@ def profile_one(which: str, launches: int = 3) -> int:
     from attention_online_softmax_gb300 import build
     build.build()
     from attention_online_softmax_gb300 import abi
-    if which.startswith("prefill"):
+    if which.startswith("prefill") or which == "bwd":
         c = configs.GQA256 if which == "prefill_d256" else configs.LONG
         x = make_prefill_inputs(c)
         q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
         o = torch.empty_like(q)
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-        for _ in range(launches):
+        if which == "bwd":
+            # The backward of the long causal MHA workload (its forward once first).
             abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale)
+            g = torch.Generator().manual_seed(c.seed + 50)
+            dout = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            ws = torch.empty(abi.attn_bwd_workspace_size(c.B, c.Hq, c.Nq, c.d), dtype=torch.uint8, device=dev)
+            for _ in range(launches):
+                abi.attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, c.causal, x.scale, workspace=ws)
+        else:
+            for _ in range(launches):
+                abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale)
+    elif which == "chunked":
+        c = configs.CHUNKED
+        q_lens, k_lens = configs.chunked_lengths(c)
+        x = inputs.paged_prefill_inputs(q_lens, k_lens, c.Hq, c.Hkv, c.d, num_pages=c.num_pages,
+                                        page_size=c.page_size, seed=c.seed)
+        q = x.q.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        args = (q, x.kcache.to(dev), x.vcache.to(dev), x.block_table.to(dev), x.cu_seqlens_q.to(dev),
+                x.seqlens_k.to(dev), o, lse, True, x.scale)
+        ws = torch.empty(max(16, abi.attn_prefill_paged_workspace_size(c.num_seqs)), dtype=torch.uint8, device=dev)
+        for _ in range(launches):
+            abi.attn_prefill_paged(*args, workspace=ws)
     else:
         Dc = configs.DECODE
         xd = make_decode_inputs()
