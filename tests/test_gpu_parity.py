@@ -223,3 +223,12 @@ def test_decode_bad_block_table_is_reported_not_read(abi):
                           d_in.block_table.to(dev), d_in.seqlens.to(dev), o, lse, 40, d_in.scale, ws)
     assert abi.attn_get_device_status() == 7
     assert abi.attn_get_device_status() == 0  # reading clears it
+
+
+def test_prefill_uneven_scheduling_groups(abi):
+    # 67 heads of 16 two-tile units: no divisor of 67 near the two-wave group
+    # size, so the heads are scheduled in groups of 23, 23 and 21; every unit
+    # of the short last group must still be computed once.
+    x = inputs.prefill_inputs(1, 67, 67, 4096, 4096, 64, seed=9, causal=True)
+    rows = inputs.check_rows(x.generator, 1, 67, 4096, 24)
+    check_prefill(abi, x, rows)
