@@ -74,3 +74,17 @@ def test_allowed_pairs_brute_force(Nq, Nk, causal, window):
                 continue
             n += 1
     assert roofline.allowed_pairs(Nq, Nk, causal, window) == n
+
+
+def test_backward_and_paged_prefill_counts_by_hand():
+    # Backward, B1 Hq4 Hkv2 N32 d16: Q, O, dO read and dQ written per query
+    # head (4 bf16 tensors of 4*32*16), K, V read and dK, dV written per kv
+    # head (4 of 2*32*16), LSE read (4*32 f32).
+    assert roofline.bwd_bytes(1, 4, 2, 32, 32, 16) == 4 * (4 * 32 * 16 * 2) + 4 * (2 * 32 * 16 * 2) + 4 * 32 * 4
+    # Chunked prefill: 2 sequences with 3 and 5 new tokens over contexts of
+    # 20 and 5 tokens, Hq 4, Hkv 2, d 16, 16-token pages.  Q and O bf16 and
+    # LSE f32 for the 8 new tokens; context K and V once per kv head; the
+    # block-table entries used (2 + 1 pages); cu_seqlens (3) and seqlens (2).
+    got = roofline.paged_prefill_bytes([3, 5], [20, 5], 4, 2, 16, 16)
+    want = (8 * 4 * 16 * 2) * 2 + 8 * 4 * 4 + 25 * 2 * 16 * 2 * 2 + 3 * 4 + 5 * 4
+    assert got == want
