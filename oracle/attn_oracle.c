@@ -44,7 +44,9 @@
  * mistake (a dropped scale, a wrong mask offset, a wrong head, a transposed
  * operand, a dropped normaliser; in the backward a dropped D term or a
  * dropped dK scale; in the chunked prefill a causal bound off by one or a
- * wrong kv head; in the additive bias an ALiBi distance of the wrong sign).
+ * wrong kv head; in the additive bias an ALiBi distance of the wrong sign;
+ * in the paged decode a page read as [Hkv][page_size][d] instead of
+ * [page_size][Hkv][d]).
  * The shipped oracle is built with 0.
  */
 #include <math.h>
@@ -357,7 +359,11 @@ int oracle_decode_paged(const uint16_t* q, const uint16_t* kcache, const uint16_
             for (t = 0; t < n; ++t) {
                 int32_t page = block_table[(int64_t)seq * max_pages_per_seq + t / page_size];
                 if (page < 0 || page >= num_pages) { ok = 0; break; }
+#if ORACLE_MUTANT == 11
+                int64_t off = (((int64_t)page * Hkv + g) * page_size + t % page_size) * d;
+#else
                 int64_t off = (((int64_t)page * page_size + t % page_size) * Hkv + g) * d;
+#endif
                 krows[t] = kcache + off;
                 vrows[t] = vcache + off;
             }

@@ -242,6 +242,24 @@ def test_paged_decode_zero_length_sequence():
     np.testing.assert_array_equal(O[2], V[page, 0])
 
 
+def test_planted_decode_layout_mistake_is_caught():
+    # A page read with its slot and head axes swapped (mutant 11) must fail the
+    # gathered-rows pin (or read a NaN slot).
+    d = inputs.decode_inputs(5, 8, 2, 16, 1, 70, num_pages=40, page_size=16, seed=16,
+                             max_pages_per_seq=5)
+    O, L, _ = oracle.decode_paged(d.q, d.kcache, d.vcache, d.block_table, d.seqlens, d.scale, mutant=11)
+    agree = True
+    for s in range(5):
+        n = int(d.seqlens[s])
+        pages = d.block_table[s, : (n + 15) // 16].long()
+        k = d.kcache[pages].reshape(-1, 2, 16)[:n].permute(1, 0, 2).unsqueeze(0)
+        v = d.vcache[pages].reshape(-1, 2, 16)[:n].permute(1, 0, 2).unsqueeze(0)
+        q = d.q[s].reshape(1, 8, 1, 16)
+        Oc, Lc, _ = oracle.attention(q, k.contiguous(), v.contiguous(), False, d.scale)
+        agree = agree and np.allclose(O[s], Oc[0, :, 0], atol=1e-9) and np.allclose(L[s], Lc[0, :, 0], atol=1e-9)
+    assert not agree
+
+
 # ------------------------------------------------------------------ mutants
 def _mutant_fails(mutant: int) -> bool:
     for case in BRUTE_CASES:
