@@ -44,7 +44,8 @@
  * mistake (a dropped scale, a wrong mask offset, a wrong head, a transposed
  * operand, a dropped normaliser; in the backward a dropped D term or a
  * dropped dK scale; in the chunked prefill a causal bound off by one or a
- * wrong kv head; in the additive bias an ALiBi distance of the wrong sign;
+ * wrong kv head; in the additive bias an ALiBi distance of the wrong sign
+ * or a left window one key too wide;
  * in the paged decode a page read as [Hkv][page_size][d] instead of
  * [page_size][Hkv][d]).
  * The shipped oracle is built with 0.
@@ -211,7 +212,11 @@ int oracle_attention_masked(const uint16_t* q, const uint16_t* k, const uint16_t
             int64_t n = 0, j;
             for (j = 0; j < Nk; ++j) {
                 if (causal && j > i + diag) continue;
+#if ORACLE_MUTANT == 12
+                if (window_left > 0 && j < i + diag - window_left) continue;  /* one key too many */
+#else
                 if (window_left > 0 && j <= i + diag - window_left) continue;
+#endif
                 double c = 0.0;
 #if ORACLE_MUTANT == 9
                 if (alibi) c += (double)alibi[h] * (double)(i - j + diag);  /* distance of the wrong sign */

@@ -157,3 +157,13 @@ def test_planted_alibi_sign_mistake_is_caught():
     C = c_matrix(B, Hq, Nq, Nk, causal, window, slopes, None)
     Ob, Lb = decimal_with_bias(bf16_np(x.q), bf16_np(x.k), bf16_np(x.v), x.scale, C)
     assert not (close(O, Ob, 1e-6) and close(L, Lb, 1e-6))
+
+
+def test_planted_window_bound_mistake_is_caught():
+    # A left window one key too wide (mutant 12) must fail the decimal pin.
+    B, Hq, Hkv, Nq, Nk, d, causal, window = 1, 2, 1, 9, 13, 4, True, 4
+    x = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, seed=721, causal=causal)
+    O, L, _ = oracle.attention_masked(x.q, x.k, x.v, causal, x.scale, window_left=window, mutant=12)
+    C = c_matrix(B, Hq, Nq, Nk, causal, window, None, None)
+    Ob, Lb = decimal_with_bias(bf16_np(x.q), bf16_np(x.k), bf16_np(x.v), x.scale, C)
+    assert not (close(O, Ob, 1e-6) and close(L, Lb, 1e-6))
