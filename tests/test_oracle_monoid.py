@@ -135,3 +135,20 @@ def test_split_decode_partials_reproduce_decode_oracle():
             Om, Lm = monoid.finalize(st)
             assert np.abs(Om - O[s, h]).max() <= 1e-12
             assert abs(Lm - L[s, h]) <= 1e-12
+
+
+def test_planted_missing_rescale_is_caught(monkeypatch):
+    # Drop the correction alpha_t = exp(m_{t-1} - m_t) (every nonempty part
+    # weighted 1): the recurrence over a partition with a rising max must
+    # then miss the definition, which is what the partition pin checks.
+    x, s, v, row = scores_and_values(305, k_scale=4.0)
+    O, L, _ = oracle.attention(x.q, x.k, x.v, False, x.scale)
+    O = O.reshape(-1, O.shape[-1])[0]
+    L = float(np.asarray(L).reshape(-1)[0])
+    order = np.argsort(s)  # ascending scores: the running max rises at every block
+    part = [order[i:i + 8] for i in range(0, len(s), 8)]
+    Oo, Lo = monoid.finalize(monoid.recurrence(s, v, part))
+    assert np.abs(Oo - O).max() <= 1e-12 and abs(Lo - L) <= 1e-12  # the unplanted recurrence agrees
+    monkeypatch.setattr(monoid, "_weight", lambda m_part, m: 0.0 if m_part == -math.inf else 1.0)
+    Oo, Lo = monoid.finalize(monoid.recurrence(s, v, part))
+    assert np.abs(Oo - O).max() > 1e-6 or abs(Lo - L) > 1e-6
