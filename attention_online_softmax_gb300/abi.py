@@ -67,6 +67,10 @@ _lib.attn_launch_count.argtypes = []
 _lib.attn_launch_count.restype = ctypes.c_uint64
 _lib.attn_abi_version.argtypes = []
 _lib.attn_abi_version.restype = _i
+_lib.attn_fwd_kernel_name.argtypes = [_i, _i, _i, _i]
+_lib.attn_fwd_kernel_name.restype = ctypes.c_char_p
+_lib.attn_decode_kernel_name.argtypes = [_i, _i, _i, _i, _i]
+_lib.attn_decode_kernel_name.restype = ctypes.c_char_p
 
 ATTN_OK = 0
 ATTN_BF16 = 0
@@ -77,7 +81,7 @@ EXPORTS = ("attn_fwd", "attn_fwd_masked", "attn_prefill_paged_workspace_size", "
            "attn_bwd_workspace_size", "attn_bwd", "attn_probe_dram_latency",
            "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_static",
            "attn_get_device_status", "attn_selftest_wait_timeout", "attn_status_string",
-           "attn_launch_count", "attn_abi_version")
+           "attn_launch_count", "attn_abi_version", "attn_fwd_kernel_name", "attn_decode_kernel_name")
 
 #: size of the scratch array built into the library for attn_decode_paged_static
 STATIC_SCRATCH_BYTES = 64 << 20
@@ -103,6 +107,16 @@ def attn_launch_count() -> int:
 
 def attn_abi_version() -> int:
     return int(_lib.attn_abi_version())
+
+
+def attn_fwd_kernel_name(B: int, Hq: int, Nq: int, d: int) -> str:
+    """The kernel instantiation attn_fwd launches for these sizes ("" if rejected)."""
+    return _lib.attn_fwd_kernel_name(int(B), int(Hq), int(Nq), int(d)).decode()
+
+
+def attn_decode_kernel_name(num_seqs: int, Hq: int, Hkv: int, d: int, max_seqlen: int) -> str:
+    """The kernel instantiation attn_decode_paged launches for these sizes ("" if rejected)."""
+    return _lib.attn_decode_kernel_name(int(num_seqs), int(Hq), int(Hkv), int(d), int(max_seqlen)).decode()
 
 
 def _stream_ptr(stream) -> int | None:

@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -43,37 +44,118 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// The current device must be a GB300-class part (compute capability 10.3).
-attn_status check_device() {
+// Per-device facts looked up once (the calls that query them cost host time
+// on every launch otherwise): whether the device is usable here, and its SM count.
+std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, else 1 + attn_status of the check
+std::atomic<int> g_dev_sms[kMaxDevices];    // 0 unknown
+
+int current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
-    return ATTN_ERR_NO_DEVICE;
+    return -1;
   }
+  return dev;
+}
+
+// The current device must be a GB300-class part (compute capability 10.3).
+attn_status check_device() {
+  const int dev = current_device();
+  if (dev < 0) return ATTN_ERR_NO_DEVICE;
+  if (dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  const int known = g_dev_state[dev].load(std::memory_order_relaxed);
+  if (known != 0) return static_cast<attn_status>(known - 1);
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_NO_DEVICE;
   }
-  if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
-  return ATTN_OK;
+  const attn_status st = (major != 10 || minor != 3) ? ATTN_ERR_UNSUPPORTED : ATTN_OK;
+  g_dev_state[dev].store(1 + static_cast<int>(st), std::memory_order_relaxed);
+  return st;
+}
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device, calling the runtime only when the limit must grow.  One
+// cache per kernel (the function-local static of each Kern: the template is
+// keyed by the kernel's address, not its type, which instantiations share).
+template <auto Kern>
+bool ensure_smem(int bytes) {
+  static std::atomic<int> set_to[kMaxDevices];
+  const auto kern = Kern;
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return false;
+  if (set_to[dev].load(std::memory_order_relaxed) >= bytes) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  int cur = set_to[dev].load(std::memory_order_relaxed);
+  while (cur < bytes && !set_to[dev].compare_exchange_weak(cur, bytes, std::memory_order_relaxed)) {
+  }
+  return true;
+}
+
+// Tensor maps encoded for earlier calls, keyed by every argument of the
+// encoding (a map depends only on them: the base address, sizes, strides, box
+// and swizzle), so a repeated call on the same buffers skips the encoder.
+struct MapKey {
+  uint64_t v[18];
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool valid;
+};
+constexpr int kMapCache = 64;
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const cuuint64_t* dims,
+                  const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.v[0] = static_cast<uint64_t>(dtype) | (static_cast<uint64_t>(rank) << 8) |
+             (static_cast<uint64_t>(swz) << 16);
+  key.v[1] = reinterpret_cast<uintptr_t>(base);
+  for (int i = 0; i < rank; ++i) {
+    key.v[2 + i] = dims[i];
+    key.v[7 + i] = box[i];
+    if (i + 1 < rank) key.v[12 + i] = strides[i];
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < kMapCache; ++i)
+      if (g_maps[i].valid && std::memcmp(&g_maps[i].key, &key, sizeof(key)) == 0) {
+        *map = g_maps[i].map;
+        return true;
+      }
+  }
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, dtype, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  MapEntry& e = g_maps[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapCache;
+  e.key = key;
+  e.map = *map;
+  e.valid = true;
+  return true;
 }
 
 // 3-D bf16 map over [heads][rows][d] with a (64 x box_rows x 1) box and the
 // 128-byte swizzle that the tcgen05 operand descriptors expect.
 bool encode_rows_map(CUtensorMap* map, const void* base, int d, int rows, int heads, int box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(heads)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 4-D bf16 map over a dense bias [Bb][Hb][Nq][Nk] (Bb, Hb = 1 when broadcast);
@@ -82,8 +164,7 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int d, int rows, int he
 // aligned base and row / head / batch strides).
 bool encode_bias_map(CUtensorMap* map, const void* base, int Nq, int Nk, int Hb, int Bb, long long sh,
                      long long sb) {
-  auto fn = encode_fn();
-  if (!fn || !aligned16(base) || Nk % 8 != 0) return false;
+  if (!aligned16(base) || Nk % 8 != 0) return false;
   const long long plane = static_cast<long long>(Nq) * Nk;
   const long long s2 = Hb > 1 ? sh : plane;
   const long long s3 = Bb > 1 ? sb : s2 * Hb;
@@ -93,27 +174,17 @@ bool encode_bias_map(CUtensorMap* map, const void* base, int Nq, int Nk, int Hb,
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(Nk) * 2, static_cast<cuuint64_t>(s2) * 2,
                            static_cast<cuuint64_t>(s3) * 2};
   cuuint32_t box[4] = {64, static_cast<cuuint32_t>(attn::kBM), 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 3-D bf16 map over packed queries [total_q][Hq][d]; one box is 128 tokens of
 // one head x 64 columns, 128-byte swizzled (the same shared-memory image as a
 // [128 rows][64 columns] box of the [B*Hq][Nq][d] layout).
 bool encode_packed_q_map(CUtensorMap* map, const void* base, int d, int Hq, int total_q) {
-  auto fn = encode_fn();
-  if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(total_q)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(Hq) * d * 2};
   cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(attn::kBM)};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 4-D bf16 map over the paged cache [pages][slots][Hkv][d] for the prefill
@@ -121,36 +192,24 @@ bool encode_packed_q_map(CUtensorMap* map, const void* base, int d, int Hq, int 
 // columns, 128-byte swizzled, so a page lands as page_size consecutive
 // 128-byte rows of a K/V tile (at a multiple of 2 KB: whole swizzle atoms).
 bool encode_paged_rows_map(CUtensorMap* map, const void* base, int d, int Hkv, int page_size, int num_pages) {
-  auto fn = encode_fn();
-  if (!fn) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hkv),
                         static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(num_pages)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(Hkv) * d * 2,
                            static_cast<cuuint64_t>(page_size) * Hkv * d * 2};
   cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(page_size), 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 4-D bf16 map over the paged cache [pages][slots][Hkv][d]; one box is the
-// [16 slots][hg heads][d] block of one page (no swizzle).
+// [16 slots][hg heads][d] block of one page at a slot offset (no swizzle).
 bool encode_page_map(CUtensorMap* map, const void* base, int d, int Hkv, int page_size, int num_pages, int hg) {
-  auto fn = encode_fn();
-  if (!fn) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hkv),
                         static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(num_pages)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(Hkv) * d * 2,
                            static_cast<cuuint64_t>(page_size) * Hkv * d * 2};
   cuuint32_t box[4] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(hg),
-                       static_cast<cuuint32_t>(page_size), 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+                       static_cast<cuuint32_t>(attn::kBox), 1};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // One thread waits on a barrier with two expected arrivals after only one
@@ -166,34 +225,36 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns) {
 }
 
 int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
-                                               cudaSuccess) {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  int n = g_dev_sms[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     return 148;
   }
+  g_dev_sms[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
-// Work counters of the persistent prefill kernel: a ring of per-launch
-// [next unit, finished CTAs] pairs, zero at load time and reset to zero by the
-// last CTA of the launch that used them.  Consecutive launches take
-// consecutive slots, so launches in flight at the same time (up to the ring
-// size, on any streams) never share a counter.
+// Work counters of the persistent prefill kernels: a ring of 64-bit words,
+// (owner tag << 32) | fetches, free (0) at load time.  Each launch gets the
+// next slot and a nonzero tag of its own; its first fetch claims the word and
+// its last fetch frees it (attn::sched_fetch).  Launches on different slots
+// never interact; a launch whose slot is still held by an earlier one (64
+// launches before it, or one replayed from a graph) waits until that launch
+// has handed out its last unit, bounded (ATTN_ERR_TIMEOUT).
 constexpr int kSchedSlots = 64;
-__device__ int g_prefill_sched[kSchedSlots][2];
+__device__ unsigned long long g_prefill_sched[kSchedSlots];
 std::atomic<uint32_t> g_sched_seq{0};
 std::mutex g_sched_mu;
-int* g_sched_base[kMaxDevices] = {};
+unsigned long long* g_sched_base[kMaxDevices] = {};
 
-attn_status sched_slot(int** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_NO_DEVICE;
-  }
-  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
-  int* base = nullptr;
+attn_status sched_slot(unsigned long long** out, unsigned* tag) {
+  const int dev = current_device();
+  if (dev < 0) return ATTN_ERR_NO_DEVICE;
+  if (dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  unsigned long long* base = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_sched_mu);
     if (g_sched_base[dev] == nullptr) {
@@ -202,11 +263,13 @@ attn_status sched_slot(int** out) {
         cudaGetLastError();
         return ATTN_ERR_LAUNCH;
       }
-      g_sched_base[dev] = static_cast<int*>(ptr);
+      g_sched_base[dev] = static_cast<unsigned long long*>(ptr);
     }
     base = g_sched_base[dev];
   }
-  *out = base + 2 * (g_sched_seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+  const uint32_t seq = g_sched_seq.fetch_add(1, std::memory_order_relaxed);
+  *out = base + seq % kSchedSlots;
+  *tag = seq % 0xFFFFFFFFu + 1u;  // never 0 (the free word)
   return ATTN_OK;
 }
 
@@ -224,21 +287,36 @@ int sched_group(int BH, int want) {
   return (BH + groups - 1) / groups;
 }
 
+// K/V ring depth of each prefill instantiation, by head dim, query tiles per
+// unit and variant (plain, additive bias read directly, staged dense bias,
+// paged).  The launches below and attn_fwd_kernel_name() both read it.
+constexpr int fwd_stages(int d, int nq, int bias, bool paged) {
+  return paged ? (d == 64 ? (nq == 2 ? 10 : 12) : d == 128 ? (nq == 2 ? 5 : 6) : 5)
+         : bias == 2 ? (d == 64 ? 8 : d == 128 ? 4 : 3)
+         : bias == 1 ? (d == 64 ? 12 : d == 128 ? 6 : 5)
+                     : (d == 64 ? (nq == 2 ? 10 : 12) : d == 128 ? (nq == 2 ? 4 : 6) : 5);
+}
+
+// Two query tiles per unit (they share every K/V tile and overlap each
+// other's softmax with MMAs) for d <= 128 unless that leaves fewer than two
+// units per SM.
+bool fwd_two_tiles(long long rows_per_head, long long heads, int d) {
+  if (d > 128) return false;
+  return ((rows_per_head + 2 * attn::kBM - 1) / (2 * attn::kBM)) * heads >= 2LL * sm_count();
+}
+
 template <int D, int NQ, int STAGES, int BIAS = 0>
 attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            const CUtensorMap& mb, attn::PrefillParams p, int BH, cudaStream_t stream) {
   using L = attn::PrefillLayout<D, NQ, STAGES, attn::bias_slots<BIAS>(), attn::psep_path<BIAS, false>()>;
   auto kern = attn::prefill_fwd_kernel<D, NQ, STAGES, BIAS>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_LAUNCH;
-  }
+  if (!ensure_smem<attn::prefill_fwd_kernel<D, NQ, STAGES, BIAS>>(L::kAlloc)) return ATTN_ERR_LAUNCH;
   p.n_units = (p.Nq + attn::kBM * NQ - 1) / (attn::kBM * NQ);
   const int sms = sm_count();
   p.group = sched_group(BH, (2 * sms + p.n_units - 1) / p.n_units);
   const long long units = static_cast<long long>(p.n_units) * BH;
   if (units > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
-  const attn_status st = sched_slot(&p.sched);
+  const attn_status st = sched_slot(&p.sched, &p.sched_tag);
   if (st != ATTN_OK) return st;
   // Persistent: one CTA per SM (or fewer when there are fewer units).
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
@@ -256,11 +334,8 @@ attn_status launch_prefill_paged(const CUtensorMap& mq, const CUtensorMap& mk, c
                                  attn::PrefillParams p, int total_q, cudaStream_t stream) {
   using L = attn::PrefillLayout<D, NQ, STAGES, 0, attn::psep_path<0, true>()>;
   auto kern = attn::prefill_fwd_kernel<D, NQ, STAGES, 0, true>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_LAUNCH;
-  }
-  const attn_status st = sched_slot(&p.sched);
+  if (!ensure_smem<attn::prefill_fwd_kernel<D, NQ, STAGES, 0, true>>(L::kAlloc)) return ATTN_ERR_LAUNCH;
+  const attn_status st = sched_slot(&p.sched, &p.sched_tag);
   if (st != ATTN_OK) return st;
   attn::paged_plan_kernel<<<1, 1024, 0, stream>>>(p.cu_q, p.seqlens_k, p.num_seqs, total_q, p.Hq, p.max_pages,
                                                    p.page_size, attn::kBM * NQ,
@@ -276,88 +351,138 @@ attn_status launch_prefill_paged(const CUtensorMap& mq, const CUtensorMap& mk, c
 
 // ---------------------------------------------------------------- decode plan
 struct DecodePlan {
-  int hg = 1;
+  int gw = 1;       // query heads per compute warp
+  int wph = 1;      // compute warps per key/value head
+  int hg = 1;       // key/value heads per work item
+  int ngroups = 1;  // Hkv / hg
   int chunk = attn::kChunkMax;
   int n_splits = 1;
   size_t ws_o_floats = 0;
+  size_t ws_cnt_off = 0;  // byte offset of the merge counters
   size_t ws_bytes = 0;
 };
 
 bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int max_seqlen, DecodePlan* out) {
   if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_seqlen < 0) return false;
   if (d != 64 && d != 128 && d != 256) return false;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return false;
   DecodePlan pl;
+  pl.gw = G < 8 ? G : 8;
+  pl.wph = G / pl.gw;
   for (int c : {8, 4, 2, 1}) {
-    if (Hkv % c == 0 && c * d <= 1024) {
+    if (Hkv % c == 0 && c * pl.wph <= 8 && c * d <= 1024) {
       pl.hg = c;
       break;
     }
   }
-  const long long groups = static_cast<long long>(num_seqs) * (Hkv / pl.hg);
+  pl.ngroups = Hkv / pl.hg;
+  const long long groups = static_cast<long long>(num_seqs) * pl.ngroups;
   pl.chunk = attn::kChunkMax;
   while (pl.chunk > 64 && groups * ((max_seqlen + pl.chunk - 1) / pl.chunk) < 1024) pl.chunk /= 2;
   pl.n_splits = max_seqlen > 0 ? (max_seqlen + pl.chunk - 1) / pl.chunk : 1;
+  if (pl.n_splits >= (1 << attn::kCntBits)) return false;
+  if (groups * pl.n_splits > 0x7FFFFFFFLL) return false;
   if (pl.n_splits > 1) {
     pl.ws_o_floats = static_cast<size_t>(num_seqs) * pl.n_splits * Hq * d;
     const size_t lse_floats = static_cast<size_t>(num_seqs) * pl.n_splits * Hq;
-    pl.ws_bytes = ((pl.ws_o_floats + lse_floats) * 4 + 255) & ~static_cast<size_t>(255);
+    pl.ws_cnt_off = ((pl.ws_o_floats + lse_floats) * 4 + 255) & ~static_cast<size_t>(255);
+    const size_t cnt_bytes = static_cast<size_t>(num_seqs) * pl.ngroups * pl.hg * pl.wph * 8;
+    pl.ws_bytes = (pl.ws_cnt_off + cnt_bytes + 255) & ~static_cast<size_t>(255);
   }
   *out = pl;
   return true;
 }
 
-template <int D, int G>
-attn_status launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, attn::DecodeParams p,
-                          cudaStream_t stream) {
-  const int scores_bytes = p.hg * p.chunk * G * 4;
-  const int fixed = scores_bytes + 2 * attn::kMaxStages * 8 + 1024;
-  auto ks = attn::decode_split_kernel<D, G>;
-  // Ring depth: two CTAs per SM when registers allow it (113 KB each), else
-  // one CTA per SM with a deeper ring, so that enough page bytes are in flight.
-  int stages = (113 * 1024 - fixed) / p.stage_bytes;
-  stages = stages < 2 ? 2 : (stages > 4 ? 4 : stages);
-  {
-    int per_sm = 0;
-    const int threads = (p.hg + 1) * 32;
-    if (cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) == cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ks, threads, stages * p.stage_bytes + fixed) ==
-            cudaSuccess &&
-        per_sm < 2) {
-      const int deep = (200 * 1024 - fixed) / p.stage_bytes;
-      stages = deep > attn::kMaxStages ? attn::kMaxStages : (deep < stages ? stages : deep);
-    }
+std::atomic<uint64_t> g_decode_epoch{0};
+
+// Decode grid: persistent (CTAs take items from a counter) or one CTA per item.
+constexpr bool kDecodePersistent = true;
+constexpr int kDecodeCtasPerSm = 0;  // 0: chosen by decode_shape
+
+// Blocks of `kern` that fit on one SM with `smem` bytes of dynamic shared
+// memory (0 when the query fails).
+template <auto Kern>
+int blocks_per_sm(int threads, int smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Kern, threads, smem) != cudaSuccess) {
     cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// Ring depth and CTAs per SM of the decode kernel: two CTAs per SM when the
+// registers allow it and two rings of at least two stages fit (113 KB of
+// shared memory each), else one CTA per SM with a deeper ring; either way
+// enough page bytes are in flight to keep HBM busy.
+template <auto Kern>
+bool decode_shape(int threads, int fixed, int stage_bytes, int* stages, int* per_sm) {
+  constexpr int kTwo = 113 * 1024, kOne = 220 * 1024;
+  // The answer for the last shape asked on each device (one cache per kernel).
+  struct Shape {
+    int threads, fixed, stage_bytes, stages, per_sm;
+  };
+  static std::mutex mu;
+  static Shape last[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const Shape& c = last[dev];
+    if (c.stages > 0 && c.threads == threads && c.fixed == fixed && c.stage_bytes == stage_bytes) {
+      *stages = c.stages;
+      *per_sm = c.per_sm;
+      return true;
+    }
+  }
+  if (!ensure_smem<Kern>(kOne)) return false;
+  int st2 = (kTwo - fixed) / stage_bytes;
+  if (st2 > attn::kMaxStages) st2 = attn::kMaxStages;
+  if (st2 >= 2 && blocks_per_sm<Kern>(threads, st2 * stage_bytes + fixed) >= 2) {
+    *stages = st2;
+    *per_sm = 2;
+  } else {
+    int st1 = (kOne - fixed) / stage_bytes;
+    if (st1 > attn::kMaxStages) st1 = attn::kMaxStages;
+    if (st1 < 2) return false;
+    *stages = st1;
+    *per_sm = 1;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  last[dev] = Shape{threads, fixed, stage_bytes, *stages, *per_sm};
+  return true;
+}
+
+template <int D, int GW, int WPH>
+attn_status launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, attn::DecodeParams p, cudaStream_t stream) {
+  constexpr auto kern = attn::decode_kernel<D, GW, WPH>;
+  const int nw = p.hg * WPH;
+  const int threads = (nw + 1) * 32;
+  const int fixed = attn::decode_fixed_bytes(nw, p.chunk, GW);
+  int stages = 0, per_sm = 0;
+  if (!decode_shape<kern>(threads, fixed, p.stage_bytes, &stages, &per_sm)) return ATTN_ERR_LAUNCH;
+  if (kDecodeCtasPerSm == 1 && per_sm == 2) {
+    per_sm = 1;
+    stages = (220 * 1024 - fixed) / p.stage_bytes;
+    if (stages > attn::kMaxStages) stages = attn::kMaxStages;
   }
   p.stages = stages;
   const int smem = stages * p.stage_bytes + fixed;
-  if (cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_LAUNCH;
+  const long long units = static_cast<long long>(p.num_seqs) * p.n_splits * p.ngroups;
+  const long long slots = kDecodePersistent ? static_cast<long long>(per_sm) * sm_count() : units;
+  const unsigned grid = static_cast<unsigned>(units < slots ? units : slots);
+  if (grid == 0) return ATTN_OK;
+  p.sched = nullptr;
+  if (kDecodePersistent) {
+    const attn_status st = sched_slot(&p.sched, &p.sched_tag);
+    if (st != ATTN_OK) return st;
   }
-  const long long gx = static_cast<long long>(p.num_seqs) * p.n_splits;
-  if (gx > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
-  ks<<<dim3(static_cast<unsigned>(gx), p.Hkv / p.hg), (p.hg + 1) * 32, smem, stream>>>(mk, mv, p);
+  // Epochs run over [1, 2^40 - 2]: never 0 (a reset word) nor all ones.
+  p.epoch = g_decode_epoch.fetch_add(1, std::memory_order_relaxed) % ((1ull << 40) - 2) + 1;
+  kern<<<dim3(grid), threads, smem, stream>>>(mk, mv, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  if (p.n_splits > 1) {
-    // Programmatic dependent launch: the combine grid is scheduled while the
-    // split grid drains and waits (griddepcontrol.wait) for its partials.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.num_seqs, (p.Hq + 3) / 4);
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, attn::decode_combine_kernel<D>, p) != cudaSuccess) {
-      cudaGetLastError();
-      return ATTN_ERR_LAUNCH;
-    }
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-  }
   return ATTN_OK;
 }
 
@@ -365,10 +490,11 @@ template <int D>
 attn_status launch_decode_g(int G, const CUtensorMap& mk, const CUtensorMap& mv, const attn::DecodeParams& p,
                             cudaStream_t s) {
   switch (G) {
-    case 1: return launch_decode<D, 1>(mk, mv, p, s);
-    case 2: return launch_decode<D, 2>(mk, mv, p, s);
-    case 4: return launch_decode<D, 4>(mk, mv, p, s);
-    case 8: return launch_decode<D, 8>(mk, mv, p, s);
+    case 1: return launch_decode<D, 1, 1>(mk, mv, p, s);
+    case 2: return launch_decode<D, 2, 1>(mk, mv, p, s);
+    case 4: return launch_decode<D, 4, 1>(mk, mv, p, s);
+    case 8: return launch_decode<D, 8, 1>(mk, mv, p, s);
+    case 16: return launch_decode<D, 8, 2>(mk, mv, p, s);
     default: return ATTN_ERR_UNSUPPORTED;
   }
 }
@@ -477,6 +603,7 @@ attn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o
   p.n_units = 0;
   p.group = 1;
   p.sched = nullptr;
+  p.sched_tag = 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.window = mask ? mask->window_left : 0;
   p.alibi = mask ? mask->alibi_slopes : nullptr;
@@ -486,10 +613,7 @@ attn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o
   p.bias_hmul = 0;
   p.bias_bmul = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // Two query tiles per CTA (they share every K/V tile and overlap each
-  // other's softmax with MMAs) unless that leaves the GPU under-filled.
-  const long long pairs = static_cast<long long>((Nq + 2 * attn::kBM - 1) / (2 * attn::kBM)) * B * Hq;
-  const bool two = pairs >= 2LL * sm_count();
+  const bool two = fwd_two_tiles(Nq, static_cast<long long>(B) * Hq, d);
   if (p.bias != nullptr && Nk > 0) {
     // A dense bias whose layout TMA can tile is staged into shared memory by
     // the producer (coalesced, asynchronous); any other layout is read by the
@@ -501,9 +625,9 @@ attn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o
       p.bias_hmul = Hb > 1 ? 1 : 0;
       p.bias_bmul = Bb > 1 ? 1 : 0;
       switch (d) {
-        case 64: return launch_prefill<64, 1, 8, 2>(mq, mk, mv, mb, p, B * Hq, s);
-        case 128: return launch_prefill<128, 1, 4, 2>(mq, mk, mv, mb, p, B * Hq, s);
-        case 256: return launch_prefill<256, 1, 3, 2>(mq, mk, mv, mb, p, B * Hq, s);
+        case 64: return launch_prefill<64, 1, fwd_stages(64, 1, 2, false), 2>(mq, mk, mv, mb, p, B * Hq, s);
+        case 128: return launch_prefill<128, 1, fwd_stages(128, 1, 2, false), 2>(mq, mk, mv, mb, p, B * Hq, s);
+        case 256: return launch_prefill<256, 1, fwd_stages(256, 1, 2, false), 2>(mq, mk, mv, mb, p, B * Hq, s);
         default: return ATTN_ERR_UNSUPPORTED;
       }
     }
@@ -512,22 +636,30 @@ attn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o
     // Additive-bias variants: one query tile per unit (the per-score bias
     // terms need the registers a second tile's pipeline would take).
     switch (d) {
-      case 64: return launch_prefill<64, 1, 12, 1>(mq, mk, mv, mq, p, B * Hq, s);
-      case 128: return launch_prefill<128, 1, 6, 1>(mq, mk, mv, mq, p, B * Hq, s);
-      case 256: return launch_prefill<256, 1, 5, 1>(mq, mk, mv, mq, p, B * Hq, s);
+      case 64: return launch_prefill<64, 1, fwd_stages(64, 1, 1, false), 1>(mq, mk, mv, mq, p, B * Hq, s);
+      case 128: return launch_prefill<128, 1, fwd_stages(128, 1, 1, false), 1>(mq, mk, mv, mq, p, B * Hq, s);
+      case 256: return launch_prefill<256, 1, fwd_stages(256, 1, 1, false), 1>(mq, mk, mv, mq, p, B * Hq, s);
       default: return ATTN_ERR_UNSUPPORTED;
     }
   }
   switch (d) {
     case 64:
-      return two ? launch_prefill<64, 2, 10>(mq, mk, mv, mq, p, B * Hq, s)
-                 : launch_prefill<64, 1, 12>(mq, mk, mv, mq, p, B * Hq, s);
+      return two ? launch_prefill<64, 2, fwd_stages(64, 2, 0, false)>(mq, mk, mv, mq, p, B * Hq, s)
+                 : launch_prefill<64, 1, fwd_stages(64, 1, 0, false)>(mq, mk, mv, mq, p, B * Hq, s);
     case 128:
-      return two ? launch_prefill<128, 2, 4>(mq, mk, mv, mq, p, B * Hq, s)
-                 : launch_prefill<128, 1, 6>(mq, mk, mv, mq, p, B * Hq, s);
-    case 256: return launch_prefill<256, 1, 5>(mq, mk, mv, mq, p, B * Hq, s);
+      return two ? launch_prefill<128, 2, fwd_stages(128, 2, 0, false)>(mq, mk, mv, mq, p, B * Hq, s)
+                 : launch_prefill<128, 1, fwd_stages(128, 1, 0, false)>(mq, mk, mv, mq, p, B * Hq, s);
+    case 256: return launch_prefill<256, 1, fwd_stages(256, 1, 0, false)>(mq, mk, mv, mq, p, B * Hq, s);
   }
   return ATTN_ERR_UNSUPPORTED;
+}
+
+const char* attn_fwd_kernel_name(int B, int Hq, int Nq, int d) {
+  static thread_local char buf[96];
+  if (B <= 0 || Hq <= 0 || Nq <= 0 || (d != 64 && d != 128 && d != 256)) return "";
+  const int nq = fwd_two_tiles(Nq, static_cast<long long>(B) * Hq, d) ? 2 : 1;
+  std::snprintf(buf, sizeof(buf), "prefill_fwd_kernel<%d,%d,%d,0,0>", d, nq, fwd_stages(d, nq, 0, false));
+  return buf;
 }
 
 size_t attn_prefill_paged_workspace_size(int num_seqs) {
@@ -591,12 +723,12 @@ attn_status attn_prefill_paged(const void* q, const void* kcache, const void* vc
   const bool two = (static_cast<long long>(total_q) / (2 * attn::kBM)) * Hq >= 2LL * sm_count();
   switch (d) {
     case 64:
-      return two ? launch_prefill_paged<64, 2, 10>(mq, mk, mv, p, total_q, s)
-                 : launch_prefill_paged<64, 1, 12>(mq, mk, mv, p, total_q, s);
+      return two ? launch_prefill_paged<64, 2, fwd_stages(64, 2, 0, true)>(mq, mk, mv, p, total_q, s)
+                 : launch_prefill_paged<64, 1, fwd_stages(64, 1, 0, true)>(mq, mk, mv, p, total_q, s);
     case 128:
-      return two ? launch_prefill_paged<128, 2, 5>(mq, mk, mv, p, total_q, s)
-                 : launch_prefill_paged<128, 1, 6>(mq, mk, mv, p, total_q, s);
-    case 256: return launch_prefill_paged<256, 1, 5>(mq, mk, mv, p, total_q, s);
+      return two ? launch_prefill_paged<128, 2, fwd_stages(128, 2, 0, true)>(mq, mk, mv, p, total_q, s)
+                 : launch_prefill_paged<128, 1, fwd_stages(128, 1, 0, true)>(mq, mk, mv, p, total_q, s);
+    case 256: return launch_prefill_paged<256, 1, fwd_stages(256, 1, 0, true)>(mq, mk, mv, p, total_q, s);
   }
   return ATTN_ERR_UNSUPPORTED;
 }
@@ -616,9 +748,9 @@ attn_status attn_decode_paged(const void* q, const void* kcache, const void* vca
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (o_dtype != ATTN_BF16 && o_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
-  if (page_size != attn::kPage) return ATTN_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return ATTN_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return ATTN_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(max_seqlen) > static_cast<long long>(max_pages_per_seq) * page_size)
     return ATTN_ERR_INVALID_ARG;
   if (num_seqs == 0) return ATTN_OK;
@@ -626,7 +758,7 @@ attn_status attn_decode_paged(const void* q, const void* kcache, const void* vca
       !aligned16(seqlens) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_MISALIGNED;
   DecodePlan pl;
-  if (!decode_plan(num_seqs, Hq, Hkv, d, max_seqlen, &pl)) return ATTN_ERR_INVALID_ARG;
+  if (!decode_plan(num_seqs, Hq, Hkv, d, max_seqlen, &pl)) return ATTN_ERR_UNSUPPORTED;
   if (pl.ws_bytes > 0 && (!aligned16(workspace) || workspace_bytes < pl.ws_bytes)) return ATTN_ERR_WORKSPACE;
   attn_status st = check_device();
   if (st != ATTN_OK) return st;
@@ -637,24 +769,29 @@ attn_status attn_decode_paged(const void* q, const void* kcache, const void* vca
     return ATTN_ERR_LAUNCH;
 
   attn::DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
   p.q = static_cast<const uint16_t*>(q);
   p.block_table = block_table;
   p.seqlens = seqlens;
   p.o = o;
   p.lse = lse;
-  p.ws_o = static_cast<float*>(workspace);
-  p.ws_lse = pl.ws_bytes > 0 ? static_cast<float*>(workspace) + pl.ws_o_floats : nullptr;
+  if (pl.ws_bytes > 0) {
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_lse = static_cast<float*>(workspace) + pl.ws_o_floats;
+    p.ws_cnt = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + pl.ws_cnt_off);
+  }
   p.num_seqs = num_seqs;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.num_pages = num_pages;
   p.max_pages = max_pages_per_seq;
   p.max_seqlen = max_seqlen;
+  p.page_size = page_size;
   p.chunk = pl.chunk;
   p.n_splits = pl.n_splits;
   p.hg = pl.hg;
-  p.stages = 2;
-  p.stage_bytes = page_size * pl.hg * d * 2;
+  p.ngroups = pl.ngroups;
+  p.stage_bytes = attn::kBox * pl.hg * d * 2;
   p.o_f32 = o_dtype == ATTN_F32 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -664,6 +801,14 @@ attn_status attn_decode_paged(const void* q, const void* kcache, const void* vca
     case 256: return launch_decode_g<256>(G, mk, mv, p, s);
   }
   return ATTN_ERR_UNSUPPORTED;
+}
+
+const char* attn_decode_kernel_name(int num_seqs, int Hq, int Hkv, int d, int max_seqlen) {
+  static thread_local char buf[96];
+  DecodePlan pl;
+  if (num_seqs <= 0 || !decode_plan(num_seqs, Hq, Hkv, d, max_seqlen, &pl)) return "";
+  std::snprintf(buf, sizeof(buf), "decode_kernel<%d,%d,%d>", d, pl.gw, pl.wph);
+  return buf;
 }
 
 attn_status attn_decode_paged_static(const void* q, const void* kcache, const void* vcache,
@@ -722,10 +867,11 @@ attn_status attn_get_device_status(attn_stream_t stream) {
 
 extern "C" attn_status attn_probe_dram_latency(const uint32_t* chain, size_t chain_len, int hops,
                                                unsigned long long* out_ns, attn_stream_t stream) {
-  if (chain == nullptr || out_ns == nullptr || hops <= 0 || chain_len == 0) return ATTN_ERR_INVALID_ARG;
+  if (chain == nullptr || out_ns == nullptr || hops <= 0 || chain_len == 0 || chain_len > 0xFFFFFFFFull)
+    return ATTN_ERR_INVALID_ARG;
   attn_status st = check_device();
   if (st != ATTN_OK) return st;
-  attn::dram_latency_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(chain, hops, out_ns);
+  attn::dram_latency_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(chain, chain_len, hops, out_ns);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return ATTN_OK;

@@ -16,8 +16,11 @@
 //                                     f32 dQ accumulator by TMA reduce-adds
 // The 1/sqrt(d)-style scale is applied to dK at the end and to dQ as it is
 // accumulated.  Roles: warp 0 TMA producer, warp 1 MMA issuer (one thread),
-// warps 2..5 one thread per key row (weights, dS) and then one thread per
-// query row (the dQ tile's accumulation), with bounded waits everywhere.
+// warps 2..9 two per TMEM lane quarter: each thread takes one key row and half
+// of the item's 128 query columns (weights, dS), then one query row and half
+// of the head dim (the dQ tile's accumulation), with bounded waits everywhere.
+// Each half writes its P^T and dS^T (bf16) over its own half of the dP^T
+// columns, so the two threads of a key row never touch each other's columns.
 #pragma once
 
 #include "ptx.cuh"
@@ -39,7 +42,7 @@ struct BwdParams {
 
 template <int D, int STAGES>
 struct BwdLayout {
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 320;
   static constexpr int kTile = 128 * D * 2;           // one [128][D] bf16 tile, 64-column swizzled boxes
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTile;
@@ -47,7 +50,8 @@ struct BwdLayout {
   static constexpr int kStage = 2 * kTile;
   static constexpr int kDSOff = kQOff + STAGES * kStage;   // dS^T [128 keys][128 queries] bf16
   static constexpr int kDSBytes = 128 * 128 * 2;
-  static constexpr int kRowOff = kDSOff + kDSBytes;   // 2 x (LSE[128], D[128]) f32, one per item parity
+  // 2 x (-LSE log2 e [128], D[128]) f32, one per item parity
+  static constexpr int kRowOff = kDSOff + kDSBytes;
   static constexpr int kRowBytes = 2 * 128 * 4;
   static constexpr int kBarOff = kRowOff + 2 * kRowBytes;
   // kv_full, q_full[S], q_empty[S], s_full, dp_full, ds_full, dq_full, dq_free, dkv_done, rows_ready[2],
@@ -57,9 +61,9 @@ struct BwdLayout {
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 128;         // the base is checked for 1024-byte alignment
   // Tensor memory columns: dK, dV accumulators, the S^T slot, the dP^T slot
-  // (later dS^T in its first 64 columns and P^T in its last 64), and the dQ
-  // tile (its own columns when they fit, else the S^T slot, free once S^T has
-  // been read).
+  // (later, for query half h of the item, dS^T in columns [64h, 64h + 32)
+  // and P^T in [64h + 32, 64h + 64)), and the dQ tile (its own columns when
+  // they fit, else the S^T slot, free once S^T has been read).
   static constexpr int kColDK = 0;
   static constexpr int kColDV = D;
   static constexpr int kColS = 2 * D;
@@ -128,7 +132,7 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
@@ -156,7 +160,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* dq_free = dq_full + 1;
   uint64_t* dkv_done = dq_free + 1;
   uint64_t* rows_ready = dkv_done + 1;  // [2]: the item's LSE / D values are in shared memory
-  // dQ tiles leave through two 16 KB staging buffers in the dS region:
+  // dQ tiles leave through two 16 KB staging buffers in the dS region, one
+  // per half of the weight warps:
   uint64_t* red_full = rows_ready + 2;  // [2] a [128 rows][32 columns] f32 chunk is staged
   uint64_t* red_free = red_full + 2;    // [2] the TMA reduce has finished reading it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -187,9 +192,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, 4);
+    mbar_init(ds_full, 8);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 4);
+    mbar_init(dq_free, 8);
     mbar_init(dkv_done, 1);
     mbar_init(&rows_ready[0], 128);
     mbar_init(&rows_ready[1], 128);
@@ -302,17 +307,20 @@ __global__ void __launch_bounds__(192, 1)
           umma_bf16_ss(tmem + L::kColDQ, dS_a + o, dK_b + o, kIdQ, kk > 0);
         }
         umma_commit(dq_full);
-        // dV += P^T dO, dK += dS^T Q (K = 128 query rows; A from TMEM).
+        // dV += P^T dO, dK += dS^T Q (K = 128 query rows; A from TMEM: the 16
+        // queries of step kk lie in query half kk / 4, at P^T or dS^T
+        // columns 64 (kk / 4) + 32 + 8 (kk % 4), resp. 64 (kk / 4) + 8 (kk % 4)).
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
-          umma_bf16_ts(tmem + L::kColDV, tmem + L::kColDP + 64 + kk * 8, dO_mn + o, kIdG,
-                       (n > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t pcol = (kk >> 2) * 64 + 32 + (kk & 3) * 8;
+          umma_bf16_ts(tmem + L::kColDV, tmem + L::kColDP + pcol, dO_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
-          umma_bf16_ts(tmem + L::kColDK, tmem + L::kColDP + kk * 8, dQ_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t dcol = (kk >> 2) * 64 + (kk & 3) * 8;
+          umma_bf16_ts(tmem + L::kColDK, tmem + L::kColDP + dcol, dQ_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&q_empty[st]);
       }
@@ -322,99 +330,111 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- key rows, then query rows
-    const int quarter = warp & 3;
+    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;         // query columns (weights) / head-dim columns (dQ) of this thread
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int kj = k0 + row;  // this thread's key
+    const int c0 = half * 64; // first query column of this thread's half
+    const bool issuer = lane == 0 && quarter == 2;  // the first warp of each half issues its dQ reduces
     bool ok = true;
-    // This thread's query row of an item: its LSE and D, read one item ahead.
-    auto row_vals = [&](int n, float& l, float& dd) {
-      l = 0.f;
+    // A query row's -LSE log2(e) (-inf for a row that saw no key: its weights
+    // are 0) and D, read one item ahead by the first half.
+    auto row_vals = [&](int n, float& nl2, float& dd) {
+      nl2 = -INFINITY;
       dd = 0.f;
       if (n < n_items) {
         const int qi = item_q0(n) + row;
         if (qi < p.Nq) {
           const size_t r = static_cast<size_t>(item_bh(n)) * p.Nq + qi;
-          l = __ldg(p.lse + r);
+          const float l = __ldg(p.lse + r);
+          nl2 = l == -INFINITY ? -INFINITY : -l * 1.4426950408889634f;
           dd = __ldg(p.dsum + r);
         }
       }
     };
-    float l_next, d_next;
-    row_vals(0, l_next, d_next);
+    float l_next = 0.f, d_next = 0.f;
+    if (half == 0) row_vals(0, l_next, d_next);
+    const float sl = p.scale_log2;
     for (int n = 0; ok && n < n_items; ++n) {
       const int bh = item_bh(n), q0 = item_q0(n);
-      // The item's 128 LSE and D values: one per thread into shared memory,
-      // then everyone reads all of them (a bounded barrier of the 128 threads).
-      float* lse = reinterpret_cast<float*>(smem + L::kRowOff + (n & 1) * L::kRowBytes);
-      float* dsum = lse + 128;
-      lse[row] = l_next;
-      dsum[row] = d_next;
-      mbar_arrive(&rows_ready[n & 1]);
-      row_vals(n + 1, l_next, d_next);
+      // The item's 128 row values: one per first-half thread into shared
+      // memory, then every weight thread reads the 64 of its half.
+      float* nls = reinterpret_cast<float*>(smem + L::kRowOff + (n & 1) * L::kRowBytes);
+      float* dsum = nls + 128;
+      if (half == 0) {
+        nls[row] = l_next;
+        dsum[row] = d_next;
+        mbar_arrive(&rows_ready[n & 1]);
+        row_vals(n + 1, l_next, d_next);
+      }
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&rows_ready[n & 1], (n >> 1) & 1, 49));
       if (!ok) break;
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(dp_full, n & 1, 51));
       if (!ok) break;
       tc_fence_after();
-      // The whole dP^T row first: its columns then take dS^T and P^T.
-      uint32_t dp[128];
-      tmem_ld32(lane_base + L::kColDP + 0, *reinterpret_cast<uint32_t(*)[32]>(dp + 0));
-      tmem_ld32(lane_base + L::kColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(dp + 32));
-      tmem_ld32(lane_base + L::kColDP + 64, *reinterpret_cast<uint32_t(*)[32]>(dp + 64));
-      tmem_ld32(lane_base + L::kColDP + 96, *reinterpret_cast<uint32_t(*)[32]>(dp + 96));
+      // This half's 64 dP^T columns first: their columns then take dS^T and P^T.
+      uint32_t dp[64];
+      tmem_ld32(lane_base + L::kColDP + c0, *reinterpret_cast<uint32_t(*)[32]>(dp + 0));
+      tmem_ld32(lane_base + L::kColDP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dp + 32));
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(s_full, n & 1, 50));
       if (!ok) break;
       tc_fence_after();
       // Query c of the tile is allowed for this key iff c < Nq - q0, and
-      // (causal) kj <= q0 + c + diag.
-      const int c_hi = p.Nq - q0;                           // columns >= c_hi: past Nq
+      // (causal) kj <= q0 + c + diag; tiles wholly inside skip the test.
+      const int c_hi = p.Nq - q0;                               // columns >= c_hi: past Nq
       const int c_lo = p.causal ? kj - diag - q0 : -0x7FFFFFFF;  // columns < c_lo: masked
       const bool key_ok = kj < p.Nk;
-      const uint32_t ds_row = sbase + L::kDSOff + row * 128;
+      const bool masked = !(key_ok && c_lo <= c0 && c_hi >= c0 + 64);
+      const uint32_t ds_row = sbase + L::kDSOff + half * (128 * 128) + row * 128;
       if (n > 0) {
-        // The dS region held the previous item's staged dQ chunks: their TMA
-        // reduces must have finished reading it.
-        const int g1 = n * (D / 32) - 1;  // that item's last chunk
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[g1 & 1], (g1 >> 1) & 1, 54) &&
-                                         mbar_wait(&red_free[(g1 - 1) & 1], ((g1 - 1) >> 1) & 1, 55));
+        // This half's part of the dS region was the staging buffer of its
+        // previous dQ chunks: their TMA reduces must have finished reading it.
+        const int g1 = n * (D / 64) - 1;  // this half's last staging use of the previous item
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[half], g1 & 1, 54));
         if (!ok) break;
       }
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {  // 32 query columns per chunk
-        uint32_t s[32];
-        tmem_ld32(lane_base + L::kColS + ch * 32, s);
+      for (int ch = 0; ch < 2; ++ch) {  // 32 query columns per chunk
+        uint32_t sv[32];
+        tmem_ld32(lane_base + L::kColS + c0 + ch * 32, sv);
         uint32_t pw[16], dw[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pe[2], de[2];
+        for (int e = 0; e < 32; e += 4) {
+          const int c = c0 + ch * 32 + e;
+          const uint4 nl4 = ld_shared_v4(smem_u32(nls + c));
+          const uint4 dd4 = ld_shared_v4(smem_u32(dsum + c));
+          const float nl[4] = {__uint_as_float(nl4.x), __uint_as_float(nl4.y), __uint_as_float(nl4.z),
+                               __uint_as_float(nl4.w)};
+          const float dd[4] = {__uint_as_float(dd4.x), __uint_as_float(dd4.y), __uint_as_float(dd4.z),
+                               __uint_as_float(dd4.w)};
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = ch * 32 + e + u;
-            const float l2 = lse[c];
-            // LSE = -inf: the row saw no key; its weights are 0.
-            const float m2 = (l2 == -INFINITY) ? INFINITY : l2 * 1.4426950408889634f;
-            const bool allowed = key_ok && c < c_hi && c >= c_lo;
-            const float pv = allowed ? ex2(fmaf(__uint_as_float(s[e + u]), p.scale_log2, -m2)) : 0.f;
-            pe[u] = pv;
-            de[u] = pv * (__uint_as_float(dp[c]) - dsum[c]);
+          for (int u = 0; u < 4; u += 2) {
+            float x0, x1, p0, p1, t0, t1, d0, d1;
+            ffma2(x0, x1, __uint_as_float(sv[e + u]), __uint_as_float(sv[e + u + 1]), sl, sl, nl[u], nl[u + 1]);
+            p0 = ex2(x0);
+            p1 = ex2(x1);
+            if (masked) {
+              const int cc = c + u;
+              if (!(key_ok && cc < c_hi && cc >= c_lo)) p0 = 0.f;
+              if (!(key_ok && cc + 1 < c_hi && cc + 1 >= c_lo)) p1 = 0.f;
+            }
+            fsub2(t0, t1, __uint_as_float(dp[ch * 32 + e + u]), __uint_as_float(dp[ch * 32 + e + u + 1]), dd[u],
+                  dd[u + 1]);
+            fmul2(d0, d1, p0, p1, t0, t1);
+            pw[(e + u) >> 1] = pack_bf16(p0, p1);
+            dw[(e + u) >> 1] = pack_bf16(d0, d1);
           }
-          pw[e >> 1] = pack_bf16(pe[0], pe[1]);
-          dw[e >> 1] = pack_bf16(de[0], de[1]);
         }
-        // dS^T into the first half of the dP^T slot, P^T into its second half
-        // (the row is already in registers).
-        tmem_st16(lane_base + L::kColDP + ch * 16, dw);
-        tmem_st16(lane_base + L::kColDP + 64 + ch * 16, pw);
-        // dS^T row into shared memory: 16-byte unit u of the 64-query half h at
-        // position u ^ (row & 7) (128-byte swizzle).
+        // dS^T and P^T over this half's dP^T columns (the row is in registers).
+        tmem_st16(lane_base + L::kColDP + c0 + ch * 16, dw);
+        tmem_st16(lane_base + L::kColDP + c0 + 32 + ch * 16, pw);
+        // dS^T row into shared memory: 16-byte unit uu of this half's 64-query
+        // box at position uu ^ (row & 7) (128-byte swizzle).
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
-          const int u = ch * 4 + u4;  // 16-byte unit over the 128 queries
-          const int h = u >> 3;
-          const int uu = u & 7;
-          st_shared_v4(ds_row + h * (128 * 128) + ((uu ^ (row & 7)) << 4), dw[4 * u4], dw[4 * u4 + 1],
-                       dw[4 * u4 + 2], dw[4 * u4 + 3]);
+          const int uu = ch * 4 + u4;
+          st_shared_v4(ds_row + ((uu ^ (row & 7)) << 4), dw[4 * u4], dw[4 * u4 + 1], dw[4 * u4 + 2], dw[4 * u4 + 3]);
         }
       }
       tmem_st_wait();
@@ -423,33 +443,34 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
 
-      // dQ tile rows (TMEM lane = query row): scale and add into the accumulator.
+      // dQ tile rows (TMEM lane = query row), this half's D/2 columns: scale
+      // and add into the accumulator.
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(dq_full, n & 1, 52));
       if (!ok) break;
       tc_fence_after();
       // 32 columns at a time: scale, stage as [128 rows][32] f32 (128-byte
-      // swizzle, conflict-free row writes) in a 16 KB buffer of the dS region
-      // (free: the dQ product has read dS), and one thread adds the chunk
-      // into the f32 accumulator with a TMA reduce.
-      const bool issuer = threadIdx.x == 64;
+      // swizzle, conflict-free row writes) in this half's 16 KB buffer of the
+      // dS region (free: the dQ product has read dS), and the half's issuing
+      // thread adds the chunk into the f32 accumulator with a TMA reduce.
+      constexpr int kCh = D / 64;  // chunks per half
 #pragma unroll 1
-      for (int ch = 0; ok && ch < D / 32; ++ch) {
-        const int g = n * (D / 32) + ch;  // running chunk index
-        const int buf = g & 1;
+      for (int ch = 0; ok && ch < kCh; ++ch) {
+        const int g = n * kCh + ch;  // this half's running staging use
         uint32_t v[32];
-        tmem_ld32(lane_base + L::kColDQ + ch * 32, v);
-        if (ch == D / 32 - 1) {
-          // The whole dQ tile is in registers or staged: the next dQ product may start.
+        tmem_ld32(lane_base + L::kColDQ + half * (D / 2) + ch * 32, v);
+        if (ch == kCh - 1) {
+          // This thread's part of the dQ tile is in registers: once every
+          // weight warp got here, the next dQ product may start.
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(dq_free);
         }
-        if (g >= 2 && ch >= 2) {
-          // Chunk g - 2 used this buffer within this item.
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[buf], ((g - 2) >> 1) & 1, 56));
+        if (ch > 0) {
+          // The previous chunk of this item used the same buffer.
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[half], (g - 1) & 1, 56));
           if (!ok) break;
         }
-        const uint32_t stg = sbase + L::kDSOff + buf * (128 * 128) + row * 128;
+        const uint32_t stg = sbase + L::kDSOff + half * (128 * 128) + row * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           st_shared_v4(stg + ((k ^ (row & 7)) << 4), __float_as_uint(__uint_as_float(v[4 * k]) * p.scale),
@@ -457,20 +478,15 @@ __global__ void __launch_bounds__(192, 1)
                        __float_as_uint(__uint_as_float(v[4 * k + 2]) * p.scale),
                        __float_as_uint(__uint_as_float(v[4 * k + 3]) * p.scale));
         fence_proxy_async_smem();
-        mbar_arrive(&red_full[buf]);
+        mbar_arrive(&red_full[half]);
         if (issuer) {
-          if (!mbar_wait(&red_full[buf], (g >> 1) & 1, 57)) {
+          if (!mbar_wait(&red_full[half], g & 1, 57)) {
             ok = false;
           } else {
-            tma_reduce_add_3d(&tmDQ, smem + L::kDSOff + buf * (128 * 128), ch * 32, q0, bh);
+            tma_reduce_add_3d(&tmDQ, smem + L::kDSOff + half * (128 * 128), half * (D / 2) + ch * 32, q0, bh);
             bulk_commit();
-            // Chunks before g have been read once at most one group is pending.
-            bulk_wait_read<1>();
-            if (ch > 0) mbar_arrive(&red_free[(g - 1) & 1]);
-            if (ch == D / 32 - 1) {
-              bulk_wait_read<0>();
-              mbar_arrive(&red_free[buf]);
-            }
+            bulk_wait_read<0>();
+            mbar_arrive(&red_free[half]);
           }
         }
         ok = __all_sync(0xFFFFFFFFu, ok);
@@ -478,9 +494,10 @@ __global__ void __launch_bounds__(192, 1)
       if (!ok) break;
     }
 
-    // dK, dV rows of this key (zeros when no query row sees the tile).  The
-    // tensor-memory loads are warp-collective: every lane runs them, and only
-    // the stores depend on the lane's key being inside Nk.
+    // dK, dV rows of this key (zeros when no query row sees the tile), this
+    // half's D/2 columns.  The tensor-memory loads are warp-collective: every
+    // lane runs them, and only the stores depend on the lane's key being
+    // inside Nk.
     if (ok && n_items > 0) {
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(dkv_done, 0, 53));
       if (ok) tc_fence_after();
@@ -494,7 +511,7 @@ __global__ void __launch_bounds__(192, 1)
         const float mul = which == 0 ? p.scale : 1.f;
         void* outp = which == 0 ? p.dk : p.dv;
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
+        for (int ch = half * (D / 64); ch < (half + 1) * (D / 64); ++ch) {
           uint32_t v[32];
           if (n_items > 0) {
             tmem_ld32(lane_base + col + ch * 32, v);
@@ -526,7 +543,7 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   // Every dQ reduce of this CTA must have completed before it exits.
-  if (threadIdx.x == 64) bulk_wait_all();
+  if (warp >= 2 && lane == 0 && (warp & 3) == 2) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

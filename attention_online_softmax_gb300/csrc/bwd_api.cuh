@@ -12,16 +12,10 @@ size_t bwd_align(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 // 3-D f32 map over the dQ accumulator [B*Hq][Nq][d]; one box is [128 rows][32
 // columns], 128-byte swizzled (the staging layout of the backward kernel).
 bool encode_dq_map(CUtensorMap* map, void* base, int d, int rows, int heads) {
-  auto fn = encode_fn();
-  if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(rows) * d * 4};
   cuuint32_t box[3] = {32, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int D, int STAGES>
@@ -29,10 +23,7 @@ attn_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
                        const CUtensorMap& mdq, const attn::BwdParams& p, cudaStream_t stream) {
   using L = attn::BwdLayout<D, STAGES>;
   auto kern = attn::attn_bwd_kernel<D, STAGES>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_LAUNCH;
-  }
+  if (!ensure_smem<attn::attn_bwd_kernel<D, STAGES>>(L::kAlloc)) return ATTN_ERR_LAUNCH;
   const long long grid = static_cast<long long>(p.B) * p.Hkv * ((p.Nk + 127) / 128);
   if (grid > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
   if (grid == 0) return ATTN_OK;

@@ -56,13 +56,6 @@
 
 #include "ptx.cuh"
 
-#ifndef ATTN_MMA_WAIT
-#define ATTN_MMA_WAIT mbar_wait
-#endif
-#ifndef ATTN_SOFTMAX_WAIT
-#define ATTN_SOFTMAX_WAIT mbar_wait
-#endif
-
 namespace attn {
 
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
@@ -76,7 +69,8 @@ constexpr int kStepR = 16;
 struct PrefillParams {
   void* o;
   float* lse;
-  int* sched;        // this launch's [work counter, finished-CTA counter], both 0 at launch
+  unsigned long long* sched;  // this launch's counter slot: (owner tag << 32) | fetches; 0 when free
+  unsigned sched_tag;         // this launch's nonzero owner tag
   int B, Hq, Hkv, Nq, Nk;
   int causal;
   int o_f32;
@@ -99,6 +93,7 @@ struct PrefillParams {
   const int32_t* seq_order;    // [num_seqs] sequences in dispatch order, longest context first (plan kernel)
   int num_seqs, max_pages, page_size, num_pages;
 };
+
 
 template <int D, int NQ, int STAGES, int BSLOTS = 0, bool PSEP = false>
 struct PrefillLayout {
@@ -424,11 +419,18 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       for (int i = 0; i < STAGES; ++i) slot_rel[i] = -1;
       int q_uses = 0;
       bool ok = true;
+      bool owned = false;       // this CTA's first fetch found or claimed the launch's counter
+      bool fetched_last = false;  // this CTA made its final fetch (or needs none)
       for (int n = 0; ok; ++n) {
         // Take the next unit, decode it and publish it (idx -1: no work left).
         const int slot = n % kUnitQ;
         if (!mbar_wait(&unit_empty[slot], ((n / kUnitQ) & 1) ^ 1, 4)) break;
-        const int idx = atomicAdd(p.sched, 1);
+        int idx = static_cast<int>(blockIdx.x);
+        if (n > 0) {
+          const int c = sched_fetch(p.sched, p.sched_tag, owned, total_units);
+          idx = c < 0 ? total_units : static_cast<int>(gridDim.x) + c;
+          fetched_last = idx >= total_units;
+        }
         Unit<NQ> u;
         if (idx < total_units) {
           u = unit_of<NQ, false>(p, idx);
@@ -490,14 +492,21 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
           }
         }
       }
-      // Drain: never leave the CTA with a copy still writing shared memory.
-      if (q_uses > 0) mbar_wait(q_full, (q_uses - 1) & 1, 2);
+      // A CTA that stopped early still makes its final fetch, so that the
+      // launch's fetches add up and the counter slot is freed.
+      while (!fetched_last) {
+        const int c = sched_fetch(p.sched, p.sched_tag, owned, total_units);
+        fetched_last = c < 0 || static_cast<int>(gridDim.x) + c >= total_units;
+      }
+      // Drain: never leave the CTA with a copy still writing shared memory
+      // (after one wait gives up, the rest are not attempted).
+      bool drained = q_uses == 0 || mbar_wait(q_full, (q_uses - 1) & 1, 2);
       if (kStepRing) {
-        for (int st = max(0, step - kStepR); st < step; ++st)
-          mbar_wait(&step_full[st % kStepR], (st / kStepR) & 1, 3);
+        for (int st = max(0, step - kStepR); drained && st < step; ++st)
+          drained = mbar_wait(&step_full[st % kStepR], (st / kStepR) & 1, 3);
       } else {
-        for (int it = max(0, item - STAGES); it < item; ++it)
-          mbar_wait(&kv_full[it % STAGES], (it / STAGES) & 1, 3);
+        for (int it = max(0, item - STAGES); drained && it < item; ++it)
+          drained = mbar_wait(&kv_full[it % STAGES], (it / STAGES) & 1, 3);
       }
     }
     __syncwarp();
@@ -528,10 +537,20 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     const bool issuer = g_l < kBN / ps;
     int item = 0, q_uses = 0, tails = 0;
     bool ok = true;
+    bool owned = false;  // lane 0: this CTA's first fetch found or claimed the launch's counter
+    // Lane 0: this CTA made its final fetch, or needs none (no first unit).
+    bool fetched_last = static_cast<int>(blockIdx.x) >= total_units;
     for (int n = 0; ok; ++n) {
       const int slot = n % kUnitQ;
       int idx = -2;
-      if (lane == 0 && mbar_wait(&unit_empty[slot], ((n / kUnitQ) & 1) ^ 1, 4)) idx = atomicAdd(p.sched, 1);
+      if (lane == 0 && mbar_wait(&unit_empty[slot], ((n / kUnitQ) & 1) ^ 1, 4)) {
+        idx = static_cast<int>(blockIdx.x);
+        if (n > 0) {
+          const int c = sched_fetch(p.sched, p.sched_tag, owned, total_units);
+          idx = c < 0 ? total_units : static_cast<int>(gridDim.x) + c;
+          fetched_last = idx >= total_units;
+        }
+      }
       idx = __shfl_sync(kFull, idx, 0);
       if (idx == -2) break;
       Unit<NQ> u;
@@ -639,10 +658,16 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       }
     }
     if (lane == 0) {
-      // Drain: never leave the CTA with a copy still writing shared memory.
-      if (q_uses > 0) mbar_wait(q_full, (q_uses - 1) & 1, 2);
-      for (int it = max(0, item - STAGES); it < item; ++it)
-        mbar_wait(&kv_full[it % STAGES], (it / STAGES) & 1, 3);
+      // A CTA that stopped early still makes its final fetch (see sched_fetch).
+      while (!fetched_last) {
+        const int c = sched_fetch(p.sched, p.sched_tag, owned, total_units);
+        fetched_last = c < 0 || static_cast<int>(gridDim.x) + c >= total_units;
+      }
+      // Drain: never leave the CTA with a copy still writing shared memory
+      // (after one wait gives up, the rest are not attempted).
+      bool drained = q_uses == 0 || mbar_wait(q_full, (q_uses - 1) & 1, 2);
+      for (int it = max(0, item - STAGES); drained && it < item; ++it)
+        drained = mbar_wait(&kv_full[it % STAGES], (it / STAGES) & 1, 3);
     }
     __syncwarp();
   } else if (BIAS == 2 && warp == 2 + 4 * NQ) {
@@ -701,7 +726,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       bool ok = true;
 
       auto wait_item = [&](int item, int where) {
-        return ATTN_MMA_WAIT(&kv_full[item % STAGES], (item / STAGES) & 1, where);
+        return mbar_wait(&kv_full[item % STAGES], (item / STAGES) & 1, where);
       };
       // S = Q_j K_t^T into S slot `slot`; waits for each K item in turn.
       auto issue_s = [&](int j, int slot, int kitem, bool wait) -> bool {
@@ -752,7 +777,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       // have read O_j out of tensor memory.
       auto wait_o_free = [&](int j) -> bool {
         if (o_uses[j] == 0) return true;
-        if (!ATTN_MMA_WAIT(&o_free[j], (o_uses[j] - 1) & 1, 16)) return false;
+        if (!mbar_wait(&o_free[j], (o_uses[j] - 1) & 1, 16)) return false;
         tc_fence_after();
         return true;
       };
@@ -776,7 +801,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
           auto s_tile = [&](int t) -> bool {
             const int c = c0 + t;
             if (c >= 2) {
-              if (!ATTN_MMA_WAIT(&s_free[c & 1], ((c - 2) >> 1) & 1, 18)) return false;
+              if (!mbar_wait(&s_free[c & 1], ((c - 2) >> 1) & 1, 18)) return false;
               tc_fence_after();
             }
             const int kit = item0 + k_pos<1, true>(t) * L::kH;
@@ -788,7 +813,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
           };
           auto pv_tile = [&](int t) -> bool {
             const int c = c0 + t;
-            if (!ATTN_MMA_WAIT(&p_full[c & 1], (c >> 1) & 1, 12)) return false;
+            if (!mbar_wait(&p_full[c & 1], (c >> 1) & 1, 12)) return false;
             tc_fence_after();
             if (t == 0 && !wait_o_free(0)) return false;
             const int vit = item0 + v_pos<1, true>(t, T) * L::kH;
@@ -827,7 +852,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
               bool waitedV = false, waitedK = false;
               if (kStepRing) {
                 // Both of the step's items on one barrier (every step reads one).
-                ok = ATTN_MMA_WAIT(&step_full[step % kStepR], (step / kStepR) & 1, 13);
+                ok = mbar_wait(&step_full[step % kStepR], (step / kStepR) & 1, 13);
                 if (!ok) break;
                 tc_fence_after();
                 waitedV = waitedK = true;
@@ -835,7 +860,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
 #pragma unroll
               for (int j = 0; j < NQ; ++j) {
                 if (t >= 1 && ta - 1 >= u.lo[j] && ta - 1 < u.hi[j]) {
-                  ok = ATTN_MMA_WAIT(&p_full[j], (cnt[j] - 1) & 1, 12);
+                  ok = mbar_wait(&p_full[j], (cnt[j] - 1) & 1, 12);
                   if (!ok) break;
                   tc_fence_after();
                   if (ta - 1 == u.lo[j]) {
@@ -880,7 +905,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
               }
               if (t >= 1) {
                 const int c = cnt[0] - (t < T ? 2 : 1);  // running index of tile t-1
-                ok = ATTN_MMA_WAIT(&p_full[c & 1], (c >> 1) & 1, 12);
+                ok = mbar_wait(&p_full[c & 1], (c >> 1) & 1, 12);
                 if (!ok) break;
                 tc_fence_after();
                 if (t - 1 == 0) {
@@ -957,7 +982,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
         const int t = u.lo[j] + ti;  // absolute key tile
         const int slot = NQ == 2 ? j : (cnt & 1);
         const uint32_t s_par = NQ == 2 ? (cnt & 1) : ((cnt >> 1) & 1);
-        ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(&s_full[slot], s_par, 20));
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_full[slot], s_par, 20));
         if (!ok) break;
         tc_fence_after();
         uint32_t r[kBN];
@@ -979,7 +1004,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
           // swizzle), so the 8 rows of each quarter-warp phase hit distinct banks.
           const float base = slope2 * static_cast<float>(k0 - qrow - diag);
           const int bs = bcnt % bias_ring<BIAS>();
-          ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(&bias_full[bs], (bcnt / bias_ring<BIAS>()) & 1, 24));
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bias_full[bs], (bcnt / bias_ring<BIAS>()) & 1, 24));
           if (!ok) break;
           const uint32_t brow_s = sbase + L::kBiasOff + bs * L::kBiasBytes + row * 128;
 #pragma unroll
@@ -1079,8 +1104,8 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
             // O holds tile t-1's contribution only once PV(t-1) is complete;
             // P V products are counted like the tiles (one per tile).
             ok = __all_sync(0xFFFFFFFFu,
-                            L::kPSep ? ATTN_SOFTMAX_WAIT(&pv_free[(cnt - 1) & 1], ((cnt - 1) >> 1) & 1, 21)
-                                     : ATTN_SOFTMAX_WAIT(pv_done, (cnt - 1) & 1, 21));
+                            L::kPSep ? mbar_wait(&pv_free[(cnt - 1) & 1], ((cnt - 1) >> 1) & 1, 21)
+                                     : mbar_wait(pv_done, (cnt - 1) & 1, 21));
             if (!ok) break;
             tc_fence_after();
           }
@@ -1102,7 +1127,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
         if (L::kPSep) {
           // P slot `slot` is free once the P V product of tile cnt - 2 is done.
           if (cnt >= 2) {
-            ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(&pv_free[slot], ((cnt - 2) >> 1) & 1, 27));
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(&pv_free[slot], ((cnt - 2) >> 1) & 1, 27));
             if (!ok) break;
             tc_fence_after();
           }
@@ -1119,7 +1144,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       if (!ok) break;
 
       if (nt > 0) {
-        ok = __all_sync(0xFFFFFFFFu, ATTN_SOFTMAX_WAIT(&o_done[j], o_uses & 1, 22));
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&o_done[j], o_uses & 1, 22));
         if (!ok) break;
         tc_fence_after();
       }
@@ -1178,15 +1203,6 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
-  }
-  if (threadIdx.x == 0) {
-    // The last CTA to finish resets this launch's counters for a later launch.
-    __threadfence();
-    if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
-      p.sched[0] = 0;
-      p.sched[1] = 0;
-      __threadfence();
-    }
   }
 }
 

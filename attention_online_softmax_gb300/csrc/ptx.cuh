@@ -153,6 +153,55 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, ui
   }
 }
 
+// Dynamic work distribution of a persistent grid (prefill and decode).  CTA b starts on unit b
+// (no atomic on the launch's critical path); every later unit comes from a
+// shared counter: unit = gridDim.x + fetch.  Each CTA with a first unit makes
+// exactly one final fetch (one whose unit is past the end), so a launch with
+// U units and G CTAs makes exactly U fetches in all, numbered 0 .. U - 1.
+//
+// The counter is one 64-bit word of a small ring in device memory, shared by
+// the launches that map to the same ring slot: (owner tag << 32) | fetches,
+// 0 when free.  A CTA's first fetch claims a free word for its launch's tag
+// (compare-and-swap from 0, which hands out fetch 0) or finds it already
+// claimed by its own launch; the fetch numbered U - 1 -- the launch's last
+// -- sets the word back to 0.  A word held by another launch (a launch that
+// is still handing out units from the same slot) is waited for, bounded;
+// giving up records ATTN_ERR_TIMEOUT and the CTA takes no further unit.
+// Returns the fetch number, or -1 after such a timeout.
+__device__ __forceinline__ int sched_fetch(unsigned long long* word, unsigned tag, bool& owned, int fetches) {
+  int c;
+  if (owned) {
+    c = static_cast<int>(atomicAdd(word, 1ull) & 0xFFFFFFFFull);
+  } else {
+    const unsigned long long mine = static_cast<unsigned long long>(tag) << 32;
+    unsigned long long old = atomicCAS(word, 0ull, mine | 1ull);
+    uint64_t t0 = 0;
+    while (true) {
+      if (old == 0ull) {  // claimed: this is fetch 0
+        c = 0;
+        break;
+      }
+      if ((old >> 32) == tag) {  // already claimed by this launch
+        c = static_cast<int>(atomicAdd(word, 1ull) & 0xFFFFFFFFull);
+        break;
+      }
+      // Held by another launch that still hands out units.
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        report_error(6 /* ATTN_ERR_TIMEOUT */, 60, static_cast<int>(old >> 32));
+        return -1;
+      }
+      __nanosleep(512);
+      old = atomicCAS(word, 0ull, mine | 1ull);
+    }
+    owned = true;
+  }
+  if (c == fetches - 1) atomicExch(word, 0ull);  // the launch's last fetch frees the slot
+  return c;
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -263,6 +312,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
         "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
         "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// 64 consecutive 32-bit TMEM columns of this thread's lane, completed before return.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(taddr)
       : "memory");
 }
@@ -403,6 +473,22 @@ __device__ __forceinline__ void fadd2(float& y0, float& y1, float a0, float a1, 
   asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
       "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
       "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void fmul2(float& y0, float& y1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void fsub2(float& y0, float& y1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
       : "=f"(y0), "=f"(y1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }

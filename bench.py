@@ -296,7 +296,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-config table")
-    ap.add_argument("--profile", choices=["prefill", "prefill_d256", "decode", "bwd", "chunked"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "prefill_d256", "tiny", "block", "decode", "bwd", "chunked"],
+                    default=None,
                     help="run one kernel of the step a few times (for an ncu capture) and exit")
     args = ap.parse_args(argv)
     rank, world, local = dist_env()
@@ -393,12 +394,12 @@ def main(argv=None):
 
     extra = None
     if not args.no_extra and rank == 0:
-        extra = per_config_table(abi, dev, stream, peaks)
+        extra = per_config_table(abi, dev, stream, peaks, with_cpu=not args.no_cpu_baseline)
 
-    # Decode time floor: traffic at the measured bandwidth plus the launches
-    # and one DRAM round trip the two-kernel split/combine stage cannot avoid.
+    # Decode time floor: traffic at the measured bandwidth plus the launch and
+    # one DRAM round trip the stage cannot avoid.
     launch_s, dram_s = launch_and_latency_floor(dev, stream, abi)
-    dec_kernels = 2 if ws_bytes > 0 else 1
+    dec_kernels = 1  # the merge of chunk partials runs inside the one decode kernel
     dec_floor = dec_bytes / (peaks.hbm_gbs * 1e9) + dec_kernels * launch_s + dram_s
 
     cpu = None
@@ -425,12 +426,13 @@ def main(argv=None):
                                       "launch_us": launch_s * 1e6, "kernels": dec_kernels,
                                       "dram_latency_us": dram_s * 1e6,
                                       "measured_over_floor": mean_dec / dec_floor}},
-            "roofline": {"bound": "tensor", "kernel": "prefill_fwd_kernel<128,2,4,0,0> (d128, two query tiles per CTA)",
+            "roofline": {"bound": "tensor", "kernel": abi.attn_fwd_kernel_name(P.B, P.Hq, P.Nq, P.d),
                          "achieved": pre_tflops, "peak": peaks.bf16_tflops, "unit": "TFLOP/s",
                          "frac": pre_tflops / peaks.bf16_tflops, "peak_source": peak_src,
                          "traffic": traffic_from_profiles("prefill_fwd_c3"),
                          "algorithmic": {"flops": pre_flops, "bytes": pre_bytes}},
-            "roofline_decode": {"bound": "hbm", "kernel": "decode_split_kernel<128,4> + decode_combine",
+            "roofline_decode": {"bound": "hbm",
+                                "kernel": abi.attn_decode_kernel_name(Dc.num_seqs, Dc.Hq, Dc.Hkv, Dc.d, xd.max_seqlen),
                                 "achieved": dec_gbs, "peak": peaks.hbm_gbs, "unit": "GB/s",
                                 "frac": dec_gbs / peaks.hbm_gbs, "peak_source": peak_src,
                                 "traffic": traffic_from_profiles("decode_c5")},
@@ -453,8 +455,8 @@ def profile_one(which: str, launches: int = 3) -> int:
     from attention_online_softmax_gb300 import build
     build.build()
     from attention_online_softmax_gb300 import abi
-    if which.startswith("prefill") or which == "bwd":
-        c = configs.GQA256 if which == "prefill_d256" else configs.LONG
+    if which.startswith("prefill") or which in ("bwd", "tiny", "block"):
+        c = {"prefill_d256": configs.GQA256, "tiny": configs.TINY, "block": configs.BLOCK}.get(which, configs.LONG)
         x = make_prefill_inputs(c)
         q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
         o = torch.empty_like(q)
@@ -601,8 +603,168 @@ def measure_e2e(abi, xp, xd, dev, stream, steps, floor_s, world):
             "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * t / steps, "steps": steps}
 
 
-def per_config_table(abi, dev, stream, peaks, reps: int = 30):
-    """Each workload timed alone (median of reps, L2 flushed before each)."""
+def gpu_median(call, stream, flush, reps: int, graph: bool = True):
+    """Median, p10, p90 seconds of `call` on the device (L2 flushed before each rep).
+
+    With `graph`, the call is captured once into a CUDA graph and each rep
+    replays it, so the events bracket the kernels alone: an eager call from
+    Python can leave the GPU idle while the host prepares the launch, which
+    for a kernel of a few microseconds would be most of what the events see.
+    """
+    # `call` launches on torch's current stream (it must not name a stream:
+    # under capture the current stream is the capturing one).
+    for _ in range(3):
+        call()
+    run = call
+    if graph:
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                call()
+        stream.wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize()
+        run = g.replay
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    ts.sort()
+    return statistics.median(ts), ts[len(ts) // 10], ts[(9 * len(ts)) // 10]
+
+
+# ---------------------------------------------------------------- CPU oracle per workload
+# The oracle (f64, C with OpenMP over rows) timed on the host cores beside each
+# workload's GPU time: a baseline, not the target.  Small workloads run whole;
+# large ones on a seeded sample of query rows calibrated to about `target_s`,
+# extrapolated to the whole workload by allowed (query, key) pairs (the
+# oracle's work per row is proportional to the keys the row sees).
+CPU_TARGET_S = 1.5
+
+
+def _row_keys(rows, Nq: int, Nk: int, causal: bool, window: int = 0):
+    import numpy as np
+    i = np.asarray(rows, dtype=np.int64) % Nq
+    diag = Nk - Nq
+    hi = np.minimum(Nk - 1, i + diag) if causal else np.full(i.shape, Nk - 1)
+    lo = np.maximum(0, i + diag - window + 1) if window > 0 else np.zeros(i.shape, dtype=np.int64)
+    return np.clip(hi - lo + 1, 0, None)
+
+
+def _calibrated(run, total_rows: int, seed: int, first: int = 64, target_s: float = CPU_TARGET_S):
+    """run(rows) -> (seconds, threads) on a seeded sample sized to ~target_s."""
+    g = torch.Generator().manual_seed(seed)
+    order = torch.randperm(total_rows, generator=g).numpy()
+    n = min(total_rows, first)
+    t, th = run(order[:n])
+    if n < total_rows and t < target_s:
+        n = min(total_rows, max(n + 1, int(n * target_s / max(t, 1e-4))))
+        t, th = run(order[:n])
+    return order[:n], t, th
+
+
+def cpu_prefill(c, x):
+    import numpy as np
+    import oracle
+    total = c.B * c.Hq * c.Nq
+    masked = bool(c.window or c.alibi or c.bias is not None)
+    slopes, bias, strides = None, None, (0, 0)
+    if masked:
+        slopes, bias = make_mask_inputs(c)
+        if bias is not None:
+            strides = (bias.stride(0) if bias.shape[0] == c.B else 0, bias.stride(1))
+
+    def run(rows):
+        t0 = time.perf_counter()
+        if masked:
+            _, _, th = oracle.attention_masked(x.q, x.k, x.v, c.causal, x.scale, window_left=c.window,
+                                               alibi=slopes, bias=bias, bias_strides=strides, rows=rows)
+        else:
+            _, _, th = oracle.attention(x.q, x.k, x.v, c.causal, x.scale, rows=rows)
+        return time.perf_counter() - t0, th
+
+    rows, t, th = _calibrated(run, total, seed=c.seed + 900)
+    full_pairs = c.B * c.Hq * roofline.allowed_pairs(c.Nq, c.Nk, c.causal, c.window)
+    sample_pairs = int(_row_keys(rows, c.Nq, c.Nk, c.causal, c.window).sum())
+    out = {"kind": "oracle", "cores": th, "sample_rows": int(len(rows)), "total_rows": total,
+           "seconds": t, "rows_per_s": len(rows) / t}
+    if len(rows) == total:
+        out["full_s"] = t
+    else:
+        out["extrapolated_full_s"] = t * full_pairs / max(sample_pairs, 1)
+        out["extrapolation"] = "sample time x (all allowed pairs / sampled rows' allowed pairs)"
+    if c is configs.TINY:
+        t0 = time.perf_counter()
+        _, _, th1 = oracle.attention(x.q, x.k, x.v, c.causal, x.scale, threads=1)
+        out["full_s_1_thread"] = time.perf_counter() - t0
+        out["threads_1"] = th1
+    return out
+
+
+def cpu_decode(xd):
+    import oracle
+    t0 = time.perf_counter()
+    _, _, th = oracle.decode_paged(xd.q, xd.kcache, xd.vcache, xd.block_table, xd.seqlens, xd.scale)
+    t = time.perf_counter() - t0
+    return {"kind": "oracle", "cores": th, "full_s": t, "seconds": t,
+            "sample": "every sequence and head"}
+
+
+def cpu_chunked(c, x, q_lens, k_lens):
+    import numpy as np
+    import oracle
+    total = sum(q_lens) * c.Hq
+    # allowed keys of each packed (token, head) row: token i of a chunk sees
+    # keys 0 .. i + k_len - q_len (causal).
+    keys = np.concatenate([np.arange(q) + (k - q) + 1 for q, k in zip(q_lens, k_lens)])
+
+    def run(rows):
+        t0 = time.perf_counter()
+        _, _, th = oracle.prefill_paged(x.q, x.kcache, x.vcache, x.block_table, x.cu_seqlens_q, x.seqlens_k,
+                                        True, x.scale, rows=rows)
+        return time.perf_counter() - t0, th
+
+    rows, t, th = _calibrated(run, total, seed=c.seed + 900)
+    full_pairs = int(keys.sum()) * c.Hq
+    sample_pairs = int(keys[np.asarray(rows) // c.Hq].sum())
+    return {"kind": "oracle", "cores": th, "sample_rows": int(len(rows)), "total_rows": total, "seconds": t,
+            "rows_per_s": len(rows) / t, "extrapolated_full_s": t * full_pairs / max(sample_pairs, 1),
+            "extrapolation": "sample time x (all allowed pairs / sampled rows' allowed pairs)"}
+
+
+def cpu_bwd(c, x, dout):
+    import oracle
+    # One (batch, head) slice: for MHA the workload is B*Hq independent copies of it.
+    t0 = time.perf_counter()
+    _, _, _, th = oracle.attention_bwd(x.q[:1, :1], x.k[:1, :1], x.v[:1, :1], dout[:1, :1], c.causal, x.scale)
+    t = time.perf_counter() - t0
+    return {"kind": "oracle", "cores": th, "seconds": t, "sample": "one (batch, head) slice of the workload",
+            "extrapolated_full_s": t * c.B * c.Hq, "extrapolation": "slice time x B*Hq (independent heads)"}
+
+
+def _row(t, p10, p90, fl, by, peaks, cpu, **extra):
+    bound = roofline.bound_rate(fl, by, peaks)
+    out = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_of_peak": fl / t / (peaks.bf16_tflops * 1e12),
+           "frac_of_bound": fl / t / bound, "p10_us": p10 * 1e6, "p90_us": p90 * 1e6}
+    out.update(extra)
+    if cpu is not None:
+        full = cpu.get("full_s", cpu.get("extrapolated_full_s"))
+        out["cpu"] = cpu
+        out["gpu_speedup_over_cpu"] = full / t
+    return out
+
+
+def per_config_table(abi, dev, stream, peaks, reps: int = 30, with_cpu: bool = True):
+    """Each workload timed alone (median of reps, L2 flushed before each), with
+    the oracle timed beside it on the host cores."""
     out = {}
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for c in configs.PREFILL_CONFIGS:
@@ -610,24 +772,15 @@ def per_config_table(abi, dev, stream, peaks, reps: int = 30):
         q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
         o = torch.empty_like(q)
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-        for _ in range(3):
-            abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale, stream)
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale, stream)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) * 1e-3)
-        t = statistics.median(ts)
+        fwd = lambda: abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale)  # noqa: E731
+        t, p10, p90 = gpu_median(fwd, stream, flush, reps)
         fl = roofline.prefill_flops(c.B, c.Hq, c.Nq, c.Nk, c.d, c.causal)
         by = roofline.prefill_bytes(c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d)
-        bound = roofline.bound_rate(fl, by, peaks)
-        out[c.name] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_of_peak": fl / t / (peaks.bf16_tflops * 1e12),
-                       "frac_of_bound": fl / t / bound, "p10_us": sorted(ts)[len(ts) // 10] * 1e6,
-                       "p90_us": sorted(ts)[(9 * len(ts)) // 10] * 1e6}
+        extra = {"kernel": abi.attn_fwd_kernel_name(c.B, c.Hq, c.Nq, c.d), "timing": "CUDA-graph replay"}
+        if t < 50e-6:
+            # the same call issued eagerly from Python: includes the host's launch latency
+            extra["us_eager"] = gpu_median(fwd, stream, flush, reps, graph=False)[0] * 1e6
+        out[c.name] = _row(t, p10, p90, fl, by, peaks, cpu_prefill(c, x) if with_cpu else None, **extra)
         del q, k, v, o, lse
     for c in configs.MASKED_CONFIGS:
         x = make_prefill_inputs(c)
@@ -640,62 +793,36 @@ def per_config_table(abi, dev, stream, peaks, reps: int = 30):
 
         def call():
             abi.attn_fwd_masked(q, k, v, o, lse, c.causal, x.scale, window_left=c.window, alibi=slopes,
-                                bias=bias, stream=stream)
-        for _ in range(3):
-            call()
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            call()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) * 1e-3)
-        t = statistics.median(ts)
+                                bias=bias)
+        t, p10, p90 = gpu_median(call, stream, flush, reps)
         fl = roofline.masked_flops(c.B, c.Hq, c.Nq, c.Nk, c.d, c.causal, c.window)
         by = roofline.prefill_bytes(c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d)
         if bias is not None:
             by += bias.numel() * 2
-        bound = roofline.bound_rate(fl, by, peaks)
-        out[c.name] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_of_peak": fl / t / (peaks.bf16_tflops * 1e12),
-                       "frac_of_bound": fl / t / bound, "flops": "4 d per allowed (query, key) pair",
-                       "p10_us": sorted(ts)[len(ts) // 10] * 1e6, "p90_us": sorted(ts)[(9 * len(ts)) // 10] * 1e6}
+        out[c.name] = _row(t, p10, p90, fl, by, peaks, cpu_prefill(c, x) if with_cpu else None,
+                           flops="4 d per allowed (query, key) pair")
         del q, k, v, o, lse, slopes, bias
     # Backward of the long causal MHA workload (forward output and LSE as inputs).
-    c = configs.LONG
-    x = make_prefill_inputs(c)
-    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
-    o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-    abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale, stream)
-    g = torch.Generator().manual_seed(c.seed + 50)
-    dout = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(abi.attn_bwd_workspace_size(c.B, c.Hq, c.Nq, c.d), dtype=torch.uint8, device=dev)
-
-    def call_bwd():
-        abi.attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, c.causal, x.scale, workspace=ws, stream=stream)
-    for _ in range(3):
-        call_bwd()
-    ts = []
-    for _ in range(reps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        call_bwd()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ts.append(e0.elapsed_time(e1) * 1e-3)
-    t = statistics.median(ts)
-    fl = 2.5 * roofline.prefill_flops(c.B, c.Hq, c.Nq, c.Nk, c.d, c.causal)
-    by = roofline.bwd_bytes(c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d)
-    bound = roofline.bound_rate(fl, by, peaks)
-    out["bwd_" + c.name] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_of_peak": fl / t / (peaks.bf16_tflops * 1e12),
-                            "frac_of_bound": fl / t / bound,
-                            "flops": "5 products of 2 N^2 d per head = 2.5x the forward's",
-                            "p10_us": sorted(ts)[len(ts) // 10] * 1e6, "p90_us": sorted(ts)[(9 * len(ts)) // 10] * 1e6}
-    del q, k, v, o, lse, dout, dq, dk, dv, ws
+    for c in configs.BWD_CONFIGS:
+        x = make_prefill_inputs(c)
+        q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale, stream)
+        g = torch.Generator().manual_seed(c.seed + 50)
+        dout_h = torch.randn(x.q.shape, generator=g).to(torch.bfloat16)
+        dout = dout_h.to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(abi.attn_bwd_workspace_size(c.B, c.Hq, c.Nq, c.d), dtype=torch.uint8, device=dev)
+        t, p10, p90 = gpu_median(
+            lambda: abi.attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, c.causal, x.scale, workspace=ws),
+            stream, flush, reps)
+        fl = 2.5 * roofline.prefill_flops(c.B, c.Hq, c.Nq, c.Nk, c.d, c.causal)
+        by = roofline.bwd_bytes(c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d)
+        cpu = cpu_bwd(c, x, dout_h) if with_cpu and c.Hq == c.Hkv else None
+        out["bwd_" + c.name] = _row(t, p10, p90, fl, by, peaks, cpu,
+                                    flops="5 products of 2 N^2 d per head = 2.5x the forward's")
+        del q, k, v, o, lse, dout, dq, dk, dv, ws
     # Chunked prefill against the paged cache.
     c = configs.CHUNKED
     q_lens, k_lens = configs.chunked_lengths(c)
@@ -707,28 +834,34 @@ def per_config_table(abi, dev, stream, peaks, reps: int = 30):
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
     ws = torch.empty(max(16, abi.attn_prefill_paged_workspace_size(c.num_seqs)), dtype=torch.uint8, device=dev)
-
-    def call_paged():
-        abi.attn_prefill_paged(q, kc, vc, bt, cu, sk, o, lse, True, x.scale, workspace=ws, stream=stream)
-    for _ in range(3):
-        call_paged()
-    ts = []
-    for _ in range(reps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        call_paged()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ts.append(e0.elapsed_time(e1) * 1e-3)
-    t = statistics.median(ts)
+    t, p10, p90 = gpu_median(
+        lambda: abi.attn_prefill_paged(q, kc, vc, bt, cu, sk, o, lse, True, x.scale, workspace=ws),
+        stream, flush, reps)
     fl = sum(4.0 * c.Hq * c.d * roofline.allowed_pairs(a, b, True) for a, b in zip(q_lens, k_lens))
     by = roofline.paged_prefill_bytes(q_lens, k_lens, c.Hq, c.Hkv, c.d, c.page_size)
-    bound = roofline.bound_rate(fl, by, peaks)
-    out[c.name] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_of_peak": fl / t / (peaks.bf16_tflops * 1e12),
-                   "frac_of_bound": fl / t / bound, "flops": "4 d per allowed (query, key) pair",
-                   "p10_us": sorted(ts)[len(ts) // 10] * 1e6, "p90_us": sorted(ts)[(9 * len(ts)) // 10] * 1e6}
+    out[c.name] = _row(t, p10, p90, fl, by, peaks, cpu_chunked(c, x, q_lens, k_lens) if with_cpu else None,
+                       flops="4 d per allowed (query, key) pair")
     del q, kc, vc, o, lse, ws
+    # Paged decode alone (HBM-bound: reported as GB/s against the copy ceiling).
+    Dc = configs.DECODE
+    xd = make_decode_inputs()
+    dq_, kc, vc = xd.q.to(dev), xd.kcache.to(dev), xd.vcache.to(dev)
+    bt, sl = xd.block_table.to(dev), xd.seqlens.to(dev)
+    do = torch.empty_like(dq_)
+    dlse = torch.empty(dq_.shape[:2], dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, abi.attn_decode_workspace_size(Dc.num_seqs, Dc.Hq, Dc.Hkv, Dc.d, xd.max_seqlen)),
+                     dtype=torch.uint8, device=dev)
+    t, p10, p90 = gpu_median(
+        lambda: abi.attn_decode_paged(dq_, kc, vc, bt, sl, do, dlse, xd.max_seqlen, xd.scale, ws),
+        stream, flush, reps)
+    by = roofline.decode_bytes(xd.seqlens.tolist(), Dc.Hq, Dc.Hkv, Dc.d, Dc.page_size)
+    row = {"us": t * 1e6, "gbs": by / t / 1e9, "frac_of_hbm": by / t / (peaks.hbm_gbs * 1e9),
+           "p10_us": p10 * 1e6, "p90_us": p90 * 1e6, "bytes": by}
+    if with_cpu:
+        row["cpu"] = cpu_decode(xd)
+        row["gpu_speedup_over_cpu"] = row["cpu"]["full_s"] / t
+    out[Dc.name] = row
+    del dq_, kc, vc, bt, sl, do, dlse, ws
     torch.cuda.empty_cache()
     return out
 

@@ -41,6 +41,45 @@ def test_header_declares_the_documented_entry_points():
         assert name in syms
 
 
+PAGE_TITLES = ("Compilers and Kernels", "Tang: a compiler that derives GPU kernels and bounds how fast they can run",
+               "Don't Write Kernels, Derive Them")
+
+
+def declaration_comments():
+    """(name, the comment block that documents it) for every ATTN_API declaration."""
+    text = open(HEADER).read()
+    out = []
+    for m in re.finditer(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text):
+        start = text.rfind("/*", 0, m.start())
+        end = text.find("*/", start)
+        assert 0 <= start < end < m.start(), m.group(1)
+        out.append((m.group(1), " ".join(text[start:end].replace("*", " ").split())))
+    return out
+
+
+def test_every_declaration_cites_its_passage_or_says_it_has_none():
+    decls = declaration_comments()
+    assert len(decls) == len(declared_symbols())
+    for name, comment in decls:
+        cited = re.search(r'Source: "([^"]+)"', comment)
+        if cited:
+            assert cited.group(1) in PAGE_TITLES, (name, cited.group(1))
+        else:
+            assert "no counterpart" in comment, name
+    cites = dict(decls)
+    for name in ("attn_fwd", "attn_decode_paged", "attn_decode_workspace_size", "attn_fwd_masked",
+                 "attn_prefill_paged", "attn_bwd"):
+        assert "Source:" in cites[name], name
+
+
+def test_fwd_kernel_name_follows_the_dispatch(abi):
+    # Names only; no launch.  d = 256 never takes two query tiles per unit.
+    assert abi.attn_fwd_kernel_name(1, 16, 16384, 256) == "prefill_fwd_kernel<256,1,5,0,0>"
+    assert abi.attn_fwd_kernel_name(1, 2, 128, 64).startswith("prefill_fwd_kernel<64,1,")
+    assert abi.attn_fwd_kernel_name(2, 32, 4096, 128).startswith("prefill_fwd_kernel<128,2,")
+    assert abi.attn_fwd_kernel_name(1, 2, 128, 96) == ""
+
+
 def test_library_exports_every_declared_symbol(abi):
     lib = ctypes.CDLL(build.LIB)
     for name in declared_symbols():
@@ -99,9 +138,11 @@ def dec(abi, num_seqs=4, Hq=32, Hkv=8, d=128, page=16, pages=100, max_pages=32, 
 
 def test_decode_rejects_bad_arguments(abi):
     before = abi.attn_launch_count()
-    assert dec(abi, page=32) == UNSUPPORTED
+    assert dec(abi, page=8) == UNSUPPORTED
+    assert dec(abi, page=48) == UNSUPPORTED
+    assert dec(abi, page=256) == UNSUPPORTED
     assert dec(abi, d=80) == UNSUPPORTED
-    assert dec(abi, Hq=64, Hkv=4) == UNSUPPORTED      # group of 16
+    assert dec(abi, Hq=128, Hkv=4) == UNSUPPORTED     # group of 32
     assert dec(abi, Hq=24, Hkv=8) == UNSUPPORTED      # group of 3
     assert dec(abi, Hq=30, Hkv=8) == INVALID
     assert dec(abi, max_len=513, max_pages=32) == INVALID  # beyond the block table
@@ -121,17 +162,33 @@ def test_decode_rejects_bad_arguments(abi):
 
 def test_decode_workspace_size_is_a_pure_plan(abi):
     ws = abi.attn_decode_workspace_size
-    # 64 sequences x 8 kv heads: one 8-head group per CTA, 256-token chunks,
-    # ceil(8192 / 256) = 32 splits of (128 + 1) floats per query head.
-    assert ws(64, 32, 8, 128, 8192) == ((64 * 32 * 32 * 129 * 4 + 255) // 256) * 256
+    up = lambda n: (n + 255) // 256 * 256
+
+    def expect(S, Hq, splits, d, groups, warps):
+        # split partials (d + 1 floats per query head and split), then one
+        # 8-byte merge counter per (sequence, head group, compute warp)
+        return up(up(S * splits * Hq * (d + 1) * 4) + S * groups * warps * 8)
+    # 64 sequences x 8 kv heads: one 8-head group per work item, 256-token
+    # chunks, ceil(8192 / 256) = 32 splits; 8 compute warps.
+    assert ws(64, 32, 8, 128, 8192) == expect(64, 32, 32, 128, 1, 8)
     # a sequence that fits one chunk needs no partials
     assert ws(4096, 32, 8, 128, 256) == 0
     assert ws(1, 32, 8, 128, 0) == 0
     # few sequences: smaller chunks to fill the GPU, more splits
-    assert ws(1, 8, 8, 128, 4096) == ((1 * 64 * 8 * 129 * 4 + 255) // 256) * 256
+    assert ws(1, 8, 8, 128, 4096) == expect(1, 8, 64, 128, 1, 8)
+    # a group of 16 query heads: two warps per kv head, so 4 kv heads per item
+    assert ws(64, 64, 4, 128, 8192) == expect(64, 64, 32, 128, 1, 8)
     assert ws(4, 30, 8, 128, 512) == 0          # invalid -> 0
     assert ws(4, 32, 8, 96, 512) == 0
+    assert ws(4, 128, 4, 128, 512) == 0         # group of 32
     assert ws(64, 32, 8, 128, 8192) == ws(64, 32, 8, 128, 8192)
+
+
+def test_decode_kernel_name_follows_the_plan(abi):
+    assert abi.attn_decode_kernel_name(64, 32, 8, 128, 8192) == "decode_kernel<128,4,1>"
+    assert abi.attn_decode_kernel_name(8, 64, 4, 64, 1000) == "decode_kernel<64,8,2>"
+    assert abi.attn_decode_kernel_name(8, 8, 8, 256, 1000) == "decode_kernel<256,1,1>"
+    assert abi.attn_decode_kernel_name(8, 24, 8, 128, 1000) == ""
 
 
 def test_paged_prefill_workspace_size(abi):

@@ -203,6 +203,107 @@ def test_decode_small_cases(abi, case):
     check_decode(abi, d_in)
 
 
+PAGED_DECODE = [
+    # num_seqs, Hq, Hkv, d, page_size, lengths
+    (4, 32, 8, 128, 32, [1, 31, 33, 700]),       # contexts ending mid-page
+    (3, 16, 4, 64, 64, [64, 65, 1500]),
+    (3, 8, 2, 256, 128, [127, 128, 2049]),
+    (5, 32, 2, 128, 16, [17, 300, 1, 4000, 256]),  # a group of 16 query heads
+    (3, 64, 4, 64, 128, [900, 1, 5000]),           # group of 16, 128-token pages
+    (2, 16, 1, 256, 32, [70, 3000]),               # MQA-style group of 16 at d = 256
+]
+
+
+@pytest.mark.parametrize("case", PAGED_DECODE)
+def test_decode_page_sizes_and_groups(abi, case):
+    S, Hq, Hkv, d, page, lens = case
+    pages = sum((L + page - 1) // page for L in lens) + 5
+    d_in = inputs.decode_inputs(S, Hq, Hkv, d, 0, max(lens), num_pages=pages, page_size=page,
+                                seed=3000 + sum(lens) + page, lengths=lens,
+                                max_pages_per_seq=(max(lens) + page - 1) // page + 1)
+    check_decode(abi, d_in)
+
+
+def test_decode_workspace_reuse_determinism_and_graph_replay(abi):
+    # One workspace for several calls: its merge counters must come back
+    # reset, so a second call (other inputs), a repeat of the first (bitwise
+    # equal) and two replays of a captured call (same epoch) all merge right.
+    dev = torch.device("cuda")
+    cases = [inputs.decode_inputs(6, 32, 8, 128, 300, 3000, num_pages=1200, page_size=16, seed=41),
+             inputs.decode_inputs(6, 32, 8, 128, 300, 3000, num_pages=1200, page_size=16, seed=42)]
+    need = max(abi.attn_decode_workspace_size(6, 32, 8, 128, c.max_seqlen) for c in cases)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=dev)
+
+    def call(c, o, lse):
+        abi.attn_decode_paged(c.q.to(dev), c.kcache.to(dev), c.vcache.to(dev), c.block_table.to(dev),
+                              c.seqlens.to(dev), o, lse, c.max_seqlen, c.scale, ws)
+
+    outs = []
+    for c in cases + cases[:1]:
+        o = torch.full((6, 32, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+        lse = torch.full((6, 32), float("nan"), dtype=torch.float32, device=dev)
+        call(c, o, lse)
+        torch.cuda.synchronize()
+        assert abi.attn_get_device_status() == 0
+        outs.append((o.float().cpu().numpy(), lse.cpu().numpy()))
+    for c, (o, lse) in zip(cases, outs):
+        o_ref, lse_ref, _ = oracle.decode_paged(c.q, c.kcache, c.vcache, c.block_table, c.seqlens, c.scale)
+        compare(o, lse, o_ref, lse_ref, True)
+    assert np.array_equal(outs[0][0], outs[2][0]) and np.array_equal(outs[0][1], outs[2][1])
+
+    c = cases[1]
+    q, kc, vc = c.q.to(dev), c.kcache.to(dev), c.vcache.to(dev)
+    bt, sl = c.block_table.to(dev), c.seqlens.to(dev)
+    o = torch.full((6, 32, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((6, 32), float("nan"), dtype=torch.float32, device=dev)
+    abi.attn_decode_paged(q, kc, vc, bt, sl, o, lse, c.max_seqlen, c.scale, ws)  # warm-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            abi.attn_decode_paged(q, kc, vc, bt, sl, o, lse, c.max_seqlen, c.scale, ws)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        o.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert abi.attn_get_device_status() == 0
+        assert np.array_equal(o.float().cpu().numpy(), outs[1][0])
+        assert np.array_equal(lse.cpu().numpy(), outs[1][1])
+
+
+def test_prefill_graph_replay(abi):
+    # A captured prefill keeps its work-counter slot; consecutive replays
+    # must each compute every unit (the slot is freed by each replay's last
+    # fetch).
+    dev = torch.device("cuda")
+    x = inputs.prefill_inputs(1, 8, 8, 1000, 1000, 128, seed=43, causal=True)
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    abi.attn_fwd(q, k, v, o, lse, True, x.scale)
+    torch.cuda.synchronize()
+    ref_o, ref_l = o.float().cpu().numpy(), lse.cpu().numpy()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            abi.attn_fwd(q, k, v, o, lse, True, x.scale)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        o.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert abi.attn_get_device_status() == 0
+        assert np.array_equal(o.float().cpu().numpy(), ref_o)
+        assert np.array_equal(lse.cpu().numpy(), ref_l)
+
+
 def test_decode_config(abi):
     c = configs.DECODE
     d_in = inputs.decode_inputs(c.num_seqs, c.Hq, c.Hkv, c.d, c.len_lo, c.len_hi, c.num_pages,
