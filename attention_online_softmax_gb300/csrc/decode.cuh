@@ -2,10 +2,13 @@
 // against a paged KV cache, as a bandwidth-bound GEMV-class stage.
 //
 // Work item = (sequence, chunk of up to 256 cached tokens, group of hg
-// key/value heads), in sequence-major order.  Either one CTA per item slot
-// (slots past a sequence's end exit at once), or a persistent grid (one or
-// two CTAs per SM) in which CTA b starts on item b and takes the rest from a
-// shared counter (sched_fetch), skipping chunks past a sequence's end.  One
+// key/value heads), ordered by chunk index from the last to the first: the
+// slots past a sequence's end and the sequences' partial last chunks come
+// first, and the launch ends on the uniform layer of first chunks, after which
+// every sequence's merge runs at once.  Either one CTA per item slot (slots
+// past a sequence's end exit at once), or a persistent grid (one or two CTAs
+// per SM) in which CTA b starts on item b and takes the rest from a shared
+// counter (sched_fetch), skipping chunks past a sequence's end.  One
 // producer thread streams each item's cached tokens with TMA in boxes of
 // [16 slots][hg heads][d] (first the K boxes, then the V boxes) into a ring
 // of shared-memory stages that runs on across the items of a CTA; for page
@@ -140,64 +143,91 @@ __device__ __forceinline__ bool merge_arrive(unsigned long long* cnt, unsigned l
   return false;
 }
 
-// Merge the chunk partials of (seq, head): one warp, lanes own D/32 elements.
-// Partials are read through L2 (ld.global.cg): other CTAs wrote them during
-// this kernel.
-template <int D>
-__device__ __forceinline__ void merge_head(const DecodeParams& p, int seq, int head, int ns, int lane) {
+// Merge the chunk partials of query heads [head0, head0 + GW) of `seq`: one
+// warp, lanes own D/32 elements of every row.  The rows of U chunks of all GW
+// heads are loaded together, so the walk over the chunks takes few L2 round
+// trips.  Partials are read through L2 (ld.global.cg): other CTAs wrote them
+// during this kernel.
+template <int D, int GW>
+__device__ __forceinline__ void merge_heads(const DecodeParams& p, int seq, int head0, int ns, int lane) {
   constexpr int E = D / 32;
-  const size_t row0 = static_cast<size_t>(seq) * p.n_splits * p.Hq + head;
-  float m = -INFINITY;
-  for (int c = lane; c < ns; c += 32) m = fmaxf(m, __ldcg(p.ws_lse + row0 + static_cast<size_t>(c) * p.Hq));
+  constexpr int U0 = 32 / (GW * E);
+  constexpr int U = U0 < 1 ? 1 : (U0 > 4 ? 4 : U0);  // chunks whose rows are loaded together
+  const size_t row0 = static_cast<size_t>(seq) * p.n_splits * p.Hq + head0;  // (chunk 0, head0)
+  float m[GW];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-  float acc[E];
+  for (int g = 0; g < GW; ++g) m[g] = -INFINITY;
+  for (int c = lane; c < ns; c += 32)
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
+    for (int g = 0; g < GW; ++g) m[g] = fmaxf(m[g], __ldcg(p.ws_lse + row0 + static_cast<size_t>(c) * p.Hq + g));
+#pragma unroll
+  for (int g = 0; g < GW; ++g)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m[g] = fmaxf(m[g], __shfl_xor_sync(0xFFFFFFFFu, m[g], off));
   // m = -inf only if every chunk was empty, which a multi-chunk sequence never is.
+  float acc[GW][E], wsum[GW];
+#pragma unroll
+  for (int g = 0; g < GW; ++g) {
+    wsum[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
+  }
   for (int c0 = 0; c0 < ns; c0 += 32) {
     const int cl = c0 + lane;
-    const float wl =
-        cl < ns ? ex2((__ldcg(p.ws_lse + row0 + static_cast<size_t>(cl) * p.Hq) - m) * 1.4426950408889634f) : 0.f;
-    wsum += wl;
+    float wl[GW];
+#pragma unroll
+    for (int g = 0; g < GW; ++g) {
+      wl[g] = cl < ns ? ex2((__ldcg(p.ws_lse + row0 + static_cast<size_t>(cl) * p.Hq + g) - m[g]) *
+                            1.4426950408889634f)
+                      : 0.f;
+      wsum[g] += wl[g];
+    }
     const int nb = min(32, ns - c0);
-    for (int k = 0; k < nb; k += 4) {
-      float v[4][E];
+    for (int k = 0; k < nb; k += U) {
+      float v[U][GW][E];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int c = min(c0 + k + u, ns - 1);  // in range; weight 0 past the end
-        const float* src = p.ws_o + (row0 + static_cast<size_t>(c) * p.Hq) * D + lane * E;
 #pragma unroll
-        for (int e = 0; e < E; e += 2) {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + e));
-          v[u][e] = x.x;
-          v[u][e + 1] = x.y;
+        for (int g = 0; g < GW; ++g) {
+          const float* src = p.ws_o + (row0 + static_cast<size_t>(c) * p.Hq + g) * D + lane * E;
+#pragma unroll
+          for (int e = 0; e < E; e += 2) {
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(src + e));
+            v[u][g][e] = x.x;
+            v[u][g][e + 1] = x.y;
+          }
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float w = __shfl_sync(0xFFFFFFFFu, wl, (k + u) & 31);
-        if (k + u >= nb) w = 0.f;
+      for (int u = 0; u < U; ++u)
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
-      }
+        for (int g = 0; g < GW; ++g) {
+          float w = __shfl_sync(0xFFFFFFFFu, wl[g], (k + u) & 31);
+          if (k + u >= nb) w = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[g][e] = fmaf(w, v[u][g][e], acc[g][e]);
+        }
     }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, off);
-  const float inv = 1.f / wsum;
-  const size_t off = (static_cast<size_t>(seq) * p.Hq + head) * D + lane * E;
-  if (p.o_f32) {
-    float* dst = static_cast<float*>(p.o) + off;
+  for (int g = 0; g < GW; ++g) {
 #pragma unroll
-    for (int e = 0; e < E; e += 2) *reinterpret_cast<float2*>(dst + e) = make_float2(acc[e] * inv, acc[e + 1] * inv);
-  } else {
-    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.o) + off);
+    for (int off = 16; off > 0; off >>= 1) wsum[g] += __shfl_xor_sync(0xFFFFFFFFu, wsum[g], off);
+    const float inv = 1.f / wsum[g];
+    const size_t off = (static_cast<size_t>(seq) * p.Hq + head0 + g) * D + lane * E;
+    if (p.o_f32) {
+      float* dst = static_cast<float*>(p.o) + off;
 #pragma unroll
-    for (int e = 0; e < E; e += 2) dst[e / 2] = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+      for (int e = 0; e < E; e += 2)
+        *reinterpret_cast<float2*>(dst + e) = make_float2(acc[g][e] * inv, acc[g][e + 1] * inv);
+    } else {
+      uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.o) + off);
+#pragma unroll
+      for (int e = 0; e < E; e += 2) dst[e / 2] = pack_bf16(acc[g][e] * inv, acc[g][e + 1] * inv);
+    }
+    if (lane == 0) p.lse[static_cast<size_t>(seq) * p.Hq + head0 + g] = m[g] + logf(wsum[g]);
   }
-  if (lane == 0) p.lse[static_cast<size_t>(seq) * p.Hq + head] = m + logf(wsum);
 }
 
 struct DecodeItem {
@@ -210,15 +240,16 @@ __host__ __device__ constexpr int decode_fixed_bytes(int warps, int chunk, int g
   return warps * chunk * gw * 4 + (2 * kMaxStages + 2 * kItemQ) * 8 + kItemQ * 16 + 1024;
 }
 
+// Up to four query heads per warp and d <= 128: two CTAs per SM (registers capped for it).
 template <int D, int GW, int WPH>
-__global__ void __launch_bounds__(288)
+__global__ void __launch_bounds__(288, (GW <= 4 && D <= 128) ? 2 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p) {
   using S = DecodeShape<D, GW>;
   constexpr int G = GW * WPH;  // query heads per key/value head
   const int nw = p.hg * WPH;   // compute warps
   const int U = p.num_seqs * p.n_splits * p.ngroups;
-  const int per_seq = p.n_splits * p.ngroups;
+  const int per_layer = p.num_seqs * p.ngroups;  // items of one chunk index
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -259,10 +290,11 @@ __global__ void __launch_bounds__(288)
       int n = 0;    // items published
       int w = static_cast<int>(blockIdx.x);  // first item: static (the grid is never larger than U)
       while (ok && w < U) {
-        const int seq = w / per_seq;
-        const int rem = w - seq * per_seq;
-        const int ch = rem / p.ngroups;
-        const int grp = rem - ch * p.ngroups;
+        const int layer = w / per_layer;
+        const int rem = w - layer * per_layer;
+        const int ch = p.n_splits - 1 - layer;
+        const int seq = rem / p.ngroups;
+        const int grp = rem - seq * p.ngroups;
         const int L = decode_len(p, seq, ch == 0 && grp == 0);
         // Chunk 0 is always an item (a sequence of length 0 still gets O = 0,
         // LSE = -inf); later chunks only while they hold tokens.
@@ -507,8 +539,7 @@ __global__ void __launch_bounds__(288)
         last = __shfl_sync(0xFFFFFFFFu, last, 0);
         if (last) {
           __threadfence();
-#pragma unroll 1
-          for (int g = 0; g < GW; ++g) merge_head<D>(p, seq, head0 + g, nch, lane);
+          merge_heads<D, GW>(p, seq, head0, nch, lane);
         }
       }
     }
