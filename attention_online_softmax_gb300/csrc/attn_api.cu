@@ -351,14 +351,12 @@ attn_status launch_prefill_paged(const CUtensorMap& mq, const CUtensorMap& mk, c
 
 // ---------------------------------------------------------------- decode plan
 struct DecodePlan {
-  int gw = 1;       // query heads per compute warp
-  int wph = 1;      // compute warps per key/value head
-  int hg = 1;       // key/value heads per work item
-  int ngroups = 1;  // Hkv / hg
+  int gw = 1;   // query heads per compute warp
+  int wph = 1;  // compute warps per key/value head
+  int hg = 1;   // key/value heads per CTA
   int chunk = attn::kChunkMax;
   int n_splits = 1;
   size_t ws_o_floats = 0;
-  size_t ws_cnt_off = 0;  // byte offset of the merge counters
   size_t ws_bytes = 0;
 };
 
@@ -376,31 +374,21 @@ bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int max_seqlen, DecodePla
       break;
     }
   }
-  pl.ngroups = Hkv / pl.hg;
-  const long long groups = static_cast<long long>(num_seqs) * pl.ngroups;
+  const long long groups = static_cast<long long>(num_seqs) * (Hkv / pl.hg);
   pl.chunk = attn::kChunkMax;
   while (pl.chunk > 64 && groups * ((max_seqlen + pl.chunk - 1) / pl.chunk) < 1024) pl.chunk /= 2;
   pl.n_splits = max_seqlen > 0 ? (max_seqlen + pl.chunk - 1) / pl.chunk : 1;
-  if (pl.n_splits >= (1 << attn::kCntBits)) return false;
-  if (groups * pl.n_splits > 0x7FFFFFFFLL) return false;
+  if (static_cast<long long>(num_seqs) * pl.n_splits > 0x7FFFFFFFLL) return false;
   if (pl.n_splits > 1) {
     pl.ws_o_floats = static_cast<size_t>(num_seqs) * pl.n_splits * Hq * d;
     const size_t lse_floats = static_cast<size_t>(num_seqs) * pl.n_splits * Hq;
-    pl.ws_cnt_off = ((pl.ws_o_floats + lse_floats) * 4 + 255) & ~static_cast<size_t>(255);
-    const size_t cnt_bytes = static_cast<size_t>(num_seqs) * pl.ngroups * pl.hg * pl.wph * 8;
-    pl.ws_bytes = (pl.ws_cnt_off + cnt_bytes + 255) & ~static_cast<size_t>(255);
+    pl.ws_bytes = ((pl.ws_o_floats + lse_floats) * 4 + 255) & ~static_cast<size_t>(255);
   }
   *out = pl;
   return true;
 }
 
-std::atomic<uint64_t> g_decode_epoch{0};
-
-// Decode grid: persistent (CTAs take items from a counter) or one CTA per item.
-constexpr bool kDecodePersistent = true;
-constexpr int kDecodeCtasPerSm = 0;  // 0: chosen by decode_shape
-
-// Blocks of `kern` that fit on one SM with `smem` bytes of dynamic shared
+// Blocks of `Kern` that fit on one SM with `smem` bytes of dynamic shared
 // memory (0 when the query fails).
 template <auto Kern>
 int blocks_per_sm(int threads, int smem) {
@@ -412,16 +400,16 @@ int blocks_per_sm(int threads, int smem) {
   return n;
 }
 
-// Ring depth and CTAs per SM of the decode kernel: two CTAs per SM when the
-// registers allow it and two rings of at least two stages fit (113 KB of
-// shared memory each), else one CTA per SM with a deeper ring; either way
-// enough page bytes are in flight to keep HBM busy.
+// Ring depth of the split kernel: two CTAs per SM when the registers allow it
+// and two rings of at least two stages fit (113 KB of shared memory each),
+// else one CTA per SM with a deeper ring; either way enough page bytes are in
+// flight to keep HBM busy.  The answer for the last shape asked on each
+// device is kept (one cache per kernel).
 template <auto Kern>
-bool decode_shape(int threads, int fixed, int stage_bytes, int* stages, int* per_sm) {
+bool decode_stages(int threads, int fixed, int stage_bytes, int* stages) {
   constexpr int kTwo = 113 * 1024, kOne = 220 * 1024;
-  // The answer for the last shape asked on each device (one cache per kernel).
   struct Shape {
-    int threads, fixed, stage_bytes, stages, per_sm;
+    int threads, fixed, stage_bytes, stages;
   };
   static std::mutex mu;
   static Shape last[kMaxDevices];
@@ -432,7 +420,6 @@ bool decode_shape(int threads, int fixed, int stage_bytes, int* stages, int* per
     const Shape& c = last[dev];
     if (c.stages > 0 && c.threads == threads && c.fixed == fixed && c.stage_bytes == stage_bytes) {
       *stages = c.stages;
-      *per_sm = c.per_sm;
       return true;
     }
   }
@@ -441,48 +428,52 @@ bool decode_shape(int threads, int fixed, int stage_bytes, int* stages, int* per
   if (st2 > attn::kMaxStages) st2 = attn::kMaxStages;
   if (st2 >= 2 && blocks_per_sm<Kern>(threads, st2 * stage_bytes + fixed) >= 2) {
     *stages = st2;
-    *per_sm = 2;
   } else {
     int st1 = (kOne - fixed) / stage_bytes;
     if (st1 > attn::kMaxStages) st1 = attn::kMaxStages;
     if (st1 < 2) return false;
     *stages = st1;
-    *per_sm = 1;
   }
   std::lock_guard<std::mutex> lock(mu);
-  last[dev] = Shape{threads, fixed, stage_bytes, *stages, *per_sm};
+  last[dev] = Shape{threads, fixed, stage_bytes, *stages};
   return true;
 }
 
 template <int D, int GW, int WPH>
 attn_status launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, attn::DecodeParams p, cudaStream_t stream) {
-  constexpr auto kern = attn::decode_kernel<D, GW, WPH>;
+  constexpr auto ks = attn::decode_split_kernel<D, GW, WPH>;
   const int nw = p.hg * WPH;
   const int threads = (nw + 1) * 32;
-  const int fixed = attn::decode_fixed_bytes(nw, p.chunk, GW);
-  int stages = 0, per_sm = 0;
-  if (!decode_shape<kern>(threads, fixed, p.stage_bytes, &stages, &per_sm)) return ATTN_ERR_LAUNCH;
-  if (kDecodeCtasPerSm == 1 && per_sm == 2) {
-    per_sm = 1;
-    stages = (220 * 1024 - fixed) / p.stage_bytes;
-    if (stages > attn::kMaxStages) stages = attn::kMaxStages;
-  }
+  // scores, the ring's barriers and the slack for aligning the base
+  const int fixed = nw * p.chunk * GW * 4 + 2 * attn::kMaxStages * 8 + 1024;
+  int stages = 0;
+  if (!decode_stages<ks>(threads, fixed, p.stage_bytes, &stages)) return ATTN_ERR_LAUNCH;
   p.stages = stages;
   const int smem = stages * p.stage_bytes + fixed;
-  const long long units = static_cast<long long>(p.num_seqs) * p.n_splits * p.ngroups;
-  const long long slots = kDecodePersistent ? static_cast<long long>(per_sm) * sm_count() : units;
-  const unsigned grid = static_cast<unsigned>(units < slots ? units : slots);
-  if (grid == 0) return ATTN_OK;
-  p.sched = nullptr;
-  if (kDecodePersistent) {
-    const attn_status st = sched_slot(&p.sched, &p.sched_tag);
-    if (st != ATTN_OK) return st;
-  }
-  // Epochs run over [1, 2^40 - 2]: never 0 (a reset word) nor all ones.
-  p.epoch = g_decode_epoch.fetch_add(1, std::memory_order_relaxed) % ((1ull << 40) - 2) + 1;
-  kern<<<dim3(grid), threads, smem, stream>>>(mk, mv, p);
+  const long long gx = static_cast<long long>(p.num_seqs) * p.n_splits;
+  if (gx > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
+  ks<<<dim3(static_cast<unsigned>(gx), p.Hkv / p.hg), threads, smem, stream>>>(mk, mv, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (p.n_splits > 1) {
+    // Programmatic dependent launch: the combine grid is scheduled while the
+    // split grid drains and waits (griddepcontrol.wait) for its partials.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_seqs, (p.Hq + 3) / 4);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, attn::decode_combine_kernel<D>, p) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
   return ATTN_OK;
 }
 
@@ -778,7 +769,6 @@ attn_status attn_decode_paged(const void* q, const void* kcache, const void* vca
   if (pl.ws_bytes > 0) {
     p.ws_o = static_cast<float*>(workspace);
     p.ws_lse = static_cast<float*>(workspace) + pl.ws_o_floats;
-    p.ws_cnt = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + pl.ws_cnt_off);
   }
   p.num_seqs = num_seqs;
   p.Hq = Hq;
@@ -790,7 +780,6 @@ attn_status attn_decode_paged(const void* q, const void* kcache, const void* vca
   p.chunk = pl.chunk;
   p.n_splits = pl.n_splits;
   p.hg = pl.hg;
-  p.ngroups = pl.ngroups;
   p.stage_bytes = attn::kBox * pl.hg * d * 2;
   p.o_f32 = o_dtype == ATTN_F32 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -807,7 +796,8 @@ const char* attn_decode_kernel_name(int num_seqs, int Hq, int Hkv, int d, int ma
   static thread_local char buf[96];
   DecodePlan pl;
   if (num_seqs <= 0 || !decode_plan(num_seqs, Hq, Hkv, d, max_seqlen, &pl)) return "";
-  std::snprintf(buf, sizeof(buf), "decode_kernel<%d,%d,%d>", d, pl.gw, pl.wph);
+  std::snprintf(buf, sizeof(buf), "decode_split_kernel<%d,%d,%d>%s", d, pl.gw, pl.wph,
+                pl.n_splits > 1 ? " + decode_combine_kernel" : "");
   return buf;
 }
 

@@ -55,8 +55,8 @@ struct BwdLayout {
   static constexpr int kRowBytes = 2 * 128 * 4;
   static constexpr int kBarOff = kRowOff + 2 * kRowBytes;
   // kv_full, q_full[S], q_empty[S], s_full, dp_full, ds_full, dq_full, dq_free, dkv_done, rows_ready[2],
-  // red_full[2 halves][2 buffers], red_free[2][2]
-  static constexpr int kNumBars = 1 + 2 * STAGES + 6 + 2 + 8;
+  // red_full[2], red_free[2]
+  static constexpr int kNumBars = 1 + 2 * STAGES + 6 + 2 + 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 128;         // the base is checked for 1024-byte alignment
@@ -160,10 +160,10 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* dq_free = dq_full + 1;
   uint64_t* dkv_done = dq_free + 1;
   uint64_t* rows_ready = dkv_done + 1;  // [2]: the item's LSE / D values are in shared memory
-  // dQ tiles leave through the dS region: each half of the weight warps owns
-  // 16 KB of it as two alternating 8 KB staging buffers of [128 rows][16] f32.
-  uint64_t* red_full = rows_ready + 2;  // [half][buffer] a chunk is staged
-  uint64_t* red_free = red_full + 4;    // [half][buffer] the TMA reduce has finished reading it
+  // dQ tiles leave through two 16 KB staging buffers in the dS region, one
+  // per half of the weight warps:
+  uint64_t* red_full = rows_ready + 2;  // [2] a [128 rows][32 columns] f32 chunk is staged
+  uint64_t* red_free = red_full + 2;    // [2] the TMA reduce has finished reading it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
 
   const int warp = threadIdx.x >> 5;
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(dkv_done, 1);
     mbar_init(&rows_ready[0], 128);
     mbar_init(&rows_ready[1], 128);
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&red_full[i], 128);
       mbar_init(&red_free[i], 1);
     }
@@ -337,7 +337,6 @@ __global__ void __launch_bounds__(320, 1)
     const int kj = k0 + row;  // this thread's key
     const int c0 = half * 64; // first query column of this thread's half
     const bool issuer = lane == 0 && quarter == 2;  // the first warp of each half issues its dQ reduces
-    constexpr int kDqCh = D / 32;                    // 16-column dQ chunks per half
     bool ok = true;
     // A query row's -LSE log2(e) (-inf for a row that saw no key: its weights
     // are 0) and D, read one item ahead by the first half.
@@ -389,12 +388,10 @@ __global__ void __launch_bounds__(320, 1)
       const bool masked = !(key_ok && c_lo <= c0 && c_hi >= c0 + 64);
       const uint32_t ds_row = sbase + L::kDSOff + half * (128 * 128) + row * 128;
       if (n > 0) {
-        // This half's part of the dS region held its staging buffers for the
-        // previous item's dQ chunks: their TMA reduces must have finished
-        // reading both.
-        const int g1 = n * kDqCh - 1;  // this half's last staging use of the previous item
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[half * 2 + (g1 & 1)], (g1 >> 1) & 1, 54) &&
-                                         mbar_wait(&red_free[half * 2 + ((g1 - 1) & 1)], ((g1 - 1) >> 1) & 1, 55));
+        // This half's part of the dS region was the staging buffer of its
+        // previous dQ chunks: their TMA reduces must have finished reading it.
+        const int g1 = n * (D / 64) - 1;  // this half's last staging use of the previous item
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[half], g1 & 1, 54));
         if (!ok) break;
       }
 #pragma unroll
@@ -446,62 +443,53 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
 
-      // dQ tile rows (TMEM lane = query row), this half's D/2 columns: read
-      // them out of tensor memory at once (the next dQ product may then
-      // start), scale, and add them into the f32 accumulator 16 columns at a
-      // time: each chunk is staged as [128 rows][16] f32 (64-byte swizzle,
-      // conflict-free row writes) in one of the half's two 8 KB buffers of
-      // the dS region (free: the dQ product has read dS), and the half's
-      // issuing thread adds it with a TMA reduce while the next chunk is staged.
+      // dQ tile rows (TMEM lane = query row), this half's D/2 columns: scale
+      // and add into the accumulator.
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(dq_full, n & 1, 52));
       if (!ok) break;
       tc_fence_after();
-      uint32_t v[D / 2];
-      if constexpr (D == 128) {
-        tmem_ld64(lane_base + L::kColDQ + half * (D / 2), *reinterpret_cast<uint32_t(*)[64]>(v));
-      } else {
-        tmem_ld32(lane_base + L::kColDQ + half * (D / 2), *reinterpret_cast<uint32_t(*)[32]>(v));
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
-#pragma unroll
-      for (int ch = 0; ch < kDqCh; ++ch) {
-        const int g = n * kDqCh + ch;  // this half's running staging use
-        const int bi = half * 2 + (g & 1);
-        if (g >= 2) {
-          // Use g - 2 of this buffer must have been read by its TMA reduce.
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[bi], ((g >> 1) - 1) & 1, 56));
+      // 32 columns at a time: scale, stage as [128 rows][32] f32 (128-byte
+      // swizzle, conflict-free row writes) in this half's 16 KB buffer of the
+      // dS region (free: the dQ product has read dS), and the half's issuing
+      // thread adds the chunk into the f32 accumulator with a TMA reduce.
+      constexpr int kCh = D / 64;  // chunks per half
+#pragma unroll 1
+      for (int ch = 0; ok && ch < kCh; ++ch) {
+        const int g = n * kCh + ch;  // this half's running staging use
+        uint32_t v[32];
+        tmem_ld32(lane_base + L::kColDQ + half * (D / 2) + ch * 32, v);
+        if (ch == kCh - 1) {
+          // This thread's part of the dQ tile is in registers: once every
+          // weight warp got here, the next dQ product may start.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dq_free);
+        }
+        if (ch > 0) {
+          // The previous chunk of this item used the same buffer.
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[half], (g - 1) & 1, 56));
           if (!ok) break;
         }
-        const uint32_t stg = sbase + L::kDSOff + half * (128 * 128) + (g & 1) * (128 * 64) + row * 64;
+        const uint32_t stg = sbase + L::kDSOff + half * (128 * 128) + row * 128;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          st_shared_v4(stg + ((k ^ ((row >> 1) & 3)) << 4), __float_as_uint(__uint_as_float(v[16 * ch + 4 * k]) * p.scale),
-                       __float_as_uint(__uint_as_float(v[16 * ch + 4 * k + 1]) * p.scale),
-                       __float_as_uint(__uint_as_float(v[16 * ch + 4 * k + 2]) * p.scale),
-                       __float_as_uint(__uint_as_float(v[16 * ch + 4 * k + 3]) * p.scale));
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(stg + ((k ^ (row & 7)) << 4), __float_as_uint(__uint_as_float(v[4 * k]) * p.scale),
+                       __float_as_uint(__uint_as_float(v[4 * k + 1]) * p.scale),
+                       __float_as_uint(__uint_as_float(v[4 * k + 2]) * p.scale),
+                       __float_as_uint(__uint_as_float(v[4 * k + 3]) * p.scale));
         fence_proxy_async_smem();
-        mbar_arrive(&red_full[bi]);
+        mbar_arrive(&red_full[half]);
         if (issuer) {
-          if (!mbar_wait(&red_full[bi], (g >> 1) & 1, 57)) {
+          if (!mbar_wait(&red_full[half], g & 1, 57)) {
             ok = false;
           } else {
-            tma_reduce_add_3d(&tmDQ, smem + L::kDSOff + half * (128 * 128) + (g & 1) * (128 * 64),
-                              half * (D / 2) + ch * 16, q0, bh);
+            tma_reduce_add_3d(&tmDQ, smem + L::kDSOff + half * (128 * 128), half * (D / 2) + ch * 32, q0, bh);
             bulk_commit();
-            // Chunks before g have been read once at most one group is pending.
-            bulk_wait_read<1>();
-            // (use g - 1 of the previous item was released after its reduce)
-            if (ch > 0) mbar_arrive(&red_free[half * 2 + ((g - 1) & 1)]);
-            if (ch == kDqCh - 1) {
-              bulk_wait_read<0>();
-              mbar_arrive(&red_free[bi]);
-            }
+            bulk_wait_read<0>();
+            mbar_arrive(&red_free[half]);
           }
         }
         ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok) break;
       }
       if (!ok) break;
     }

@@ -9,13 +9,13 @@ namespace {
 
 size_t bwd_align(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
-// 3-D f32 map over the dQ accumulator [B*Hq][Nq][d]; one box is [128 rows][16
-// columns], 64-byte swizzled (the staging layout of the backward kernel).
+// 3-D f32 map over the dQ accumulator [B*Hq][Nq][d]; one box is [128 rows][32
+// columns], 128-byte swizzled (the staging layout of the backward kernel).
 bool encode_dq_map(CUtensorMap* map, void* base, int d, int rows, int heads) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(rows) * d * 4};
-  cuuint32_t box[3] = {16, 128, 1};
-  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+  cuuint32_t box[3] = {32, 128, 1};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int D, int STAGES>

@@ -396,10 +396,10 @@ def main(argv=None):
     if not args.no_extra and rank == 0:
         extra = per_config_table(abi, dev, stream, peaks, with_cpu=not args.no_cpu_baseline)
 
-    # Decode time floor: traffic at the measured bandwidth plus the launch and
-    # one DRAM round trip the stage cannot avoid.
+    # Decode time floor: traffic at the measured bandwidth plus the launches
+    # and one DRAM round trip the split/combine stage cannot avoid.
     launch_s, dram_s = launch_and_latency_floor(dev, stream, abi)
-    dec_kernels = 1  # the merge of chunk partials runs inside the one decode kernel
+    dec_kernels = 2 if ws_bytes > 0 else 1  # split kernel (+ combine when sequences span chunks)
     dec_floor = dec_bytes / (peaks.hbm_gbs * 1e9) + dec_kernels * launch_s + dram_s
 
     cpu = None

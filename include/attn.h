@@ -261,9 +261,9 @@ ATTN_API size_t attn_decode_workspace_size(int num_seqs, int Hq, int Hkv, int d,
 /*
  * Paged decode: one query row per sequence and query head against that
  * sequence's cached keys/values, split over key chunks whose partial states
- * are merged by the online-softmax monoid.  One kernel: a persistent grid
- * streams the chunks, and the chunk that completes a sequence merges its
- * partials (sequences that fit one chunk are written directly).
+ * are merged by the online-softmax monoid (a split kernel, then a combine
+ * kernel launched as its programmatic dependent; sequences that fit one chunk
+ * are finished by the split kernel).
  * Source: "Don't Write Kernels, Derive Them", section "What happened" (paged
  * KV-cache access, logsumexp); "Tang: a compiler that derives GPU kernels and
  * bounds how fast they can run", abstract (online softmax as a monoid; decode
@@ -279,14 +279,10 @@ ATTN_API size_t attn_decode_workspace_size(int num_seqs, int Hq, int Hkv, int d,
  *   max_seqlen:  host-side upper bound of seqlens (sizes the work split)
  *   scale:       as for attn_fwd: finite and > 0
  *   workspace:   device scratch of at least attn_decode_workspace_size() bytes,
- *                16-byte aligned, owned by the caller, contents ignored (the
- *                merge counters it holds are tagged with a per-call epoch, and
- *                each call leaves them reset); it must not be shared by two
- *                calls that overlap on the GPU.
+ *                16-byte aligned, owned by the caller, contents ignored; it
+ *                must not be shared by two calls that overlap on the GPU.
  * Hq / Hkv (query heads per key/value head) must be 1, 2, 4, 8 or 16.  The
- * query row attends every cached token (no mask).  Work is handed out from a
- * counter slot of the ring described at attn_fwd, with the same rules for
- * calls in flight and for CUDA graphs.
+ * query row attends every cached token (no mask).
  */
 ATTN_API attn_status attn_decode_paged(const void* q, const void* kcache, const void* vcache,
                               const int32_t* block_table, const int32_t* seqlens,
@@ -372,9 +368,9 @@ ATTN_API int attn_abi_version(void);
  * kernel a profile or a roofline figure belongs to). */
 ATTN_API const char* attn_fwd_kernel_name(int B, int Hq, int Nq, int d);
 
-/* The kernel instantiation attn_decode_paged() launches for these sizes, e.g.
- * "decode_kernel<128,4,1>" (head dim, query heads per warp, warps per
- * key/value head); "" for sizes it rejects.  Thread-local storage as for
+/* The kernels attn_decode_paged() launches for these sizes, e.g.
+ * "decode_split_kernel<128,4,1> + decode_combine_kernel" (head dim, query
+ * heads per warp, warps per key/value head); "" for sizes it rejects.  Thread-local storage as for
  * attn_fwd_kernel_name.  The pages have no counterpart (a measurement
  * convenience). */
 ATTN_API const char* attn_decode_kernel_name(int num_seqs, int Hq, int Hkv, int d, int max_seqlen);

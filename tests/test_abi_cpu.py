@@ -164,20 +164,19 @@ def test_decode_workspace_size_is_a_pure_plan(abi):
     ws = abi.attn_decode_workspace_size
     up = lambda n: (n + 255) // 256 * 256
 
-    def expect(S, Hq, splits, d, groups, warps):
-        # split partials (d + 1 floats per query head and split), then one
-        # 8-byte merge counter per (sequence, head group, compute warp)
-        return up(up(S * splits * Hq * (d + 1) * 4) + S * groups * warps * 8)
-    # 64 sequences x 8 kv heads: one 8-head group per work item, 256-token
-    # chunks, ceil(8192 / 256) = 32 splits; 8 compute warps.
-    assert ws(64, 32, 8, 128, 8192) == expect(64, 32, 32, 128, 1, 8)
+    def expect(S, Hq, splits, d):
+        # split partials: d + 1 floats per sequence, split and query head
+        return up(S * splits * Hq * (d + 1) * 4)
+    # 64 sequences x 8 kv heads: one 8-head group per CTA, 256-token chunks,
+    # ceil(8192 / 256) = 32 splits.
+    assert ws(64, 32, 8, 128, 8192) == expect(64, 32, 32, 128)
     # a sequence that fits one chunk needs no partials
     assert ws(4096, 32, 8, 128, 256) == 0
     assert ws(1, 32, 8, 128, 0) == 0
     # few sequences: smaller chunks to fill the GPU, more splits
-    assert ws(1, 8, 8, 128, 4096) == expect(1, 8, 64, 128, 1, 8)
-    # a group of 16 query heads: two warps per kv head, so 4 kv heads per item
-    assert ws(64, 64, 4, 128, 8192) == expect(64, 64, 32, 128, 1, 8)
+    assert ws(1, 8, 8, 128, 4096) == expect(1, 8, 64, 128)
+    # a group of 16 query heads: two warps per kv head, 4 kv heads per CTA
+    assert ws(64, 64, 4, 128, 8192) == expect(64, 64, 32, 128)
     assert ws(4, 30, 8, 128, 512) == 0          # invalid -> 0
     assert ws(4, 32, 8, 96, 512) == 0
     assert ws(4, 128, 4, 128, 512) == 0         # group of 32
@@ -185,9 +184,11 @@ def test_decode_workspace_size_is_a_pure_plan(abi):
 
 
 def test_decode_kernel_name_follows_the_plan(abi):
-    assert abi.attn_decode_kernel_name(64, 32, 8, 128, 8192) == "decode_kernel<128,4,1>"
-    assert abi.attn_decode_kernel_name(8, 64, 4, 64, 1000) == "decode_kernel<64,8,2>"
-    assert abi.attn_decode_kernel_name(8, 8, 8, 256, 1000) == "decode_kernel<256,1,1>"
+    combine = " + decode_combine_kernel"
+    assert abi.attn_decode_kernel_name(64, 32, 8, 128, 8192) == "decode_split_kernel<128,4,1>" + combine
+    assert abi.attn_decode_kernel_name(8, 64, 4, 64, 1000) == "decode_split_kernel<64,8,2>" + combine
+    assert abi.attn_decode_kernel_name(8, 8, 8, 256, 1000) == "decode_split_kernel<256,1,1>" + combine
+    assert abi.attn_decode_kernel_name(4096, 32, 8, 128, 256) == "decode_split_kernel<128,4,1>"
     assert abi.attn_decode_kernel_name(8, 24, 8, 128, 1000) == ""
 
 
