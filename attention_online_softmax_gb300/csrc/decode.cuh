@@ -214,12 +214,23 @@ __global__ void __launch_bounds__(288, (GW <= 4 && D <= 128) ? 2 : 1)
           const uint4 w = ld_shared_v4(kb + slot * slot_stride);
           const float k8[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
                                bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+          if constexpr (GW == 1) {
+            float a = qf[0][0] * k8[0];
 #pragma unroll
-          for (int g = 0; g < GW; ++g) {
-            float a = qf[g][0] * k8[0];
+            for (int e = 1; e < 8; ++e) a = fmaf(qf[0][e], k8[e], a);
+            part[r] = a;
+          } else {
+            // Two query heads per paired f32x2 multiply-add (the same
+            // operations, in the same order, as one head at a time).
 #pragma unroll
-            for (int e = 1; e < 8; ++e) a = fmaf(qf[g][e], k8[e], a);
-            part[r * GW + g] = a;
+            for (int g = 0; g < GW; g += 2) {
+              float a0, a1;
+              fmul2(a0, a1, qf[g][0], qf[g + 1][0], k8[0], k8[0]);
+#pragma unroll
+              for (int e = 1; e < 8; ++e) ffma2(a0, a1, qf[g][e], qf[g + 1][e], k8[e], k8[e], a0, a1);
+              part[r * GW + g] = a0;
+              part[r * GW + g + 1] = a1;
+            }
           }
         }
         lane_reduce<S::NV, S::LPT, S::SCAT, S::LEVELS>(part, lane);
@@ -284,7 +295,8 @@ __global__ void __launch_bounds__(288, (GW <= 4 && D <= 128) ? 2 : 1)
 #pragma unroll
           for (int g = 0; g < GW; ++g)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pg[g], v8[e], acc[g][e]);
+            for (int e = 0; e < 8; e += 2)
+              ffma2(acc[g][e], acc[g][e + 1], pg[g], pg[g], v8[e], v8[e + 1], acc[g][e], acc[g][e + 1]);
         }
       }
       __syncwarp();
