@@ -54,7 +54,7 @@ DECODE = DecodeConfig("paged_gqa32to8_decode_64seq_d128_len512to8192", 64, 32, 8
 
 PREFILL_CONFIGS = (TINY, BLOCK, LONG, LONG_K4, GQA256)
 # Workloads whose backward is timed (the forward's O and LSE as inputs).
-BWD_CONFIGS = (LONG,)
+BWD_CONFIGS = (LONG, GQA256)
 
 # Additive-bias workloads ("Compilers and Kernels": S = Q K^T / sqrt(d) + C).
 WINDOW = PrefillConfig("causal_window1024_b2_h32_n4096_d128", 2, 32, 32, 4096, 4096, 128, True, 5,

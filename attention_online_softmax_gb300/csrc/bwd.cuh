@@ -74,9 +74,10 @@ struct BwdLayout {
   static_assert(D == 64 || D == 128, "backward head dims");
 };
 
-// D[r] = sum_c O[r][c] dO[r][c] (f32) and the dQ accumulator zeroed; one warp per row.
+// D[r] = sum_c O[r][c] dO[r][c] (f32), one warp per row, and the dQ
+// accumulator (zero4 float4 words, whatever its layout) zeroed.
 __global__ void bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, float* Dsum, float* dq_acc, long long rows,
-                                int d) {
+                                int d, long long zero4) {
   const int lane = threadIdx.x & 31;
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
@@ -91,14 +92,14 @@ __global__ void bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, float* 
         acc = fmaf(bf16lo(aw[e]), bf16lo(bw[e]), acc);
         acc = fmaf(bf16hi(aw[e]), bf16hi(bw[e]), acc);
       }
-      float4* z = reinterpret_cast<float4*>(dq_acc + r * d + c);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
     if (lane == 0) Dsum[r] = acc;
   }
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    reinterpret_cast<float4*>(dq_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // dq = dq_acc as bf16 (RNE) or f32.

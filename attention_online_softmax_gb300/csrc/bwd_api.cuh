@@ -4,6 +4,7 @@
 #pragma once
 
 #include "bwd.cuh"
+#include "bwd_wide.cuh"
 
 namespace {
 
@@ -33,14 +34,51 @@ attn_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
   return ATTN_OK;
 }
 
+// d = 256: the f32 dQ accumulator is kept transposed, [B*Hq][256][ld] with
+// ld = Nq rounded up to 4 (16-byte rows); one box is [128 head-dim rows][32
+// queries], 128-byte swizzled.
+int bwd_wide_ld(int Nq) { return (Nq + 3) & ~3; }
+
+bool encode_dqt_map(CUtensorMap* map, void* base, int Nq, int ld, int heads) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(Nq), 256, static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, static_cast<cuuint64_t>(ld) * 256 * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+attn_status launch_bwd_wide(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                            const CUtensorMap& mdo, const CUtensorMap& mdqt, const attn::BwdParams& p,
+                            cudaStream_t stream) {
+  using L = attn::BwdWideLayout;
+  if (!ensure_smem<attn::attn_bwd_wide_kernel>(L::kAlloc)) return ATTN_ERR_LAUNCH;
+  // Two CTAs (head-dim halves) per (key tile, batch, kv head), key tile 0 first.
+  const long long grid = 2LL * p.B * p.Hkv * ((p.Nk + 127) / 128);
+  if (grid > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
+  if (grid == 0) return ATTN_OK;
+  attn::attn_bwd_wide_kernel<<<dim3(static_cast<unsigned>(grid)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mdo,
+                                                                                                   mdqt, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return ATTN_OK;
+}
+
+// Bytes of the f32 dQ accumulator for head dim d.
+size_t bwd_acc_bytes(int B, int Hq, int Nq, int d) {
+  const size_t bh = static_cast<size_t>(B) * Hq;
+  return d == 256 ? bh * 256 * static_cast<size_t>(bwd_wide_ld(Nq)) * sizeof(float)
+                  : bh * static_cast<size_t>(Nq) * d * sizeof(float);
+}
+
+bool bwd_head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
+
 }  // namespace
 
 extern "C" {
 
 size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int d) {
-  if (B < 0 || Hq <= 0 || Nq < 0 || (d != 64 && d != 128)) return 0;
+  if (B < 0 || Hq <= 0 || Nq < 0 || !bwd_head_dim_ok(d)) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * Nq;
-  return bwd_align(rows * sizeof(float)) + bwd_align(rows * d * sizeof(float));
+  return bwd_align(rows * sizeof(float)) + bwd_align(bwd_acc_bytes(B, Hq, Nq, d));
 }
 
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -51,7 +89,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (grad_dtype != ATTN_BF16 && grad_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!bwd_head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * Hq > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || (Nq == 0 && Nk == 0)) return ATTN_OK;
   if (Nq > 0 && (!aligned16(q) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) || !aligned16(dq)))
@@ -71,7 +109,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
     const long long blocks = std::min<long long>((static_cast<long long>(rows) + 7) / 8, 8LL * sms);
     attn::bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), dsum, dq_acc,
-        static_cast<long long>(rows), d);
+        static_cast<long long>(rows), d, static_cast<long long>(bwd_acc_bytes(B, Hq, Nq, d) / 16));
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }
@@ -83,13 +121,16 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
     const void* db = Nq > 0 ? dout : k;
     const int nq_map = Nq > 0 ? Nq : Nk;
     const int bh_map = Nq > 0 ? B * Hq : B * Hkv;
-    if (!encode_rows_map(&mq, qb, d, nq_map, bh_map, 128) || !encode_rows_map(&mdo, db, d, nq_map, bh_map, 128) ||
+    const int qbox = d == 256 ? attn::BwdWideLayout::kBQ : 128;
+    if (!encode_rows_map(&mq, qb, d, nq_map, bh_map, qbox) || !encode_rows_map(&mdo, db, d, nq_map, bh_map, qbox) ||
         !encode_rows_map(&mk, k, d, Nk, B * Hkv, 128) || !encode_rows_map(&mv, v, d, Nk, B * Hkv, 128))
       return ATTN_ERR_LAUNCH;
     // With Nq == 0 no dQ chunk is ever written; the map then describes one row.
-    if (!encode_dq_map(&mdq, Nq > 0 ? static_cast<void*>(dq_acc) : workspace, d, Nq > 0 ? Nq : 1,
-                       Nq > 0 ? B * Hq : 1))
-      return ATTN_ERR_LAUNCH;
+    void* acc_base = Nq > 0 ? static_cast<void*>(dq_acc) : workspace;
+    const bool acc_ok = d == 256 ? encode_dqt_map(&mdq, acc_base, Nq > 0 ? Nq : 1, bwd_wide_ld(Nq > 0 ? Nq : 1),
+                                                  Nq > 0 ? B * Hq : 1)
+                                 : encode_dq_map(&mdq, acc_base, d, Nq > 0 ? Nq : 1, Nq > 0 ? B * Hq : 1);
+    if (!acc_ok) return ATTN_ERR_LAUNCH;
     attn::BwdParams p;
     p.dk = dk;
     p.dv = dv;
@@ -105,11 +146,21 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
     p.g_f32 = grad_dtype == ATTN_F32 ? 1 : 0;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
-    st = d == 64 ? launch_bwd<64, 3>(mq, mk, mv, mdo, mdq, p, s) : launch_bwd<128, 2>(mq, mk, mv, mdo, mdq, p, s);
+    st = d == 64    ? launch_bwd<64, 3>(mq, mk, mv, mdo, mdq, p, s)
+         : d == 128 ? launch_bwd<128, 2>(mq, mk, mv, mdo, mdq, p, s)
+                    : launch_bwd_wide(mq, mk, mv, mdo, mdq, p, s);
     if (st != ATTN_OK) return st;
   }
 
-  if (rows > 0) {
+  if (rows > 0 && d == 256) {
+    // Transpose the [bh][d][q] accumulator back to dQ[bh][q][d].
+    const dim3 grid(static_cast<unsigned>((Nq + 31) / 32), 256 / 32,
+                    static_cast<unsigned>(std::min<long long>(static_cast<long long>(B) * Hq, 65535)));
+    attn::bwd_post_transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(dq_acc, dq, B * Hq, Nq, bwd_wide_ld(Nq), 256,
+                                                                  grad_dtype == ATTN_F32 ? 1 : 0);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  } else if (rows > 0) {
     const long long n4 = static_cast<long long>(rows) * d / 4;
     const long long blocks = std::min<long long>((n4 + 255) / 256, 8LL * sms);
     attn::bwd_post_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(dq_acc, dq, n4,

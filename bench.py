@@ -296,7 +296,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-config table")
-    ap.add_argument("--profile", choices=["prefill", "prefill_d256", "tiny", "block", "decode", "bwd", "chunked"],
+    ap.add_argument("--profile", choices=["prefill", "prefill_d256", "tiny", "block", "decode", "bwd", "bwd_d256", "chunked"],
                     default=None,
                     help="run one kernel of the step a few times (for an ncu capture) and exit")
     args = ap.parse_args(argv)
@@ -455,14 +455,15 @@ def profile_one(which: str, launches: int = 3) -> int:
     from attention_online_softmax_gb300 import build
     build.build()
     from attention_online_softmax_gb300 import abi
-    if which.startswith("prefill") or which in ("bwd", "tiny", "block"):
-        c = {"prefill_d256": configs.GQA256, "tiny": configs.TINY, "block": configs.BLOCK}.get(which, configs.LONG)
+    if which.startswith("prefill") or which in ("bwd", "bwd_d256", "tiny", "block"):
+        c = {"prefill_d256": configs.GQA256, "bwd_d256": configs.GQA256, "tiny": configs.TINY,
+             "block": configs.BLOCK}.get(which, configs.LONG)
         x = make_prefill_inputs(c)
         q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
         o = torch.empty_like(q)
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-        if which == "bwd":
-            # The backward of the long causal MHA workload (its forward once first).
+        if which.startswith("bwd"):
+            # The backward of a long causal workload (its forward once first).
             abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale)
             g = torch.Generator().manual_seed(c.seed + 50)
             dout = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(dev)
@@ -742,12 +743,25 @@ def cpu_chunked(c, x, q_lens, k_lens):
 
 def cpu_bwd(c, x, dout):
     import oracle
-    # One (batch, head) slice: for MHA the workload is B*Hq independent copies of it.
+    # One query head with its kv head.  For causal Nq == Nk only the first
+    # n0 rows are run: that prefix is the same computation for its rows (a
+    # row sees only keys up to itself).  Extrapolated to the workload by
+    # allowed (query, key) pairs.
+    n0 = min(c.Nq, 4096 if c.d <= 128 else 2048) if (c.causal and c.Nq == c.Nk) else c.Nq
+    nk0 = n0 if (c.causal and c.Nq == c.Nk) else c.Nk
+    sl = (slice(0, 1), slice(0, 1), slice(0, n0))
+    slk = (slice(0, 1), slice(0, 1), slice(0, nk0))
     t0 = time.perf_counter()
-    _, _, _, th = oracle.attention_bwd(x.q[:1, :1], x.k[:1, :1], x.v[:1, :1], dout[:1, :1], c.causal, x.scale)
+    _, _, _, th = oracle.attention_bwd(x.q[sl].contiguous(), x.k[slk].contiguous(), x.v[slk].contiguous(),
+                                       dout[sl].contiguous(), c.causal, x.scale)
     t = time.perf_counter() - t0
-    return {"kind": "oracle", "cores": th, "seconds": t, "sample": "one (batch, head) slice of the workload",
-            "extrapolated_full_s": t * c.B * c.Hq, "extrapolation": "slice time x B*Hq (independent heads)"}
+
+    def pairs(nq, nk):
+        return nq * (nq + 1) / 2 if (c.causal and nq == nk) else nq * nk
+    full = t * c.B * c.Hq * pairs(c.Nq, c.Nk) / pairs(n0, nk0)
+    sample = "one (batch, query head) slice" + (f", its first {n0} rows" if n0 < c.Nq else "")
+    return {"kind": "oracle", "cores": th, "seconds": t, "sample": sample,
+            "extrapolated_full_s": full, "extrapolation": "sample time x (all allowed pairs / sampled pairs)"}
 
 
 def _row(t, p10, p90, fl, by, peaks, cpu, **extra):
@@ -802,7 +816,7 @@ def per_config_table(abi, dev, stream, peaks, reps: int = 30, with_cpu: bool = T
         out[c.name] = _row(t, p10, p90, fl, by, peaks, cpu_prefill(c, x) if with_cpu else None,
                            flops="4 d per allowed (query, key) pair")
         del q, k, v, o, lse, slopes, bias
-    # Backward of the long causal MHA workload (forward output and LSE as inputs).
+    # Backward of the long causal workloads (forward output and LSE as inputs).
     for c in configs.BWD_CONFIGS:
         x = make_prefill_inputs(c)
         q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
@@ -819,7 +833,7 @@ def per_config_table(abi, dev, stream, peaks, reps: int = 30, with_cpu: bool = T
             stream, flush, reps)
         fl = 2.5 * roofline.prefill_flops(c.B, c.Hq, c.Nq, c.Nk, c.d, c.causal)
         by = roofline.bwd_bytes(c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d)
-        cpu = cpu_bwd(c, x, dout_h) if with_cpu and c.Hq == c.Hkv else None
+        cpu = cpu_bwd(c, x, dout_h) if with_cpu else None
         out["bwd_" + c.name] = _row(t, p10, p90, fl, by, peaks, cpu,
                                     flops="5 products of 2 N^2 d per head = 2.5x the forward's")
         del q, k, v, o, lse, dout, dq, dk, dv, ws

@@ -81,6 +81,9 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
             lib.oracle_attention_bwd.argtypes = [p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float,
                                                  p, p, p, i]
             lib.oracle_attention_bwd.restype = i
+            lib.oracle_attention_bwd_dq_rows.argtypes = [p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float,
+                                                         p, i64, p, i]
+            lib.oracle_attention_bwd_dq_rows.restype = i
             _LIBS[mutant] = lib
         return lib
 
@@ -230,6 +233,26 @@ def attention_bwd(q, k, v, dout, causal: bool, scale: float, threads: int = 0, m
     if rc < 0:
         raise ValueError(f"oracle_attention_bwd rejected its arguments ({rc})")
     return dq, dk, dv, rc
+
+
+def attention_bwd_dq_rows(q, k, v, dout, causal: bool, scale: float, rows, threads: int = 0):
+    """dQ of the listed flat query rows ((b * Hq + h) * Nq + i) only, by the
+    same per-row steps as attention_bwd (see oracle_attention_bwd_dq_rows in
+    attn_oracle.c), float64: [len(rows), d].  Costs one row's keys per row.
+    """
+    qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
+    B, Hq, Nq, d = qb.shape
+    _, Hkv, Nk, _ = kb.shape
+    if gb.shape != qb.shape or vb.shape != kb.shape:
+        raise ValueError("q/dout or k/v shape mismatch")
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.empty((r.shape[0], d), dtype=np.float64)
+    rc = _load().oracle_attention_bwd_dq_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), B, Hq, Hkv, Nq, Nk, d,
+                                              int(bool(causal)), float(scale), _ptr(r), int(r.shape[0]),
+                                              _ptr(out), int(threads))
+    if rc < 0:
+        raise ValueError(f"oracle_attention_bwd_dq_rows rejected its arguments ({rc})")
+    return out
 
 
 def prefill_paged(q, kcache, vcache, block_table, cu_seqlens_q, seqlens_k, causal: bool,

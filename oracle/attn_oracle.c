@@ -617,3 +617,91 @@ int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v
     }
     return nthreads;
 }
+
+/*
+ * dQ for selected query rows only, by the per-row steps of
+ * oracle_attention_bwd above (the weights of the row from its scores, its
+ * output, D = dO . O, dP = dO V^T over the row's keys, dQ = scale * sum_j
+ * P_j (dP_j - D) K_j): rows[r] = (b * Hq + h) * Nq + i, out[r][d].  The
+ * cost is one row's keys per row, so rows of a long sequence can be checked
+ * one by one.  Returns the threads used, or -1 on invalid arguments.
+ */
+int oracle_attention_bwd_dq_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                                 int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                                 const int64_t* rows, int64_t nrows, double* out, int threads) {
+    const double sc = (double)scale;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || d <= 0 || nrows < 0) return -1;
+    {
+        int64_t r;
+        for (r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= (int64_t)B * Hq * Nq) return -1;
+    }
+    const int group = Hq / Hkv;
+    int nthreads = 1;
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+#endif
+#pragma omp parallel
+    {
+#ifdef _OPENMP
+#pragma omp single
+        nthreads = omp_get_num_threads();
+#endif
+        double* p = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        double* dp = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        double* o = (double*)malloc(sizeof(double) * (size_t)d);
+        int64_t r;
+#pragma omp for schedule(dynamic, 1)
+        for (r = 0; r < nrows; ++r) {
+            const int64_t row = rows[r];
+            const int64_t bh = row / Nq, i = row % Nq;
+            const int64_t b = bh / Hq, h = bh % Hq, g = h / group;
+            const uint16_t* kb = k + (b * Hkv + g) * (int64_t)Nk * d;
+            const uint16_t* vb = v + (b * Hkv + g) * (int64_t)Nk * d;
+            const uint16_t* qi = q + row * d;
+            const uint16_t* doi = dout + row * d;
+            double* dqi = out + r * d;
+            int64_t n = Nk, j;
+            int c;
+            for (c = 0; c < d; ++c) dqi[c] = 0.0;
+            if (causal) {
+                n = i + (int64_t)Nk - (int64_t)Nq + 1;
+                if (n < 0) n = 0;
+                if (n > Nk) n = Nk;
+            }
+            if (n == 0) continue;
+            double m = -INFINITY;
+            for (j = 0; j < n; ++j) {
+                double s = 0.0;
+                for (c = 0; c < d; ++c) s += bf16_to_double(qi[c]) * bf16_to_double(kb[j * d + c]);
+                p[j] = s * sc;
+                if (p[j] > m) m = p[j];
+            }
+            double l = 0.0;
+            for (j = 0; j < n; ++j) {
+                p[j] = exp(p[j] - m);
+                l += p[j];
+            }
+            for (c = 0; c < d; ++c) o[c] = 0.0;
+            for (j = 0; j < n; ++j) {
+                p[j] /= l;
+                for (c = 0; c < d; ++c) o[c] += p[j] * bf16_to_double(vb[j * d + c]);
+            }
+            double D = 0.0;
+            for (c = 0; c < d; ++c) D += bf16_to_double(doi[c]) * o[c];
+            for (j = 0; j < n; ++j) {
+                double s = 0.0;
+                for (c = 0; c < d; ++c) s += bf16_to_double(doi[c]) * bf16_to_double(vb[j * d + c]);
+                dp[j] = s;
+            }
+            for (j = 0; j < n; ++j) {
+                const double ds = p[j] * (dp[j] - D);
+                for (c = 0; c < d; ++c) dqi[c] += sc * ds * bf16_to_double(kb[j * d + c]);
+            }
+        }
+        free(p);
+        free(dp);
+        free(o);
+    }
+    return nthreads;
+}

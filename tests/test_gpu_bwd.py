@@ -91,6 +91,13 @@ SHAPES = [
     (1, 2, 1, 300, 77, 128, True),      # Nq > Nk: rows without keys
     (1, 8, 2, 256, 384, 64, False),     # GQA 4:1, several key tiles
     (2, 4, 4, 640, 640, 128, True),
+    # d = 256: two CTAs per key tile (head-dim halves), 64-query items.
+    (1, 2, 2, 128, 128, 256, False),
+    (1, 2, 2, 200, 200, 256, True),     # ragged
+    (2, 4, 2, 77, 300, 256, True),      # Nq < Nk (Nq not a multiple of 4), GQA
+    (1, 2, 1, 300, 77, 256, True),      # Nq > Nk: rows without keys
+    (1, 8, 2, 256, 384, 256, False),    # GQA 4:1, several key tiles
+    (1, 4, 1, 640, 640, 256, True),
 ]
 
 
@@ -152,3 +159,37 @@ def test_bwd_full_config_sampled_heads(abi):
         for name, a, r in zip(("dq", "dk", "dv"), got, ref):
             err = np.abs(a[sl] - r)
             assert np.all(err <= grad_bound(r, False)), (name, b, h, err.max())
+
+
+def test_bwd_d256_gqa_shape_shorter(abi):
+    # The long d = 256 workload's head layout (B1, 16 query heads on 2 kv
+    # heads, causal) at N = 2048, every gradient element against the oracle.
+    c = configs.GQA256
+    x = inputs.prefill_inputs(c.B, c.Hq, c.Hkv, 2048, 2048, c.d, seed=c.seed + 60, causal=c.causal)
+    check_bwd(abi, x, seed=c.seed + 61)
+
+
+def test_bwd_d256_full_config_sampled(abi):
+    # The benchmark's d = 256 backward launch (causal GQA B1 Hq16 Hkv2 N16384)
+    # checked on seeded query rows of dQ, which the oracle computes one by
+    # one, and on the closed-form sums over keys that hold at any size:
+    # rows of P sum to 1 (sum_j dV_j = sum of dO over the rows that see a
+    # key) and rows of dS sum to 0 (sum_j dK_j = 0).
+    c = configs.GQA256
+    x = inputs.prefill_inputs(c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.seed, c.causal)
+    g = torch.Generator().manual_seed(c.seed + 50)
+    dout = torch.randn(x.q.shape, generator=g).to(torch.bfloat16)
+    dq, dk, dv = run_bwd(abi, x, dout, torch.float32)
+    rows = np.random.default_rng(c.seed + 51).choice(c.B * c.Hq * c.Nq, size=96, replace=False)
+    ref = oracle.attention_bwd_dq_rows(x.q, x.k, x.v, dout, True, x.scale, rows)
+    got = dq.reshape(-1, c.d)[rows]
+    assert np.all(np.abs(got - ref) <= grad_bound(ref, False)), np.abs(got - ref).max()
+    # Sums over keys, per (batch, kv head, column).  The kernel rounds P and
+    # dS to bf16 (2^-9 relative): the sums carry about 2^-9 of the summed
+    # magnitudes, which the bounds below allow four times over.
+    go = dout.double().numpy().reshape(c.B, c.Hkv, c.Hq // c.Hkv, c.Nq, c.d)
+    want_dv = go.sum(axis=(2, 3))   # causal with Nq == Nk: every row sees a key
+    tol_dv = 2.0 ** -7 * np.abs(dv).sum(axis=2) + 1e-3
+    assert np.all(np.abs(dv.sum(axis=2) - want_dv) <= tol_dv), np.abs(dv.sum(axis=2) - want_dv).max()
+    tol_dk = 2.0 ** -7 * np.abs(dk).sum(axis=2) + 1e-3
+    assert np.all(np.abs(dk.sum(axis=2)) <= tol_dk), np.abs(dk.sum(axis=2)).max()

@@ -143,3 +143,39 @@ def test_planted_backward_mistakes_are_caught(mutant):
     agree = (np.allclose(dq, q.grad.numpy(), atol=1e-9) and np.allclose(dk, k.grad.numpy(), atol=1e-9)
              and np.allclose(dv, v.grad.numpy(), atol=1e-9))
     assert not agree
+
+
+@pytest.mark.parametrize("causal,shape", [(False, (1, 2, 1, 5, 6, 4)), (True, (1, 2, 2, 6, 6, 4)),
+                                          (True, (1, 1, 1, 7, 4, 3))])
+def test_bwd_dq_rows_match_finite_differences(causal, shape):
+    # The per-row dQ function against central differences of the plain
+    # forward, on every row (rows without keys included).
+    B, Hq, Hkv, Nq, Nk, d = shape
+    x = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, seed=60 + Nq, causal=causal)
+    dout = dout_for((B, Hq, Nq, d), 61)
+    rows = np.arange(B * Hq * Nq)
+    got = oracle.attention_bwd_dq_rows(x.q, x.k, x.v, dout, causal, x.scale, rows)
+    q, k, v, go = bf16_np(x.q), bf16_np(x.k), bf16_np(x.v), bf16_np(dout)
+    h = 1e-6
+    rng = np.random.default_rng(5)
+    for r in rows:
+        c = int(rng.integers(0, d))
+        idx = np.unravel_index(int(r), (B, Hq, Nq)) + (c,)
+        plus, minus = q.copy(), q.copy()
+        plus[idx] += h
+        minus[idx] -= h
+        fd = (forward_loss(plus, k, v, go, causal, x.scale) - forward_loss(minus, k, v, go, causal, x.scale)) / (2 * h)
+        assert abs(fd - got[r, c]) <= 1e-6 * max(1.0, abs(fd)), (r, c, fd, got[r, c])
+
+
+def test_bwd_dq_rows_equal_the_full_backward():
+    # Sampled rows of a GQA causal case with Nq != Nk, in shuffled order.
+    B, Hq, Hkv, Nq, Nk, d = 2, 4, 2, 37, 53, 16
+    x = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, seed=62, causal=True)
+    dout = dout_for((B, Hq, Nq, d), 63)
+    dq = oracle.attention_bwd(x.q, x.k, x.v, dout, True, x.scale)[0].reshape(-1, d)
+    rows = np.random.default_rng(7).permutation(B * Hq * Nq)[:40]
+    got = oracle.attention_bwd_dq_rows(x.q, x.k, x.v, dout, True, x.scale, rows)
+    np.testing.assert_allclose(got, dq[rows], rtol=0, atol=1e-13)
+    with pytest.raises(ValueError):
+        oracle.attention_bwd_dq_rows(x.q, x.k, x.v, dout, True, x.scale, [B * Hq * Nq])
