@@ -84,6 +84,9 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
             lib.oracle_attention_bwd_dq_rows.argtypes = [p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float,
                                                          p, i64, p, i]
             lib.oracle_attention_bwd_dq_rows.restype = i
+            lib.oracle_attention_masked_bwd.argtypes = [p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float,
+                                                        i, p, p, i64, i64, p, p, p, i]
+            lib.oracle_attention_masked_bwd.restype = i
             _LIBS[mutant] = lib
         return lib
 
@@ -232,6 +235,36 @@ def attention_bwd(q, k, v, dout, causal: bool, scale: float, threads: int = 0, m
                                       int(threads))
     if rc < 0:
         raise ValueError(f"oracle_attention_bwd rejected its arguments ({rc})")
+    return dq, dk, dv, rc
+
+
+def attention_masked_bwd(q, k, v, dout, causal: bool, scale: float, window_left: int = 0, alibi=None,
+                         bias=None, bias_strides=(0, 0), threads: int = 0):
+    """Gradients (dQ, dK, dV) of attention_masked's output for the upstream
+    gradient dout (see oracle_attention_masked_bwd in attn_oracle.c), float64.
+
+    alibi, bias and bias_strides as in attention_masked.  Returns
+    (dQ [B,Hq,Nq,d], dK [B,Hkv,Nk,d], dV [B,Hkv,Nk,d], threads_used).
+    """
+    qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
+    B, Hq, Nq, d = qb.shape
+    _, Hkv, Nk, _ = kb.shape
+    if gb.shape != qb.shape or vb.shape != kb.shape:
+        raise ValueError("q/dout or k/v shape mismatch")
+    al = None if alibi is None else np.ascontiguousarray(np.asarray(_host(alibi), dtype=np.float32))
+    if al is not None and al.shape != (Hq,):
+        raise ValueError("alibi must have one slope per query head")
+    bb = None if bias is None else _bits(bias).reshape(-1)
+    dq = np.empty((B, Hq, Nq, d), dtype=np.float64)
+    dk = np.empty((B, Hkv, Nk, d), dtype=np.float64)
+    dv = np.empty((B, Hkv, Nk, d), dtype=np.float64)
+    rc = _load().oracle_attention_masked_bwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), B, Hq, Hkv, Nq, Nk, d,
+                                             int(bool(causal)), float(scale), int(window_left),
+                                             None if al is None else _ptr(al), None if bb is None else _ptr(bb),
+                                             int(bias_strides[0]), int(bias_strides[1]), _ptr(dq), _ptr(dk),
+                                             _ptr(dv), int(threads))
+    if rc < 0:
+        raise ValueError(f"oracle_attention_masked_bwd rejected its arguments ({rc})")
     return dq, dk, dv, rc
 
 

@@ -637,16 +637,9 @@ int oracle_attention_bwd_dq_rows(const uint16_t* q, const uint16_t* k, const uin
             if (rows[r] < 0 || rows[r] >= (int64_t)B * Hq * Nq) return -1;
     }
     const int group = Hq / Hkv;
-    int nthreads = 1;
-#ifdef _OPENMP
-    if (threads > 0) omp_set_num_threads(threads);
-#endif
-#pragma omp parallel
+    const int nthreads = oracle_threads(threads);
+#pragma omp parallel num_threads(nthreads)
     {
-#ifdef _OPENMP
-#pragma omp single
-        nthreads = omp_get_num_threads();
-#endif
         double* p = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
         double* dp = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
         double* o = (double*)malloc(sizeof(double) * (size_t)d);
@@ -701,6 +694,110 @@ int oracle_attention_bwd_dq_rows(const uint16_t* q, const uint16_t* k, const uin
         }
         free(p);
         free(dp);
+        free(o);
+    }
+    return nthreads;
+}
+
+/*
+ * Backward of oracle_attention_masked: the same derivative as
+ * oracle_attention_bwd (dV = P^T dO, dS = P * (dP - D), dQ = scale dS K,
+ * dK = scale dS^T Q), with the weights P of the biased scores
+ * S_ij = scale q_i . k_j + C_ij over the keys the causal mask and the left
+ * window allow, C_ij = alibi[h] (j - i - (Nk - Nq)) + bias[b sb + h sh + i Nk + j].
+ * A key whose score is -inf, and every key of a row with no finite score,
+ * takes no gradient.  Layouts and return value as oracle_attention_bwd.
+ */
+int oracle_attention_masked_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                                int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                                int window_left, const float* alibi, const uint16_t* bias, int64_t bias_sb,
+                                int64_t bias_sh, double* dq, double* dk, double* dv, int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0 || d <= 0 || window_left < 0) return -1;
+    if (Hq % Hkv != 0) return -1;
+    const int group = Hq / Hkv;
+    const double sc = (double)scale;
+    nthreads = oracle_threads(nthreads);
+    memset(dq, 0, sizeof(double) * (size_t)B * Hq * Nq * d);
+    memset(dk, 0, sizeof(double) * (size_t)B * Hkv * Nk * d);
+    memset(dv, 0, sizeof(double) * (size_t)B * Hkv * Nk * d);
+    const int64_t pairs = (int64_t)B * Hkv;
+    const int64_t diag = (int64_t)Nk - (int64_t)Nq;
+
+#pragma omp parallel num_threads(nthreads)
+    {
+        const size_t cap = (size_t)(Nk > 0 ? Nk : 1);
+        double* p = (double*)malloc(sizeof(double) * cap);
+        double* dp = (double*)malloc(sizeof(double) * cap);
+        int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * cap);
+        double* o = (double*)malloc(sizeof(double) * (size_t)d);
+        int64_t w;
+        /* one (batch, kv head) per task: its dK and dV rows are written by it alone */
+#pragma omp for schedule(dynamic, 1)
+        for (w = 0; w < pairs; ++w) {
+            const int64_t b = w / Hkv, g = w % Hkv;
+            const uint16_t* kb = k + (b * Hkv + g) * (int64_t)Nk * d;
+            const uint16_t* vb = v + (b * Hkv + g) * (int64_t)Nk * d;
+            double* dkb = dk + (b * Hkv + g) * (int64_t)Nk * d;
+            double* dvb = dv + (b * Hkv + g) * (int64_t)Nk * d;
+            int hh;
+            for (hh = 0; hh < group; ++hh) {
+                const int64_t h = g * group + hh;
+                int64_t i;
+                for (i = 0; i < Nq; ++i) {
+                    const int64_t row = (b * Hq + h) * (int64_t)Nq + i;
+                    const uint16_t* qi = q + row * d;
+                    const uint16_t* doi = dout + row * d;
+                    int64_t n = 0, j, t;
+                    int c;
+                    double m = -INFINITY;
+                    /* the allowed keys of row i and their biased scores */
+                    for (j = 0; j < Nk; ++j) {
+                        if (causal && j > i + diag) continue;
+                        if (window_left > 0 && j <= i + diag - window_left) continue;
+                        double s = 0.0;
+                        for (c = 0; c < d; ++c) s += bf16_to_double(qi[c]) * bf16_to_double(kb[j * d + c]);
+                        s *= sc;
+                        if (alibi) s += (double)alibi[h] * (double)(j - i - diag);
+                        if (bias) s += bf16_to_double(bias[b * bias_sb + h * bias_sh + i * (int64_t)Nk + j]);
+                        keys[n] = j;
+                        p[n] = s;
+                        if (s > m) m = s;
+                        ++n;
+                    }
+                    if (n == 0 || m == -INFINITY) continue;
+                    double l = 0.0;
+                    for (t = 0; t < n; ++t) {
+                        p[t] = exp(p[t] - m);
+                        l += p[t];
+                    }
+                    for (c = 0; c < d; ++c) o[c] = 0.0;
+                    for (t = 0; t < n; ++t) {
+                        p[t] /= l;
+                        for (c = 0; c < d; ++c) o[c] += p[t] * bf16_to_double(vb[keys[t] * d + c]);
+                    }
+                    double D = 0.0;
+                    for (c = 0; c < d; ++c) D += bf16_to_double(doi[c]) * o[c];
+                    for (t = 0; t < n; ++t) {
+                        double s = 0.0;
+                        for (c = 0; c < d; ++c) s += bf16_to_double(doi[c]) * bf16_to_double(vb[keys[t] * d + c]);
+                        dp[t] = s;
+                    }
+                    double* dqi = dq + row * d;
+                    for (t = 0; t < n; ++t) {
+                        const double ds = p[t] * (dp[t] - D);
+                        const int64_t jj = keys[t];
+                        for (c = 0; c < d; ++c) {
+                            dqi[c] += sc * ds * bf16_to_double(kb[jj * d + c]);
+                            dkb[jj * d + c] += sc * ds * bf16_to_double(qi[c]);
+                            dvb[jj * d + c] += p[t] * bf16_to_double(doi[c]);
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+        free(keys);
         free(o);
     }
     return nthreads;
