@@ -47,6 +47,9 @@ _lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
 _lib.attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, ctypes.c_float,
                           _i, _vp, ctypes.c_size_t, _vp]
 _lib.attn_bwd.restype = _i
+_lib.attn_bwd_masked.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                 ctypes.c_float, ctypes.POINTER(AttnMask), _i, _vp, ctypes.c_size_t, _vp]
+_lib.attn_bwd_masked.restype = _i
 _lib.attn_probe_dram_latency.argtypes = [_vp, ctypes.c_size_t, _i, _vp, _vp]
 _lib.attn_probe_dram_latency.restype = _i
 _lib.attn_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
@@ -78,7 +81,7 @@ ATTN_F32 = 1
 
 #: every symbol include/attn.h declares
 EXPORTS = ("attn_fwd", "attn_fwd_masked", "attn_prefill_paged_workspace_size", "attn_prefill_paged",
-           "attn_bwd_workspace_size", "attn_bwd", "attn_probe_dram_latency",
+           "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_masked", "attn_probe_dram_latency",
            "attn_decode_workspace_size", "attn_decode_paged", "attn_decode_paged_static",
            "attn_get_device_status", "attn_selftest_wait_timeout", "attn_status_string",
            "attn_launch_count", "attn_abi_version", "attn_fwd_kernel_name", "attn_decode_kernel_name")
@@ -183,21 +186,7 @@ def attn_fwd_masked(q, k, v, o, lse, causal: bool, scale: float, window_left: in
     _, Hkv, Nk, _ = k.shape
     if tuple(o.shape) != (B, Hq, Nq, d) or tuple(lse.shape) != (B, Hq, Nq) or v.shape != k.shape:
         raise ValueError("shape mismatch between q, k, v, o, lse")
-    m = AttnMask(int(window_left), None, None, 0, 0)
-    if alibi is not None:
-        _need(alibi, torch.float32, "alibi")
-        if alibi.numel() != Hq:
-            raise ValueError("alibi must hold Hq slopes")
-        m.alibi_slopes = alibi.data_ptr()
-    if bias is not None:
-        if bias.dtype != torch.bfloat16 or not bias.is_cuda or bias.dim() != 4:
-            raise TypeError("bias must be a 4-D CUDA bfloat16 tensor")
-        if tuple(bias.shape[2:]) != (Nq, Nk) or (Nk > 1 and bias.stride(3) != 1) or \
-                (Nq > 1 and bias.stride(2) != Nk):
-            raise ValueError("bias must end in contiguous [Nq, Nk]")
-        m.bias = bias.data_ptr()
-        m.bias_stride_b = bias.stride(0) if bias.shape[0] == B else 0
-        m.bias_stride_h = bias.stride(1) if bias.shape[1] == Hq else 0
+    m = _mask_struct(Hq, B, Nq, Nk, window_left, alibi, bias)
     st = _lib.attn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
                               int(bool(causal)), float(scale), ctypes.byref(m),
                               ATTN_F32 if o.dtype == torch.float32 else ATTN_BF16, _stream_ptr(stream))
@@ -245,9 +234,32 @@ def attn_bwd_workspace_size(B: int, Hq: int, Nq: int, d: int) -> int:
     return int(_lib.attn_bwd_workspace_size(int(B), int(Hq), int(Nq), int(d)))
 
 
-def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool, scale: float, workspace=None, stream=None) -> None:
-    """Backward of attn_fwd: dq [B,Hq,Nq,d], dk, dv [B,Hkv,Nk,d] (all bf16 or
-    all f32) from q, k, v, the forward's o and lse, and the upstream dout."""
+def _mask_struct(Hq: int, B: int, Nq: int, Nk: int, window_left: int, alibi, bias):
+    import torch
+    m = AttnMask(int(window_left), None, None, 0, 0)
+    if alibi is not None:
+        _need(alibi, torch.float32, "alibi")
+        if alibi.numel() != Hq:
+            raise ValueError("alibi must hold Hq slopes")
+        m.alibi_slopes = alibi.data_ptr()
+    if bias is not None:
+        if bias.dtype != torch.bfloat16 or not bias.is_cuda or bias.dim() != 4:
+            raise TypeError("bias must be a 4-D CUDA bfloat16 tensor")
+        if tuple(bias.shape[2:]) != (Nq, Nk) or (Nk > 1 and bias.stride(3) != 1) or \
+                (Nq > 1 and bias.stride(2) != Nk):
+            raise ValueError("bias must end in contiguous [Nq, Nk]")
+        m.bias = bias.data_ptr()
+        m.bias_stride_b = bias.stride(0) if bias.shape[0] == B else 0
+        m.bias_stride_h = bias.stride(1) if bias.shape[1] == Hq else 0
+    return m
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool, scale: float, workspace=None, stream=None,
+             window_left: int = 0, alibi=None, bias=None) -> None:
+    """Backward of attn_fwd (or, with window_left / alibi / bias, of
+    attn_fwd_masked with the same bias): dq [B,Hq,Nq,d], dk, dv [B,Hkv,Nk,d]
+    (all bf16 or all f32) from q, k, v, the forward's o and lse, and the
+    upstream dout."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _need(t, torch.bfloat16, n)
@@ -265,10 +277,17 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool, scale: float, work
     need = attn_bwd_workspace_size(B, Hq, Nq, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    gdt = ATTN_F32 if gd == torch.float32 else ATTN_BF16
+    if window_left or alibi is not None or bias is not None:
+        m = _mask_struct(Hq, B, Nq, Nk, window_left, alibi, bias)
+        st = _lib.attn_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
+                                  ctypes.byref(m), gdt, _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+        _check(st, "attn_bwd_masked")
+        return
     st = _lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-                       B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
-                       ATTN_F32 if gd == torch.float32 else ATTN_BF16, _ptr(workspace), workspace.numel(),
-                       _stream_ptr(stream))
+                       B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale), gdt, _ptr(workspace),
+                       workspace.numel(), _stream_ptr(stream))
     _check(st, "attn_bwd")
 
 

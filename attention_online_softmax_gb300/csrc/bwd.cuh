@@ -38,7 +38,58 @@ struct BwdParams {
   int g_f32;           // gradients written as f32 (else bf16)
   float scale;         // > 0
   float scale_log2;    // scale * log2(e)
+  // Additive bias C of the forward (used by the BIAS instantiations only):
+  int window_left;                // > 0: query i keeps keys j > i + (Nk - Nq) - window_left
+  const float* alibi;             // [Hq] slopes or null: C += alibi[h] (j - i - (Nk - Nq))
+  const uint16_t* bias;           // bf16 or null: C += bias[b sb + h sh + i Nk + j]
+  long long bias_sb, bias_sh;
 };
+
+// The bias of one query head for one key row of the backward's weight phase:
+// per query column c of the item, log2(e) * C at (query q0 + c, key kj).
+struct BwdBiasRow {
+  float alibi_l2;        // alibi slope * log2(e) (0 without ALiBi)
+  float alibi_base;      // alibi slope * log2(e) * (kj - (Nk - Nq) - q0)
+  const uint16_t* brow;  // bias + b sb + h sh + q0 Nk + kj, or null
+  long long bstride;     // Nk
+};
+
+__device__ __forceinline__ BwdBiasRow bwd_bias_row(const BwdParams& p, int bh, int q0, int kj) {
+  BwdBiasRow r;
+  const int b = bh / p.Hq, h = bh - b * p.Hq;
+  const float sl = p.alibi ? __ldg(p.alibi + h) * 1.4426950408889634f : 0.f;
+  r.alibi_l2 = sl;
+  r.alibi_base = sl * static_cast<float>(kj - (p.Nk - p.Nq) - q0);
+  r.brow = p.bias ? p.bias + b * p.bias_sb + h * p.bias_sh + static_cast<long long>(q0) * p.Nk + kj : nullptr;
+  r.bstride = p.Nk;
+  return r;
+}
+
+// log2(e) * C at query column c of a key row (the dense bias is read only
+// where the element is allowed).
+__device__ __forceinline__ float bwd_bias_at(const BwdBiasRow& r, int c, bool key_ok, int c_lo, int c_hi) {
+  float v = r.alibi_base - r.alibi_l2 * static_cast<float>(c);
+  if (r.brow != nullptr && key_ok && c >= c_lo && c < c_hi)
+    v += bf16lo(static_cast<uint32_t>(__ldg(r.brow + c * r.bstride))) * 1.4426950408889634f;
+  return v;
+}
+
+// Query tiles [qt_lo, qt_hi) of rows bq whose rows see some key of the key
+// tile [k0, k0 + 128): causal keeps rows i >= k0 - (Nk - Nq), a left window
+// rows i <= min(k0 + 127, Nk - 1) - (Nk - Nq) + window - 1.
+__device__ __forceinline__ void bwd_query_tiles(const BwdParams& p, int k0, int bq, int& qt_lo, int& qt_hi) {
+  const int diag = p.Nk - p.Nq;
+  const int ntq = (p.Nq + bq - 1) / bq;
+  qt_lo = 0;
+  qt_hi = ntq;
+  if (p.causal) qt_lo = max(0, (k0 - diag) / bq);
+  if (p.causal && k0 - diag >= p.Nq) qt_lo = ntq;
+  if (p.window_left > 0) {
+    const int i_max = min(k0 + 127, p.Nk - 1) - diag + p.window_left - 1;
+    qt_hi = i_max < 0 ? 0 : min(ntq, i_max / bq + 1);
+  }
+  if (qt_hi < qt_lo) qt_hi = qt_lo;
+}
 
 template <int D, int STAGES>
 struct BwdLayout {
@@ -132,7 +183,7 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-template <int D, int STAGES>
+template <int D, int STAGES, bool BIAS>
 __global__ void __launch_bounds__(320, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -177,12 +228,9 @@ __global__ void __launch_bounds__(320, 1)
   const int k0 = kt * 128;
   const int G = p.Hq / p.Hkv;
   const int diag = p.Nk - p.Nq;
-  const int ntq = (p.Nq + 127) / 128;
-  // Query tiles whose rows see some key of this tile: i >= k0 - diag when causal.
-  int qt_lo = 0;
-  if (p.causal) qt_lo = max(0, (k0 - diag) / 128);
-  if (p.causal && k0 - diag >= p.Nq) qt_lo = ntq;
-  const int per_head = ntq - qt_lo;
+  int qt_lo, qt_hi;
+  bwd_query_tiles(p, k0, 128, qt_lo, qt_hi);
+  const int per_head = qt_hi - qt_lo;
   const int n_items = G * per_head;
 
   if (threadIdx.x == 0) {
@@ -383,10 +431,13 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       // Query c of the tile is allowed for this key iff c < Nq - q0, and
       // (causal) kj <= q0 + c + diag; tiles wholly inside skip the test.
-      const int c_hi = p.Nq - q0;                               // columns >= c_hi: past Nq
+      int c_hi = p.Nq - q0;                                     // columns >= c_hi: past Nq
       const int c_lo = p.causal ? kj - diag - q0 : -0x7FFFFFFF;  // columns < c_lo: masked
+      if (BIAS && p.window_left > 0) c_hi = min(c_hi, kj - diag + p.window_left - q0);  // left window
       const bool key_ok = kj < p.Nk;
       const bool masked = !(key_ok && c_lo <= c0 && c_hi >= c0 + 64);
+      BwdBiasRow br;
+      if constexpr (BIAS) br = bwd_bias_row(p, bh, q0, kj);
       const uint32_t ds_row = sbase + L::kDSOff + half * (128 * 128) + row * 128;
       if (n > 0) {
         // This half's part of the dS region was the staging buffer of its
@@ -413,6 +464,10 @@ __global__ void __launch_bounds__(320, 1)
           for (int u = 0; u < 4; u += 2) {
             float x0, x1, p0, p1, t0, t1, d0, d1;
             ffma2(x0, x1, __uint_as_float(sv[e + u]), __uint_as_float(sv[e + u + 1]), sl, sl, nl[u], nl[u + 1]);
+            if constexpr (BIAS) {
+              x0 += bwd_bias_at(br, c + u, key_ok, c_lo, c_hi);
+              x1 += bwd_bias_at(br, c + u + 1, key_ok, c_lo, c_hi);
+            }
             p0 = ex2(x0);
             p1 = ex2(x1);
             if (masked) {

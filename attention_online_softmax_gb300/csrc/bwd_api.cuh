@@ -19,12 +19,12 @@ bool encode_dq_map(CUtensorMap* map, void* base, int d, int rows, int heads) {
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int D, int STAGES>
+template <int D, int STAGES, bool BIAS>
 attn_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
                        const CUtensorMap& mdq, const attn::BwdParams& p, cudaStream_t stream) {
   using L = attn::BwdLayout<D, STAGES>;
-  auto kern = attn::attn_bwd_kernel<D, STAGES>;
-  if (!ensure_smem<attn::attn_bwd_kernel<D, STAGES>>(L::kAlloc)) return ATTN_ERR_LAUNCH;
+  auto kern = attn::attn_bwd_kernel<D, STAGES, BIAS>;
+  if (!ensure_smem<attn::attn_bwd_kernel<D, STAGES, BIAS>>(L::kAlloc)) return ATTN_ERR_LAUNCH;
   const long long grid = static_cast<long long>(p.B) * p.Hkv * ((p.Nk + 127) / 128);
   if (grid > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
   if (grid == 0) return ATTN_OK;
@@ -46,17 +46,18 @@ bool encode_dqt_map(CUtensorMap* map, void* base, int Nq, int ld, int heads) {
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+template <bool BIAS>
 attn_status launch_bwd_wide(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const CUtensorMap& mdo, const CUtensorMap& mdqt, const attn::BwdParams& p,
                             cudaStream_t stream) {
   using L = attn::BwdWideLayout;
-  if (!ensure_smem<attn::attn_bwd_wide_kernel>(L::kAlloc)) return ATTN_ERR_LAUNCH;
+  if (!ensure_smem<attn::attn_bwd_wide_kernel<BIAS>>(L::kAlloc)) return ATTN_ERR_LAUNCH;
   // Two CTAs (head-dim halves) per (key tile, batch, kv head), key tile 0 first.
   const long long grid = 2LL * p.B * p.Hkv * ((p.Nk + 127) / 128);
   if (grid > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
   if (grid == 0) return ATTN_OK;
-  attn::attn_bwd_wide_kernel<<<dim3(static_cast<unsigned>(grid)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mdo,
-                                                                                                   mdqt, p);
+  attn::attn_bwd_wide_kernel<BIAS>
+      <<<dim3(static_cast<unsigned>(grid)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mdo, mdqt, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return ATTN_OK;
@@ -70,6 +71,19 @@ size_t bwd_acc_bytes(int B, int Hq, int Nq, int d) {
 }
 
 bool bwd_head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
+
+template <bool BIAS>
+attn_status launch_bwd_d(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const CUtensorMap& mdo, const CUtensorMap& mdq, const attn::BwdParams& p, cudaStream_t s) {
+  return d == 64    ? launch_bwd<64, 3, BIAS>(mq, mk, mv, mdo, mdq, p, s)
+         : d == 128 ? launch_bwd<128, 2, BIAS>(mq, mk, mv, mdo, mdq, p, s)
+                    : launch_bwd_wide<BIAS>(mq, mk, mv, mdo, mdq, p, s);
+}
+
+attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                     float scale, const attn_mask* mask, attn_dtype grad_dtype, void* workspace,
+                     size_t workspace_bytes, attn_stream_t stream);
 
 }  // namespace
 
@@ -85,12 +99,38 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
                      float scale, attn_dtype grad_dtype, void* workspace, size_t workspace_bytes,
                      attn_stream_t stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, causal, scale, nullptr, grad_dtype,
+                  workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_masked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                            const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
+                            int d, int causal, float scale, const attn_mask* mask, attn_dtype grad_dtype,
+                            void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, causal, scale, mask, grad_dtype,
+                  workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                     float scale, const attn_mask* mask, attn_dtype grad_dtype, void* workspace,
+                     size_t workspace_bytes, attn_stream_t stream) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (grad_dtype != ATTN_BF16 && grad_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
   if (!bwd_head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * Hq > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
+  const bool biased = mask != nullptr && (mask->window_left != 0 || mask->alibi_slopes || mask->bias);
+  if (biased) {
+    if (mask->window_left < 0 || mask->bias_stride_b < 0 || mask->bias_stride_h < 0) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(mask->alibi_slopes) & 3u) || (reinterpret_cast<uintptr_t>(mask->bias) & 3u))
+      return ATTN_ERR_MISALIGNED;
+  }
   if (B == 0 || (Nq == 0 && Nk == 0)) return ATTN_OK;
   if (Nq > 0 && (!aligned16(q) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) || !aligned16(dq)))
     return ATTN_ERR_MISALIGNED;
@@ -146,9 +186,12 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
     p.g_f32 = grad_dtype == ATTN_F32 ? 1 : 0;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
-    st = d == 64    ? launch_bwd<64, 3>(mq, mk, mv, mdo, mdq, p, s)
-         : d == 128 ? launch_bwd<128, 2>(mq, mk, mv, mdo, mdq, p, s)
-                    : launch_bwd_wide(mq, mk, mv, mdo, mdq, p, s);
+    p.window_left = biased ? mask->window_left : 0;
+    p.alibi = biased ? mask->alibi_slopes : nullptr;
+    p.bias = biased ? static_cast<const uint16_t*>(mask->bias) : nullptr;
+    p.bias_sb = biased ? mask->bias_stride_b : 0;
+    p.bias_sh = biased ? mask->bias_stride_h : 0;
+    st = biased ? launch_bwd_d<true>(d, mq, mk, mv, mdo, mdq, p, s) : launch_bwd_d<false>(d, mq, mk, mv, mdo, mdq, p, s);
     if (st != ATTN_OK) return st;
   }
 
@@ -171,4 +214,4 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   return ATTN_OK;
 }
 
-}  // extern "C"
+}  // namespace

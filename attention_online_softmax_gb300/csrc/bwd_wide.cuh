@@ -87,6 +87,7 @@ __global__ void bwd_post_transpose_kernel(const float* dqT, void* dq, int BH, in
   }
 }
 
+template <bool BIAS>
 __global__ void __launch_bounds__(320, 1)
     attn_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -132,11 +133,9 @@ __global__ void __launch_bounds__(320, 1)
   const int k0 = kt * 128;
   const int G = p.Hq / p.Hkv;
   const int diag = p.Nk - p.Nq;
-  const int ntq = (p.Nq + BQ - 1) / BQ;
-  int qt_lo = 0;
-  if (p.causal) qt_lo = max(0, (k0 - diag) / BQ);
-  if (p.causal && k0 - diag >= p.Nq) qt_lo = ntq;
-  const int per_head = ntq - qt_lo;
+  int qt_lo, qt_hi;
+  bwd_query_tiles(p, k0, BQ, qt_lo, qt_hi);
+  const int per_head = qt_hi - qt_lo;
   const int n_items = G * per_head;
 
   if (threadIdx.x == 0) {
@@ -346,10 +345,13 @@ __global__ void __launch_bounds__(320, 1)
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[0], (n - 1) & 1, 84));
         if (!ok) break;
       }
-      const int c_hi = p.Nq - q0;
+      int c_hi = p.Nq - q0;
       const int c_lo = p.causal ? kj - diag - q0 : -0x7FFFFFFF;
+      if (BIAS && p.window_left > 0) c_hi = min(c_hi, kj - diag + p.window_left - q0);  // left window
       const bool key_ok = kj < p.Nk;
       const bool masked = !(key_ok && c_lo <= c0 && c_hi >= c0 + 32);
+      BwdBiasRow br;
+      if constexpr (BIAS) br = bwd_bias_row(p, bh, q0, kj);
       uint32_t pw[16], dw[16];
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
@@ -364,6 +366,10 @@ __global__ void __launch_bounds__(320, 1)
         for (int u = 0; u < 4; u += 2) {
           float x0, x1, p0, p1, t0, t1, d0, d1;
           ffma2(x0, x1, __uint_as_float(sv[e + u]), __uint_as_float(sv[e + u + 1]), sl, sl, nl[u], nl[u + 1]);
+          if constexpr (BIAS) {
+            x0 += bwd_bias_at(br, c + u, key_ok, c_lo, c_hi);
+            x1 += bwd_bias_at(br, c + u + 1, key_ok, c_lo, c_hi);
+          }
           p0 = ex2(x0);
           p1 = ex2(x1);
           if (masked) {

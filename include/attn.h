@@ -230,6 +230,25 @@ ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const
                               size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * Backward pass of attn_fwd_masked: attn_bwd for the biased scores
+ * S = scale Q K^T + C, with `mask` the one passed to the forward (NULL: same
+ * as attn_bwd).  The formulas of attn_bwd hold with P the biased weights; a
+ * key the mask disallows, or whose bias is -inf, takes no gradient, and no
+ * gradient with respect to C is formed.  Key tiles wholly outside a left
+ * window are skipped.  Arguments, workspace, kernels and determinism as
+ * attn_bwd; the bias is read once per (key tile, query tile) pair it covers.
+ * Source: "Compilers and Kernels", section "FlashAttention changes the
+ * algorithm around IO" (the additive term C of the score definition; the
+ * backward recomputes the weights); "Tang: a compiler that derives GPU
+ * kernels and bounds how fast they can run", abstract (fused backward).
+ */
+ATTN_API attn_status attn_bwd_masked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                     const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                                     int Nq, int Nk, int d, int causal, float scale, const attn_mask* mask,
+                                     attn_dtype grad_dtype, void* workspace, size_t workspace_bytes,
+                                     attn_stream_t stream);
+
+/*
  * Measurement aid for the decode time floor: one thread follows
  * idx = chain[idx] (starting at 0) for `hops` dependent loads that bypass L1
  * and writes the elapsed nanoseconds to out_ns[0] (out_ns[1] receives the last
