@@ -764,6 +764,21 @@ def cpu_bwd(c, x, dout):
             "extrapolated_full_s": full, "extrapolation": "sample time x (all allowed pairs / sampled pairs)"}
 
 
+def cpu_bwd_masked(c, x, dout, slopes, bias):
+    import oracle
+    # One (batch, head) slice (MHA: every head costs the same allowed pairs).
+    sl = (slice(0, 1), slice(0, 1))
+    bsl = None if bias is None else bias[sl].contiguous()
+    t0 = time.perf_counter()
+    _, _, _, th = oracle.attention_masked_bwd(
+        x.q[sl].contiguous(), x.k[sl].contiguous(), x.v[sl].contiguous(), dout[sl].contiguous(), c.causal,
+        x.scale, window_left=c.window, alibi=None if slopes is None else slopes[:1].numpy(), bias=bsl,
+        bias_strides=(0, 0))
+    t = time.perf_counter() - t0
+    return {"kind": "oracle", "cores": th, "seconds": t, "sample": "one (batch, head) slice of the workload",
+            "extrapolated_full_s": t * c.B * c.Hq, "extrapolation": "slice time x B*Hq (equal heads)"}
+
+
 def _row(t, p10, p90, fl, by, peaks, cpu, **extra):
     bound = roofline.bound_rate(fl, by, peaks)
     out = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_of_peak": fl / t / (peaks.bf16_tflops * 1e12),
@@ -837,6 +852,33 @@ def per_config_table(abi, dev, stream, peaks, reps: int = 30, with_cpu: bool = T
         out["bwd_" + c.name] = _row(t, p10, p90, fl, by, peaks, cpu,
                                     flops="5 products of 2 N^2 d per head = 2.5x the forward's")
         del q, k, v, o, lse, dout, dq, dk, dv, ws
+    # Backward through the additive bias (the masked forward's O and LSE as inputs).
+    for c in configs.MASKED_CONFIGS:
+        x = make_prefill_inputs(c)
+        q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        slopes, bias = make_mask_inputs(c)
+        slopes_d = None if slopes is None else slopes.to(dev)
+        bias_d = None if bias is None else bias.to(dev)
+        kw = dict(window_left=c.window, alibi=slopes_d, bias=bias_d)
+        abi.attn_fwd_masked(q, k, v, o, lse, c.causal, x.scale, **kw)
+        g = torch.Generator().manual_seed(c.seed + 50)
+        dout_h = torch.randn(x.q.shape, generator=g).to(torch.bfloat16)
+        dout = dout_h.to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(abi.attn_bwd_workspace_size(c.B, c.Hq, c.Nq, c.d), dtype=torch.uint8, device=dev)
+        t, p10, p90 = gpu_median(
+            lambda: abi.attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, c.causal, x.scale, workspace=ws, **kw),
+            stream, flush, reps)
+        fl = 2.5 * roofline.masked_flops(c.B, c.Hq, c.Nq, c.Nk, c.d, c.causal, c.window)
+        by = roofline.bwd_bytes(c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d)
+        if bias is not None:
+            by += bias.numel() * 2
+        cpu = cpu_bwd_masked(c, x, dout_h, slopes, bias) if with_cpu else None
+        out["bwd_" + c.name] = _row(t, p10, p90, fl, by, peaks, cpu,
+                                    flops="2.5 x (4 d per allowed (query, key) pair)")
+        del q, k, v, o, lse, dout, dq, dk, dv, ws, slopes_d, bias_d
     # Chunked prefill against the paged cache.
     c = configs.CHUNKED
     q_lens, k_lens = configs.chunked_lengths(c)
