@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libattn_gb300.so")
 SOURCES = [os.path.join(CSRC, "attn_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "prefill_fwd.cuh", "decode.cuh", "bwd.cuh", "bwd_api.cuh", "probe.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "prefill_fwd.cuh", "decode.cuh", "bwd.cuh", "bwd_wide.cuh", "bwd_api.cuh", "probe.cuh")] + [
     os.path.join(INCLUDE, "attn.h")]
 
 

@@ -31,8 +31,22 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
+#: the C source of the oracle
+SOURCE = _SRC
 _LOCK = threading.Lock()
 _LIBS: dict[int, ctypes.CDLL] = {}
+# Patched copies of the source with one planted mistake each, registered by
+# the test-suite under a number (``mutant=`` of the functions below).
+_MUTANT_SOURCES: dict[int, str] = {}
+
+
+def register_source(mutant: int, path: str) -> None:
+    """Use the C file at ``path`` for ``mutant=mutant`` (mutant > 0)."""
+    if mutant <= 0:
+        raise ValueError("mutant numbers are positive; 0 is the oracle itself")
+    with _LOCK:
+        _MUTANT_SOURCES[mutant] = path
+        _LIBS.pop(mutant, None)
 
 
 def lib_path(mutant: int = 0) -> str:
@@ -41,15 +55,20 @@ def lib_path(mutant: int = 0) -> str:
 
 
 def build(mutant: int = 0, force: bool = False) -> str:
-    """Compile the C oracle with gcc (-O2, OpenMP).  Returns the .so path."""
+    """Compile the C oracle (or a registered mutant copy) with gcc (-O2,
+    OpenMP).  Returns the .so path."""
+    src = _SRC
+    if mutant != 0:
+        src = _MUTANT_SOURCES.get(mutant)
+        if src is None:
+            raise ValueError(f"no source registered for mutant {mutant}")
     out = lib_path(mutant)
     if (not force and os.path.exists(out)
-            and os.path.getmtime(out) >= os.path.getmtime(_SRC)):
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tmp = f"{out}.{os.getpid()}.tmp"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
-           f"-DORACLE_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", src, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out

@@ -39,16 +39,9 @@
  * block_table[s][t / page_size], slot t % page_size, of a cache laid out as
  * [num_pages][page_size][Hkv][d].
  *
- * Build switch ORACLE_MUTANT (default 0) plants one deliberate mistake; it
- * exists only so the test-suite can show that its pins catch each kind of
- * mistake (a dropped scale, a wrong mask offset, a wrong head, a transposed
- * operand, a dropped normaliser; in the backward a dropped D term or a
- * dropped dK scale; in the chunked prefill a causal bound off by one or a
- * wrong kv head; in the additive bias an ALiBi distance of the wrong sign
- * or a left window one key too wide;
- * in the paged decode a page read as [Hkv][page_size][d] instead of
- * [page_size][Hkv][d]).
- * The shipped oracle is built with 0.
+ * The test-suite builds copies of this file with one deliberate mistake
+ * planted (tests/oracle_mutants.py) to show that its pins catch each kind of
+ * mistake; this file itself holds none.
  */
 #include <math.h>
 #include <stdint.h>
@@ -56,10 +49,6 @@
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
-#endif
-
-#ifndef ORACLE_MUTANT
-#define ORACLE_MUTANT 0
 #endif
 
 /* bfloat16 is the upper half of an IEEE binary32; widening is exact. */
@@ -92,19 +81,9 @@ static void attend_row(const uint16_t* q, const uint16_t* const* krows,
     for (j = 0; j < n_keys; ++j) {
         double s = 0.0;
         for (c = 0; c < d; ++c) {
-#if ORACLE_MUTANT == 4
-            /* transposed operand: reads the key matrix column-wise */
-            s += bf16_to_double(q[c]) * bf16_to_double(krows[c % n_keys][j % d]);
-#else
             s += bf16_to_double(q[c]) * bf16_to_double(krows[j][c]);
-#endif
         }
-#if ORACLE_MUTANT == 1
-        /* dropped scale */
-        (void)scale;
-#else
         s *= scale;
-#endif
         scratch[j] = s;
         if (s > m) m = s;
     }
@@ -116,12 +95,7 @@ static void attend_row(const uint16_t* q, const uint16_t* const* krows,
         l += p;
         for (c = 0; c < d; ++c) o[c] += p * bf16_to_double(vrows[j][c]);
     }
-#if ORACLE_MUTANT == 5
-    /* dropped normaliser */
-    (void)l;
-#else
     for (c = 0; c < d; ++c) o[c] /= l;
-#endif
     *lse = m + log(l);
 }
 
@@ -212,17 +186,9 @@ int oracle_attention_masked(const uint16_t* q, const uint16_t* k, const uint16_t
             int64_t n = 0, j;
             for (j = 0; j < Nk; ++j) {
                 if (causal && j > i + diag) continue;
-#if ORACLE_MUTANT == 12
-                if (window_left > 0 && j < i + diag - window_left) continue;  /* one key too many */
-#else
                 if (window_left > 0 && j <= i + diag - window_left) continue;
-#endif
                 double c = 0.0;
-#if ORACLE_MUTANT == 9
-                if (alibi) c += (double)alibi[h] * (double)(i - j + diag);  /* distance of the wrong sign */
-#else
                 if (alibi) c += (double)alibi[h] * (double)(j - i - diag);
-#endif
                 if (bias) c += bf16_to_double(bias[b * bias_sb + h * bias_sh + i * (int64_t)Nk + j]);
                 krows[n] = kb + j * d;
                 vrows[n] = vb + j * d;
@@ -279,18 +245,10 @@ int oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
             int64_t bh = flat / Nq;
             int64_t h = bh % Hq;
             int64_t b = bh / Hq;
-#if ORACLE_MUTANT == 3
-            int64_t g = h % Hkv; /* wrong head mapping */
-#else
             int64_t g = h / group;
-#endif
             int64_t n_allowed = Nk;
             if (causal) {
-#if ORACLE_MUTANT == 2
-                int64_t last = i; /* wrong alignment: ignores Nk - Nq */
-#else
                 int64_t last = i + (int64_t)Nk - (int64_t)Nq;
-#endif
                 n_allowed = last + 1;
                 if (n_allowed < 0) n_allowed = 0;
                 if (n_allowed > Nk) n_allowed = Nk;
@@ -364,11 +322,7 @@ int oracle_decode_paged(const uint16_t* q, const uint16_t* kcache, const uint16_
             for (t = 0; t < n; ++t) {
                 int32_t page = block_table[(int64_t)seq * max_pages_per_seq + t / page_size];
                 if (page < 0 || page >= num_pages) { ok = 0; break; }
-#if ORACLE_MUTANT == 11
-                int64_t off = (((int64_t)page * Hkv + g) * page_size + t % page_size) * d;
-#else
                 int64_t off = (((int64_t)page * page_size + t % page_size) * Hkv + g) * d;
-#endif
                 krows[t] = kcache + off;
                 vrows[t] = vcache + off;
             }
@@ -459,19 +413,11 @@ int oracle_prefill_paged(const uint16_t* q, const uint16_t* kcache, const uint16
             const int64_t k_len = seqlens_k[seq];
             const int64_t i = token - cu_seqlens_q[seq];
             const int64_t diag = k_len - q_len;
-#if ORACLE_MUTANT == 8
-            int64_t hi = causal ? i + diag : k_len;  /* causal bound off by one */
-#else
             int64_t hi = causal ? i + diag + 1 : k_len;
-#endif
             if (hi > k_len) hi = k_len;
             int64_t lo = window_left > 0 ? i + diag - window_left + 1 : 0;
             if (lo < 0) lo = 0;
-#if ORACLE_MUTANT == 10
-            const int g = h % Hkv;  /* wrong kv head */
-#else
             const int g = h / group;
-#endif
             int64_t t, n = 0;
             int ok = 1;
             for (t = lo; t < hi; ++t, ++n) {
@@ -593,18 +539,10 @@ int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v
                     }
                     double* dqi = dq + row * d;
                     for (j = 0; j < n; ++j) {
-#if ORACLE_MUTANT == 6
-                        const double ds = p[j] * dp[j];  /* dropped D */
-#else
                         const double ds = p[j] * (dp[j] - D);
-#endif
                         for (c = 0; c < d; ++c) {
                             dqi[c] += sc * ds * bf16_to_double(kb[j * d + c]);
-#if ORACLE_MUTANT == 7
-                            dkb[j * d + c] += ds * bf16_to_double(qi[c]);  /* dropped scale */
-#else
                             dkb[j * d + c] += sc * ds * bf16_to_double(qi[c]);
-#endif
                             dvb[j * d + c] += p[j] * bf16_to_double(doi[c]);
                         }
                     }

@@ -17,8 +17,11 @@ import pytest
 import torch
 
 import oracle
+import oracle_mutants
 from attention_online_softmax_gb300 import inputs
 from test_oracle_pins import bf16_np, close
+
+oracle_mutants.register_all()
 
 
 def c_matrix(B, Hq, Nq, Nk, causal, window, slopes, bias):

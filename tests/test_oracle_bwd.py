@@ -15,8 +15,11 @@ import pytest
 import torch
 
 import oracle
+import oracle_mutants
 from attention_online_softmax_gb300 import inputs
 from test_oracle_pins import bf16_np
+
+oracle_mutants.register_all()
 
 
 def dout_for(shape, seed):

@@ -17,9 +17,12 @@ import pytest
 import torch
 
 import oracle
+import oracle_mutants
 from attention_online_softmax_gb300 import inputs
 from test_oracle_bias import decimal_with_bias
 from test_oracle_pins import bf16_np, close
+
+oracle_mutants.register_all()
 
 
 def gather(x, s):

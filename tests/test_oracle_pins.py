@@ -23,7 +23,10 @@ import pytest
 import torch
 
 import oracle
+import oracle_mutants
 from attention_online_softmax_gb300 import inputs
+
+oracle_mutants.register_all()
 
 
 def bf16_np(t: torch.Tensor) -> np.ndarray:
