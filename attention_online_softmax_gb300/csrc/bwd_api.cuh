@@ -34,29 +34,31 @@ attn_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
   return ATTN_OK;
 }
 
-// d = 256: the f32 dQ accumulator is kept transposed, [B*Hq][256][ld] with
-// ld = Nq rounded up to 4 (16-byte rows); one box is [128 head-dim rows][32
-// queries], 128-byte swizzled.
+// Head dims served by the 64-query-item kernel (bwd_wide.cuh): its f32 dQ
+// accumulator is kept transposed, [B*Hq][d][ld] with ld = Nq rounded up to 4
+// (16-byte rows); one box is [128 head-dim rows][32 queries], 128-byte
+// swizzled.
+bool bwd_uses_wide(int d) { return d >= 128; }
 int bwd_wide_ld(int Nq) { return (Nq + 3) & ~3; }
 
-bool encode_dqt_map(CUtensorMap* map, void* base, int Nq, int ld, int heads) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(Nq), 256, static_cast<cuuint64_t>(heads)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, static_cast<cuuint64_t>(ld) * 256 * 4};
+bool encode_dqt_map(CUtensorMap* map, void* base, int Nq, int ld, int d, int heads) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(Nq), static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, static_cast<cuuint64_t>(ld) * d * 4};
   cuuint32_t box[3] = {32, 128, 1};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <bool BIAS>
+template <int D, int STAGES, bool BIAS>
 attn_status launch_bwd_wide(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const CUtensorMap& mdo, const CUtensorMap& mdqt, const attn::BwdParams& p,
                             cudaStream_t stream) {
-  using L = attn::BwdWideLayout;
-  if (!ensure_smem<attn::attn_bwd_wide_kernel<BIAS>>(L::kAlloc)) return ATTN_ERR_LAUNCH;
-  // Two CTAs (head-dim halves) per (key tile, batch, kv head), key tile 0 first.
-  const long long grid = 2LL * p.B * p.Hkv * ((p.Nk + 127) / 128);
+  using L = attn::BwdWideLayout<D, STAGES>;
+  if (!ensure_smem<attn::attn_bwd_wide_kernel<D, STAGES, BIAS>>(L::kAlloc)) return ATTN_ERR_LAUNCH;
+  // kSplit CTAs (head-dim halves) per (key tile, batch, kv head), key tile 0 first.
+  const long long grid = static_cast<long long>(L::kSplit) * p.B * p.Hkv * ((p.Nk + 127) / 128);
   if (grid > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
   if (grid == 0) return ATTN_OK;
-  attn::attn_bwd_wide_kernel<BIAS>
+  attn::attn_bwd_wide_kernel<D, STAGES, BIAS>
       <<<dim3(static_cast<unsigned>(grid)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mdo, mdqt, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -66,8 +68,8 @@ attn_status launch_bwd_wide(const CUtensorMap& mq, const CUtensorMap& mk, const 
 // Bytes of the f32 dQ accumulator for head dim d.
 size_t bwd_acc_bytes(int B, int Hq, int Nq, int d) {
   const size_t bh = static_cast<size_t>(B) * Hq;
-  return d == 256 ? bh * 256 * static_cast<size_t>(bwd_wide_ld(Nq)) * sizeof(float)
-                  : bh * static_cast<size_t>(Nq) * d * sizeof(float);
+  return bwd_uses_wide(d) ? bh * d * static_cast<size_t>(bwd_wide_ld(Nq)) * sizeof(float)
+                          : bh * static_cast<size_t>(Nq) * d * sizeof(float);
 }
 
 bool bwd_head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
@@ -76,8 +78,8 @@ template <bool BIAS>
 attn_status launch_bwd_d(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, const CUtensorMap& mdq, const attn::BwdParams& p, cudaStream_t s) {
   return d == 64    ? launch_bwd<64, 3, BIAS>(mq, mk, mv, mdo, mdq, p, s)
-         : d == 128 ? launch_bwd<128, 2, BIAS>(mq, mk, mv, mdo, mdq, p, s)
-                    : launch_bwd_wide<BIAS>(mq, mk, mv, mdo, mdq, p, s);
+         : d == 128 ? launch_bwd_wide<128, 3, BIAS>(mq, mk, mv, mdo, mdq, p, s)
+                    : launch_bwd_wide<256, 1, BIAS>(mq, mk, mv, mdo, mdq, p, s);
 }
 
 attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -161,15 +163,15 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
     const void* db = Nq > 0 ? dout : k;
     const int nq_map = Nq > 0 ? Nq : Nk;
     const int bh_map = Nq > 0 ? B * Hq : B * Hkv;
-    const int qbox = d == 256 ? attn::BwdWideLayout::kBQ : 128;
+    const int qbox = bwd_uses_wide(d) ? 64 : 128;
     if (!encode_rows_map(&mq, qb, d, nq_map, bh_map, qbox) || !encode_rows_map(&mdo, db, d, nq_map, bh_map, qbox) ||
         !encode_rows_map(&mk, k, d, Nk, B * Hkv, 128) || !encode_rows_map(&mv, v, d, Nk, B * Hkv, 128))
       return ATTN_ERR_LAUNCH;
     // With Nq == 0 no dQ chunk is ever written; the map then describes one row.
     void* acc_base = Nq > 0 ? static_cast<void*>(dq_acc) : workspace;
-    const bool acc_ok = d == 256 ? encode_dqt_map(&mdq, acc_base, Nq > 0 ? Nq : 1, bwd_wide_ld(Nq > 0 ? Nq : 1),
-                                                  Nq > 0 ? B * Hq : 1)
-                                 : encode_dq_map(&mdq, acc_base, d, Nq > 0 ? Nq : 1, Nq > 0 ? B * Hq : 1);
+    const bool acc_ok = bwd_uses_wide(d) ? encode_dqt_map(&mdq, acc_base, Nq > 0 ? Nq : 1,
+                                                          bwd_wide_ld(Nq > 0 ? Nq : 1), d, Nq > 0 ? B * Hq : 1)
+                                         : encode_dq_map(&mdq, acc_base, d, Nq > 0 ? Nq : 1, Nq > 0 ? B * Hq : 1);
     if (!acc_ok) return ATTN_ERR_LAUNCH;
     attn::BwdParams p;
     p.dk = dk;
@@ -195,11 +197,11 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
     if (st != ATTN_OK) return st;
   }
 
-  if (rows > 0 && d == 256) {
+  if (rows > 0 && bwd_uses_wide(d)) {
     // Transpose the [bh][d][q] accumulator back to dQ[bh][q][d].
-    const dim3 grid(static_cast<unsigned>((Nq + 31) / 32), 256 / 32,
+    const dim3 grid(static_cast<unsigned>((Nq + 31) / 32), static_cast<unsigned>(d / 32),
                     static_cast<unsigned>(std::min<long long>(static_cast<long long>(B) * Hq, 65535)));
-    attn::bwd_post_transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(dq_acc, dq, B * Hq, Nq, bwd_wide_ld(Nq), 256,
+    attn::bwd_post_transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(dq_acc, dq, B * Hq, Nq, bwd_wide_ld(Nq), d,
                                                                   grad_dtype == ATTN_F32 ? 1 : 0);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     g_launches.fetch_add(1, std::memory_order_relaxed);

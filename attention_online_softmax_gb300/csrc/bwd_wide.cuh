@@ -1,62 +1,79 @@
-// Attention backward at head dim 256 (the same products as bwd.cuh: the
-// derivative of the forward of "Compilers and Kernels", section
-// "FlashAttention changes the algorithm around IO", with the weights
-// recomputed from the saved row logsumexp as in the flash-style backward of
-// "Tang: a compiler that derives GPU kernels and bounds how fast they can run",
-// abstract; head dim 256 is the "derived head-dim-256 attention" there).
+// Attention backward at head dims 128 and 256 (the same products as bwd.cuh,
+// which serves d = 64: the derivative of the forward of "Compilers and
+// Kernels", section "FlashAttention changes the algorithm around IO", with the
+// weights recomputed from the saved row logsumexp as in the flash-style
+// backward of "Tang: a compiler that derives GPU kernels and bounds how fast
+// they can run", abstract; head dim 256 is the "derived head-dim-256
+// attention" there).
 //
-// At d = 256 the dK and dV accumulators of one 128-key tile alone fill the
-// 512 tensor-memory columns, so a key tile is served by two CTAs, one per
-// half of the head dim (h = 0, 1): CTA h keeps dK[:, h], dV[:, h] (128 columns
-// each) and adds dQ[:, h].  Both recompute the full S^T and dP^T (contraction
-// over all 256 columns), which costs 32 of every 56 products of an item twice
-// but needs no exchange between the two.  K and V (64 KB each) stay in shared
-// memory; items are 64-query tiles (Q and dO 32 KB each, one stage), so the
-// score tiles are N = 64 products:
-//   S^T  = K Q^T        [128 keys][64 queries]    (tensor memory, 64 columns)
+// One CTA keeps a 128-key tile's K and V in shared memory and its dK, dV
+// accumulators (128 head-dim columns each) in tensor memory, and walks every
+// (query head of the group, 64-row query tile) whose rows see its keys.  At
+// d = 256 the two accumulators of a key tile alone would fill the 512
+// tensor-memory columns, so the tile is served by two CTAs, one per half of
+// the head dim (h = 0, 1): CTA h keeps dK[:, h], dV[:, h] and adds dQ[:, h].
+// Both recompute the full S^T and dP^T (contraction over all 256 columns),
+// which costs 32 of every 56 products of an item twice but needs no exchange
+// between the two.  Per item (score tiles are N = 64 products):
+//   S^T  = K Q^T        [128 keys][64 queries]
 //   dP^T = V dO^T       [128 keys][64 queries]
-//   P^T, dS^T as in bf16 over the dP^T columns
+//   P^T, dS^T as bf16 over the dP^T columns
 //   dV_h += P^T dO_h,  dK_h += dS^T Q_h            (A from tensor memory)
 //   dQ^T_h = K_h^T dS^T [128 head-dim rows][64 queries] (dS^T staged in shared
 //            memory), added to a transposed f32 accumulator dQacc^T[bh][d][q]
 //            by TMA reduce-adds; the post kernel transposes it back.
-// Tensor memory: dK_h 128, dV_h 128, S^T 64, dP^T 64, dQ^T 64 columns.
-// Roles as in bwd.cuh: warp 0 TMA producer, warp 1 MMA issuer, warps 2..9 two
-// per TMEM lane quarter, each thread one key row and 32 of the item's 64 query
-// columns (weights), then one head-dim row and 32 query columns (dQ^T).
+// Tensor memory: dK_h 128, dV_h 128, and two slots of S^T (then dQ^T) and dP^T
+// (then P^T, dS^T), 64 columns each: the next item's score products run while
+// the weight warps work on the current item.
+// Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2..9 two per TMEM lane
+// quarter, each thread one key row and 32 of the item's 64 query columns (the
+// weights), warps 10..13 one per lane quarter, each thread one head-dim row of
+// dQ^T (its read-out and TMA reduce-adds), so the weights of one item and the
+// read-out of the previous one run side by side.
 #pragma once
 
 #include "bwd.cuh"
 
 namespace attn {
 
+template <int D, int STAGES>
 struct BwdWideLayout {
-  static constexpr int D = 256;
-  static constexpr int kThreads = 320;
+  static_assert(D == 128 || D == 256, "head dims of the 64-query-item backward");
+  static constexpr int kSplit = D / 128;               // CTAs per key tile (head-dim halves at D = 256)
+  static constexpr int kThreads = 448;
   static constexpr int kBQ = 64;                       // query rows per item
-  static constexpr int kKVTile = 128 * D * 2;          // [128 keys][256] bf16: 4 boxes [128][64] of 16 KB
-  static constexpr int kQTile = kBQ * D * 2;           // [64 rows][256] bf16: 4 boxes [64][64] of 8 KB
+  static constexpr int kKVTile = 128 * D * 2;          // [128 keys][D] bf16: D/64 boxes [128][64] of 16 KB
+  static constexpr int kQTile = kBQ * D * 2;           // [64 rows][D] bf16: D/64 boxes [64][64] of 8 KB
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kKVTile;
-  static constexpr int kQOff = kVOff + kKVTile;
-  static constexpr int kDOOff = kQOff + kQTile;
-  static constexpr int kDSOff = kDOOff + kQTile;       // dS^T [128 keys][64 queries] bf16 (16 KB), then
-                                                       // half 0's dQ^T staging [128][32] f32
-  static constexpr int kStgOff = kDSOff + 16384;       // half 1's dQ^T staging [128][32] f32
-  static constexpr int kRowOff = kStgOff + 16384;      // 2 x (-LSE log2 e [64], D [64]) f32
+  static constexpr int kQOff = kVOff + kKVTile;        // STAGES x (Q tile, dO tile)
+  static constexpr int kStage = 2 * kQTile;
+  static constexpr int kDSOff = kQOff + STAGES * kStage;  // dS^T [128 keys][64 queries] bf16 (16 KB)
+  // dQ^T staging, [128 head-dim rows][32 queries] f32 chunks: two buffers at
+  // D = 128, one at D = 256 (no room for a second).
+  static constexpr int kNumStg = D == 128 ? 2 : 1;
+  static constexpr int kStgOff = kDSOff + 16384;
+  static constexpr int kRowOff = kStgOff + kNumStg * 16384;  // 2 x (-LSE log2 e [64], D [64]) f32
   static constexpr int kRowBytes = 2 * kBQ * 4;
   static constexpr int kBarOff = kRowOff + 2 * kRowBytes;
-  // kv_full, q_full, q_empty, do_full, do_empty, s_full, dp_full, ds_full, dq_full, dq_free, dkv_done,
-  // rows_ready[2], red_full[2], red_free[2]
-  static constexpr int kNumBars = 17;
+  // kv_full, stage_full[S], stage_empty[S], q_full[S], q_empty[S], scores_full[2] (S^T and dP^T of a
+  // slot), ds_full, dq_full, dq_free, dkv_done, rows_ready[2], red_full[2], red_free[2] (per staging
+  // buffer).  With two or more stages an item's Q and dO share stage_full / stage_empty; with one stage
+  // (D = 256) dO uses those and Q its own pair, so that dO, which the item's first product reads and
+  // whose last reader (dV) finishes first, moves on its own.
+  static constexpr bool kSplitOps = STAGES == 1;
+  static constexpr int kNumBars = 1 + 4 * STAGES + 2 + 4 + 6;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 128;          // the base is checked for 1024-byte alignment
+  // Tensor memory: dK_h, dV_h, then two slots (items alternate) of S^T
+  // (64 columns; after the weights have read it, the item's dQ^T) and of
+  // dP^T (64 columns; query half h's dS^T in [32h, 32h + 16) and P^T in
+  // [32h + 16, 32h + 32) once read).
   static constexpr int kColDK = 0;
   static constexpr int kColDV = 128;
-  static constexpr int kColS = 256;
-  static constexpr int kColDP = 320;                   // half h: dS^T in [32h, 32h + 16), P^T in [32h + 16, 32h + 32)
-  static constexpr int kColDQ = 384;
+  static constexpr int kColS = 256;                    // slot b at kColS + 64 b
+  static constexpr int kColDP = 384;                   // slot b at kColDP + 64 b
   static_assert(kBytes + 128 <= 232448, "shared memory budget");
 };
 
@@ -87,13 +104,12 @@ __global__ void bwd_post_transpose_kernel(const float* dqT, void* dq, int BH, in
   }
 }
 
-template <bool BIAS>
-__global__ void __launch_bounds__(320, 1)
+template <int D, int STAGES, bool BIAS>
+__global__ void __launch_bounds__(448, 1)
     attn_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const __grid_constant__ CUtensorMap tmDQT, const BwdParams p) {
-  using L = BwdWideLayout;
-  constexpr int D = L::D;
+  using L = BwdWideLayout<D, STAGES>;
   constexpr int BQ = L::kBQ;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -107,27 +123,29 @@ __global__ void __launch_bounds__(320, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* kv_full = bars;
-  uint64_t* q_full = bars + 1;
-  uint64_t* q_empty = bars + 2;
-  uint64_t* do_full = bars + 3;
-  uint64_t* do_empty = bars + 4;
-  uint64_t* s_full = bars + 5;
-  uint64_t* dp_full = bars + 6;
-  uint64_t* ds_full = bars + 7;
-  uint64_t* dq_full = bars + 8;
-  uint64_t* dq_free = bars + 9;
-  uint64_t* dkv_done = bars + 10;
-  uint64_t* rows_ready = bars + 11;  // [2]
-  uint64_t* red_full = bars + 13;    // [2] a half's [128][32] f32 dQ^T chunk is staged
-  uint64_t* red_free = bars + 15;    // [2] its TMA reduce has finished reading the staging buffer
+  uint64_t* stage_full = bars + 1;                // [STAGES] an item's Q and dO have landed
+  uint64_t* stage_empty = stage_full + STAGES;    // [STAGES] its dK product (the last reader) is done
+  uint64_t* q_full = stage_empty + STAGES;        // [STAGES] Q has landed (one stage only)
+  uint64_t* q_empty = q_full + STAGES;            // [STAGES] its dK product is done (one stage only)
+  uint64_t* scores_full = q_empty + STAGES;       // [2] per slot: S^T and dP^T are in tensor memory
+  uint64_t* ds_full = scores_full + 2;
+  uint64_t* dq_full = ds_full + 1;
+  uint64_t* dq_free = dq_full + 1;
+  uint64_t* dkv_done = dq_free + 1;
+  uint64_t* rows_ready = dkv_done + 1;  // [2]
+  uint64_t* red_full = rows_ready + 2;  // [2] a [128][32] f32 dQ^T chunk is staged in buffer b
+  uint64_t* red_free = red_full + 2;    // [2] buffer b's previous TMA reduce has finished reading it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int BHkv = p.B * p.Hkv;
-  const int h = static_cast<int>(blockIdx.x & 1u);         // head-dim half of dK, dV, dQ
-  const int kt = static_cast<int>(blockIdx.x >> 1) / BHkv;  // key tile 0 first (seen by the most rows)
-  const int bkv = static_cast<int>(blockIdx.x >> 1) - kt * BHkv;
+  // Head-dim half of dK, dV, dQ at D = 256 (two CTAs per key tile); key tile
+  // 0 first (seen by the most rows).
+  const int h = L::kSplit == 2 ? static_cast<int>(blockIdx.x & 1u) : 0;
+  const int blk = L::kSplit == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int kt = blk / BHkv;
+  const int bkv = blk - kt * BHkv;
   const int b = bkv / p.Hkv;
   const int kvh = bkv - b * p.Hkv;
   const int k0 = kt * 128;
@@ -140,15 +158,18 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    mbar_init(do_full, 1);
-    mbar_init(do_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(dp_full, 1);
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(&stage_full[st], 1);
+      mbar_init(&stage_empty[st], 1);
+      mbar_init(&q_full[st], 1);
+      mbar_init(&q_empty[st], 1);
+    }
+    for (int b2 = 0; b2 < 2; ++b2) {
+      mbar_init(&scores_full[b2], 1);
+    }
     mbar_init(ds_full, 8);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 8);
+    mbar_init(dq_free, 4);
     mbar_init(dkv_done, 1);
     mbar_init(&rows_ready[0], BQ);
     mbar_init(&rows_ready[1], BQ);
@@ -183,30 +204,40 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(smem + L::kKOff + c * (128 * 128), &tmK, kv_full, c * 64, k0, bkv);
         tma_load_3d(smem + L::kVOff + c * (128 * 128), &tmV, kv_full, c * 64, k0, bkv);
       }
-      int n_do = 0, n_q = 0;  // loads issued
+      int n_ld = 0;  // items loaded
       for (int n = 0; n < n_items; ++n) {
         const int bh = item_bh(n), q0 = item_q0(n);
-        // dO first: the item's first product (dP^T) reads it, and its slot
-        // frees after the previous item's dV product, before Q's (dK).
-        if (!mbar_wait(do_empty, (n & 1) ^ 1, 70)) break;
-        mbar_expect_tx(do_full, L::kQTile);
+        const int st = n % STAGES;
+        uint8_t* stage = smem + L::kQOff + st * L::kStage;
+        const uint32_t par = ((n / STAGES) & 1) ^ 1;
+        if (!mbar_wait(&stage_empty[st], par, 70)) break;
+        mbar_expect_tx(&stage_full[st], L::kSplitOps ? L::kQTile : 2 * L::kQTile);
+        // dO first: the item's first product (dP^T) reads it.
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::kDOOff + c * (BQ * 128), &tmDO, do_full, c * 64, q0, bh);
-        n_do = n + 1;
-        if (!mbar_wait(q_empty, (n & 1) ^ 1, 71)) break;
-        mbar_expect_tx(q_full, L::kQTile);
+          tma_load_3d(stage + L::kQTile + c * (BQ * 128), &tmDO, &stage_full[st], c * 64, q0, bh);
+        uint64_t* qbar = &stage_full[st];
+        if (L::kSplitOps) {
+          if (!mbar_wait(&q_empty[st], par, 71)) {
+            n_ld = n;  // dO of item n is in flight: drained below with Q not issued
+            mbar_wait(&stage_full[st], (n / STAGES) & 1, 74);
+            break;
+          }
+          qbar = &q_full[st];
+          mbar_expect_tx(qbar, L::kQTile);
+        }
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::kQOff + c * (BQ * 128), &tmQ, q_full, c * 64, q0, bh);
-        n_q = n + 1;
+          tma_load_3d(stage + c * (BQ * 128), &tmQ, qbar, c * 64, q0, bh);
+        n_ld = n + 1;
       }
-      // Drain: never leave the CTA with a copy still writing shared memory.
-      // One stage each: a load is issued only after the previous one was
-      // consumed, so only the last of each can still be in flight.
+      // Drain: never leave the CTA with a copy still writing shared memory
+      // (a load is issued only once the one STAGES earlier was consumed).
       mbar_wait(kv_full, 0, 72);
-      if (n_do > 0) mbar_wait(do_full, (n_do - 1) & 1, 73);
-      if (n_q > 0) mbar_wait(q_full, (n_q - 1) & 1, 74);
+      for (int it = max(0, n_ld - STAGES); it < n_ld; ++it) {
+        mbar_wait(&stage_full[it % STAGES], (it / STAGES) & 1, 73);
+        if (L::kSplitOps) mbar_wait(&q_full[it % STAGES], (it / STAGES) & 1, 73);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -217,89 +248,178 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t kIdQ = idesc_bf16_f32(128, BQ, 1, 1);   // dQ^T_h: A (K_h^T), B (dS^T) MN-major
       const uint64_t dK_a = sdesc_sw128(sbase + L::kKOff, 16, 1024);
       const uint64_t dV_a = sdesc_sw128(sbase + L::kVOff, 16, 1024);
-      const uint64_t dQ_b = sdesc_sw128(sbase + L::kQOff, 16, 1024);
-      const uint64_t dO_b = sdesc_sw128(sbase + L::kDOOff, 16, 1024);
       // Head-dim half h: boxes 2h, 2h + 1 of K (16 KB apart) and of Q, dO (8 KB apart).
       const uint64_t dKh_mn = sdesc_sw128(sbase + L::kKOff + h * 2 * (128 * 128), 128 * 128, 1024);
-      const uint64_t dQh_mn = sdesc_sw128(sbase + L::kQOff + h * 2 * (BQ * 128), BQ * 128, 1024);
-      const uint64_t dOh_mn = sdesc_sw128(sbase + L::kDOOff + h * 2 * (BQ * 128), BQ * 128, 1024);
       const uint64_t dS_mn = sdesc_sw128(sbase + L::kDSOff, BQ * 128, 1024);
+      constexpr bool kEarlyScores = STAGES >= 2;
       bool ok = mbar_wait(kv_full, 0, 75);
       if (ok) tc_fence_after();
+      // The score products of item m into slot m & 1: dP^T = V dO^T, then
+      // S^T = K Q^T (K = D).
+      auto issue_scores = [&](int m) -> bool {
+        const int st = m % STAGES;
+        const uint32_t par = (m / STAGES) & 1;
+        const uint32_t qs = sbase + L::kQOff + st * L::kStage;
+        const uint64_t dQ_b = sdesc_sw128(qs, 16, 1024);
+        const uint64_t dO_b = sdesc_sw128(qs + L::kQTile, 16, 1024);
+        const int b2 = m & 1;
+        if (!mbar_wait(&stage_full[st], par, 76)) return false;  // dO (and Q unless split)
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4);
+          umma_bf16_ss(tmem + L::kColDP + b2 * BQ, dV_a + oa, dO_b + ob, kIdS, kk > 0);
+        }
+        if (L::kSplitOps) {
+          if (!mbar_wait(&q_full[st], par, 77)) return false;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4);
+          umma_bf16_ss(tmem + L::kColS + b2 * BQ, dK_a + oa, dQ_b + ob, kIdS, kk > 0);
+        }
+        umma_commit(&scores_full[b2]);
+        return true;
+      };
+      if (ok) ok = issue_scores(0);
       for (int n = 0; ok && n < n_items; ++n) {
-        // dP^T = V dO^T (K = 256): its slot is free once the previous item's
-        // dV and dK products (issued earlier) have read P^T and dS^T from it.
-        ok = mbar_wait(do_full, n & 1, 76);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
-          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4);
-          umma_bf16_ss(tmem + L::kColDP, dV_a + oa, dO_b + ob, kIdS, kk > 0);
-        }
-        umma_commit(dp_full);
-        // S^T = K Q^T (K = 256): the previous item's weights read S^T before
-        // they signalled ds_full, which this thread waited for.
-        ok = mbar_wait(q_full, n & 1, 77);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
-          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4);
-          umma_bf16_ss(tmem + L::kColS, dK_a + oa, dQ_b + ob, kIdS, kk > 0);
-        }
-        umma_commit(s_full);
-        ok = mbar_wait(ds_full, n & 1, 78);
-        if (!ok) break;
-        tc_fence_after();
-        if (n > 0) {
-          // The previous dQ^T tile must have been read out of its columns.
+        const int st = n % STAGES;
+        const int b2 = n & 1;
+        const uint32_t qs = sbase + L::kQOff + st * L::kStage;
+        const uint64_t dQh_mn = sdesc_sw128(qs + h * 2 * (BQ * 128), BQ * 128, 1024);
+        const uint64_t dOh_mn = sdesc_sw128(qs + L::kQTile + h * 2 * (BQ * 128), BQ * 128, 1024);
+        // The next item's score products go to the slot that last held item
+        // n - 1: S^T's columns took dQ^T_{n-1}, which must have been read out
+        // (waited for here, before dQ^T_n is issued, for every item: once
+        // dQ^T_n is issued the read-out could see dq_full complete twice and
+        // the phase parity would no longer tell the two apart); dP^T's held
+        // P^T and dS^T of n - 1, read by dV and dK products issued earlier.  With two or more Q / dO
+        // stages the products are issued before this item's weights are done
+        // and run while the weight warps work; with one stage their loads
+        // wait for this item's dV and dK products, so they follow those.
+        const bool more = n + 1 < n_items;
+        if (n >= 1) {
           ok = mbar_wait(dq_free, (n - 1) & 1, 79);
           if (!ok) break;
           tc_fence_after();
         }
-        // dQ^T_h = K_h^T dS^T (K = 128 keys) first, so that its read-out
+        if (kEarlyScores && more) {
+          ok = issue_scores(n + 1);
+          if (!ok) break;
+        }
+        ok = mbar_wait(ds_full, n & 1, 78);
+        if (!ok) break;
+        tc_fence_after();
+        // dQ^T_h = K_h^T dS^T (K = 128 keys) into the S^T columns of slot
+        // n & 1 (the weights have read S^T_n), first, so that its read-out
         // overlaps the dV and dK products.
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
-          umma_bf16_ss(tmem + L::kColDQ, dKh_mn + o, dS_mn + o, kIdQ, kk > 0);
+          umma_bf16_ss(tmem + L::kColS + b2 * BQ, dKh_mn + o, dS_mn + o, kIdQ, kk > 0);
         }
         umma_commit(dq_full);
         // dV_h += P^T dO_h, dK_h += dS^T Q_h (K = 64 queries; the 16 queries
         // of step kk lie in query half kk / 2: P^T at columns 32 (kk / 2) + 16
-        // + 8 (kk % 2), dS^T at 32 (kk / 2) + 8 (kk % 2)).
+        // + 8 (kk % 2) of the dP^T slot, dS^T at 32 (kk / 2) + 8 (kk % 2)).
+        const uint32_t dp_slot = tmem + L::kColDP + b2 * BQ;
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
           const uint32_t pcol = (kk >> 1) * 32 + 16 + (kk & 1) * 8;
-          umma_bf16_ts(tmem + L::kColDV, tmem + L::kColDP + pcol, dOh_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + L::kColDV, dp_slot + pcol, dOh_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(do_empty);
+        if (L::kSplitOps) umma_commit(&stage_empty[st]);  // dO's last reader
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
           const uint32_t dcol = (kk >> 1) * 32 + (kk & 1) * 8;
-          umma_bf16_ts(tmem + L::kColDK, tmem + L::kColDP + dcol, dQh_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + L::kColDK, dp_slot + dcol, dQh_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(q_empty);
+        umma_commit(L::kSplitOps ? &q_empty[st] : &stage_empty[st]);
+        if (!kEarlyScores && more) {
+          ok = issue_scores(n + 1);
+          if (!ok) break;
+        }
       }
       umma_commit(dkv_done);
       mbar_wait(dkv_done, 0, 80);
     }
     __syncwarp();
+  } else if (warp >= 10) {
+    // ---------------------------------------------------------------- dQ^T read-out
+    // dQ^T of item m (TMEM lane = head-dim row of half h, in the S^T columns
+    // of slot m & 1), 32 query columns at a time: scale, stage [128 rows][32]
+    // f32 (128-byte swizzle), and one thread adds the chunk into the f32
+    // accumulator with a TMA reduce.  A buffer is written again once its
+    // previous reduce has read it (the issuing thread waits for that read only
+    // then, so reduces overlap the next chunks).
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const bool issuer = warp == 10 && lane == 0;
+    bool ok = true;
+    for (int m = 0; ok && m < n_items; ++m) {
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(dq_full, m & 1, 85));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[2][32];
+      tmem_ld32(lane_base + L::kColS + (m & 1) * BQ, v[0]);
+      tmem_ld32(lane_base + L::kColS + (m & 1) * BQ + 32, v[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_free);
+      const int bh = item_bh(m), q0 = item_q0(m);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int b = L::kNumStg == 2 ? c : 0;
+        const int use = L::kNumStg == 2 ? m : 2 * m + c;  // uses of buffer b so far
+        if (use > 0) {
+          if (issuer) {
+            // The reduce that last used buffer b is the latest but one of this
+            // thread's (two buffers) or its latest (one buffer).
+            if (L::kNumStg == 2) bulk_wait_read<1>();
+            else bulk_wait_read<0>();
+            mbar_arrive(&red_free[b]);
+          }
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[b], (use - 1) & 1, 86));
+          if (!ok) break;
+        }
+        const uint32_t stg = sbase + L::kStgOff + b * 16384 + row * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(stg + ((k ^ (row & 7)) << 4), __float_as_uint(__uint_as_float(v[c][4 * k]) * p.scale),
+                       __float_as_uint(__uint_as_float(v[c][4 * k + 1]) * p.scale),
+                       __float_as_uint(__uint_as_float(v[c][4 * k + 2]) * p.scale),
+                       __float_as_uint(__uint_as_float(v[c][4 * k + 3]) * p.scale));
+        fence_proxy_async_smem();
+        mbar_arrive(&red_full[b]);
+        if (issuer) {
+          if (!mbar_wait(&red_full[b], use & 1, 87)) {
+            ok = false;
+          } else {
+            tma_reduce_add_3d(&tmDQT, smem + L::kStgOff + b * 16384, q0 + c * 32, h * 128, bh);
+            bulk_commit();
+          }
+        }
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) break;
+      }
+    }
+    // Every dQ^T reduce of this CTA must have completed before it exits.
+    if (issuer) bulk_wait_all();
   } else {
-    // ---------------------------------------------------------------- key rows, then head-dim rows
+    // ---------------------------------------------------------------- key rows: the weights
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;         // query columns [32 half, 32 half + 32) of the item
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int kj = k0 + row;                  // this thread's key (weights)
+    const int kj = k0 + row;                  // this thread's key
     const int c0 = half * 32;
     const bool row_writer = half == 0 && row < BQ;
-    const bool issuer = lane == 0 && quarter == 2;  // the first warp of each half issues its dQ^T reduce
     bool ok = true;
     auto row_vals = [&](int n, float& nl2, float& dd) {
       nl2 = -INFINITY;
@@ -319,6 +439,8 @@ __global__ void __launch_bounds__(320, 1)
     const float sl = p.scale_log2;
     for (int n = 0; ok && n < n_items; ++n) {
       const int bh = item_bh(n), q0 = item_q0(n);
+      const int b2 = n & 1;
+      const uint32_t slot_par = (n >> 1) & 1;
       float* nls = reinterpret_cast<float*>(smem + L::kRowOff + (n & 1) * L::kRowBytes);
       float* dsum = nls + BQ;
       if (row_writer) {
@@ -329,22 +451,14 @@ __global__ void __launch_bounds__(320, 1)
       }
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&rows_ready[n & 1], (n >> 1) & 1, 81));
       if (!ok) break;
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(dp_full, n & 1, 82));
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&scores_full[b2], slot_par, 82));
       if (!ok) break;
       tc_fence_after();
+      const uint32_t dp_cols = lane_base + L::kColDP + b2 * BQ + c0;
       uint32_t dp[32];
-      tmem_ld32(lane_base + L::kColDP + c0, dp);
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(s_full, n & 1, 83));
-      if (!ok) break;
-      tc_fence_after();
+      tmem_ld32(dp_cols, dp);
       uint32_t sv[32];
-      tmem_ld32(lane_base + L::kColS + c0, sv);
-      if (n > 0) {
-        // The dS^T region was half 0's staging buffer for the previous item:
-        // its TMA reduce must have finished reading it.
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[0], (n - 1) & 1, 84));
-        if (!ok) break;
-      }
+      tmem_ld32(lane_base + L::kColS + b2 * BQ + c0, sv);
       int c_hi = p.Nq - q0;
       const int c_lo = p.causal ? kj - diag - q0 : -0x7FFFFFFF;
       if (BIAS && p.window_left > 0) c_hi = min(c_hi, kj - diag + p.window_left - q0);  // left window
@@ -383,10 +497,16 @@ __global__ void __launch_bounds__(320, 1)
           dw[(e + u) >> 1] = pack_bf16(d0, d1);
         }
       }
-      // dS^T and P^T over this half's dP^T columns, dS^T into shared memory
-      // (row `row`, 16-byte units 4 half .. 4 half + 3 in the 128-byte swizzle).
-      tmem_st16(lane_base + L::kColDP + c0, dw);
-      tmem_st16(lane_base + L::kColDP + c0 + 16, pw);
+      // dS^T and P^T over this half's dP^T columns of the slot.
+      tmem_st16(dp_cols, dw);
+      tmem_st16(dp_cols + 16, pw);
+      if (n > 0) {
+        // dS^T into shared memory once the previous item's dQ^T product, its
+        // other reader, has completed (row `row`, 16-byte units 4 half ..
+        // 4 half + 3 in the 128-byte swizzle).
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(dq_full, (n - 1) & 1, 84));
+        if (!ok) break;
+      }
       const uint32_t ds_row = sbase + L::kDSOff + row * 128;
 #pragma unroll
       for (int u4 = 0; u4 < 4; ++u4) {
@@ -398,43 +518,6 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
-
-      // dQ^T rows (TMEM lane = head-dim row of half h), this thread's 32
-      // query columns: scale, stage [128 rows][32] f32 (128-byte swizzle),
-      // and the half's issuing thread adds the chunk with a TMA reduce.
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(dq_full, n & 1, 85));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t v[32];
-      tmem_ld32(lane_base + L::kColDQ + c0, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
-      if (half == 1 && n > 0) {
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[1], (n - 1) & 1, 86));
-        if (!ok) break;
-      }
-      const uint32_t stg_base = half == 0 ? L::kDSOff : L::kStgOff;
-      const uint32_t stg = sbase + stg_base + row * 128;
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        st_shared_v4(stg + ((k ^ (row & 7)) << 4), __float_as_uint(__uint_as_float(v[4 * k]) * p.scale),
-                     __float_as_uint(__uint_as_float(v[4 * k + 1]) * p.scale),
-                     __float_as_uint(__uint_as_float(v[4 * k + 2]) * p.scale),
-                     __float_as_uint(__uint_as_float(v[4 * k + 3]) * p.scale));
-      fence_proxy_async_smem();
-      mbar_arrive(&red_full[half]);
-      if (issuer) {
-        if (!mbar_wait(&red_full[half], n & 1, 87)) {
-          ok = false;
-        } else {
-          tma_reduce_add_3d(&tmDQT, smem + stg_base, q0 + c0, h * 128, bh);
-          bulk_commit();
-          bulk_wait_read<0>();
-          mbar_arrive(&red_free[half]);
-        }
-      }
-      ok = __all_sync(0xFFFFFFFFu, ok);
     }
 
     // dK_h, dV_h rows of this key (zeros when no query row sees the tile):
@@ -484,8 +567,6 @@ __global__ void __launch_bounds__(320, 1)
     }
   }
 
-  // Every dQ^T reduce of this CTA must have completed before it exits.
-  if (warp >= 2 && lane == 0 && (warp & 3) == 2) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
