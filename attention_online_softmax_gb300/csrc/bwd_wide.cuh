@@ -25,11 +25,12 @@
 // Tensor memory: dK_h 128, dV_h 128, and two slots of S^T (then dQ^T) and dP^T
 // (then P^T, dS^T), 64 columns each: the next item's score products run while
 // the weight warps work on the current item.
-// Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2..9 two per TMEM lane
-// quarter, each thread one key row and 32 of the item's 64 query columns (the
-// weights), warps 10..13 one per lane quarter, each thread one head-dim row of
-// dQ^T (its read-out and TMA reduce-adds), so the weights of one item and the
-// read-out of the previous one run side by side.
+// Roles: warp 0 TMA producer; warp 1 issues the score products and warp 14
+// the gradient products (one thread each); warps 2..9, two per TMEM lane
+// quarter, compute the weights (each thread one key row and 32 of the item's
+// 64 query columns); warps 10..13, one per lane quarter, read dQ^T out (each
+// thread one head-dim row) and add it with TMA reduce-adds, so the weights of
+// one item and the read-out of the previous one run side by side.
 #pragma once
 
 #include "bwd.cuh"
@@ -40,7 +41,7 @@ template <int D, int STAGES>
 struct BwdWideLayout {
   static_assert(D == 128 || D == 256, "head dims of the 64-query-item backward");
   static constexpr int kSplit = D / 128;               // CTAs per key tile (head-dim halves at D = 256)
-  static constexpr int kThreads = 448;
+  static constexpr int kThreads = 480;
   static constexpr int kBQ = 64;                       // query rows per item
   static constexpr int kKVTile = 128 * D * 2;          // [128 keys][D] bf16: D/64 boxes [128][64] of 16 KB
   static constexpr int kQTile = kBQ * D * 2;           // [64 rows][D] bf16: D/64 boxes [64][64] of 8 KB
@@ -57,12 +58,13 @@ struct BwdWideLayout {
   static constexpr int kRowBytes = 2 * kBQ * 4;
   static constexpr int kBarOff = kRowOff + 2 * kRowBytes;
   // kv_full, stage_full[S], stage_empty[S], q_full[S], q_empty[S], scores_full[2] (S^T and dP^T of a
-  // slot), ds_full, dq_full, dq_free, dkv_done, rows_ready[2], red_full[2], red_free[2] (per staging
+  // slot), ds_full, dq_full, dq_free[2] (per slot), dkv_done, sc_done, rows_ready[2], red_full[2],
+  // red_free[2] (per staging
   // buffer).  With two or more stages an item's Q and dO share stage_full / stage_empty; with one stage
   // (D = 256) dO uses those and Q its own pair, so that dO, which the item's first product reads and
   // whose last reader (dV) finishes first, moves on its own.
   static constexpr bool kSplitOps = STAGES == 1;
-  static constexpr int kNumBars = 1 + 4 * STAGES + 2 + 4 + 6;
+  static constexpr int kNumBars = 1 + 4 * STAGES + 2 + 6 + 6;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 128;          // the base is checked for 1024-byte alignment
@@ -105,7 +107,7 @@ __global__ void bwd_post_transpose_kernel(const float* dqT, void* dq, int BH, in
 }
 
 template <int D, int STAGES, bool BIAS>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(480, 1)
     attn_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const __grid_constant__ CUtensorMap tmDQT, const BwdParams p) {
@@ -130,9 +132,10 @@ __global__ void __launch_bounds__(448, 1)
   uint64_t* scores_full = q_empty + STAGES;       // [2] per slot: S^T and dP^T are in tensor memory
   uint64_t* ds_full = scores_full + 2;
   uint64_t* dq_full = ds_full + 1;
-  uint64_t* dq_free = dq_full + 1;
-  uint64_t* dkv_done = dq_free + 1;
-  uint64_t* rows_ready = dkv_done + 1;  // [2]
+  uint64_t* dq_free = dq_full + 1;      // [2] per slot: its dQ^T has been read out
+  uint64_t* dkv_done = dq_free + 2;
+  uint64_t* sc_done = dkv_done + 1;     // the score issuer's products have completed
+  uint64_t* rows_ready = sc_done + 1;   // [2]
   uint64_t* red_full = rows_ready + 2;  // [2] a [128][32] f32 dQ^T chunk is staged in buffer b
   uint64_t* red_free = red_full + 2;    // [2] buffer b's previous TMA reduce has finished reading it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -169,8 +172,10 @@ __global__ void __launch_bounds__(448, 1)
     }
     mbar_init(ds_full, 8);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 4);
+    mbar_init(&dq_free[0], 4);
+    mbar_init(&dq_free[1], 4);
     mbar_init(dkv_done, 1);
+    mbar_init(sc_done, 1);
     mbar_init(&rows_ready[0], BQ);
     mbar_init(&rows_ready[1], BQ);
     for (int i = 0; i < 2; ++i) {
@@ -240,8 +245,13 @@ __global__ void __launch_bounds__(448, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == 14) {
+    // ---------------------------------------------------------------- MMA issuers
+    // Warp 1 issues every item's score products (dP^T, S^T), warp 14 its
+    // gradient products (dQ^T, dV, dK), each from one thread: a thread that
+    // blocks on a full tensor pipe or on a barrier does not hold up the
+    // other's instructions.  Products of different threads are not ordered,
+    // so every reuse of a slot waits for the barrier of its last reader.
     if (lane == 0 && n_items > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, BQ, 0, 0);   // S^T, dP^T: K-major A and B, N = 64
       constexpr uint32_t kIdG = idesc_bf16_f32(128, 128, 0, 1);  // dV_h, dK_h: A from TMEM, B MN-major
@@ -251,105 +261,108 @@ __global__ void __launch_bounds__(448, 1)
       // Head-dim half h: boxes 2h, 2h + 1 of K (16 KB apart) and of Q, dO (8 KB apart).
       const uint64_t dKh_mn = sdesc_sw128(sbase + L::kKOff + h * 2 * (128 * 128), 128 * 128, 1024);
       const uint64_t dS_mn = sdesc_sw128(sbase + L::kDSOff, BQ * 128, 1024);
-      constexpr bool kEarlyScores = STAGES >= 2;
       bool ok = mbar_wait(kv_full, 0, 75);
       if (ok) tc_fence_after();
-      // The score products of item m into slot m & 1: dP^T = V dO^T, then
-      // S^T = K Q^T (K = D).
-      auto issue_scores = [&](int m) -> bool {
-        const int st = m % STAGES;
-        const uint32_t par = (m / STAGES) & 1;
-        const uint32_t qs = sbase + L::kQOff + st * L::kStage;
-        const uint64_t dQ_b = sdesc_sw128(qs, 16, 1024);
-        const uint64_t dO_b = sdesc_sw128(qs + L::kQTile, 16, 1024);
-        const int b2 = m & 1;
-        if (!mbar_wait(&stage_full[st], par, 76)) return false;  // dO (and Q unless split)
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
-          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4);
-          umma_bf16_ss(tmem + L::kColDP + b2 * BQ, dV_a + oa, dO_b + ob, kIdS, kk > 0);
-        }
-        if (L::kSplitOps) {
-          if (!mbar_wait(&q_full[st], par, 77)) return false;
-          tc_fence_after();
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
-          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4);
-          umma_bf16_ss(tmem + L::kColS + b2 * BQ, dK_a + oa, dQ_b + ob, kIdS, kk > 0);
-        }
-        umma_commit(&scores_full[b2]);
-        return true;
-      };
-      if (ok) ok = issue_scores(0);
-      for (int n = 0; ok && n < n_items; ++n) {
-        const int st = n % STAGES;
-        const int b2 = n & 1;
-        const uint32_t qs = sbase + L::kQOff + st * L::kStage;
-        const uint64_t dQh_mn = sdesc_sw128(qs + h * 2 * (BQ * 128), BQ * 128, 1024);
-        const uint64_t dOh_mn = sdesc_sw128(qs + L::kQTile + h * 2 * (BQ * 128), BQ * 128, 1024);
-        // The next item's score products go to the slot that last held item
-        // n - 1: S^T's columns took dQ^T_{n-1}, which must have been read out
-        // (waited for here, before dQ^T_n is issued, for every item: once
-        // dQ^T_n is issued the read-out could see dq_full complete twice and
-        // the phase parity would no longer tell the two apart); dP^T's held
-        // P^T and dS^T of n - 1, read by dV and dK products issued earlier.  With two or more Q / dO
-        // stages the products are issued before this item's weights are done
-        // and run while the weight warps work; with one stage their loads
-        // wait for this item's dV and dK products, so they follow those.
-        const bool more = n + 1 < n_items;
-        if (n >= 1) {
-          ok = mbar_wait(dq_free, (n - 1) & 1, 79);
+      if (warp == 1) {
+        // Score products of item m into slot m & 1: dP^T = V dO^T, then
+        // S^T = K Q^T (K = D).  The slot last held item m - 2: its S^T
+        // columns took dQ^T_{m-2}, which must have been read out; its dP^T
+        // columns held P^T and dS^T of m - 2, read by the dV and dK products
+        // of m - 2 (waited for here with more than two stages; with one or
+        // two, the load of item m waited for them already).
+        for (int m = 0; ok && m < n_items; ++m) {
+          const int st = m % STAGES;
+          const uint32_t par = (m / STAGES) & 1;
+          const int b2 = m & 1;
+          if (m >= 2) {
+            ok = mbar_wait(&dq_free[b2], ((m - 2) >> 1) & 1, 79);
+            if (!ok) break;
+            if (STAGES > 2) {
+              ok = mbar_wait(&stage_empty[(m - 2) % STAGES], ((m - 2) / STAGES) & 1, 89);
+              if (!ok) break;
+            }
+          }
+          const uint32_t qs = sbase + L::kQOff + st * L::kStage;
+          const uint64_t dQ_b = sdesc_sw128(qs, 16, 1024);
+          const uint64_t dO_b = sdesc_sw128(qs + L::kQTile, 16, 1024);
+          ok = mbar_wait(&stage_full[st], par, 76);  // dO (and Q unless split)
           if (!ok) break;
           tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+            const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4);
+            umma_bf16_ss(tmem + L::kColDP + b2 * BQ, dV_a + oa, dO_b + ob, kIdS, kk > 0);
+          }
+          if (L::kSplitOps) {
+            ok = mbar_wait(&q_full[st], par, 77);
+            if (!ok) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+            const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4);
+            umma_bf16_ss(tmem + L::kColS + b2 * BQ, dK_a + oa, dQ_b + ob, kIdS, kk > 0);
+          }
+          umma_commit(&scores_full[b2]);
         }
-        if (kEarlyScores && more) {
-          ok = issue_scores(n + 1);
+        // Every product of this thread completes before the CTA frees the
+        // tensor memory (also when a wait above gave up).
+        umma_commit(sc_done);
+        mbar_wait(sc_done, 0, 91);
+      } else {
+        for (int n = 0; ok && n < n_items; ++n) {
+          const int st = n % STAGES;
+          const int b2 = n & 1;
+          const uint32_t qs = sbase + L::kQOff + st * L::kStage;
+          const uint64_t dQh_mn = sdesc_sw128(qs + h * 2 * (BQ * 128), BQ * 128, 1024);
+          const uint64_t dOh_mn = sdesc_sw128(qs + L::kQTile + h * 2 * (BQ * 128), BQ * 128, 1024);
+          if (n >= 1) {
+            // dQ^T_{n-1} has been read out before dQ^T_n is issued: once it
+            // is, the read-out could see dq_full complete twice and the
+            // phase parity would no longer tell the two apart.
+            ok = mbar_wait(&dq_free[(n - 1) & 1], ((n - 1) >> 1) & 1, 90);
+            if (!ok) break;
+          }
+          ok = mbar_wait(ds_full, n & 1, 78);
           if (!ok) break;
-        }
-        ok = mbar_wait(ds_full, n & 1, 78);
-        if (!ok) break;
-        tc_fence_after();
-        // dQ^T_h = K_h^T dS^T (K = 128 keys) into the S^T columns of slot
-        // n & 1 (the weights have read S^T_n), first, so that its read-out
-        // overlaps the dV and dK products.
+          tc_fence_after();
+          // dQ^T_h = K_h^T dS^T (K = 128 keys) into the S^T columns of slot
+          // n & 1 (the weights have read S^T_n), first, so that its read-out
+          // overlaps the dV and dK products.
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
-          umma_bf16_ss(tmem + L::kColS + b2 * BQ, dKh_mn + o, dS_mn + o, kIdQ, kk > 0);
-        }
-        umma_commit(dq_full);
-        // dV_h += P^T dO_h, dK_h += dS^T Q_h (K = 64 queries; the 16 queries
-        // of step kk lie in query half kk / 2: P^T at columns 32 (kk / 2) + 16
-        // + 8 (kk % 2) of the dP^T slot, dS^T at 32 (kk / 2) + 8 (kk % 2)).
-        const uint32_t dp_slot = tmem + L::kColDP + b2 * BQ;
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
+            umma_bf16_ss(tmem + L::kColS + b2 * BQ, dKh_mn + o, dS_mn + o, kIdQ, kk > 0);
+          }
+          umma_commit(dq_full);
+          // dV_h += P^T dO_h, dK_h += dS^T Q_h (K = 64 queries; the 16
+          // queries of step kk lie in query half kk / 2: P^T at columns
+          // 32 (kk / 2) + 16 + 8 (kk % 2) of the dP^T slot, dS^T at
+          // 32 (kk / 2) + 8 (kk % 2)).
+          const uint32_t dp_slot = tmem + L::kColDP + b2 * BQ;
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
-          const uint32_t pcol = (kk >> 1) * 32 + 16 + (kk & 1) * 8;
-          umma_bf16_ts(tmem + L::kColDV, dp_slot + pcol, dOh_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (L::kSplitOps) umma_commit(&stage_empty[st]);  // dO's last reader
+          for (int kk = 0; kk < BQ / 16; ++kk) {
+            const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
+            const uint32_t pcol = (kk >> 1) * 32 + 16 + (kk & 1) * 8;
+            umma_bf16_ts(tmem + L::kColDV, dp_slot + pcol, dOh_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (L::kSplitOps) umma_commit(&stage_empty[st]);  // dO's last reader
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
-          const uint32_t dcol = (kk >> 1) * 32 + (kk & 1) * 8;
-          umma_bf16_ts(tmem + L::kColDK, dp_slot + dcol, dQh_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BQ / 16; ++kk) {
+            const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
+            const uint32_t dcol = (kk >> 1) * 32 + (kk & 1) * 8;
+            umma_bf16_ts(tmem + L::kColDK, dp_slot + dcol, dQh_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(L::kSplitOps ? &q_empty[st] : &stage_empty[st]);
         }
-        umma_commit(L::kSplitOps ? &q_empty[st] : &stage_empty[st]);
-        if (!kEarlyScores && more) {
-          ok = issue_scores(n + 1);
-          if (!ok) break;
-        }
+        umma_commit(dkv_done);
+        mbar_wait(dkv_done, 0, 80);
       }
-      umma_commit(dkv_done);
-      mbar_wait(dkv_done, 0, 80);
     }
     __syncwarp();
-  } else if (warp >= 10) {
+  } else if (warp >= 10 && warp < 14) {
     // ---------------------------------------------------------------- dQ^T read-out
     // dQ^T of item m (TMEM lane = head-dim row of half h, in the S^T columns
     // of slot m & 1), 32 query columns at a time: scale, stage [128 rows][32]
@@ -371,7 +384,7 @@ __global__ void __launch_bounds__(448, 1)
       tmem_ld32(lane_base + L::kColS + (m & 1) * BQ + 32, v[1]);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
+      if (lane == 0) mbar_arrive(&dq_free[m & 1]);
       const int bh = item_bh(m), q0 = item_q0(m);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
