@@ -464,6 +464,19 @@ __global__ void __launch_bounds__(480, 1)
       }
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&rows_ready[n & 1], (n >> 1) & 1, 81));
       if (!ok) break;
+      int c_hi = p.Nq - q0;
+      const int c_lo = p.causal ? kj - diag - q0 : -0x7FFFFFFF;
+      if (BIAS && p.window_left > 0) c_hi = min(c_hi, kj - diag + p.window_left - q0);  // left window
+      const bool key_ok = kj < p.Nk;
+      const bool masked = !(key_ok && c_lo <= c0 && c_hi >= c0 + 32);
+      // The bias of this key row's 32 query columns, loaded before the wait
+      // for the scores so that the loads are in flight meanwhile.
+      float cb[BIAS ? 32 : 1];
+      if constexpr (BIAS) {
+        const BwdBiasRow br = bwd_bias_row(p, bh, q0, kj);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) cb[e] = bwd_bias_at(br, c0 + e, key_ok, c_lo, c_hi);
+      }
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&scores_full[b2], slot_par, 82));
       if (!ok) break;
       tc_fence_after();
@@ -472,13 +485,6 @@ __global__ void __launch_bounds__(480, 1)
       tmem_ld32(dp_cols, dp);
       uint32_t sv[32];
       tmem_ld32(lane_base + L::kColS + b2 * BQ + c0, sv);
-      int c_hi = p.Nq - q0;
-      const int c_lo = p.causal ? kj - diag - q0 : -0x7FFFFFFF;
-      if (BIAS && p.window_left > 0) c_hi = min(c_hi, kj - diag + p.window_left - q0);  // left window
-      const bool key_ok = kj < p.Nk;
-      const bool masked = !(key_ok && c_lo <= c0 && c_hi >= c0 + 32);
-      BwdBiasRow br;
-      if constexpr (BIAS) br = bwd_bias_row(p, bh, q0, kj);
       uint32_t pw[16], dw[16];
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
@@ -494,8 +500,8 @@ __global__ void __launch_bounds__(480, 1)
           float x0, x1, p0, p1, t0, t1, d0, d1;
           ffma2(x0, x1, __uint_as_float(sv[e + u]), __uint_as_float(sv[e + u + 1]), sl, sl, nl[u], nl[u + 1]);
           if constexpr (BIAS) {
-            x0 += bwd_bias_at(br, c + u, key_ok, c_lo, c_hi);
-            x1 += bwd_bias_at(br, c + u + 1, key_ok, c_lo, c_hi);
+            x0 += cb[e + u];
+            x1 += cb[e + u + 1];
           }
           p0 = ex2(x0);
           p1 = ex2(x1);

@@ -604,6 +604,49 @@ def measure_e2e(abi, xp, xd, dev, stream, steps, floor_s, world):
             "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * t / steps, "steps": steps}
 
 
+def back_to_back_us(make_call, set_bytes: int, calls: int = 20, reps: int = 10) -> float:
+    """Per-call time of a small workload issued back to back: CUDA graphs of
+    `calls` calls, each call on its own copy of the inputs, the copies cycled
+    so that a copy is used again only after more than 256 MiB of other inputs
+    (more than L2) have been touched: every call starts from a cold L2 without
+    a flush kernel between calls.  The events bracket a whole graph, so the
+    launch latency of one graph is spread over `calls` calls.
+
+    make_call(i) -> a zero-argument callable on input copy i (it allocates the
+    copy)."""
+    nsets = max(2, -(-(256 << 20) // max(1, set_bytes)) + 1)
+    ngraphs = -(-nsets // calls)
+    fns = [make_call(i) for i in range(nsets)]
+    for f in fns[: min(nsets, 3)]:
+        f()
+    torch.cuda.synchronize()
+    graphs = []
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for g in range(ngraphs):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=side):
+                for i in range(calls):
+                    fns[(g * calls + i) % nsets]()
+            graphs.append(gr)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for gr in graphs:
+        gr.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for r in range(reps):
+        for gr in graphs:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            gr.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3 / calls)
+    return statistics.median(ts) * 1e6
+
+
 def gpu_median(call, stream, flush, reps: int, graph: bool = True):
     """Median, p10, p90 seconds of `call` on the device (L2 flushed before each rep).
 
@@ -809,6 +852,19 @@ def per_config_table(abi, dev, stream, peaks, reps: int = 30, with_cpu: bool = T
         if t < 50e-6:
             # the same call issued eagerly from Python: includes the host's launch latency
             extra["us_eager"] = gpu_median(fwd, stream, flush, reps, graph=False)[0] * 1e6
+            # A one-element add timed the same way: the harness's own floor
+            # (event, graph launch and kernel start) that a single call pays.
+            one = torch.zeros(1, device=dev)
+            extra["us_single_call_floor"] = gpu_median(lambda: one.add_(1.0), stream, flush, reps)[0] * 1e6
+            # Back to back, every call cold in L2 (inputs cycled through more
+            # than L2): the per-call time of a stream of such calls.
+            def make_call(i, c=c, x=x):
+                qi, ki, vi = (x.q.to(dev), x.k.to(dev), x.v.to(dev)) if i > 0 else (q, k, v)
+                oi, li = torch.empty_like(qi), torch.empty(qi.shape[:3], dtype=torch.float32, device=dev)
+                return lambda: abi.attn_fwd(qi, ki, vi, oi, li, c.causal, x.scale)
+            set_bytes = 4 * q.numel() * 2 + lse.numel() * 4
+            extra["us_back_to_back"] = back_to_back_us(make_call, set_bytes)
+            extra["back_to_back"] = "20 calls per CUDA graph, inputs cycled through > 256 MiB (cold L2, no flush)"
         out[c.name] = _row(t, p10, p90, fl, by, peaks, cpu_prefill(c, x) if with_cpu else None, **extra)
         del q, k, v, o, lse
     for c in configs.MASKED_CONFIGS:
