@@ -459,7 +459,7 @@ attn_status launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, attn::De
     // Programmatic dependent launch: the combine grid is scheduled while the
     // split grid drains and waits (griddepcontrol.wait) for its partials.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.num_seqs, (p.Hq + 3) / 4);
+    cfg.gridDim = dim3(p.num_seqs, p.Hq);
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

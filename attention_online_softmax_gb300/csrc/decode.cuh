@@ -356,22 +356,26 @@ __global__ void __launch_bounds__(288, (GW <= 4 && D <= 128) ? 2 : 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// One warp per (sequence, query head); lanes own D/32 consecutive elements.
-// Launched as a programmatic dependent of the split kernel: it waits on the
-// grid dependency before reading any partial.  Lane c computes the weight of
-// chunk c; the chunk rows are then read with several loads in flight.
+// One block of 4 warps per (sequence, query head); lanes own D/32 consecutive
+// elements.  Launched as a programmatic dependent of the split kernel: it
+// waits on the grid dependency before reading any partial.  Every warp takes
+// the maximum of the chunk lse values; warp w then takes chunks w, w + 4,
+// ..., eight rows in flight at a time, and the four partial sums meet in
+// shared memory.
 template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
   constexpr int E = D / 32;
+  constexpr int kRows = 8;  // chunk rows in flight per warp
+  __shared__ float s_acc[4][D];
+  __shared__ float s_w[4];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int seq = blockIdx.x;
-  const int head = blockIdx.y * 4 + warp;
-  if (head >= p.Hq) return;
+  const int head = blockIdx.y;
   const int L = decode_len(p, seq, false);
   const int ns = L > 0 ? (L + p.chunk - 1) / p.chunk : 1;
-  if (ns <= 1) return;  // finished by the split kernel
+  if (ns <= 1) return;  // finished by the split kernel (uniform for the block)
   const size_t row0 = static_cast<size_t>(seq) * p.n_splits * p.Hq + head;
   float m = -INFINITY;
   for (int c = lane; c < ns; c += 32) m = fmaxf(m, p.ws_lse[row0 + static_cast<size_t>(c) * p.Hq]);
@@ -380,49 +384,53 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  for (int c0 = 0; c0 < ns; c0 += 32) {
-    const int cl = c0 + lane;
-    const float wl =
-        cl < ns ? ex2((p.ws_lse[row0 + static_cast<size_t>(cl) * p.Hq] - m) * 1.4426950408889634f) : 0.f;
-    wsum += wl;
-    const int nb = min(32, ns - c0);
-    for (int k = 0; k < nb; k += 4) {
-      float v[4][E];
+  float wsum = 0.f;  // the same in every lane
+  for (int c0 = warp; c0 < ns; c0 += 4 * kRows) {
+    float v[kRows][E];
+    float lc[kRows];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int c = min(c0 + k + u, ns - 1);  // in range; weight 0 past the end
-        const float* src = p.ws_o + (row0 + static_cast<size_t>(c) * p.Hq) * D + lane * E;
+    for (int u = 0; u < kRows; ++u) {
+      const int c = min(c0 + 4 * u, ns - 1);  // in range; weight 0 past the end
+      const size_t r = row0 + static_cast<size_t>(c) * p.Hq;
+      lc[u] = p.ws_lse[r];
+      const float* src = p.ws_o + r * D + lane * E;
 #pragma unroll
-        for (int e = 0; e < E; e += 2) {
-          const float2 x = *reinterpret_cast<const float2*>(src + e);
-          v[u][e] = x.x;
-          v[u][e + 1] = x.y;
-        }
+      for (int e = 0; e < E; e += 2) {
+        const float2 x = *reinterpret_cast<const float2*>(src + e);
+        v[u][e] = x.x;
+        v[u][e + 1] = x.y;
       }
+    }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float w = __shfl_sync(0xFFFFFFFFu, wl, (k + u) & 31);
-        if (k + u >= nb) w = 0.f;
+    for (int u = 0; u < kRows; ++u) {
+      const float w = c0 + 4 * u < ns ? ex2((lc[u] - m) * 1.4426950408889634f) : 0.f;
+      wsum += w;
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
-      }
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
     }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, off);
-  const float inv = 1.f / wsum;
+  for (int e = 0; e < E; ++e) s_acc[warp][lane * E + e] = acc[e];
+  if (lane == 0) s_w[warp] = wsum;
+  __syncthreads();
+  if (warp != 0) return;
+  const float wt = s_w[0] + s_w[1] + s_w[2] + s_w[3];
+  const float inv = 1.f / wt;
+  float o[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    o[e] = (s_acc[0][lane * E + e] + s_acc[1][lane * E + e] + s_acc[2][lane * E + e] + s_acc[3][lane * E + e]) * inv;
   const size_t off = (static_cast<size_t>(seq) * p.Hq + head) * D + lane * E;
   if (p.o_f32) {
     float* dst = static_cast<float*>(p.o) + off;
 #pragma unroll
-    for (int e = 0; e < E; e += 2) *reinterpret_cast<float2*>(dst + e) = make_float2(acc[e] * inv, acc[e + 1] * inv);
+    for (int e = 0; e < E; e += 2) *reinterpret_cast<float2*>(dst + e) = make_float2(o[e], o[e + 1]);
   } else {
     uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.o) + off);
 #pragma unroll
-    for (int e = 0; e < E; e += 2) dst[e / 2] = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+    for (int e = 0; e < E; e += 2) dst[e / 2] = pack_bf16(o[e], o[e + 1]);
   }
-  if (lane == 0) p.lse[static_cast<size_t>(seq) * p.Hq + head] = m + logf(wsum);
+  if (lane == 0) p.lse[static_cast<size_t>(seq) * p.Hq + head] = m + logf(wt);
 }
 
 }  // namespace attn
