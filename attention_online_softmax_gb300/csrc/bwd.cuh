@@ -125,18 +125,23 @@ struct BwdLayout {
   static_assert(D == 64 || D == 128, "backward head dims");
 };
 
-// D[r] = sum_c O[r][c] dO[r][c] (f32), one warp per row, and the dQ
-// accumulator (zero4 float4 words, whatever its layout) zeroed.
+// D[r] = sum_c O[r][c] dO[r][c] (f32), d / 8 lanes per row (each lane 8
+// columns, 16-byte loads), and the dQ accumulator (zero4 float4 words)
+// zeroed.
 __global__ void bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, float* Dsum, float* dq_acc, long long rows,
                                 int d, long long zero4) {
+  const int lpr = d / 8;  // lanes per row: 8, 16 or 32
   const int lane = threadIdx.x & 31;
+  const int sub = lane % lpr;
+  const long long rows_per_warp = 32 / lpr;
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-       r += nwarps) {
+  const long long w0 = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  for (long long r0 = w0 * rows_per_warp; r0 < rows; r0 += nwarps * rows_per_warp) {
+    const long long r = r0 + lane / lpr;
     float acc = 0.f;
-    for (int c = lane * 8; c < d; c += 256) {
-      const uint4 a = *reinterpret_cast<const uint4*>(o + r * d + c);
-      const uint4 b = *reinterpret_cast<const uint4*>(dout + r * d + c);
+    if (r < rows) {
+      const uint4 a = *reinterpret_cast<const uint4*>(o + r * d + sub * 8);
+      const uint4 b = *reinterpret_cast<const uint4*>(dout + r * d + sub * 8);
       const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -144,13 +149,16 @@ __global__ void bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, float* 
         acc = fmaf(bf16hi(aw[e]), bf16hi(bw[e]), acc);
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-    if (lane == 0) Dsum[r] = acc;
+    for (int off = lpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+    if (sub == 0 && r < rows) Dsum[r] = acc;
   }
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero4;
        i += static_cast<long long>(gridDim.x) * blockDim.x)
     reinterpret_cast<float4*>(dq_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // dq = dq_acc as bf16 (RNE) or f32.

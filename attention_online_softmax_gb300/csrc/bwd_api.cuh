@@ -34,23 +34,21 @@ attn_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
   return ATTN_OK;
 }
 
-// Head dims served by the 64-query-item kernel (bwd_wide.cuh): its f32 dQ
-// accumulator is kept transposed, [B*Hq][d][ld] with ld = Nq rounded up to 4
-// (16-byte rows); one box is [128 head-dim rows][32 queries], 128-byte
-// swizzled.
+// Head dims served by the 64-query-item kernel (bwd_wide.cuh).  Its dQ
+// chunks are [32 queries][128 head-dim columns] f32, unswizzled, added into
+// the f32 accumulator [B*Hq][Nq][d].
 bool bwd_uses_wide(int d) { return d >= 128; }
-int bwd_wide_ld(int Nq) { return (Nq + 3) & ~3; }
 
-bool encode_dqt_map(CUtensorMap* map, void* base, int Nq, int ld, int d, int heads) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(Nq), static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, static_cast<cuuint64_t>(ld) * d * 4};
-  cuuint32_t box[3] = {32, 128, 1};
-  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+bool encode_dq_rows_map(CUtensorMap* map, void* base, int d, int rows, int heads) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(rows) * d * 4};
+  cuuint32_t box[3] = {128, 32, 1};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 template <int D, int STAGES, bool BIAS>
 attn_status launch_bwd_wide(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                            const CUtensorMap& mdo, const CUtensorMap& mdqt, const attn::BwdParams& p,
+                            const CUtensorMap& mdo, const CUtensorMap& mdq, const attn::BwdParams& p,
                             cudaStream_t stream) {
   using L = attn::BwdWideLayout<D, STAGES>;
   if (!ensure_smem<attn::attn_bwd_wide_kernel<D, STAGES, BIAS>>(L::kAlloc)) return ATTN_ERR_LAUNCH;
@@ -59,7 +57,7 @@ attn_status launch_bwd_wide(const CUtensorMap& mq, const CUtensorMap& mk, const 
   if (grid > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
   if (grid == 0) return ATTN_OK;
   attn::attn_bwd_wide_kernel<D, STAGES, BIAS>
-      <<<dim3(static_cast<unsigned>(grid)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mdo, mdqt, p);
+      <<<dim3(static_cast<unsigned>(grid)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mdo, mdq, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return ATTN_OK;
@@ -67,9 +65,7 @@ attn_status launch_bwd_wide(const CUtensorMap& mq, const CUtensorMap& mk, const 
 
 // Bytes of the f32 dQ accumulator for head dim d.
 size_t bwd_acc_bytes(int B, int Hq, int Nq, int d) {
-  const size_t bh = static_cast<size_t>(B) * Hq;
-  return bwd_uses_wide(d) ? bh * d * static_cast<size_t>(bwd_wide_ld(Nq)) * sizeof(float)
-                          : bh * static_cast<size_t>(Nq) * d * sizeof(float);
+  return static_cast<size_t>(B) * Hq * static_cast<size_t>(Nq) * d * sizeof(float);
 }
 
 bool bwd_head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
@@ -144,11 +140,16 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
 
   const size_t rows = static_cast<size_t>(B) * Hq * Nq;
   float* dsum = static_cast<float*>(workspace);
-  float* dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + bwd_align(rows * sizeof(float)));
+  // f32 gradients: dQ is accumulated in place in the caller's dq (zeroed by
+  // the prep kernel), so no conversion pass follows; bf16: in the workspace.
+  const bool dq_in_place = grad_dtype == ATTN_F32;
+  float* dq_acc = dq_in_place ? static_cast<float*>(dq)
+                              : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                         bwd_align(rows * sizeof(float)));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int sms = sm_count();
   if (rows > 0) {
-    const long long blocks = std::min<long long>((static_cast<long long>(rows) + 7) / 8, 8LL * sms);
+    const long long blocks = std::min<long long>((static_cast<long long>(rows) * d / 8 + 255) / 256, 16LL * sms);
     attn::bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), dsum, dq_acc,
         static_cast<long long>(rows), d, static_cast<long long>(bwd_acc_bytes(B, Hq, Nq, d) / 16));
@@ -169,8 +170,7 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
       return ATTN_ERR_LAUNCH;
     // With Nq == 0 no dQ chunk is ever written; the map then describes one row.
     void* acc_base = Nq > 0 ? static_cast<void*>(dq_acc) : workspace;
-    const bool acc_ok = bwd_uses_wide(d) ? encode_dqt_map(&mdq, acc_base, Nq > 0 ? Nq : 1,
-                                                          bwd_wide_ld(Nq > 0 ? Nq : 1), d, Nq > 0 ? B * Hq : 1)
+    const bool acc_ok = bwd_uses_wide(d) ? encode_dq_rows_map(&mdq, acc_base, d, Nq > 0 ? Nq : 1, Nq > 0 ? B * Hq : 1)
                                          : encode_dq_map(&mdq, acc_base, d, Nq > 0 ? Nq : 1, Nq > 0 ? B * Hq : 1);
     if (!acc_ok) return ATTN_ERR_LAUNCH;
     attn::BwdParams p;
@@ -197,19 +197,10 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
     if (st != ATTN_OK) return st;
   }
 
-  if (rows > 0 && bwd_uses_wide(d)) {
-    // Transpose the [bh][d][q] accumulator back to dQ[bh][q][d].
-    const dim3 grid(static_cast<unsigned>((Nq + 31) / 32), static_cast<unsigned>(d / 32),
-                    static_cast<unsigned>(std::min<long long>(static_cast<long long>(B) * Hq, 65535)));
-    attn::bwd_post_transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(dq_acc, dq, B * Hq, Nq, bwd_wide_ld(Nq), d,
-                                                                  grad_dtype == ATTN_F32 ? 1 : 0);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-  } else if (rows > 0) {
+  if (rows > 0 && !dq_in_place) {
     const long long n4 = static_cast<long long>(rows) * d / 4;
     const long long blocks = std::min<long long>((n4 + 255) / 256, 8LL * sms);
-    attn::bwd_post_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(dq_acc, dq, n4,
-                                                                      grad_dtype == ATTN_F32 ? 1 : 0);
+    attn::bwd_post_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(dq_acc, dq, n4, 0);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }

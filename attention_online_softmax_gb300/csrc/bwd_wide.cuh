@@ -20,8 +20,8 @@
 //   P^T, dS^T as bf16 over the dP^T columns
 //   dV_h += P^T dO_h,  dK_h += dS^T Q_h            (A from tensor memory)
 //   dQ^T_h = K_h^T dS^T [128 head-dim rows][64 queries] (dS^T staged in shared
-//            memory), added to a transposed f32 accumulator dQacc^T[bh][d][q]
-//            by TMA reduce-adds; the post kernel transposes it back.
+//            memory), staged back as [query][head dim] and added to the f32
+//            dQ accumulator [bh][q][d] by TMA reduce-adds.
 // Tensor memory: dK_h 128, dV_h 128, and two slots of S^T (then dQ^T) and dP^T
 // (then P^T, dS^T), 64 columns each: the next item's score products run while
 // the weight warps work on the current item.
@@ -50,7 +50,7 @@ struct BwdWideLayout {
   static constexpr int kQOff = kVOff + kKVTile;        // STAGES x (Q tile, dO tile)
   static constexpr int kStage = 2 * kQTile;
   static constexpr int kDSOff = kQOff + STAGES * kStage;  // dS^T [128 keys][64 queries] bf16 (16 KB)
-  // dQ^T staging, [128 head-dim rows][32 queries] f32 chunks: two buffers at
+  // dQ staging, [32 queries][128 head-dim columns] f32 chunks: two buffers at
   // D = 128, one at D = 256 (no room for a second).
   static constexpr int kNumStg = D == 128 ? 2 : 1;
   static constexpr int kStgOff = kDSOff + 16384;
@@ -79,38 +79,11 @@ struct BwdWideLayout {
   static_assert(kBytes + 128 <= 232448, "shared memory budget");
 };
 
-// dq[bh][q][c] = dqT[bh][c][q] (f32 accumulator, rows of ld floats) as bf16 (RNE) or f32;
-// one 32 x 32 tile per block of 32 x 8 threads.
-__global__ void bwd_post_transpose_kernel(const float* dqT, void* dq, int BH, int Nq, int ld, int d, int g_f32) {
-  __shared__ float tile[32][33];
-  const int q0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
-  for (int bh = blockIdx.z; bh < BH; bh += gridDim.z) {
-    const float* src = dqT + static_cast<size_t>(bh) * d * ld;
-    for (int r = threadIdx.y; r < 32; r += 8) {
-      const int q = q0 + threadIdx.x;
-      tile[r][threadIdx.x] = q < Nq ? src[static_cast<size_t>(c0 + r) * ld + q] : 0.f;
-    }
-    __syncthreads();
-    for (int r = threadIdx.y; r < 32; r += 8) {
-      const int q = q0 + r;
-      if (q >= Nq) continue;
-      const size_t off = (static_cast<size_t>(bh) * Nq + q) * d + c0 + threadIdx.x;
-      const float v = tile[threadIdx.x][r];
-      if (g_f32) {
-        static_cast<float*>(dq)[off] = v;
-      } else {
-        static_cast<uint16_t*>(dq)[off] = static_cast<uint16_t>(pack_bf16(v, 0.f) & 0xFFFFu);
-      }
-    }
-    __syncthreads();
-  }
-}
-
 template <int D, int STAGES, bool BIAS>
 __global__ void __launch_bounds__(480, 1)
     attn_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                         const __grid_constant__ CUtensorMap tmDQT, const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using L = BwdWideLayout<D, STAGES>;
   constexpr int BQ = L::kBQ;
   extern __shared__ uint8_t smem_raw[];
@@ -365,11 +338,13 @@ __global__ void __launch_bounds__(480, 1)
   } else if (warp >= 10 && warp < 14) {
     // ---------------------------------------------------------------- dQ^T read-out
     // dQ^T of item m (TMEM lane = head-dim row of half h, in the S^T columns
-    // of slot m & 1), 32 query columns at a time: scale, stage [128 rows][32]
-    // f32 (128-byte swizzle), and one thread adds the chunk into the f32
-    // accumulator with a TMA reduce.  A buffer is written again once its
-    // previous reduce has read it (the issuing thread waits for that read only
-    // then, so reduces overlap the next chunks).
+    // of slot m & 1), 32 query columns at a time: scaled and staged as
+    // [32 queries][128 head-dim columns] f32 -- the accumulator's own [q][d]
+    // layout (for a fixed query the warp's lanes write 32 consecutive
+    // floats) -- and one thread adds the chunk into the f32 accumulator with a
+    // TMA reduce.  A buffer is written again once its previous reduce has read
+    // it (the issuing thread waits for that read only then, so reduces
+    // overlap the next chunks).
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -401,20 +376,16 @@ __global__ void __launch_bounds__(480, 1)
           ok = __all_sync(0xFFFFFFFFu, mbar_wait(&red_free[b], (use - 1) & 1, 86));
           if (!ok) break;
         }
-        const uint32_t stg = sbase + L::kStgOff + b * 16384 + row * 128;
+        const uint32_t stg = sbase + L::kStgOff + b * 16384 + row * 4;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          st_shared_v4(stg + ((k ^ (row & 7)) << 4), __float_as_uint(__uint_as_float(v[c][4 * k]) * p.scale),
-                       __float_as_uint(__uint_as_float(v[c][4 * k + 1]) * p.scale),
-                       __float_as_uint(__uint_as_float(v[c][4 * k + 2]) * p.scale),
-                       __float_as_uint(__uint_as_float(v[c][4 * k + 3]) * p.scale));
+        for (int q = 0; q < 32; ++q) st_shared_f32(stg + q * 512, __uint_as_float(v[c][q]) * p.scale);
         fence_proxy_async_smem();
         mbar_arrive(&red_full[b]);
         if (issuer) {
           if (!mbar_wait(&red_full[b], use & 1, 87)) {
             ok = false;
           } else {
-            tma_reduce_add_3d(&tmDQT, smem + L::kStgOff + b * 16384, q0 + c * 32, h * 128, bh);
+            tma_reduce_add_3d(&tmDQ, smem + L::kStgOff + b * 16384, h * 128, q0 + c * 32, bh);
             bulk_commit();
           }
         }

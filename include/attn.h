@@ -194,9 +194,9 @@ ATTN_API attn_status attn_prefill_paged(const void* q, const void* kcache, const
 
 /*
  * Bytes of scratch memory attn_bwd() needs: D = rowsum(dO * O) per query row
- * (f32) and an f32 dQ accumulator, [B, Hq, Nq, 64] for d = 64 and the
- * transposed [B, Hq, d, round_up(Nq, 4)] for d = 128 and 256, each rounded up
- * to 256.  0 on invalid input (including d other than 64, 128, 256).
+ * (f32) and an f32 dQ accumulator [B, Hq, Nq, d] (used when the gradients
+ * are bf16; f32 gradients accumulate in dq itself), each rounded up to 256.
+ * 0 on invalid input (including d other than 64, 128, 256).
  * Source: "Compilers and Kernels", section "A kernel implements a bounded
  * contract" (a kernel states the workspace it needs).
  */
@@ -218,9 +218,9 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int d);
  *   grad_dtype.  d must be 64, 128 or 256 (else ATTN_ERR_UNSUPPORTED).
  *   workspace: device scratch of attn_bwd_workspace_size() bytes, 16-byte
  *   aligned, caller-owned, not shared by overlapping calls.
- * Three kernels on `stream` (rows D and a zeroed dQ accumulator; the fused
+ * Two or three kernels on `stream` (rows D and a zeroed dQ accumulator; the fused
  * backward, one CTA per (batch, kv head, 128-key tile), two at d = 256 (one
- * per half of the head dim); the dQ conversion, a transpose at d >= 128).
+ * per half of the head dim); the bf16 dQ conversion, when grad_dtype is bf16).
  * dK and dV are deterministic; dQ sums its per-key-tile parts with TMA
  * reduce-adds in no fixed order, so its last bits can differ from run to run.
  */

@@ -193,16 +193,14 @@ def test_decode_kernel_name_follows_the_plan(abi):
 
 
 def test_bwd_workspace_size(abi):
-    # D per query row (f32) and the f32 dQ accumulator, each rounded up to 256
-    # bytes; at d = 128 and 256 the accumulator is transposed with rows of Nq
-    # rounded up to 4 floats.
+    # D per query row (f32) and the f32 dQ accumulator [B, Hq, Nq, d], each
+    # rounded up to 256 bytes.
     ws = abi.attn_bwd_workspace_size
     up = lambda n: (n + 255) // 256 * 256
     for B, Hq, Nq in ((2, 32, 4096), (1, 3, 77), (1, 1, 1)):
         rows = B * Hq * Nq
-        assert ws(B, Hq, Nq, 64) == up(rows * 4) + up(rows * 64 * 4)
-        for d in (128, 256):
-            assert ws(B, Hq, Nq, d) == up(rows * 4) + up(B * Hq * d * ((Nq + 3) // 4 * 4) * 4)
+        for d in (64, 128, 256):
+            assert ws(B, Hq, Nq, d) == up(rows * 4) + up(rows * d * 4)
     for bad in ((1, 2, 64, 32), (1, 2, 64, 96), (1, 0, 64, 128), (-1, 2, 64, 128)):
         assert ws(*bad) == 0
 
