@@ -4,6 +4,8 @@
 // intermediates; the derivative of the forward of "Compilers and Kernels",
 // section "FlashAttention changes the algorithm around IO").
 //
+// This file's kernel serves head dim 64 (bwd_wide.cuh serves 128 and 256);
+// the prep and conversion kernels and the bias helpers serve all three.
 // Per (batch, kv head, 128-key tile) one CTA keeps K, V, and the dK, dV
 // accumulators resident and walks every (query head of the group, 128-row
 // query tile) whose rows see its keys:

@@ -57,12 +57,13 @@ struct BwdWideLayout {
   static constexpr int kRowOff = kStgOff + kNumStg * 16384;  // 2 x (-LSE log2 e [64], D [64]) f32
   static constexpr int kRowBytes = 2 * kBQ * 4;
   static constexpr int kBarOff = kRowOff + 2 * kRowBytes;
-  // kv_full, stage_full[S], stage_empty[S], q_full[S], q_empty[S], scores_full[2] (S^T and dP^T of a
-  // slot), ds_full, dq_full, dq_free[2] (per slot), dkv_done, sc_done, rows_ready[2], red_full[2],
-  // red_free[2] (per staging
-  // buffer).  With two or more stages an item's Q and dO share stage_full / stage_empty; with one stage
-  // (D = 256) dO uses those and Q its own pair, so that dO, which the item's first product reads and
-  // whose last reader (dV) finishes first, moves on its own.
+  // Barriers: kv_full, stage_full[S], stage_empty[S], q_full[S], q_empty[S],
+  // scores_full[2] (S^T and dP^T of a slot), ds_full, dq_full, dq_free[2]
+  // (per slot), dkv_done, sc_done, rows_ready[2], red_full[2] and
+  // red_free[2] (per staging buffer).  With two or more stages an item's Q
+  // and dO share stage_full / stage_empty; with one stage (D = 256) dO uses
+  // those and Q its own pair, so that dO, which the item's first product
+  // reads and whose last reader (dV) finishes first, moves on its own.
   static constexpr bool kSplitOps = STAGES == 1;
   static constexpr int kNumBars = 1 + 4 * STAGES + 2 + 6 + 6;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
