@@ -185,13 +185,20 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const 
       "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// global box at (x, y, z) = smem box, by the TMA unit (rows past the tensor's
+// extent are not written).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed bulk groups of this thread still read shared memory.
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D, int STAGES, bool BIAS>
 __global__ void __launch_bounds__(320, 1)
@@ -608,8 +615,9 @@ __global__ void __launch_bounds__(320, 1)
     }
   }
 
-  // Every dQ reduce of this CTA must have completed before it exits.
-  if (warp >= 2 && lane == 0 && (warp & 3) == 2) bulk_wait_all();
+  // Every dQ reduce of this CTA must have read its staging buffer before the
+  // CTA (and its shared memory) ends; the global adds complete with the grid.
+  if (warp >= 2 && lane == 0 && (warp & 3) == 2) bulk_wait_read<0>();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -48,8 +48,8 @@ bool encode_dq_rows_map(CUtensorMap* map, void* base, int d, int rows, int heads
 
 template <int D, int STAGES, bool BIAS>
 attn_status launch_bwd_wide(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                            const CUtensorMap& mdo, const CUtensorMap& mdq, const attn::BwdParams& p,
-                            cudaStream_t stream) {
+                            const CUtensorMap& mdo, const CUtensorMap& mdq, const CUtensorMap& mdk,
+                            const CUtensorMap& mdv, const attn::BwdParams& p, cudaStream_t stream) {
   using L = attn::BwdWideLayout<D, STAGES>;
   if (!ensure_smem<attn::attn_bwd_wide_kernel<D, STAGES, BIAS>>(L::kAlloc)) return ATTN_ERR_LAUNCH;
   // kSplit CTAs (head-dim halves) per (key tile, batch, kv head), key tile 0 first.
@@ -57,7 +57,7 @@ attn_status launch_bwd_wide(const CUtensorMap& mq, const CUtensorMap& mk, const 
   if (grid > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
   if (grid == 0) return ATTN_OK;
   attn::attn_bwd_wide_kernel<D, STAGES, BIAS>
-      <<<dim3(static_cast<unsigned>(grid)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mdo, mdq, p);
+      <<<dim3(static_cast<unsigned>(grid)), L::kThreads, L::kAlloc, stream>>>(mq, mk, mv, mdo, mdq, mdk, mdv, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return ATTN_OK;
@@ -72,10 +72,11 @@ bool bwd_head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
 
 template <bool BIAS>
 attn_status launch_bwd_d(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const CUtensorMap& mdo, const CUtensorMap& mdq, const attn::BwdParams& p, cudaStream_t s) {
+                         const CUtensorMap& mdo, const CUtensorMap& mdq, const CUtensorMap& mdk,
+                         const CUtensorMap& mdv, const attn::BwdParams& p, cudaStream_t s) {
   return d == 64    ? launch_bwd<64, 3, BIAS>(mq, mk, mv, mdo, mdq, p, s)
-         : d == 128 ? launch_bwd_wide<128, 3, BIAS>(mq, mk, mv, mdo, mdq, p, s)
-                    : launch_bwd_wide<256, 1, BIAS>(mq, mk, mv, mdo, mdq, p, s);
+         : d == 128 ? launch_bwd_wide<128, 3, BIAS>(mq, mk, mv, mdo, mdq, mdk, mdv, p, s)
+                    : launch_bwd_wide<256, 1, BIAS>(mq, mk, mv, mdo, mdq, mdk, mdv, p, s);
 }
 
 attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -173,6 +174,14 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
     const bool acc_ok = bwd_uses_wide(d) ? encode_dq_rows_map(&mdq, acc_base, d, Nq > 0 ? Nq : 1, Nq > 0 ? B * Hq : 1)
                                          : encode_dq_map(&mdq, acc_base, d, Nq > 0 ? Nq : 1, Nq > 0 ? B * Hq : 1);
     if (!acc_ok) return ATTN_ERR_LAUNCH;
+    // bf16 dK, dV leave the 64-query kernel by TMA stores ([128 keys][64
+    // columns] boxes, like the K and V loads); f32 ones by direct stores (the
+    // maps then describe k and are not used).
+    CUtensorMap mdk, mdv;
+    const bool bf16_out = grad_dtype == ATTN_BF16;
+    if (!encode_rows_map(&mdk, bf16_out ? dk : k, d, Nk, B * Hkv, 128) ||
+        !encode_rows_map(&mdv, bf16_out ? dv : k, d, Nk, B * Hkv, 128))
+      return ATTN_ERR_LAUNCH;
     attn::BwdParams p;
     p.dk = dk;
     p.dv = dv;
@@ -193,7 +202,8 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
     p.bias = biased ? static_cast<const uint16_t*>(mask->bias) : nullptr;
     p.bias_sb = biased ? mask->bias_stride_b : 0;
     p.bias_sh = biased ? mask->bias_stride_h : 0;
-    st = biased ? launch_bwd_d<true>(d, mq, mk, mv, mdo, mdq, p, s) : launch_bwd_d<false>(d, mq, mk, mv, mdo, mdq, p, s);
+    st = biased ? launch_bwd_d<true>(d, mq, mk, mv, mdo, mdq, mdk, mdv, p, s)
+                : launch_bwd_d<false>(d, mq, mk, mv, mdo, mdq, mdk, mdv, p, s);
     if (st != ATTN_OK) return st;
   }
 

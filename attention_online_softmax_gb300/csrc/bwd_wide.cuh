@@ -59,13 +59,13 @@ struct BwdWideLayout {
   static constexpr int kBarOff = kRowOff + 2 * kRowBytes;
   // Barriers: kv_full, stage_full[S], stage_empty[S], q_full[S], q_empty[S],
   // scores_full[2] (S^T and dP^T of a slot), ds_full, dq_full, dq_free[2]
-  // (per slot), dkv_done, sc_done, rows_ready[2], red_full[2] and
-  // red_free[2] (per staging buffer).  With two or more stages an item's Q
+  // (per slot), dkv_done, sc_done, rows_ready[2], red_full[2], red_free[2]
+  // (per staging buffer) and wo_full (dK, dV staged for their TMA stores).  With two or more stages an item's Q
   // and dO share stage_full / stage_empty; with one stage (D = 256) dO uses
   // those and Q its own pair, so that dO, which the item's first product
   // reads and whose last reader (dV) finishes first, moves on its own.
   static constexpr bool kSplitOps = STAGES == 1;
-  static constexpr int kNumBars = 1 + 4 * STAGES + 2 + 6 + 6;
+  static constexpr int kNumBars = 1 + 4 * STAGES + 2 + 6 + 6 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 128;          // the base is checked for 1024-byte alignment
@@ -84,7 +84,8 @@ template <int D, int STAGES, bool BIAS>
 __global__ void __launch_bounds__(480, 1)
     attn_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                         const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDKo,
+                         const __grid_constant__ CUtensorMap tmDVo, const BwdParams p) {
   using L = BwdWideLayout<D, STAGES>;
   constexpr int BQ = L::kBQ;
   extern __shared__ uint8_t smem_raw[];
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(480, 1)
   uint64_t* rows_ready = sc_done + 1;   // [2]
   uint64_t* red_full = rows_ready + 2;  // [2] a [128][32] f32 dQ^T chunk is staged in buffer b
   uint64_t* red_free = red_full + 2;    // [2] buffer b's previous TMA reduce has finished reading it
+  uint64_t* wo_full = red_free + 2;     // the weight warps have staged dK, dV (bf16 gradients)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
 
   const int warp = threadIdx.x >> 5;
@@ -156,6 +158,7 @@ __global__ void __launch_bounds__(480, 1)
       mbar_init(&red_full[i], 128);
       mbar_init(&red_free[i], 1);
     }
+    mbar_init(wo_full, 8);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -394,8 +397,9 @@ __global__ void __launch_bounds__(480, 1)
         if (!ok) break;
       }
     }
-    // Every dQ^T reduce of this CTA must have completed before it exits.
-    if (issuer) bulk_wait_all();
+    // Every dQ reduce of this CTA must have read its staging buffer before the
+    // CTA (and its shared memory) ends; the global adds complete with the grid.
+    if (issuer) bulk_wait_read<0>();
   } else {
     // ---------------------------------------------------------------- key rows: the weights
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
@@ -518,7 +522,46 @@ __global__ void __launch_bounds__(480, 1)
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(dkv_done, 0, 88));
       if (ok) tc_fence_after();
     }
-    if (ok) {
+    if (ok && !p.g_f32 && n_items > 0) {
+      // bf16 gradients: each thread stages its key row's 64 columns of dK_h
+      // and dV_h as bf16 in the idle Q/dO ring ([128 keys][64 columns]
+      // boxes, 128-byte swizzle: dK half 0, dK half 1, dV half 0, dV half 1),
+      // and one thread writes the four boxes with TMA stores (rows past Nk
+      // are not written).
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? L::kColDK : L::kColDV;
+        const float mul = which == 0 ? p.scale : 1.f;
+        const uint32_t box = sbase + L::kQOff + (which * 2 + half) * (128 * 128) + row * 128;
+#pragma unroll 1
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + col + (half * 2 + c2) * 32, v);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int x = 8 * u;
+            st_shared_v4(box + (((c2 * 4 + u) ^ (row & 7)) << 4),
+                         pack_bf16(__uint_as_float(v[x]) * mul, __uint_as_float(v[x + 1]) * mul),
+                         pack_bf16(__uint_as_float(v[x + 2]) * mul, __uint_as_float(v[x + 3]) * mul),
+                         pack_bf16(__uint_as_float(v[x + 4]) * mul, __uint_as_float(v[x + 5]) * mul),
+                         pack_bf16(__uint_as_float(v[x + 6]) * mul, __uint_as_float(v[x + 7]) * mul));
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(wo_full);
+      if (threadIdx.x == 64) {
+        if (mbar_wait(wo_full, 0, 92)) {
+#pragma unroll
+          for (int bx = 0; bx < 4; ++bx)
+            tma_store_3d(bx < 2 ? &tmDKo : &tmDVo, smem + L::kQOff + bx * (128 * 128), h * 128 + (bx & 1) * 64, k0,
+                         bkv);
+          bulk_commit();
+          bulk_wait_read<0>();  // the boxes are read before the CTA ends; the writes complete with the grid
+        }
+      }
+    } else if (ok) {
       const bool store = kj < p.Nk;
       const size_t off = (static_cast<size_t>(bkv) * p.Nk + kj) * D + h * 128;
 #pragma unroll 1
