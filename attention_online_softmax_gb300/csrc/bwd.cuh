@@ -41,6 +41,7 @@ struct BwdParams {
   float scale;         // > 0
   float scale_log2;    // scale * log2(e)
   // Additive bias C of the forward (used by the BIAS instantiations only):
+  int head_group;                 // (batch, kv head) pairs whose key tiles are handed out together
   int window_left;                // > 0: query i keeps keys j > i + (Nk - Nq) - window_left
   const float* alibi;             // [Hq] slopes or null: C += alibi[h] (j - i - (Nk - Nq))
   const uint16_t* bias;           // bf16 or null: C += bias[b sb + h sh + i Nk + j]

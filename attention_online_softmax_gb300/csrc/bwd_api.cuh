@@ -197,6 +197,15 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
     p.g_f32 = grad_dtype == ATTN_F32 ? 1 : 0;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
+    // Head groups for the 64-query kernel's block order: as many (batch, kv
+    // head) pairs as keep their Q, dO and f32 dQ accumulator (8 bytes per
+    // query element) within ~64 MB of L2.
+    {
+      const long long per_pair = static_cast<long long>(Hq / Hkv) * Nq * d * 8;
+      long long g = per_pair > 0 ? (64LL << 20) / per_pair : static_cast<long long>(B) * Hkv;
+      g = std::max(1LL, std::min(g, static_cast<long long>(B) * Hkv));
+      p.head_group = static_cast<int>(g);
+    }
     p.window_left = biased ? mask->window_left : 0;
     p.alibi = biased ? mask->alibi_slopes : nullptr;
     p.bias = biased ? static_cast<const uint16_t*>(mask->bias) : nullptr;
