@@ -239,8 +239,15 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int BHkv = p.B * p.Hkv;
-  const int kt = blockIdx.x / BHkv;          // key tile (longest-first: tile 0 is seen by the most rows)
-  const int bkv = blockIdx.x - kt * BHkv;    // batch * Hkv + kv head
+  // Blocks in groups of head_group (batch, kv head) pairs, key tile 0 first
+  // within a group (see bwd_wide.cuh).
+  const int nkt = (p.Nk + 127) / 128;
+  const int gspan = p.head_group * nkt;
+  const int grp = static_cast<int>(blockIdx.x) / gspan;
+  const int in_grp = static_cast<int>(blockIdx.x) - grp * gspan;
+  const int gcount = min(p.head_group, BHkv - grp * p.head_group);
+  const int kt = in_grp / gcount;
+  const int bkv = grp * p.head_group + (in_grp - kt * gcount);
   const int b = bkv / p.Hkv;
   const int kvh = bkv - b * p.Hkv;
   const int k0 = kt * 128;
