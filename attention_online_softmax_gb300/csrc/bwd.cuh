@@ -40,8 +40,9 @@ struct BwdParams {
   int g_f32;           // gradients written as f32 (else bf16)
   float scale;         // > 0
   float scale_log2;    // scale * log2(e)
-  // Additive bias C of the forward (used by the BIAS instantiations only):
   int head_group;                 // (batch, kv head) pairs whose key tiles are handed out together
+  // Additive bias C of the forward: the window in every instantiation, the
+  // ALiBi and dense terms in the BIAS ones only.
   int window_left;                // > 0: query i keeps keys j > i + (Nk - Nq) - window_left
   const float* alibi;             // [Hq] slopes or null: C += alibi[h] (j - i - (Nk - Nq))
   const uint16_t* bias;           // bf16 or null: C += bias[b sb + h sh + i Nk + j]
@@ -56,6 +57,10 @@ struct BwdBiasRow {
   const uint16_t* brow;  // bias + b sb + h sh + q0 Nk + kj, or null
   long long bstride;     // Nk
 };
+
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
 
 __device__ __forceinline__ BwdBiasRow bwd_bias_row(const BwdParams& p, int bh, int q0, int kj) {
   BwdBiasRow r;
@@ -458,7 +463,7 @@ __global__ void __launch_bounds__(320, 1)
       // (causal) kj <= q0 + c + diag; tiles wholly inside skip the test.
       int c_hi = p.Nq - q0;                                     // columns >= c_hi: past Nq
       const int c_lo = p.causal ? kj - diag - q0 : -0x7FFFFFFF;  // columns < c_lo: masked
-      if (BIAS && p.window_left > 0) c_hi = min(c_hi, kj - diag + p.window_left - q0);  // left window
+      if (p.window_left > 0) c_hi = min(c_hi, kj - diag + p.window_left - q0);  // left window
       const bool key_ok = kj < p.Nk;
       const bool masked = !(key_ok && c_lo <= c0 && c_hi >= c0 + 64);
       BwdBiasRow br;

@@ -211,7 +211,9 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
     p.bias = biased ? static_cast<const uint16_t*>(mask->bias) : nullptr;
     p.bias_sb = biased ? mask->bias_stride_b : 0;
     p.bias_sh = biased ? mask->bias_stride_h : 0;
-    st = biased ? launch_bwd_d<true>(d, mq, mk, mv, mdo, mdq, mdk, mdv, p, s)
+    // A left window alone needs no bias term: every variant applies it.
+    const bool bias_terms = p.alibi != nullptr || p.bias != nullptr;
+    st = bias_terms ? launch_bwd_d<true>(d, mq, mk, mv, mdo, mdq, mdk, mdv, p, s)
                 : launch_bwd_d<false>(d, mq, mk, mv, mdo, mdq, mdk, mdv, p, s);
     if (st != ATTN_OK) return st;
   }

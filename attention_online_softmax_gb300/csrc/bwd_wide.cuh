@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(480, 1)
       if (!ok) break;
       int c_hi = p.Nq - q0;
       const int c_lo = p.causal ? kj - diag - q0 : -0x7FFFFFFF;
-      if (BIAS && p.window_left > 0) c_hi = min(c_hi, kj - diag + p.window_left - q0);  // left window
+      if (p.window_left > 0) c_hi = min(c_hi, kj - diag + p.window_left - q0);  // left window
       const bool key_ok = kj < p.Nk;
       const bool masked = !(key_ok && c_lo <= c0 && c_hi >= c0 + 32);
       // The bias of this key row's 32 query columns, loaded before the wait
@@ -461,6 +461,15 @@ __global__ void __launch_bounds__(480, 1)
         const BwdBiasRow br = bwd_bias_row(p, bh, q0, kj);
 #pragma unroll
         for (int e = 0; e < 32; ++e) cb[e] = bwd_bias_at(br, c0 + e, key_ok, c_lo, c_hi);
+        // The next item's dense-bias lines of this warp's 32 keys (one query
+        // row per lane) into L2, so that its loads wait on L2 instead of DRAM.
+        if (p.bias != nullptr && n + 1 < n_items) {
+          const int qn = item_q0(n + 1) + c0 + lane;
+          if (qn < p.Nq && kj - lane < p.Nk) {
+            const BwdBiasRow bn = bwd_bias_row(p, item_bh(n + 1), item_q0(n + 1), kj - lane);
+            prefetch_l2(bn.brow + static_cast<long long>(c0 + lane) * bn.bstride);
+          }
+        }
       }
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(&scores_full[b2], slot_par, 82));
       if (!ok) break;

@@ -966,12 +966,16 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       // scores.  In base 2: x = s * sl + (alibi * (j - i - diag) + bias) * log2(e).
       constexpr bool biased = BIAS != 0;  // instantiated separately: the plain path keeps its registers
       const int hq = bh % p.Hq;
-      const float slope2 = p.alibi != nullptr ? p.alibi[hq] * 1.4426950408889634f : 0.f;
       const uint16_t* brow = nullptr;
       if (BIAS == 1 && p.bias != nullptr && qrow < u.nq)
         brow = p.bias + static_cast<long long>(bh / p.Hq) * p.bias_sb + static_cast<long long>(hq) * p.bias_sh +
                static_cast<long long>(qrow) * p.Nk;
-      const float mul = biased ? 1.f : sl;  // multiplier of r[] in the exponent
+      // Multiplier of r[] in the exponent: the biased paths keep r[] in
+      // natural units (s * scale + alibi * distance + bias) and convert to
+      // base 2 there.
+      const float mul = biased ? 1.4426950408889634f : sl;
+      const float scale_nat = sl * 0.6931471805599453f;
+      const float slope = p.alibi != nullptr ? p.alibi[hq] : 0.f;
       // l sums the exact weights (for LSE); lr sums the bf16-rounded weights
       // the P V product uses, so O = o / lr is an exact convex combination of
       // V rows before output rounding.
@@ -1002,7 +1006,13 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
           // Row `row` of the staged bias tile: 16 chunks of 8 keys, chunk c of
           // a 128-byte row at position c ^ (row & 7) (the TMA 128-byte
           // swizzle), so the 8 rows of each quarter-warp phase hit distinct banks.
-          const float base = slope2 * static_cast<float>(k0 - qrow - diag);
+          // Per column pair: r = s * scale + (alibi * dist + bias), two paired
+          // FMAs; dist = j - i - diag runs in four exact integer-valued chains
+          // (one per pair of an 8-key chunk), each advanced by 8 per chunk.
+          const float d00 = static_cast<float>(k0 - qrow - diag);
+          float dist[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dist[e] = d00 + static_cast<float>(e);
           const int bs = bcnt % bias_ring<BIAS>();
           ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bias_full[bs], (bcnt / bias_ring<BIAS>()) & 1, 24));
           if (!ok) break;
@@ -1014,17 +1024,20 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int cc = c * 8 + 2 * e;
-              const float b0 = fmaf(bf16lo(ws[e]), 1.4426950408889634f, base + slope2 * static_cast<float>(cc));
-              const float b1 = fmaf(bf16hi(ws[e]), 1.4426950408889634f, base + slope2 * static_cast<float>(cc + 1));
-              r[cc] = __float_as_uint(fmaf(__uint_as_float(r[cc]), sl, b0));
-              r[cc + 1] = __float_as_uint(fmaf(__uint_as_float(r[cc + 1]), sl, b1));
+              float u0, u1, y0, y1;
+              ffma2(u0, u1, slope, slope, dist[2 * e], dist[2 * e + 1], bf16lo(ws[e]), bf16hi(ws[e]));
+              ffma2(y0, y1, __uint_as_float(r[cc]), __uint_as_float(r[cc + 1]), scale_nat, scale_nat, u0, u1);
+              r[cc] = __float_as_uint(y0);
+              r[cc + 1] = __float_as_uint(y1);
+              fadd2(dist[2 * e], dist[2 * e + 1], dist[2 * e], dist[2 * e + 1], 8.f, 8.f);
             }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&bias_empty[bs]);
           ++bcnt;
         } else if (biased) {
-          const float base = slope2 * static_cast<float>(k0 - qrow - diag);
+          // The same terms in the same order as the staged path above.
+          const float d00 = static_cast<float>(k0 - qrow - diag);
           if (brow != nullptr) {
             // The row's bias for this tile, read as aligned 32-bit words (the
             // bias buffer is 4-byte aligned; when the tile starts on an odd
@@ -1040,15 +1053,22 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
 #pragma unroll
             for (int i = 0; i < kBN / 2; ++i) {
               const uint32_t pr = __funnelshift_r(wv[i], wv[i + 1], 16u * odd);
-              const float b0 = fmaf(bf16lo(pr), 1.4426950408889634f, base + slope2 * static_cast<float>(2 * i));
-              const float b1 = fmaf(bf16hi(pr), 1.4426950408889634f, base + slope2 * static_cast<float>(2 * i + 1));
-              r[2 * i] = __float_as_uint(fmaf(__uint_as_float(r[2 * i]), sl, b0));
-              r[2 * i + 1] = __float_as_uint(fmaf(__uint_as_float(r[2 * i + 1]), sl, b1));
+              float u0, u1, y0, y1;
+              ffma2(u0, u1, slope, slope, d00 + static_cast<float>(2 * i), d00 + static_cast<float>(2 * i + 1),
+                    bf16lo(pr), bf16hi(pr));
+              ffma2(y0, y1, __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), scale_nat, scale_nat, u0, u1);
+              r[2 * i] = __float_as_uint(y0);
+              r[2 * i + 1] = __float_as_uint(y1);
             }
           } else {
 #pragma unroll
-            for (int cc = 0; cc < kBN; ++cc)
-              r[cc] = __float_as_uint(fmaf(__uint_as_float(r[cc]), sl, base + slope2 * static_cast<float>(cc)));
+            for (int cc = 0; cc < kBN; cc += 2) {
+              float u0, u1, y0, y1;
+              ffma2(u0, u1, slope, slope, d00 + static_cast<float>(cc), d00 + static_cast<float>(cc + 1), 0.f, 0.f);
+              ffma2(y0, y1, __uint_as_float(r[cc]), __uint_as_float(r[cc + 1]), scale_nat, scale_nat, u0, u1);
+              r[cc] = __float_as_uint(y0);
+              r[cc + 1] = __float_as_uint(y1);
+            }
           }
         }
         const bool need_mask = (k0 + kBN > u.nk) || (p.causal && (k0 + kBN - 1 > r0 + diag)) ||
