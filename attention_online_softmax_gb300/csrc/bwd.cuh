@@ -160,24 +160,40 @@ __global__ void bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, float* 
     for (int off = lpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
     if (sub == 0 && r < rows) Dsum[r] = acc;
   }
+  // From the end, so that the rows the backward's first blocks add to are the
+  // ones still in L2 when it starts.
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero4;
        i += static_cast<long long>(gridDim.x) * blockDim.x)
-    reinterpret_cast<float4*>(dq_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    reinterpret_cast<float4*>(dq_acc)[zero4 - 1 - i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-// dq = dq_acc as bf16 (RNE) or f32.
+// dq = dq_acc as bf16 (RNE) or f32.  Each thread has four 16-byte loads in
+// flight per round, and the rounds walk the accumulator from its end: the
+// rows the backward added to last are the ones still in L2.
 __global__ void bwd_post_kernel(const float* dq_acc, void* dq, long long n4, int g_f32) {
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float4 v = reinterpret_cast<const float4*>(dq_acc)[i];
-    if (g_f32) {
-      reinterpret_cast<float4*>(dq)[i] = v;
-    } else {
-      reinterpret_cast<uint2*>(dq)[i] = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+  constexpr int kU = 4;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (long long r0 = 0; r0 < n4; r0 += kU * stride) {
+    float4 v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const long long i = n4 - 1 - (r0 + u * stride + t);
+      if (i >= 0) v[u] = reinterpret_cast<const float4*>(dq_acc)[i];
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const long long i = n4 - 1 - (r0 + u * stride + t);
+      if (i < 0) continue;
+      if (g_f32) {
+        reinterpret_cast<float4*>(dq)[i] = v[u];
+      } else {
+        reinterpret_cast<uint2*>(dq)[i] = make_uint2(pack_bf16(v[u].x, v[u].y), pack_bf16(v[u].z, v[u].w));
+      }
     }
   }
 }

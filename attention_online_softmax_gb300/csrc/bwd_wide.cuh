@@ -368,8 +368,7 @@ __global__ void __launch_bounds__(480, 1)
       if (!ok) break;
       tc_fence_after();
       uint32_t v[2][32];
-      tmem_ld32(lane_base + L::kColS + (m & 1) * BQ, v[0]);
-      tmem_ld32(lane_base + L::kColS + (m & 1) * BQ + 32, v[1]);
+      tmem_ld32x2(lane_base + L::kColS + (m & 1) * BQ, v[0], lane_base + L::kColS + (m & 1) * BQ + 32, v[1]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&dq_free[m & 1]);
@@ -475,10 +474,8 @@ __global__ void __launch_bounds__(480, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t dp_cols = lane_base + L::kColDP + b2 * BQ + c0;
-      uint32_t dp[32];
-      tmem_ld32(dp_cols, dp);
-      uint32_t sv[32];
-      tmem_ld32(lane_base + L::kColS + b2 * BQ + c0, sv);
+      uint32_t dp[32], sv[32];
+      tmem_ld32x2(dp_cols, dp, lane_base + L::kColS + b2 * BQ + c0, sv);
       uint32_t pw[16], dw[16];
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
