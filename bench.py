@@ -296,7 +296,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-config table")
-    ap.add_argument("--profile", choices=["prefill", "prefill_d256", "tiny", "block", "decode", "bwd", "bwd_d256", "chunked"],
+    ap.add_argument("--profile", choices=["prefill", "prefill_d256", "tiny", "block", "decode", "bwd", "bwd_d256", "chunked",
+                                          "alibi"],
                     default=None,
                     help="run one kernel of the step a few times (for an ncu capture) and exit")
     args = ap.parse_args(argv)
@@ -474,6 +475,23 @@ def profile_one(which: str, launches: int = 3) -> int:
         else:
             for _ in range(launches):
                 abi.attn_fwd(q, k, v, o, lse, c.causal, x.scale)
+    elif which == "alibi":
+        # The ALiBi + dense-bias workload: its forward, then its backward.
+        c = configs.ALIBI_BIAS
+        x = make_prefill_inputs(c)
+        q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        slopes, bias = make_mask_inputs(c)
+        kw = dict(window_left=c.window, alibi=slopes.to(dev), bias=bias.to(dev))
+        for _ in range(launches):
+            abi.attn_fwd_masked(q, k, v, o, lse, c.causal, x.scale, **kw)
+        g = torch.Generator().manual_seed(c.seed + 50)
+        dout = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(abi.attn_bwd_workspace_size(c.B, c.Hq, c.Nq, c.d), dtype=torch.uint8, device=dev)
+        for _ in range(launches):
+            abi.attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, c.causal, x.scale, workspace=ws, **kw)
     elif which == "chunked":
         c = configs.CHUNKED
         q_lens, k_lens = configs.chunked_lengths(c)
