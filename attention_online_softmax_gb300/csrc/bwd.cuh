@@ -82,6 +82,21 @@ __device__ __forceinline__ float bwd_bias_at(const BwdBiasRow& r, int c, bool ke
   return v;
 }
 
+// Key tile and (batch, kv head) pair of block `blk` (key-tile blocks, the
+// head-dim halves of d = 256 already folded): blocks come in groups of
+// head_group pairs, within a group key tile 0 first, so the pairs in flight
+// at once share few heads and their Q, dO and dQ accumulator stay in L2.
+__device__ __forceinline__ void bwd_block_tile(const BwdParams& p, int blk, int& kt, int& bkv) {
+  const int nkt = (p.Nk + 127) / 128;
+  const int BHkv = p.B * p.Hkv;
+  const int gspan = p.head_group * nkt;
+  const int grp = blk / gspan;
+  const int in_grp = blk - grp * gspan;
+  const int gcount = min(p.head_group, BHkv - grp * p.head_group);  // pairs in this (possibly smaller last) group
+  kt = in_grp / gcount;
+  bkv = grp * p.head_group + (in_grp - kt * gcount);
+}
+
 // Query tiles [qt_lo, qt_hi) of rows bq whose rows see some key of the key
 // tile [k0, k0 + 128): causal keeps rows i >= k0 - (Nk - Nq), a left window
 // rows i <= min(k0 + 127, Nk - 1) - (Nk - Nq) + window - 1.
@@ -259,16 +274,8 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int BHkv = p.B * p.Hkv;
-  // Blocks in groups of head_group (batch, kv head) pairs, key tile 0 first
-  // within a group (see bwd_wide.cuh).
-  const int nkt = (p.Nk + 127) / 128;
-  const int gspan = p.head_group * nkt;
-  const int grp = static_cast<int>(blockIdx.x) / gspan;
-  const int in_grp = static_cast<int>(blockIdx.x) - grp * gspan;
-  const int gcount = min(p.head_group, BHkv - grp * p.head_group);
-  const int kt = in_grp / gcount;
-  const int bkv = grp * p.head_group + (in_grp - kt * gcount);
+  int kt, bkv;
+  bwd_block_tile(p, static_cast<int>(blockIdx.x), kt, bkv);
   const int b = bkv / p.Hkv;
   const int kvh = bkv - b * p.Hkv;
   const int k0 = kt * 128;

@@ -118,22 +118,12 @@ __global__ void __launch_bounds__(480, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int BHkv = p.B * p.Hkv;
   // Head-dim half of dK, dV, dQ at D = 256 (two CTAs per key tile); key tile
   // 0 first (seen by the most rows).
   const int h = L::kSplit == 2 ? static_cast<int>(blockIdx.x & 1u) : 0;
   const int blk = L::kSplit == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  // Blocks come in groups of head_group (batch, kv head) pairs, within a
-  // group key tile 0 first: the pairs in flight at once share few heads, so
-  // their Q, dO and dQ accumulator stay in L2 while their key tiles pass.
-  const int nkt = (p.Nk + 127) / 128;
-  const int gsz = p.head_group;
-  const int gspan = gsz * nkt;
-  const int grp = blk / gspan;
-  const int in_grp = blk - grp * gspan;
-  const int gcount = min(gsz, BHkv - grp * gsz);  // pairs in this (possibly last, smaller) group
-  const int kt = in_grp / gcount;
-  const int bkv = grp * gsz + (in_grp - kt * gcount);
+  int kt, bkv;
+  bwd_block_tile(p, blk, kt, bkv);
   const int b = bkv / p.Hkv;
   const int kvh = bkv - b * p.Hkv;
   const int k0 = kt * 128;
