@@ -515,9 +515,9 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     // The whole warp: a key tile spans 128 / page_size pages, each loaded as
     // kDI / 64 boxes, one box per lane, so the boxes of an item are issued
     // together.  Lane 0 does the waits, arrivals and the Q loads.  Each lane
-    // keeps the page id of its box for the tiles t-2 .. t+1 around the latest
+    // keeps the page id of its box for the tiles t-2 .. t+2 around the latest
     // K(t) (a value tile is loaded at most two key tiles after its own): the
-    // block-table read of a tile is issued one tile ahead of its first use.  Pages past the context's end are not loaded
+    // block-table read of a tile is issued two tiles ahead of its first use.  Pages past the context's end are not loaded
     // (their keys are masked; their stale rows, real cache rows or zeros, get
     // zero weight).  A value page the context ends inside is loaded on its own
     // barrier; the warp then zeroes its slots past the end before the item is
@@ -590,6 +590,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       int pg_m2 = kNone, pg_m1 = kNone;
       int pg_cur = page_of(0);
       int pg_next = u.T > 1 ? page_of(1) : kNone;
+      int pg_next2 = u.T > 2 ? page_of(2) : kNone;
       int kt_cur = 0;  // tile of the latest K item
       for (int i = 0; i < 2 * L::kH * u.T; ++i, ++item) {
         const int st = item % STAGES;
@@ -599,7 +600,8 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
           pg_m2 = pg_m1;
           pg_m1 = pg_cur;
           pg_cur = pg_next;
-          pg_next = t + 1 < u.T ? page_of(t + 1) : kNone;
+          pg_next = pg_next2;
+          pg_next2 = t + 2 < u.T ? page_of(t + 2) : kNone;
           kt_cur = t;
         }
         int wok = 1;
