@@ -60,12 +60,13 @@ struct BwdWideLayout {
   // Barriers: kv_full, stage_full[S], stage_empty[S], q_full[S], q_empty[S],
   // scores_full[2] (S^T and dP^T of a slot), ds_full, dq_full, dq_free[2]
   // (per slot), dkv_done, sc_done, rows_ready[2], red_full[2], red_free[2]
-  // (per staging buffer) and wo_full (dK, dV staged for their TMA stores).  With two or more stages an item's Q
+  // (per staging buffer), wo_full[2] (dV, dK staged for their TMA stores)
+  // and dv_done (the last dV product has completed).  With two or more stages an item's Q
   // and dO share stage_full / stage_empty; with one stage (D = 256) dO uses
   // those and Q its own pair, so that dO, which the item's first product
   // reads and whose last reader (dV) finishes first, moves on its own.
   static constexpr bool kSplitOps = STAGES == 1;
-  static constexpr int kNumBars = 1 + 4 * STAGES + 2 + 6 + 6 + 1;
+  static constexpr int kNumBars = 1 + 4 * STAGES + 2 + 6 + 6 + 3;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 128;          // the base is checked for 1024-byte alignment
@@ -113,7 +114,8 @@ __global__ void __launch_bounds__(480, 1)
   uint64_t* rows_ready = sc_done + 1;   // [2]
   uint64_t* red_full = rows_ready + 2;  // [2] a [128][32] f32 dQ^T chunk is staged in buffer b
   uint64_t* red_free = red_full + 2;    // [2] buffer b's previous TMA reduce has finished reading it
-  uint64_t* wo_full = red_free + 2;     // the weight warps have staged dK, dV (bf16 gradients)
+  uint64_t* wo_full = red_free + 2;     // [2] the weight warps have staged dV (0), dK (1) (bf16 gradients)
+  uint64_t* dv_done = wo_full + 2;      // the last dV product has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
 
   const int warp = threadIdx.x >> 5;
@@ -157,7 +159,9 @@ __global__ void __launch_bounds__(480, 1)
       mbar_init(&red_full[i], 128);
       mbar_init(&red_free[i], 1);
     }
-    mbar_init(wo_full, 8);
+    mbar_init(&wo_full[0], 8);
+    mbar_init(&wo_full[1], 8);
+    mbar_init(dv_done, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -325,6 +329,7 @@ __global__ void __launch_bounds__(480, 1)
             umma_bf16_ts(tmem + L::kColDV, dp_slot + pcol, dOh_mn + o, kIdG, (n > 0 || kk > 0) ? 1u : 0u);
           }
           if (L::kSplitOps) umma_commit(&stage_empty[st]);  // dO's last reader
+          if (n == n_items - 1) umma_commit(dv_done);        // dV is final: its write-out may start
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk) {
             const uint64_t o = static_cast<uint64_t>((kk * (16 * 128)) >> 4);
@@ -523,50 +528,64 @@ __global__ void __launch_bounds__(480, 1)
     // dK_h, dV_h rows of this key (zeros when no query row sees the tile):
     // this thread's 64 of the CTA's 128 head-dim columns.  The tensor-memory
     // loads run on every lane; only the stores depend on the key being < Nk.
-    if (ok && n_items > 0) {
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(dkv_done, 0, 88));
-      if (ok) tc_fence_after();
-    }
     if (ok && !p.g_f32 && n_items > 0) {
-      // bf16 gradients: each thread stages its key row's 64 columns of dK_h
-      // and dV_h as bf16 in the idle Q/dO ring ([128 keys][64 columns]
-      // boxes, 128-byte swizzle: dK half 0, dK half 1, dV half 0, dV half 1),
-      // and one thread writes the four boxes with TMA stores (rows past Nk
-      // are not written).
+      // bf16 gradients, dV first (its last product completes before dK's):
+      // each thread stages its key row's 64 columns of dV_h, then of dK_h, as
+      // bf16 in the Q/dO ring ([128 keys][64 columns] boxes, 128-byte
+      // swizzle, two per tensor), and one thread writes each tensor's boxes
+      // with TMA stores as soon as they are staged (rows past Nk are not
+      // written).  dV goes where the last item's dK product cannot be
+      // reading: the next stage of the ring (two or more stages) or the dO
+      // half of the one stage (dO's last reader, dV, is done); dK, staged
+      // once every product has completed, takes the remaining 32 KB.
+      const int last = n_items - 1;
+      const uint32_t st_off[2] = {
+          static_cast<uint32_t>(STAGES == 1 ? L::kQTile : ((last + 1) % STAGES) * L::kStage),
+          static_cast<uint32_t>(STAGES == 1 ? 0 : ((last + 2) % STAGES) * L::kStage)};
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? L::kColDK : L::kColDV;
-        const float mul = which == 0 ? p.scale : 1.f;
-        const uint32_t box = sbase + L::kQOff + (which * 2 + half) * (128 * 128) + row * 128;
-#pragma unroll 1
+      for (int which = 0; which < 2 && ok; ++which) {
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(which == 0 ? dv_done : dkv_done, 0, which == 0 ? 93 : 88));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t col = which == 0 ? L::kColDV : L::kColDK;
+        const float mul = which == 0 ? 1.f : p.scale;
+        const uint32_t box = sbase + L::kQOff + st_off[which] + half * (128 * 128) + row * 128;
+        uint32_t v[2][32];
+        tmem_ld32x2(lane_base + col + half * 64, v[0], lane_base + col + half * 64 + 32, v[1]);
+#pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + col + (half * 2 + c2) * 32, v);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int x = 8 * u;
             st_shared_v4(box + (((c2 * 4 + u) ^ (row & 7)) << 4),
-                         pack_bf16(__uint_as_float(v[x]) * mul, __uint_as_float(v[x + 1]) * mul),
-                         pack_bf16(__uint_as_float(v[x + 2]) * mul, __uint_as_float(v[x + 3]) * mul),
-                         pack_bf16(__uint_as_float(v[x + 4]) * mul, __uint_as_float(v[x + 5]) * mul),
-                         pack_bf16(__uint_as_float(v[x + 6]) * mul, __uint_as_float(v[x + 7]) * mul));
+                         pack_bf16(__uint_as_float(v[c2][x]) * mul, __uint_as_float(v[c2][x + 1]) * mul),
+                         pack_bf16(__uint_as_float(v[c2][x + 2]) * mul, __uint_as_float(v[c2][x + 3]) * mul),
+                         pack_bf16(__uint_as_float(v[c2][x + 4]) * mul, __uint_as_float(v[c2][x + 5]) * mul),
+                         pack_bf16(__uint_as_float(v[c2][x + 6]) * mul, __uint_as_float(v[c2][x + 7]) * mul));
           }
         }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(wo_full);
-      if (threadIdx.x == 64) {
-        if (mbar_wait(wo_full, 0, 92)) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wo_full[which]);
+        if (threadIdx.x == 64 && mbar_wait(&wo_full[which], 0, 92)) {
 #pragma unroll
-          for (int bx = 0; bx < 4; ++bx)
-            tma_store_3d(bx < 2 ? &tmDKo : &tmDVo, smem + L::kQOff + bx * (128 * 128), h * 128 + (bx & 1) * 64, k0,
-                         bkv);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_store_3d(which == 0 ? &tmDVo : &tmDKo, smem + L::kQOff + st_off[which] + bx * (128 * 128),
+                         h * 128 + bx * 64, k0, bkv);
           bulk_commit();
-          bulk_wait_read<0>();  // the boxes are read before the CTA ends; the writes complete with the grid
         }
       }
+      // The boxes are read before the CTA ends; the writes complete with the grid.
+      if (threadIdx.x == 64) bulk_wait_read<0>();
     } else if (ok) {
+      // f32 gradients (or a key tile no query row sees: zeros), stored
+      // directly from registers once every product has completed.
+      if (n_items > 0) {
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(dkv_done, 0, 88));
+        if (ok) tc_fence_after();
+      }
+    }
+    if (ok && (p.g_f32 || n_items == 0)) {
       const bool store = kj < p.Nk;
       const size_t off = (static_cast<size_t>(bkv) * p.Nk + kj) * D + h * 128;
 #pragma unroll 1
