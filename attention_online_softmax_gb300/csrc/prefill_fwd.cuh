@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
   // Plain kernel with two query tiles: the K/V ring is gated per MMA step
   // (V(t-1) and K(t), consecutive items) rather than per item -- one barrier
   // wait and one commit per step for the issuing thread instead of two each.
-  constexpr bool kStepRing = NQ == 2 && !PAGED;
+  constexpr bool kStepRing = NQ == 2;
   static_assert(!kStepRing || L::kH == 1, "step ring: one item per K or V tile");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   Unit<NQ>* unit_q = reinterpret_cast<Unit<NQ>*>(smem + L::kMiscOff + 16);
@@ -536,6 +536,10 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     const int c_l = lane % kCh;  // and 64-column box
     const bool issuer = g_l < kBN / ps;
     int item = 0, q_uses = 0, tails = 0;
+    int step = 0;          // step ring: steps issued so far
+    int slot_rel[STAGES];  // step ring: the step that last read each slot (-1: none yet)
+#pragma unroll
+    for (int i = 0; i < STAGES; ++i) slot_rel[i] = -1;
     bool ok = true;
     bool owned = false;  // lane 0: this CTA's first fetch found or claimed the launch's counter
     // Lane 0: this CTA made its final fetch, or needs none (no first unit).
@@ -592,6 +596,85 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       int pg_next = u.T > 1 ? page_of(1) : kNone;
       int pg_next2 = u.T > 2 ? page_of(2) : kNone;
       int kt_cur = 0;  // tile of the latest K item
+      if constexpr (kStepRing) {
+        // Step t of the unit brings V(t-1) and K(t) (items 2t-1, 2t) on one
+        // barrier: the page boxes of both add their bytes, and the warp
+        // arrives once, after zeroing a value tile's slots past the context
+        // end.  A slot is refilled once the step that read it is done.
+        for (int t = 0; ok && t <= u.T; ++t, ++step) {
+          const int nv = t >= 1 ? 1 : 0, nk = t < u.T ? 1 : 0;
+          int wok = 1;
+          if (lane == 0) {
+            for (int i = 0; i < nv + nk; ++i) {
+              const int r = slot_rel[(item + i) % STAGES];
+              if (r >= 0 && !mbar_wait(&step_empty[r % kStepR], (r / kStepR) & 1, 1)) wok = 0;
+            }
+          }
+          if (!__shfl_sync(kFull, wok, 0)) {
+            ok = false;
+            break;
+          }
+          uint64_t* bar = &step_full[step % kStepR];
+          for (int i = 0; i < nv + nk; ++i, ++item) {
+            const int st = item % STAGES;
+            const int kind = i < nv ? 1 : 0;
+            const int tt = kind ? t - 1 : t;
+            if (kind == 0 && tt > 0) {
+              pg_m2 = pg_m1;
+              pg_m1 = pg_cur;
+              pg_cur = pg_next;
+              pg_next = pg_next2;
+              pg_next2 = tt + 2 < u.T ? page_of(tt + 2) : kNone;
+              kt_cur = tt;
+            }
+            // V(t-1) comes right before K(t): its pages are tile t-1's.
+            const int pg = pg_cur;
+            const int kp = (u.tmin + tt) * kBN + g_l * ps;
+            const bool valid = pg >= 0 && pg < p.num_pages;
+            if (pg != kNone && !valid) report_error(7 /* ATTN_ERR_BOUNDS */, 8, pg);
+            const bool is_tail = valid && kind == 1 && kp + ps > u.nk;
+            const uint32_t tail_mask = __ballot_sync(kFull, is_tail);
+            const uint32_t load_mask = __ballot_sync(kFull, valid && !is_tail);
+            if (lane == 0) {
+              const uint32_t box = static_cast<uint32_t>(ps) * 128u;
+              mbar_expect_tx_only(bar, __popc(load_mask) * box);
+              if (tail_mask != 0) mbar_expect_tx(tail_bar, __popc(tail_mask) * box);
+            }
+            __syncwarp();
+            if (valid)
+              tma_load_4d(smem + L::kKVOff + st * L::kKVBytes + c_l * (kBN * 128) + g_l * ps * 128,
+                          kind ? &tmV : &tmK, is_tail ? tail_bar : bar, c_l * 64, u.kvh, 0, pg);
+            slot_rel[st] = step;
+            if (tail_mask != 0) {
+              int tok = 1;
+              if (lane == 0) tok = mbar_wait(tail_bar, tails & 1, 26);
+              if (!__shfl_sync(kFull, tok, 0)) {
+                ok = false;
+                break;
+              }
+              ++tails;
+              // Zero slots [rem, ps) of the tail page in each of its boxes.
+              const int tg = (__ffs(tail_mask) - 1) / kCh;
+              const int rem = u.nk - ((u.tmin + tt) * kBN + tg * ps);
+              const int nz = ps - rem;
+              const uint32_t stage = sbase + L::kKVOff + st * L::kKVBytes;
+              for (int e = lane; e < kCh * nz * 8; e += 32) {
+                const int k16 = e & 7;
+                const int rr = e >> 3;
+                const int cc = rr / nz;
+                const int r = rem + (rr - cc * nz);
+                st_shared_v4(stage + cc * (kBN * 128) + (tg * ps + r) * 128 + k16 * 16, 0u, 0u, 0u, 0u);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
+          }
+          if (!ok) break;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar);  // the step's one arrival
+        }
+        continue;
+      }
       for (int i = 0; i < 2 * L::kH * u.T; ++i, ++item) {
         const int st = item % STAGES;
         int t, kind, hh;
@@ -668,8 +751,13 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       // Drain: never leave the CTA with a copy still writing shared memory
       // (after one wait gives up, the rest are not attempted).
       bool drained = q_uses == 0 || mbar_wait(q_full, (q_uses - 1) & 1, 2);
-      for (int it = max(0, item - STAGES); drained && it < item; ++it)
-        drained = mbar_wait(&kv_full[it % STAGES], (it / STAGES) & 1, 3);
+      if (kStepRing) {
+        for (int st = max(0, step - kStepR); drained && st < step; ++st)
+          drained = mbar_wait(&step_full[st % kStepR], (st / kStepR) & 1, 3);
+      } else {
+        for (int it = max(0, item - STAGES); drained && it < item; ++it)
+          drained = mbar_wait(&kv_full[it % STAGES], (it / STAGES) & 1, 3);
+      }
     }
     __syncwarp();
   } else if (BIAS == 2 && warp == 2 + 4 * NQ) {
