@@ -291,7 +291,7 @@ int sched_group(int BH, int want) {
 // unit and variant (plain, additive bias read directly, staged dense bias,
 // paged).  The launches below and attn_fwd_kernel_name() both read it.
 constexpr int fwd_stages(int d, int nq, int bias, bool paged) {
-  return paged ? (d == 64 ? (nq == 2 ? 10 : 12) : d == 128 ? (nq == 2 ? 5 : 6) : 5)
+  return paged ? (d == 64 ? (nq == 2 ? 10 : 12) : d == 128 ? (nq == 2 ? 4 : 6) : 5)
          : bias == 2 ? (d == 64 ? 8 : d == 128 ? 4 : 3)
          : bias == 1 ? (d == 64 ? 12 : d == 128 ? 6 : 5)
                      : (d == 64 ? (nq == 2 ? 10 : 12) : d == 128 ? (nq == 2 ? 4 : 6) : 5);
