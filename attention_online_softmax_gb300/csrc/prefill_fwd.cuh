@@ -1267,6 +1267,8 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       const size_t lse_off = PAGED ? static_cast<size_t>(u.qbase + qrow) * p.Hq + bh
                                    : static_cast<size_t>(bh) * p.Nq + qrow;
       const size_t row_off = lse_off * D;
+      // bf16 rows start 32-byte aligned when O does (a row is 128 bytes or more).
+      const bool o32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -1289,6 +1291,18 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
           for (int i = 0; i < 8; ++i)
             dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
                                  __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+        } else if (o32) {
+          // Full 32-byte sectors per store (the row's 64 bytes of this chunk).
+          uint16_t* dst = static_cast<uint16_t*>(p.o) + row_off + cc * 32;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int e = 16 * i;
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              w[k] = pack_bf16(__uint_as_float(o[e + 2 * k]) * inv, __uint_as_float(o[e + 2 * k + 1]) * inv);
+            st_global_v8(dst + 16 * i, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+          }
         } else {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + row_off + cc * 32);
 #pragma unroll
