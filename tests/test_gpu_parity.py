@@ -142,6 +142,31 @@ def test_prefill_is_deterministic(abi):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+@pytest.mark.parametrize("d,two", [(64, False), (128, True), (256, False)])
+def test_prefill_output_only_16_byte_aligned(abi, d, two):
+    # O at an address that is 16-byte but not 32-byte aligned (the contract's
+    # minimum) takes the epilogue's 16-byte stores: bitwise the result written
+    # to an aligned O.
+    heads = 160 if two else 2
+    x = inputs.prefill_inputs(1, heads, heads, 300, 300, d, seed=7100 + d, causal=True)
+    dev = torch.device("cuda")
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    shape = (1, heads, 300, d)
+    n = math.prod(shape)
+    o_al = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    raw = torch.empty(n + 16, dtype=torch.bfloat16, device=dev)
+    o_off = raw[8:8 + n].view(shape)  # 16 bytes past a 256-byte aligned base
+    assert o_off.data_ptr() % 32 == 16 and o_al.data_ptr() % 32 == 0
+    outs = []
+    for o in (o_al, o_off):
+        lse = torch.empty((1, heads, 300), dtype=torch.float32, device=dev)
+        abi.attn_fwd(q, k, v, o, lse, True, x.scale)
+        outs.append((o.clone(), lse))
+    torch.cuda.synchronize()
+    assert abi.attn_get_device_status() == 0
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
 def test_prefill_output_depends_on_every_input(abi):
     # Perturb one element of Q, K and V in turn: the affected rows must change.
     x = inputs.prefill_inputs(1, 2, 2, 256, 256, 64, seed=8, causal=False)
