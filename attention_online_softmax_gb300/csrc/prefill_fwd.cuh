@@ -300,6 +300,12 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
                        const PrefillParams p) {
   using L = PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(), psep_path<BIAS, PAGED>()>;
   static_assert(BIAS == 0 || NQ == 1, "additive-bias variants run one query tile per unit");
+  // With ALiBi slopes a unit's key tiles are taken from the last to the
+  // first: the ALiBi term grows with the key index, so the row maxima are
+  // met on the first tile taken and O seldom needs rescaling afterwards
+  // (the block recurrence gives the same result in any tile order, up to
+  // the rounding of P against a different reference maximum).
+  const bool rev_tiles = BIAS != 0 && p.alibi != nullptr;
   static_assert(!PAGED || BIAS == 0, "paged prefill: no dense bias");
   static_assert(sizeof(Unit<NQ>) <= L::kUnitBytes, "unit queue entry");
   extern __shared__ uint8_t smem_raw[];
@@ -488,7 +494,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
 #pragma unroll
             for (int c = 0; c < L::kDI / 64; ++c)
               tma_load_3d(smem + L::kKVOff + st * L::kKVBytes + c * (kBN * 128), map, &kv_full[st],
-                          hh * L::kDI + c * 64, (u.tmin + t) * kBN, u.kvh);
+                          hh * L::kDI + c * 64, (u.tmin + (rev_tiles ? u.T - 1 - t : t)) * kBN, u.kvh);
           }
         }
       }
@@ -775,7 +781,8 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
         if (u.idx < 0) break;
         const int b = u.bh / p.Hq;
         const int h = u.bh - b * p.Hq;
-        for (int t = u.lo[0]; t < u.hi[0]; ++t, ++bitem) {
+        for (int i = u.lo[0]; i < u.hi[0]; ++i, ++bitem) {
+          const int t = rev_tiles ? u.hi[0] - 1 - (i - u.lo[0]) : i;
           const int bs = bitem % bias_ring<BIAS>();
           if (!mbar_wait(&bias_empty[bs], ((bitem / bias_ring<BIAS>()) & 1) ^ 1, 6)) {
             ok = false;
@@ -1073,7 +1080,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       float l0 = 0.f, l1 = 0.f, lr0 = 0.f, lr1 = 0.f;
 
       for (int ti = 0; ti < nt; ++ti) {
-        const int t = u.lo[j] + ti;  // absolute key tile
+        const int t = rev_tiles ? u.hi[j] - 1 - ti : u.lo[j] + ti;  // absolute key tile
         const int slot = NQ == 2 ? j : (cnt & 1);
         const uint32_t s_par = NQ == 2 ? (cnt & 1) : ((cnt >> 1) & 1);
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_full[slot], s_par, 20));
