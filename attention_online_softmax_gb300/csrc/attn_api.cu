@@ -274,17 +274,26 @@ attn_status sched_slot(unsigned long long** out, unsigned* tag) {
 }
 
 // (Batch, head) pairs per scheduling group of the plain prefill: at least
-// `want` (enough heads for two waves of units), and groups of equal size --
-// a short last group would start its longest units last and leave the end of
-// the launch to a few SMs.  A divisor of BH up to twice `want` if there is
-// one, else BH split into near-equal groups of about `want`.
-int sched_group(int BH, int want) {
+// `want` (enough heads for two waves of units) unless that exceeds `cap`
+// (the most heads whose K/V stays in L2, so that each K/V tile comes from
+// DRAM once), and groups of equal size -- a short last group would start its
+// longest units last and leave the end of the launch to a few SMs.  A
+// divisor of BH from `want` up to twice `want` (and `cap`) if there is one,
+// else BH split into near-equal groups of about `want`, or of at most `cap`.
+int sched_group(int BH, int want, int cap) {
+  if (cap < 1) cap = 1;
   if (want < 1) want = 1;
+  if (want > cap) want = cap;
   if (want >= BH) return BH;
-  for (int d = want; d <= 2 * want && d <= BH; ++d)
+  for (int d = want; d <= 2 * want && d <= cap && d <= BH; ++d)
     if (BH % d == 0) return d;
-  const int groups = BH / want;
-  return (BH + groups - 1) / groups;
+  int groups = BH / want;
+  int g = (BH + groups - 1) / groups;
+  if (g > cap) {
+    groups = (BH + cap - 1) / cap;
+    g = (BH + groups - 1) / groups;
+  }
+  return g;
 }
 
 // K/V ring depth of each prefill instantiation, by head dim, query tiles per
@@ -313,7 +322,12 @@ attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const C
   if (!ensure_smem<attn::prefill_fwd_kernel<D, NQ, STAGES, BIAS>>(L::kAlloc)) return ATTN_ERR_LAUNCH;
   p.n_units = (p.Nq + attn::kBM * NQ - 1) / (attn::kBM * NQ);
   const int sms = sm_count();
-  p.group = sched_group(BH, (2 * sms + p.n_units - 1) / p.n_units);
+  // K/V bytes per query head of a group (consecutive query heads share
+  // their kv head): groups hold at most ~40 MB of K/V.
+  const long long kv_per_head =
+      std::max(1LL, 4LL * p.Nk * D / std::max(1, p.Hq / std::max(1, p.Hkv)));
+  const long long cap = std::max(1LL, std::min<long long>(BH, (40LL << 20) / kv_per_head));
+  p.group = sched_group(BH, (2 * sms + p.n_units - 1) / p.n_units, static_cast<int>(cap));
   const long long units = static_cast<long long>(p.n_units) * BH;
   if (units > 0x7FFFFFFFLL) return ATTN_ERR_UNSUPPORTED;
   const attn_status st = sched_slot(&p.sched, &p.sched_tag);
