@@ -346,7 +346,7 @@ attn_status launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const C
 template <int D, int NQ, int STAGES>
 attn_status launch_prefill_paged(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                                  attn::PrefillParams p, int total_q, cudaStream_t stream) {
-  using L = attn::PrefillLayout<D, NQ, STAGES, 0, attn::psep_path<0, true>()>;
+  using L = attn::PrefillLayout<D, NQ, STAGES, 0, attn::psep_path<0, true>(), attn::producer_warps<true>()>;
   auto kern = attn::prefill_fwd_kernel<D, NQ, STAGES, 0, true>;
   if (!ensure_smem<attn::prefill_fwd_kernel<D, NQ, STAGES, 0, true>>(L::kAlloc)) return ATTN_ERR_LAUNCH;
   const attn_status st = sched_slot(&p.sched, &p.sched_tag);

@@ -14,8 +14,9 @@
 // Units are handed out longest causal unit first within groups of heads, so
 // the uneven causal units pack well while each group's K/V stays in L2.
 //
-// Roles (64 + 128*NQ threads, plus a bias-loader warp for a staged dense bias
-// and a second MMA-issuing warp with separate P slots):
+// Roles (64 + 128*NQ threads, plus a bias-loader warp for a staged dense bias,
+// a second MMA-issuing warp with separate P slots, and a second producer warp
+// for the paged cache):
 //   warp 0        TMA producer: takes the next unit from the work counter and
 //                 passes it to the other roles through a small shared-memory
 //                 queue, loads the unit's NQ query tiles, then its K_t, V_t
@@ -95,16 +96,18 @@ struct PrefillParams {
 };
 
 
-template <int D, int NQ, int STAGES, int BSLOTS = 0, bool PSEP = false>
+template <int D, int NQ, int STAGES, int BSLOTS = 0, bool PSEP = false, int PW = 1>
 struct PrefillLayout {
   // warp 0 TMA producer, warp 1 MMA issuer, 4 softmax warps per query tile,
   // and with a staged bias one more warp that loads the bias tiles.
   // Separate P slots (PSEP, one query tile, d <= 128): a second MMA-issuing
-  // warp takes the P V products.
+  // warp takes the P V products.  PW = 2 (paged cache): a second producer
+  // warp, the last one, issues half of each item's page boxes.
   static constexpr bool kPSep = PSEP && NQ == 1 && D <= 128;
   static constexpr bool kSplit = kPSep;
   static constexpr int kPVWarp = 2 + 4 * NQ + (BSLOTS > 0 ? 1 : 0);
-  static constexpr int kThreads = 64 + 128 * NQ + (BSLOTS > 0 ? 32 : 0) + (kSplit ? 32 : 0);
+  static constexpr int kProd2Warp = 2 + 4 * NQ + (BSLOTS > 0 ? 1 : 0) + (kSplit ? 1 : 0);
+  static constexpr int kThreads = 64 + 128 * NQ + (BSLOTS > 0 ? 32 : 0) + (kSplit ? 32 : 0) + (PW - 1) * 32;
   static constexpr int kQBytes = kBM * D * 2;
   // K and V tiles stream in items of up to 128 head-dim columns (kH items per
   // tile), so with d = 256 a 64 KB tile occupies two 32 KB ring stages and
@@ -122,8 +125,8 @@ struct PrefillLayout {
   // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done,
   // (s_free[2], pv_free[2], step_full[kStepR], step_empty[kStepR] after tail_bar),
   // o_done[2], o_free[2], unit_full[Q], unit_empty[Q], mma_drain,
-  // bias_full[BSLOTS], bias_empty[BSLOTS], tail_bar
-  static constexpr int kNumBars = 2 + 2 * STAGES + 2 + 2 + 1 + 2 + 2 + 2 * kUnitQ + 1 + 2 * BSLOTS + 1 + 4 + 2 * kStepR;
+  // bias_full[BSLOTS], bias_empty[BSLOTS], tail_bar[2]
+  static constexpr int kNumBars = 2 + 2 * STAGES + 2 + 2 + 1 + 2 + 2 + 2 * kUnitQ + 1 + 2 * BSLOTS + 2 + 4 + 2 * kStepR;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, unit queue
   static constexpr int kUnitBytes = 64;                      // one decoded unit in the queue
   static constexpr int kBytes = kMiscOff + 16 + kUnitBytes * kUnitQ;
@@ -292,13 +295,19 @@ __host__ __device__ constexpr int bias_ring() { return BIAS == 2 ? 2 : 1; }  // 
 // P in the S slot with one MMA-issuing thread.
 template <int BIAS, bool PAGED>
 __host__ __device__ constexpr bool psep_path() { return BIAS == 0 && !PAGED; }
+// Producer warps: two for the paged cache, whose key tile is up to 16 page
+// boxes per item (a warp hands its lanes' TMA copies over one at a time, at
+// ~60-80 cycles each), one otherwise.
+template <bool PAGED>
+__host__ __device__ constexpr int producer_warps() { return PAGED ? 2 : 1; }
 
 template <int D, int NQ, int STAGES, int BIAS, bool PAGED = false>
-__global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(), psep_path<BIAS, PAGED>()>::kThreads, 1)
+__global__ void __launch_bounds__(
+    PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(), psep_path<BIAS, PAGED>(), producer_warps<PAGED>()>::kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
                        const PrefillParams p) {
-  using L = PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(), psep_path<BIAS, PAGED>()>;
+  using L = PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(), psep_path<BIAS, PAGED>(), producer_warps<PAGED>()>;
   static_assert(BIAS == 0 || NQ == 1, "additive-bias variants run one query tile per unit");
   // With ALiBi slopes a unit's key tiles are taken from the last to the
   // first: the ALiBi term grows with the key index, so the row maxima are
@@ -328,8 +337,8 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
   uint64_t* mma_drain = unit_empty + kUnitQ;
   uint64_t* bias_full = mma_drain + 1;
   uint64_t* bias_empty = bias_full + bias_slots<BIAS>();
-  uint64_t* tail_bar = bias_empty + bias_slots<BIAS>();  // paged: a partly filled value page
-  uint64_t* s_free = tail_bar + 1;   // [2] separate P slots: the softmax has read S from this slot
+  uint64_t* tail_bar = bias_empty + bias_slots<BIAS>();  // [2] paged: a partly filled value page, per producer warp
+  uint64_t* s_free = tail_bar + 2;   // [2] separate P slots: the softmax has read S from this slot
   uint64_t* pv_free = s_free + 2;    // [2] separate P slots: the P V product of this P slot is complete
   uint64_t* step_full = pv_free + 2;         // [kStepR] step ring: V(t-1) and K(t) have landed
   uint64_t* step_empty = step_full + kStepR;  // [kStepR] step ring: the step's products are done with them
@@ -357,7 +366,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_full[s], producer_warps<PAGED>());  // one arrival per producer warp
       mbar_init(&kv_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -368,18 +377,21 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     }
     for (int i = 0; i < kUnitQ; ++i) {
       mbar_init(&unit_full[i], 1);
-      // MMA thread + lane 0 of every softmax warp (+ the bias loader)
-      mbar_init(&unit_empty[i], 1 + 4 * NQ + (BIAS == 2 ? 1 : 0) + (L::kSplit ? 1 : 0));
+      // MMA thread + lane 0 of every softmax warp (+ the bias loader, the
+      // second MMA-issuing warp, the second producer warp)
+      mbar_init(&unit_empty[i],
+                1 + 4 * NQ + (BIAS == 2 ? 1 : 0) + (L::kSplit ? 1 : 0) + (producer_warps<PAGED>() - 1));
     }
     mbar_init(pv_done, 1);
     mbar_init(mma_drain, L::kSplit ? 2 : 1);  // one commit per MMA-issuing thread
-    mbar_init(tail_bar, 1);
+    mbar_init(&tail_bar[0], 1);
+    mbar_init(&tail_bar[1], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_free[i], 4);
       mbar_init(&pv_free[i], 1);
     }
     for (int i = 0; i < kStepR; ++i) {
-      mbar_init(&step_full[i], 1);
+      mbar_init(&step_full[i], producer_warps<PAGED>());
       mbar_init(&step_empty[i], 1);
     }
     for (int i = 0; i < bias_slots<BIAS>(); ++i) {
@@ -516,11 +528,15 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
       }
     }
     __syncwarp();
-  } else if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer, paged cache
-    // The whole warp: a key tile spans 128 / page_size pages, each loaded as
-    // kDI / 64 boxes, one box per lane, so the boxes of an item are issued
-    // together.  Lane 0 does the waits, arrivals and the Q loads.  Each lane
+  } else if (warp == 0 || (PAGED && warp == L::kProd2Warp)) {
+    // ---------------------------------------------------------------- TMA producers, paged cache
+    // Two whole warps: a key tile spans 128 / page_size pages, each loaded as
+    // kDI / 64 boxes; box b of an item goes to lane b / 2 of producer warp
+    // b % 2, so each warp issues half of an item's boxes (a warp hands its
+    // lanes' copies to the TMA unit one after the other).  Warp 0 takes the
+    // units from the work counter and publishes them; the second producer
+    // warp reads them from the unit queue.  Lane 0 of each does its waits and
+    // its arrival on the item's barrier (two per item); warp 0 loads Q.  Each lane
     // keeps the page id of its box for the tiles t-2 .. t+2 around the latest
     // K(t) (a value tile is loaded at most two key tiles after its own): the
     // block-table read of a tile is issued two tiles ahead of its first use.  Pages past the context's end are not loaded
@@ -538,9 +554,12 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     }
     const int total_units = __ldg(p.unit_prefix + p.num_seqs);
     const int ps = p.page_size;
-    const int g_l = lane / kCh;  // this lane's page within a key tile
-    const int c_l = lane % kCh;  // and 64-column box
+    const int pw = warp == 0 ? 0 : 1;  // producer warp
+    const int b_l = 2 * lane + pw;      // this lane's box of an item
+    const int g_l = b_l / kCh;          // its page within a key tile
+    const int c_l = b_l % kCh;          // and 64-column box
     const bool issuer = g_l < kBN / ps;
+    uint64_t* const tbar = &tail_bar[pw];  // this warp's partly filled value page
     int item = 0, q_uses = 0, tails = 0;
     int step = 0;          // step ring: steps issued so far
     int slot_rel[STAGES];  // step ring: the step that last read each slot (-1: none yet)
@@ -548,35 +567,46 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
     for (int i = 0; i < STAGES; ++i) slot_rel[i] = -1;
     bool ok = true;
     bool owned = false;  // lane 0: this CTA's first fetch found or claimed the launch's counter
-    // Lane 0: this CTA made its final fetch, or needs none (no first unit).
-    bool fetched_last = static_cast<int>(blockIdx.x) >= total_units;
+    // Lane 0: this CTA made its final fetch, or needs none (no first unit;
+    // the second producer warp never fetches).
+    bool fetched_last = pw == 1 || static_cast<int>(blockIdx.x) >= total_units;
     for (int n = 0; ok; ++n) {
       const int slot = n % kUnitQ;
-      int idx = -2;
-      if (lane == 0 && mbar_wait(&unit_empty[slot], ((n / kUnitQ) & 1) ^ 1, 4)) {
-        idx = static_cast<int>(blockIdx.x);
-        if (n > 0) {
-          const int c = sched_fetch(p.sched, p.sched_tag, owned, total_units);
-          idx = c < 0 ? total_units : static_cast<int>(gridDim.x) + c;
-          fetched_last = idx >= total_units;
-        }
-      }
-      idx = __shfl_sync(kFull, idx, 0);
-      if (idx == -2) break;
       Unit<NQ> u;
-      if (idx < total_units) {
-        u = unit_of<NQ, true>(p, idx);
+      if (pw == 0) {
+        int idx = -2;
+        if (lane == 0 && mbar_wait(&unit_empty[slot], ((n / kUnitQ) & 1) ^ 1, 4)) {
+          idx = static_cast<int>(blockIdx.x);
+          if (n > 0) {
+            const int c = sched_fetch(p.sched, p.sched_tag, owned, total_units);
+            idx = c < 0 ? total_units : static_cast<int>(gridDim.x) + c;
+            fetched_last = idx >= total_units;
+          }
+        }
+        idx = __shfl_sync(kFull, idx, 0);
+        if (idx == -2) break;
+        if (idx < total_units) {
+          u = unit_of<NQ, true>(p, idx);
+        } else {
+          u.idx = -1;
+        }
+        if (lane == 0) {
+          unit_q[slot] = u;
+          mbar_arrive(&unit_full[slot]);
+        }
       } else {
-        u.idx = -1;
-      }
-      if (lane == 0) {
-        unit_q[slot] = u;
-        mbar_arrive(&unit_full[slot]);
+        int got = lane == 0 ? next_unit(n, 27).idx : 0;
+        got = __shfl_sync(kFull, got, 0);
+        if (got == -2) break;
+        __syncwarp();
+        u = unit_q[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&unit_empty[slot]);
       }
       if (u.idx < 0) break;
       if (u.T == 0) continue;
       int qok = 1;
-      if (lane == 0) {
+      if (pw == 0 && lane == 0) {
         // The previous unit's last S MMA must be done with the Q tile.
         if (q_uses > 0 && !mbar_wait(q_empty, (q_uses - 1) & 1, 5)) {
           qok = 0;
@@ -591,8 +621,21 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
         }
       }
       if (!__shfl_sync(kFull, qok, 0)) break;
-      ++q_uses;
+      if (pw == 0) ++q_uses;
       const long long bt_row = static_cast<long long>(u.seq) * p.max_pages;
+      {
+        // The block-table entries of the unit's pages into L2 now, one line
+        // per lane (16-token pages: a 128-byte line every 4 key tiles), so
+        // that their reads two tiles ahead of use never wait on DRAM.
+        const long long e0 = bt_row + static_cast<long long>(u.tmin) * kBN / ps;
+        const long long e1 = bt_row + (min(static_cast<long long>(u.tmin + u.T) * kBN, static_cast<long long>(u.nk)) + ps - 1) / ps;
+        if (e1 > e0) {
+          const uintptr_t a = reinterpret_cast<uintptr_t>(p.block_table + e0);
+          const uintptr_t b = reinterpret_cast<uintptr_t>(p.block_table + e1 - 1);
+          for (uintptr_t line = (a & ~uintptr_t(127)) + uintptr_t(128) * (lane + 32 * pw); line <= b; line += 128 * 64)
+            prefetch_line_l2(reinterpret_cast<const void*>(line < a ? a : line));
+        }
+      }
       auto page_of = [&](int t) -> int {
         const int kp = (u.tmin + t) * kBN + g_l * ps;
         return (issuer && kp < u.nk) ? __ldg(p.block_table + bt_row + kp / ps) : kNone;
@@ -644,32 +687,32 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
             if (lane == 0) {
               const uint32_t box = static_cast<uint32_t>(ps) * 128u;
               mbar_expect_tx_only(bar, __popc(load_mask) * box);
-              if (tail_mask != 0) mbar_expect_tx(tail_bar, __popc(tail_mask) * box);
+              if (tail_mask != 0) mbar_expect_tx(tbar, __popc(tail_mask) * box);
             }
             __syncwarp();
             if (valid)
               tma_load_4d(smem + L::kKVOff + st * L::kKVBytes + c_l * (kBN * 128) + g_l * ps * 128,
-                          kind ? &tmV : &tmK, is_tail ? tail_bar : bar, c_l * 64, u.kvh, 0, pg);
+                          kind ? &tmV : &tmK, is_tail ? tbar : bar, c_l * 64, u.kvh, 0, pg);
             slot_rel[st] = step;
             if (tail_mask != 0) {
               int tok = 1;
-              if (lane == 0) tok = mbar_wait(tail_bar, tails & 1, 26);
+              if (lane == 0) tok = mbar_wait(tbar, tails & 1, 26);
               if (!__shfl_sync(kFull, tok, 0)) {
                 ok = false;
                 break;
               }
               ++tails;
-              // Zero slots [rem, ps) of the tail page in each of its boxes.
-              const int tg = (__ffs(tail_mask) - 1) / kCh;
+              // Zero slots [rem, ps) of this warp's box of the tail page (one
+              // page holds the context end; a warp has at most one of its boxes).
+              const int tb = 2 * (__ffs(tail_mask) - 1) + pw;
+              const int tg = tb / kCh, tc = tb % kCh;
               const int rem = u.nk - ((u.tmin + tt) * kBN + tg * ps);
               const int nz = ps - rem;
               const uint32_t stage = sbase + L::kKVOff + st * L::kKVBytes;
-              for (int e = lane; e < kCh * nz * 8; e += 32) {
+              for (int e = lane; e < nz * 8; e += 32) {
                 const int k16 = e & 7;
-                const int rr = e >> 3;
-                const int cc = rr / nz;
-                const int r = rem + (rr - cc * nz);
-                st_shared_v4(stage + cc * (kBN * 128) + (tg * ps + r) * 128 + k16 * 16, 0u, 0u, 0u, 0u);
+                const int r = rem + (e >> 3);
+                st_shared_v4(stage + tc * (kBN * 128) + (tg * ps + r) * 128 + k16 * 16, 0u, 0u, 0u, 0u);
               }
               fence_proxy_async_smem();
               __syncwarp();
@@ -677,7 +720,7 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
           }
           if (!ok) break;
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar);  // the step's one arrival
+          if (lane == 0) mbar_arrive(bar);  // this warp's one arrival of the step
         }
         continue;
       }
@@ -714,37 +757,36 @@ __global__ void __launch_bounds__(PrefillLayout<D, NQ, STAGES, bias_slots<BIAS>(
             mbar_expect_tx(&kv_full[st], __popc(load_mask) * box);  // arrives; 0 bytes completes at once
           } else {
             mbar_expect_tx_only(&kv_full[st], __popc(load_mask) * box);
-            mbar_expect_tx(tail_bar, __popc(tail_mask) * box);
+            mbar_expect_tx(tbar, __popc(tail_mask) * box);
           }
         }
         __syncwarp();
         const CUtensorMap* map = kind ? &tmV : &tmK;
         if (valid)
           tma_load_4d(smem + L::kKVOff + st * L::kKVBytes + c_l * (kBN * 128) + g_l * ps * 128, map,
-                      is_tail ? tail_bar : &kv_full[st], hh * L::kDI + c_l * 64, u.kvh, 0, pg);
+                      is_tail ? tbar : &kv_full[st], hh * L::kDI + c_l * 64, u.kvh, 0, pg);
         if (tail_mask != 0) {
           int tok = 1;
-          if (lane == 0) tok = mbar_wait(tail_bar, tails & 1, 26);
+          if (lane == 0) tok = mbar_wait(tbar, tails & 1, 26);
           if (!__shfl_sync(kFull, tok, 0)) {
             ok = false;
             break;
           }
           ++tails;
-          // Zero slots [rem, ps) of the tail page in each of its boxes.
-          const int tg = (__ffs(tail_mask) - 1) / kCh;
+          // Zero slots [rem, ps) of this warp's box of the tail page.
+          const int tb = 2 * (__ffs(tail_mask) - 1) + pw;
+          const int tg = tb / kCh, tc = tb % kCh;
           const int rem = u.nk - ((u.tmin + t) * kBN + tg * ps);
           const int nz = ps - rem;
           const uint32_t stage = sbase + L::kKVOff + st * L::kKVBytes;
-          for (int e = lane; e < kCh * nz * 8; e += 32) {
+          for (int e = lane; e < nz * 8; e += 32) {
             const int k16 = e & 7;
-            const int rr = e >> 3;
-            const int cc = rr / nz;
-            const int r = rem + (rr - cc * nz);
-            st_shared_v4(stage + cc * (kBN * 128) + (tg * ps + r) * 128 + k16 * 16, 0u, 0u, 0u, 0u);
+            const int r = rem + (e >> 3);
+            st_shared_v4(stage + tc * (kBN * 128) + (tg * ps + r) * 128 + k16 * 16, 0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&kv_full[st]);  // the item's one arrival
+          if (lane == 0) mbar_arrive(&kv_full[st]);  // this warp's one arrival of the item
         }
       }
     }

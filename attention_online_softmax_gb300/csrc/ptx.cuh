@@ -203,6 +203,12 @@ __device__ __forceinline__ int sched_fetch(unsigned long long* word, unsigned ta
 }
 
 // ----------------------------------------------------------------------- TMA
+// The 128-byte line holding `ptr` into L2 (no register written, no fault on
+// an address of the caller's allocation).
+__device__ __forceinline__ void prefetch_line_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -98,6 +98,21 @@ def test_masked_prefill(abi, case):
     check_masked(abi, x, window, slopes, bias)
 
 
+@pytest.mark.parametrize("kind", [None, "batch", "full"])  # ALiBi alone, staged bias, direct bias
+def test_alibi_slopes_of_either_sign(abi, kind):
+    # With ALiBi slopes the key tiles are taken from the last to the first.
+    # Positive slopes put each row's maximum on the first tile taken;
+    # negative ones (and a steep mix) make it grow on every tile, so O is
+    # rescaled after every key tile: the result must not depend on which.
+    B, Hq, Nq, Nk, d = 1, 4, 300, 1100 if kind != "full" else 1101, 128
+    x = inputs.prefill_inputs(B, Hq, Hq, Nq, Nk, d, seed=4150, causal=False)
+    slopes = inputs.alibi_slopes(Hq) * torch.tensor([-1.0, 1.0, -8.0, 0.5])
+    bias = None
+    if kind is not None:
+        bias = inputs.bias_inputs(bias_shape(kind, B, Hq, Nq, Nk), seed=4151, neg_inf_frac=0.02)
+    check_masked(abi, x, slopes=slopes, bias=bias)
+
+
 @pytest.mark.parametrize("Nk", [300, 296])  # direct and staged bias reads
 def test_bias_rows_all_minus_inf(abi, Nk):
     # Query rows whose bias is -inf for every key: O = 0, LSE = -inf.
