@@ -67,6 +67,11 @@ PAGED = [
     ([300], [200], 2, 2, 128, 16, True, 0),                          # k_len < q_len: rows without keys
     ([0, 130, 0, 7], [50, 130, 0, 9], 4, 2, 64, 16, True, 0),        # empty chunks and contexts
     ([5, 3], [0, 3], 2, 1, 128, 16, True, 0),                        # a chunk with no context at all
+    # One page per key tile: with d = 64 it is one box, and the second
+    # producer warp has none (it still arrives on every item's barrier);
+    # with d = 256 each producer warp has one box of it.
+    ([129, 64], [500, 70], 4, 4, 64, 128, True, 0),
+    ([100, 260], [300, 1030], 8, 1, 256, 128, True, 0),
 ]
 
 
